@@ -1,0 +1,231 @@
+"""Float64 CPU oracle for quantized-KV decode attention.
+
+TEST INFRASTRUCTURE ONLY. This module is the slow, plainly written definition
+the CUDA path is checked against. Only the test suite, the package smoke check
+and the benchmark's CPU-baseline / reference leg may import it; the product
+path never calls it and shares no code with it.
+
+Sources (page title, then section):
+  [P1] "KV Cache Quantization Perturbs Attention Through Stored Keys and Values"
+  [P2] "KV Cache Quantization Reduces Cache Bytes with Separate Accuracy and Kernel Costs"
+  [P3] "KV Cache Quantization and Per-Token Scale Placement"
+
+Every step follows the plain definition; nothing is fused, blocked or
+reordered beyond what the cited passage states. In particular the oracle does
+NOT fold the per-token key scale after the dot product, does not move the
+per-channel key factor onto the query and does not split the sequence: those
+are the GPU's rewrites and are checked separately as identities.
+
+Readings taken where the pages leave a step open:
+  * rounding is round-half-to-even of the exact quotient x/s (the [P3] listing
+    uses Python's round, which is half-to-even);
+  * the scale is stored as float32, s = RN32(amax/qmax), and codes are computed
+    from that stored scale;
+  * an all-zero vector stores codes 0 with scale 1.0 ([P3] listing);
+  * int8 codes clamp to [-127, 127] ([P3] listing clamps to +-qmax); int4 codes
+    clamp to [-8, 7] (qmax = 7); neither bound below -qmax is reachable;
+  * with a per-channel key factor c, keys are first divided by c (rounded to
+    float32) and then quantized per token; the reconstruction is c * code * s;
+  * with a recent-token window of W tokens, the last min(W, L) positions are
+    kept as their bf16 values and only older positions are quantized;
+  * the log-sum-exp is in natural-log units of the score q.k/sqrt(D).
+Every function below is pinned by tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+QMAX = {8: 127, 4: 7}
+CLAMP = {8: (-127, 127), 4: (-8, 7)}
+
+
+# ---------------------------------------------------------------- inputs
+def bf16_to_f64(bits) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float64."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- quantizer
+def quantize(x: np.ndarray, bits: int):
+    """Symmetric per-vector quantization along the last axis.
+
+    [P2] "Quantization needs a scale convention": q = clamp(round(x / s)),
+    x_hat = q * s.  [P3] "Per-token scales and where they can live": one scale
+    per token per head, computed from the vector at write time.  [P3] "The axis
+    choice is a kernel decision" (listing quantize_kv_vector): amax = max |x|,
+    zero vector -> (codes 0, scale 1.0), scale = amax / qmax.
+
+    Returns (codes int16 [..., D], scale float32 [...]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    qmax = QMAX[bits]
+    lo, hi = CLAMP[bits]
+    amax = np.max(np.abs(x), axis=-1)
+    # RN32(amax / qmax): float64 quotient then one rounding to float32.  Double
+    # rounding is harmless for a quotient of float32 operands (53 >= 2*24 + 2).
+    s = (amax / qmax).astype(np.float32)
+    s = np.where(amax == 0.0, np.float32(1.0), s).astype(np.float32)
+    quotient = x / s.astype(np.float64)[..., None]
+    codes = np.clip(np.rint(quotient), lo, hi).astype(np.int16)   # rint: half to even
+    return codes, s
+
+
+def dequantize(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """x_hat = q * s ([P2] "Quantization needs a scale convention"), exact in float64."""
+    return np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[..., None]
+
+
+def divide_by_channel_factor(k: np.ndarray, c: np.ndarray) -> np.ndarray:
+    """k'_j = RN32(k_j / c_j): the per-channel key factor taken out before the
+    per-token quantizer ([P3] "The axis choice is a kernel decision": the
+    per-channel factor is moved onto the query)."""
+    return (np.asarray(k, np.float64) / np.asarray(c, np.float64)).astype(np.float32).astype(np.float64)
+
+
+def quantize_keys(k: np.ndarray, bits: int, c: np.ndarray | None = None):
+    """Per-token key quantization, optionally after the per-channel factor."""
+    x = k if c is None else divide_by_channel_factor(k, c)
+    return quantize(x, bits)
+
+
+def reconstruct_keys(codes, scale, c=None) -> np.ndarray:
+    """k_hat = c * (q * s); without a factor, k_hat = q * s."""
+    kh = dequantize(codes, scale)
+    return kh if c is None else kh * np.asarray(c, np.float64)
+
+
+# ---------------------------------------------------------------- attention
+def attention(q: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray):
+    """Plain softmax attention of one or more queries over T cached tokens.
+
+    [P1] "Key error acts before the softmax": s = q K^T / sqrt(d), a = softmax(s),
+    o = a V.  [P2] "Keys and values need not have identical error sensitivity":
+    score_i = q^T k_hat_i / sqrt(D), output = sum_i softmax(score)_i v_hat_i.
+
+    q [G, D], k_hat [T, D], v_hat [T, D] -> (o [G, D], lse [G]) with
+    lse = ln sum_i exp(score_i).  T == 0 gives o = 0 and lse = -inf.
+    """
+    q = np.atleast_2d(np.asarray(q, np.float64))
+    G, D = q.shape
+    T = k_hat.shape[0]
+    if T == 0:
+        return np.zeros((G, v_hat.shape[1] if v_hat.ndim == 2 else D)), np.full(G, -np.inf)
+    scores = (q @ np.asarray(k_hat, np.float64).T) / np.sqrt(D)        # [G, T]
+    m = scores.max(axis=1, keepdims=True)
+    e = np.exp(scores - m)
+    l = e.sum(axis=1, keepdims=True)
+    a = e / l
+    o = a @ np.asarray(v_hat, np.float64)
+    lse = m[:, 0] + np.log(l[:, 0])
+    return o, lse
+
+
+def attention_weights(q: np.ndarray, k_hat: np.ndarray) -> np.ndarray:
+    """a = softmax(q K^T / sqrt(d)) ([P1] "Key error acts before the softmax")."""
+    q = np.atleast_2d(np.asarray(q, np.float64))
+    scores = (q @ np.asarray(k_hat, np.float64).T) / np.sqrt(q.shape[1])
+    e = np.exp(scores - scores.max(axis=1, keepdims=True))
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def lse_merge(parts):
+    """Combine attention over disjoint token subsets given (o_p, lse_p) each.
+
+    A softmax over the union equals the lse-weighted mix of the per-subset
+    softmaxes: o = sum_p exp(lse_p - lse) o_p with lse = ln sum_p exp(lse_p).
+    Used only to pin that splitting the sequence does not change the result.
+    """
+    lses = np.stack([p[1] for p in parts])            # [P, G]
+    M = lses.max(axis=0)
+    w = np.exp(lses - M)
+    tot = w.sum(axis=0)
+    o = sum(w[i][:, None] * parts[i][0] for i in range(len(parts))) / tot[:, None]
+    return o, M + np.log(tot)
+
+
+# ---------------------------------------------------------------- one cached sequence
+def window_split(length: int, window: int) -> int:
+    """Number of leading positions that are quantized when the last ``window``
+    positions stay in bf16 ([P1] "Cache growth changes the serving trade":
+    recent tokens in higher precision, older ones quantized)."""
+    if window <= 0:
+        return length
+    return max(length - window, 0)
+
+
+def quantize_sequence(k, v, k_bits: int, v_bits: int, window: int = 0, c=None):
+    """Store one sequence: k, v float64 [L, H, D] (exact bf16 values).
+
+    Returns a dict with the quantized prefix (codes/scales for K and V) and the
+    bf16 window values (float64).  16-bit formats store the values unchanged.
+    """
+    L = k.shape[0]
+    Lq = window_split(L, window)
+    st = {"Lq": Lq, "k_bits": k_bits, "v_bits": v_bits, "c": c}
+    if k_bits == 16:
+        st["k_plain"] = k[:Lq]
+    else:
+        st["k_codes"], st["k_scale"] = quantize_keys(k[:Lq], k_bits, c)
+    if v_bits == 16:
+        st["v_plain"] = v[:Lq]
+    else:
+        st["v_codes"], st["v_scale"] = quantize(v[:Lq], v_bits)
+    st["k_window"] = k[Lq:]
+    st["v_window"] = v[Lq:]
+    return st
+
+
+def reconstruct_sequence(st, head: int):
+    """k_hat, v_hat [L, D] of one KV head: dequantized prefix then bf16 window."""
+    c = st["c"]
+    if st["k_bits"] == 16:
+        kq = st["k_plain"][:, head]
+    else:
+        kq = reconstruct_keys(st["k_codes"][:, head], st["k_scale"][:, head],
+                              None if c is None else c[head])
+    if st["v_bits"] == 16:
+        vq = st["v_plain"][:, head]
+    else:
+        vq = dequantize(st["v_codes"][:, head], st["v_scale"][:, head])
+    k_hat = np.concatenate([kq, st["k_window"][:, head]], axis=0)
+    v_hat = np.concatenate([vq, st["v_window"][:, head]], axis=0)
+    return k_hat, v_hat
+
+
+def decode_sequence(q_bits, st, kv_heads: int):
+    """One decode step of one sequence: q_bits [H_q, D] bf16 bits.
+
+    Query head h reads KV head h // (H_q / H_kv) (grouped-query sharing; the
+    pages' one-head formulas applied per head).  Returns (o [H_q, D], lse [H_q]).
+    """
+    q = bf16_to_f64(q_bits)
+    H_q, D = q.shape
+    G = H_q // kv_heads
+    o = np.zeros((H_q, D))
+    lse = np.zeros(H_q)
+    for h in range(kv_heads):
+        k_hat, v_hat = reconstruct_sequence(st, h)
+        o[h * G:(h + 1) * G], lse[h * G:(h + 1) * G] = attention(q[h * G:(h + 1) * G], k_hat, v_hat)
+    return o, lse
+
+
+# ---------------------------------------------------------------- byte accounting
+def kv_payload_bytes(layers: int, kv_heads: int, head_dim: int, tokens: int, bytes_per_elem: float) -> float:
+    """KV_bytes = 2 * L * H_kv * D * T * b ([P2] "Cache precision is separate from
+    weight precision"): the factor 2 is keys plus values; metadata excluded."""
+    return 2 * layers * kv_heads * head_dim * tokens * bytes_per_elem
+
+
+def metadata_fraction(head_dim: int, bits: int, metadata_bytes: int) -> float:
+    """Per-token metadata over the code bytes of one head vector ([P3] "Per-token
+    scales and where they can live")."""
+    return metadata_bytes / (head_dim * bits / 8)
+
+
+def cache_bytes_per_token_head(head_dim: int, k_bits: int, v_bits: int, scale_bytes: int = 4) -> int:
+    """Bytes read per cached token per KV head: codes plus one scale for each of
+    K and V (no scale for a 16-bit cache)."""
+    kb = head_dim * k_bits // 8 + (0 if k_bits == 16 else scale_bytes)
+    vb = head_dim * v_bits // 8 + (0 if v_bits == 16 else scale_bytes)
+    return kb + vb

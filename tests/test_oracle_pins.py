@@ -1,0 +1,437 @@
+"""Pins of the float64 oracle against what the pages and mathematics fix.
+
+None of these re-type the oracle's formulas: each checks it against exact
+rational arithmetic, a closed form, a printed number, an invariant, or a
+textbook library routine, chosen so that a dropped term, a wrong sign or index,
+a transposed operand or the wrong rounding rule fails at least one test.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvq_oracle as O
+from synth import f32_to_bf16_bits
+
+RNG = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------- exact helpers (test-side)
+def rne_int(r: Fraction) -> int:
+    """Round a rational to the nearest integer, ties to even (exact)."""
+    fl = math.floor(r)
+    rem = r - fl
+    if rem > Fraction(1, 2):
+        return fl + 1
+    if rem < Fraction(1, 2):
+        return fl
+    return fl if fl % 2 == 0 else fl + 1
+
+
+def rn_float32(r: Fraction) -> Fraction:
+    """Round a positive rational to the nearest binary32 value (ties to even),
+    including the subnormal range, exactly."""
+    assert r > 0
+    e = math.floor(math.log2(r.numerator) - math.log2(r.denominator))
+    while Fraction(2) ** e > r:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= r:
+        e += 1
+    e = max(e, -126)                     # subnormals share the minimum exponent
+    ulp = Fraction(2) ** (e - 23)
+    return rne_int(r / ulp) * ulp
+
+
+def exact_quantize(xs, bits):
+    """Exact rational restatement of the page definition (float32 stored scale)."""
+    qmax = {8: 127, 4: 7}[bits]
+    lo, hi = {8: (-127, 127), 4: (-8, 7)}[bits]
+    fr = [Fraction(float(x)) for x in xs]
+    amax = max(abs(f) for f in fr)
+    if amax == 0:
+        return [0] * len(fr), Fraction(1)
+    s = rn_float32(amax / qmax)
+    return [min(hi, max(lo, rne_int(f / s))) for f in fr], s
+
+
+def bf16_vec(n, scale=1.0, dist="normal"):
+    x = RNG.standard_normal(n).astype(np.float32) * np.float32(scale)
+    if dist == "t3":
+        x = RNG.standard_t(3, n).astype(np.float32)
+    return O.bf16_to_f64(f32_to_bf16_bits(x))
+
+
+# ---------------------------------------------------------------- quantizer pins
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantizer_matches_exact_rational_brute_force(bits):
+    for trial in range(300):
+        n = int(RNG.integers(1, 40))
+        dist = "t3" if trial % 3 == 0 else "normal"
+        x = bf16_vec(n, scale=float(2.0 ** RNG.integers(-20, 20)), dist=dist)
+        codes, s = O.quantize(x, bits)
+        ref_codes, ref_s = exact_quantize(x, bits)
+        assert Fraction(float(s)) == ref_s
+        assert list(map(int, codes)) == ref_codes
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantizer_exact_ties_round_to_even(bits):
+    qmax = O.QMAX[bits]
+    for k in range(-10, 10):
+        s = 2.0 ** k
+        # amax = qmax * s makes the stored scale exactly s; the rest sit on ties
+        halves = [n + 0.5 for n in range(-qmax, qmax)]
+        x = np.array([qmax * s] + [h * s for h in halves])
+        codes, sc = O.quantize(x, bits)
+        assert float(sc) == s
+        expect = [qmax] + [rne_int(Fraction(h)) for h in halves]
+        assert list(map(int, codes)) == expect
+        # ties to even: never an odd code on a tie
+        assert all(int(c) % 2 == 0 for c in codes[1:])
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantizer_near_ties(bits):
+    qmax = O.QMAX[bits]
+    s = 2.0 ** -3
+    for n in range(0, qmax):
+        tie = (n + 0.5) * s
+        up = np.nextafter(np.float32(tie), np.float32(np.inf)).astype(np.float64)
+        dn = np.nextafter(np.float32(tie), np.float32(-np.inf)).astype(np.float64)
+        codes, sc = O.quantize(np.array([qmax * s, up, dn, -up, -dn]), bits)
+        assert list(map(int, codes)) == [qmax, n + 1, n, -(n + 1), -n]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantizer_invariants(bits):
+    qmax = O.QMAX[bits]
+    x = O.bf16_to_f64(f32_to_bf16_bits(RNG.standard_normal((500, 128)).astype(np.float32)))
+    codes, s = O.quantize(x, bits)
+    err = np.abs(x - codes * s.astype(np.float64)[:, None])     # code*s exact in float64
+    assert np.all(err <= s.astype(np.float64)[:, None] / 2)
+    assert np.all(np.abs(codes).max(axis=1) == qmax)           # amax element hits qmax
+    assert codes.min() >= -qmax and codes.max() <= qmax
+
+
+def test_quantizer_zero_vector():
+    for bits in (8, 4):
+        codes, s = O.quantize(np.zeros((3, 128)), bits)
+        assert np.all(codes == 0) and np.all(s == np.float32(1.0))
+
+
+def test_quantizer_golden_worked_examples(golden_dir):
+    with open(os.path.join(golden_dir, "quantize_worked.txt")) as f:
+        rows = [l for l in f if l.strip() and not l.startswith("#")]
+    assert len(rows) >= 4
+    for row in rows:
+        bits, scale, vals, codes = [p.strip() for p in row.split("|")]
+        x = np.array([float(v) for v in vals.split(",")])
+        c, s = O.quantize(x, int(bits))
+        assert float(s) == float(scale)
+        assert list(map(int, c)) == [int(v) for v in codes.split(",")]
+
+
+def _page_listing_restated(vec, qmax):
+    """The page listing's semantics restated: float64 scale, Python round."""
+    amax = max(abs(float(v)) for v in vec)
+    if amax == 0.0:
+        return [0] * len(vec), 1.0
+    scale = amax / qmax
+    return [max(-qmax, min(qmax, round(float(v) / scale))) for v in vec], scale
+
+
+def test_quantizer_agrees_with_page_listing_except_near_ties():
+    """Codes from the float32 stored scale agree with the page's float64-scale
+    listing except where x/s is within a few float32 ulps of a half-integer."""
+    n_checked = 0
+    for _ in range(200):
+        x = bf16_vec(128)
+        codes, s = O.quantize(x, 8)
+        ref, scale64 = _page_listing_restated(x, 127)
+        assert abs(float(s) - scale64) <= scale64 * 2.0 ** -24
+        for xi, c, r in zip(x, codes, ref):
+            frac = abs(xi / scale64) % 1.0
+            if abs(frac - 0.5) < 1e-5:
+                continue
+            assert int(c) == r
+            n_checked += 1
+    assert n_checked > 20000
+
+
+def test_quantizer_subnormal_inputs():
+    # bf16 subnormals (below 2^-126) and the smallest bf16 subnormal 2^-133
+    for bits in (8, 4):
+        tiny = np.array([2.0 ** -133, -3 * 2.0 ** -133, 5 * 2.0 ** -130, 2.0 ** -127, 0.0])
+        codes, s = O.quantize(tiny, bits)
+        ref_codes, ref_s = exact_quantize(tiny, bits)
+        assert Fraction(float(s)) == ref_s and float(s) > 0
+        assert list(map(int, codes)) == ref_codes
+        err = np.abs(tiny - codes * float(s))
+        assert np.all(err <= float(s) / 2)
+
+
+def test_channel_factor_division_is_float32_rounded():
+    k = bf16_vec(64)
+    c = np.abs(bf16_vec(64)) + 0.5
+    kp = O.divide_by_channel_factor(k, c.astype(np.float32))
+    for a, b, r in zip(k, c.astype(np.float32), kp):
+        assert Fraction(float(r)) == (rn_float32(abs(Fraction(float(a)) / Fraction(float(b)))) * (1 if a >= 0 else -1) if a != 0 else 0)
+
+
+# ---------------------------------------------------------------- fold identities
+def test_scale_fold_after_integer_dot_is_exact_in_rationals():
+    """(q . k_int) * s == q . (k_int * s) exactly; the float64 oracle's
+    dequantize-then-dot agrees with the folded order to a few ulps."""
+    for _ in range(50):
+        q = bf16_vec(128)
+        k = bf16_vec(128)
+        codes, s = O.quantize(k, 8)
+        qf = [Fraction(float(v)) for v in q]
+        sf = Fraction(float(s))
+        folded = sum(a * int(c) for a, c in zip(qf, codes)) * sf
+        unfolded = sum(a * (int(c) * sf) for a, c in zip(qf, codes))
+        assert folded == unfolded
+        oracle_dot = float(q @ O.dequantize(codes, s))
+        assert abs(oracle_dot - float(folded)) <= 1e-13 * max(1.0, abs(float(folded)))
+
+
+def test_channel_factor_moved_onto_query_is_exact_in_rationals():
+    """(q (.) c) . k' == q . (c (.) k') exactly, and the oracle reconstruction
+    c * code * s is what a folded-query dot would see."""
+    q = bf16_vec(128)
+    k = bf16_vec(128)
+    c = (np.abs(bf16_vec(128)) + 0.25).astype(np.float32).astype(np.float64)
+    codes, s = O.quantize_keys(k, 4, c)
+    kp = O.dequantize(codes, s)
+    lhs = sum(Fraction(float(a)) * Fraction(float(cc)) * Fraction(float(b)) for a, cc, b in zip(q, c, kp))
+    rhs = sum(Fraction(float(a)) * (Fraction(float(cc)) * Fraction(float(b))) for a, cc, b in zip(q, c, kp))
+    assert lhs == rhs
+    kh = O.reconstruct_keys(codes, s, c)
+    assert abs(float(q @ kh) - float(rhs)) <= 1e-12 * max(1.0, abs(float(rhs)))
+
+
+# ---------------------------------------------------------------- attention pins
+def test_attention_matches_torch_sdpa_float64():
+    for T in (1, 2, 7, 64, 300):
+        for G in (1, 4, 8):
+            q = bf16_vec(G * 128).reshape(G, 128)
+            k = bf16_vec(T * 128).reshape(T, 128)
+            v = bf16_vec(T * 128).reshape(T, 128)
+            o, lse = O.attention(q, k, v)
+            tq = torch.from_numpy(q)[None, :, None, :]          # [G, 1 query, D] as batch of heads
+            tk = torch.from_numpy(k)[None, None].expand(1, G, T, 128)
+            tv = torch.from_numpy(v)[None, None].expand(1, G, T, 128)
+            ref = torch.nn.functional.scaled_dot_product_attention(tq.transpose(0, 1).reshape(1, G, 1, 128), tk, tv)
+            np.testing.assert_allclose(o, ref[0, :, 0].numpy(), rtol=0, atol=1e-13)
+            ref_lse = torch.logsumexp(torch.from_numpy(q @ k.T / math.sqrt(128)), dim=1).numpy()
+            np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_attention_weights_sum_to_one():
+    q = bf16_vec(4 * 128).reshape(4, 128)
+    k = bf16_vec(1000 * 128).reshape(1000, 128) * 3
+    a = O.attention_weights(q, k)
+    assert np.all(np.abs(a.sum(axis=1) - 1.0) <= 1e-15 * 1000)
+    assert np.all(a >= 0)
+
+
+def test_attention_single_token_returns_that_value():
+    q = bf16_vec(3 * 128).reshape(3, 128)
+    k = bf16_vec(128).reshape(1, 128)
+    v = bf16_vec(128).reshape(1, 128)
+    o, lse = O.attention(q, k, v)
+    assert np.array_equal(o, np.repeat(v, 3, axis=0))
+    np.testing.assert_allclose(lse, (q @ k[0]) / math.sqrt(128), rtol=0, atol=1e-14)
+
+
+def test_attention_identical_keys_or_zero_query_gives_mean():
+    T = 37
+    v = bf16_vec(T * 128).reshape(T, 128)
+    k_same = np.repeat(bf16_vec(128).reshape(1, 128), T, axis=0)
+    q = bf16_vec(2 * 128).reshape(2, 128)
+    o, lse = O.attention(q, k_same, v)
+    np.testing.assert_allclose(o, np.repeat(v.mean(axis=0, keepdims=True), 2, axis=0), rtol=0, atol=1e-14)
+    o0, lse0 = O.attention(np.zeros((1, 128)), bf16_vec(T * 128).reshape(T, 128), v)
+    np.testing.assert_allclose(o0[0], v.mean(axis=0), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse0, [math.log(T)], rtol=0, atol=1e-14)
+
+
+def test_attention_empty_sequence_convention():
+    o, lse = O.attention(np.ones((2, 128)), np.zeros((0, 128)), np.zeros((0, 128)))
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+def test_attention_two_token_closed_form():
+    """T = 2: a_0 = 1 / (1 + exp(s_1 - s_0)) (logistic form of softmax)."""
+    q = bf16_vec(128).reshape(1, 128)
+    k = bf16_vec(256).reshape(2, 128)
+    v = bf16_vec(256).reshape(2, 128)
+    s0, s1 = (k @ q[0]) / math.sqrt(128)
+    a0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    o, _ = O.attention(q, k, v)
+    np.testing.assert_allclose(o[0], a0 * v[0] + (1 - a0) * v[1], rtol=0, atol=1e-14)
+
+
+def test_attention_high_precision_brute_force():
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 50
+    q = bf16_vec(2 * 8).reshape(2, 8)
+    k = bf16_vec(5 * 8).reshape(5, 8)
+    v = bf16_vec(5 * 8).reshape(5, 8)
+    o, lse = O.attention(q, k, v)
+    for g in range(2):
+        sc = [mp.fsum(mp.mpf(q[g, j]) * mp.mpf(k[i, j]) for j in range(8)) / mp.sqrt(8) for i in range(5)]
+        den = mp.fsum(mp.exp(s) for s in sc)
+        for d in range(8):
+            num = mp.fsum(mp.exp(sc[i]) * mp.mpf(v[i, d]) for i in range(5))
+            assert abs(float(num / den) - o[g, d]) <= 1e-14
+        assert abs(float(mp.log(den)) - lse[g]) <= 1e-14
+
+
+def test_split_merge_equals_single_pass():
+    q = bf16_vec(4 * 128).reshape(4, 128)
+    T = 517
+    k = bf16_vec(T * 128).reshape(T, 128) * 2
+    v = bf16_vec(T * 128).reshape(T, 128)
+    o, lse = O.attention(q, k, v)
+    for cuts in ([100, 300], [1, 2, 3, 516], [256]):
+        edges = [0] + cuts + [T]
+        parts = [O.attention(q, k[a:b], v[a:b]) for a, b in zip(edges[:-1], edges[1:])]
+        om, lm = O.lse_merge(parts)
+        np.testing.assert_allclose(om, o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lm, lse, rtol=0, atol=1e-12)
+
+
+def test_perturbation_identities():
+    """s' - s = q E_K^T / sqrt(d) and, for fixed a, o' - o = a E_V."""
+    d = 128
+    q = bf16_vec(d).reshape(1, d)
+    k = bf16_vec(50 * d).reshape(50, d)
+    v = bf16_vec(50 * d).reshape(50, d)
+    codes, s = O.quantize(k, 4)
+    e_k = O.dequantize(codes, s) - k
+    s_exact = (q @ k.T) / math.sqrt(d)
+    s_pert = (q @ (k + e_k).T) / math.sqrt(d)
+    np.testing.assert_allclose(s_pert - s_exact, (q @ e_k.T) / math.sqrt(d), rtol=0, atol=1e-13)
+    a = O.attention_weights(q, k)
+    vc, vs = O.quantize(v, 4)
+    e_v = O.dequantize(vc, vs) - v
+    np.testing.assert_allclose(a @ (v + e_v) - a @ v, a @ e_v, rtol=0, atol=1e-14)
+    # with exact keys the oracle output moves by exactly a E_V
+    o_exact, _ = O.attention(q, k, v)
+    o_q, _ = O.attention(q, k, v + e_v)
+    np.testing.assert_allclose(o_q - o_exact, a @ e_v, rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- window and sequence assembly
+def test_window_covering_whole_sequence_reduces_to_plain_attention():
+    L, H, G = 90, 2, 4
+    k = bf16_vec(L * H * 128).reshape(L, H, 128)
+    v = bf16_vec(L * H * 128).reshape(L, H, 128)
+    qb = f32_to_bf16_bits(RNG.standard_normal((H * G, 128)).astype(np.float32))
+    st = O.quantize_sequence(k, v, 8, 8, window=128)
+    assert st["Lq"] == 0
+    o, lse = O.decode_sequence(qb, st, H)
+    q = O.bf16_to_f64(qb)
+    for h in range(H):
+        tk = torch.from_numpy(k[:, h])[None, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[h * G:(h + 1) * G])[None, :, None], tk.expand(1, G, L, 128),
+            torch.from_numpy(v[:, h])[None, None].expand(1, G, L, 128))
+        np.testing.assert_allclose(o[h * G:(h + 1) * G], ref[0, :, 0].numpy(), rtol=0, atol=1e-13)
+
+
+def test_window_split_positions():
+    assert O.window_split(4096, 128) == 3968
+    assert O.window_split(100, 128) == 0
+    assert O.window_split(128, 128) == 0
+    assert O.window_split(129, 128) == 1
+    assert O.window_split(77, 0) == 77
+
+
+def test_sequence_reconstruction_orders_quantized_then_window():
+    L, H = 40, 1
+    k = bf16_vec(L * H * 128).reshape(L, H, 128)
+    v = bf16_vec(L * H * 128).reshape(L, H, 128)
+    st = O.quantize_sequence(k, v, 8, 4, window=16)
+    kh, vh = O.reconstruct_sequence(st, 0)
+    assert kh.shape == (L, 128)
+    assert np.array_equal(kh[24:], k[24:, 0]) and np.array_equal(vh[24:], v[24:, 0])
+    assert np.all(np.abs(kh[:24] - k[:24, 0]) <= np.abs(k[:24, 0]).max(axis=1, keepdims=True) / 127 / 2 * 1.0000001)
+
+
+def test_grouped_query_heads_read_their_kv_head():
+    L, H, G = 20, 3, 2
+    k = bf16_vec(L * H * 128).reshape(L, H, 128)
+    v = bf16_vec(L * H * 128).reshape(L, H, 128)
+    qb = f32_to_bf16_bits(RNG.standard_normal((H * G, 128)).astype(np.float32))
+    st = O.quantize_sequence(k, v, 16, 16)
+    o, _ = O.decode_sequence(qb, st, H)
+    q = O.bf16_to_f64(qb)
+    for hq in range(H * G):
+        ref, _ = O.attention(q[hq:hq + 1], k[:, hq // G], v[:, hq // G])
+        np.testing.assert_allclose(o[hq], ref[0], rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- byte accounting
+def test_metadata_fractions_match_printed_values(golden_dir):
+    with open(os.path.join(golden_dir, "metadata_fractions.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    assert len(rows) == 4
+    for d, bits, meta, pct in rows:
+        frac = O.metadata_fraction(int(d), int(bits), int(meta))
+        assert round(100 * frac) == int(pct) or math.floor(100 * frac) == int(pct)
+    assert O.metadata_fraction(128, 8, 4) == 0.03125
+    assert O.metadata_fraction(128, 4, 4) == 0.0625
+    assert O.metadata_fraction(128, 2, 4) == 0.125
+
+
+def test_kv_payload_formula(golden_dir):
+    with open(os.path.join(golden_dir, "kv_payload.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for L, H, D, T, b, expect in rows:
+        assert O.kv_payload_bytes(int(L), int(H), int(D), int(T), float(b)) == float(expect)
+    assert O.kv_payload_bytes(1, 8, 128, 4096, 1) * 2 == O.kv_payload_bytes(1, 8, 128, 4096, 2)
+
+
+def test_cache_bytes_per_token_include_scales():
+    assert O.cache_bytes_per_token_head(128, 8, 8) == 264
+    assert O.cache_bytes_per_token_head(128, 4, 4) == 136
+    assert O.cache_bytes_per_token_head(128, 4, 8) == 200
+    assert O.cache_bytes_per_token_head(128, 16, 16) == 512
+    # payload part equals the page formula per token per head (b = bits / 8)
+    for kb, vb in ((8, 8), (4, 4), (16, 16)):
+        pay = O.kv_payload_bytes(1, 1, 128, 1, kb / 8) if kb == vb else None
+        extra = 0 if kb == 16 else 8
+        assert O.cache_bytes_per_token_head(128, kb, vb) == pay + extra
+
+
+# ---------------------------------------------------------------- planted mistakes are caught
+def test_pins_catch_a_planted_rounding_mistake(monkeypatch):
+    """Half-away-from-zero instead of half-to-even must fail the tie pin."""
+    real = np.rint
+    monkeypatch.setattr(O.np, "rint", lambda a: np.trunc(a + np.copysign(0.5, a)))
+    x = np.array([127 * 0.25, 0.625])          # 0.625 / 0.25 = 2.5 -> 2 (even), not 3
+    codes, _ = O.quantize(x, 8)
+    assert int(codes[1]) == 3                  # the planted mistake shows ...
+    monkeypatch.setattr(O.np, "rint", real)
+    codes, _ = O.quantize(x, 8)
+    assert int(codes[1]) == 2 == rne_int(Fraction(5, 2))   # ... and the pin distinguishes it
+
+
+def test_pins_catch_a_planted_missing_sqrt_d(monkeypatch):
+    q = bf16_vec(2 * 128).reshape(2, 128)
+    k = bf16_vec(9 * 128).reshape(9, 128)
+    v = bf16_vec(9 * 128).reshape(9, 128)
+    monkeypatch.setattr(O.np, "sqrt", lambda x: 1.0)
+    o_bad, _ = O.attention(q, k, v)
+    monkeypatch.undo()
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None, :, None], torch.from_numpy(k)[None, None].expand(1, 2, 9, 128),
+        torch.from_numpy(v)[None, None].expand(1, 2, 9, 128))[0, :, 0].numpy()
+    assert np.max(np.abs(o_bad - ref)) > 1e-3
+    o_good, _ = O.attention(q, k, v)
+    assert np.max(np.abs(o_good - ref)) < 1e-13
