@@ -1,0 +1,448 @@
+"""Benchmark of the quantized-KV decode hot path on one or more GPUs.
+
+One step = one decode step of the workload (for the paged serving workload:
+kvq_append of one new token per sequence, then kvq_decode) over a cache that
+is already resident in HBM.  The timed region holds exactly --steps steps,
+bracketed by a barrier and a device synchronize; steps rotate over enough
+identical cache replicas that the bytes cycled exceed 4x the L2 size (or the
+cache alone exceeds L2), so every step reads its cache from HBM.
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle
+(the reference arm of this build) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "gqa_int8_window128_b8_t4096"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("kvq_decode.cu", "kvq_device.cuh"):
+        h.update(open(os.path.join(ROOT, "quantized_kv_cache_07_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, valid only for the
+    decode sources it was captured from (matched by source hash)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = decode_kernel_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload and parts[1] == kernel \
+                and parts[2] == want:
+            return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cache_bytes_per_step(inp) -> int:
+    """Algorithmic bytes one decode step reads: codes + scales of every cached
+    quantized token and the bf16 window tokens, per KV head."""
+    w = inp.workload
+    L = inp.decode_lengths.astype(int)
+    D = w.head_dim
+    per_q = D * w.k_bits // 8 + D * w.v_bits // 8 + (0 if w.k_bits == 16 else 8)
+    if w.window:
+        lq = [max(int(l) - w.window, 0) for l in L]
+        lw = [int(l) - x for l, x in zip(L, lq)]
+        return w.kv_heads * (per_q * sum(lq) + 4 * D * sum(lw))
+    return w.kv_heads * per_q * int(sum(L))
+
+
+# ------------------------------------------------------------------ reference arm / CPU baseline
+CPU_SAMPLE_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from synth import WORKLOADS, make_inputs
+from oracle import kvq_oracle as O
+w = WORKLOADS[{name!r}]
+if {bf16}:
+    w = w.with_(k_bits=16, v_bits=16, window=0, channel_factor=False)
+inp = make_inputs(w)
+G = w.group
+budget = {budget}
+rng = np.random.default_rng(5)
+units = [(int(b), int(h)) for b in rng.permutation(w.batch) for h in range(w.kv_heads)]
+per_tok = 128 * w.k_bits // 8 + 128 * w.v_bits // 8 + (0 if w.k_bits == 16 else 8)
+tot_t, tot_b, n, i = 0.0, 0, 0, 0
+while tot_t < budget or n == 0:
+    b, h = units[i % len(units)]; i += 1
+    a, e = inp.seq_offsets[b], inp.seq_offsets[b + 1]
+    k = O.bf16_to_f64(inp.k[a:e, h:h+1]); v = O.bf16_to_f64(inp.v[a:e, h:h+1])
+    if w.append_one:
+        k = np.concatenate([k, O.bf16_to_f64(inp.k_new[b:b+1, h:h+1])])
+        v = np.concatenate([v, O.bf16_to_f64(inp.v_new[b:b+1, h:h+1])])
+    c = None if inp.channel_factor is None else inp.channel_factor[h:h+1].astype(np.float64)
+    st = O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c)   # the stored cache: untimed
+    t1 = time.perf_counter()
+    kh, vh = O.reconstruct_sequence(st, 0)
+    O.attention(O.bf16_to_f64(inp.q[b, h*G:(h+1)*G]), kh, vh)
+    tot_t += time.perf_counter() - t1
+    L = k.shape[0]; Lq = st["Lq"]
+    tot_b += per_tok * Lq + 512 * (L - Lq); n += 1
+print(json.dumps({{"seconds": tot_t, "bytes": tot_b, "units": n}}))
+"""
+
+
+def run_cpu_sample(name: str, budget_s: float, steps: int = 1, bf16: bool = False):
+    """Time the oracle's decode (dequantize + attention, float64) on a bounded
+    sample of the workload's units, in a fresh single-threaded process."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = CPU_SAMPLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, bf16=bf16)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    if res.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + res.stderr[-2000:])
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    return d
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the same-design bf16-cache comparison run")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--stream-ctas", type=int, default=0)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from quantized_kv_cache_07_gb300 import _lib
+    from quantized_kv_cache_07_gb300.build import build
+    from quantized_kv_cache_07_gb300.cache import DecodeWorkspace, cache_for_inputs, fill_from_inputs
+    from synth import WORKLOADS, make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    _lib.load()
+
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20
+
+    def build_replicas(inp_, k_bits=None):
+        base = cache_for_inputs(inp_, dev)
+        table, lens = fill_from_inputs(base, inp_, dev)
+        nbytes = base.allocated_bytes()
+        reps = max(1, math.ceil(4 * l2 / max(cache_bytes_per_step(inp_), 1)))
+        reps = min(reps, 64)
+        replicas = [base]
+        for _ in range(reps - 1):
+            c = cache_for_inputs(inp_, dev)
+            for name in ("k_codes", "v_codes", "k_scales", "v_scales", "k_window", "v_window"):
+                src, dst = getattr(base, name), getattr(c, name)
+                if src is not None:
+                    dst.copy_(src)
+            replicas.append(c)
+        torch.cuda.synchronize()
+        return replicas, table, lens, nbytes
+
+    def run_arm(inp_, label):
+        wl = inp_.workload
+        replicas, table, lens, alloc = build_replicas(inp_)
+        B, Hq = wl.batch, wl.q_heads
+        q = torch.from_numpy(inp_.q.view(np.int16)).to(dev).view(torch.bfloat16)
+        out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        ws = DecodeWorkspace(replicas[0], B, Hq, args.stream_ctas)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        dec_lens = torch.from_numpy(inp_.decode_lengths.astype(np.int32)).to(dev)
+        if wl.append_one:
+            kt = torch.from_numpy(inp_.k_new.view(np.int16)).to(dev).view(torch.bfloat16)
+            vt = torch.from_numpy(inp_.v_new.view(np.int16)).to(dev).view(torch.bfloat16)
+            si = torch.arange(B, dtype=torch.int32, device=dev)
+            po = torch.from_numpy(inp_.lengths.astype(np.int32)).to(dev)
+        stream = torch.cuda.current_stream(dev)
+        launches_per_step = 2 if wl.append_one else 1
+
+        def step(k, ev0=None, ev1=None, q_=None, kt_=None, vt_=None):
+            c = replicas[k % len(replicas)]
+            if wl.append_one:
+                _lib.kvq_append(c.desc, kt if kt_ is None else kt_, vt if vt_ is None else vt_, si, po,
+                                _lib.APPEND_QUANT, table, B, inp_.max_blocks, err_word=err)
+            if ev0 is not None:
+                ev0.record(stream)
+            _lib.kvq_decode(c.desc, q if q_ is None else q_, B, Hq, dec_lens, table, inp_.max_blocks, out,
+                            lse=lse, workspace=ws.buf, workspace_bytes=ws.nbytes,
+                            stream_ctas=args.stream_ctas, err_word=err)
+            if ev1 is not None:
+                ev1.record(stream)
+
+        for k in range(max(args.warmup, 3)):
+            step(k)
+        torch.cuda.synchronize()
+        # soak (untimed) so the clock sampler sees the load for >= ~1 s
+        t_est = time.perf_counter()
+        for k in range(20):
+            step(k)
+        torch.cuda.synchronize()
+        per = max((time.perf_counter() - t_est) / 20, 1e-6)
+        soak = int(min(max(1.0 / per, 0), 200000))
+        K = args.steps
+        dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            for k in range(soak):
+                step(k)
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize()
+            e_start.record(stream)
+            for k in range(K):
+                step(k, *dec_ev[k])
+            e_end.record(stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                dist.barrier()
+        ms_total = e_start.elapsed_time(e_end)
+        dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+        # e2e through the public API: pinned host q (and new tokens) in, output out, every step
+        q_host = torch.from_numpy(inp_.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+        out_host = torch.empty((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
+        q_dev = torch.empty_like(q)
+        h2d = q_host.numel() * 2
+        extra = None
+        if wl.append_one:
+            kh = torch.from_numpy(inp_.k_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+            vh = torch.from_numpy(inp_.v_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+            kd, vd = torch.empty_like(kt), torch.empty_like(vt)
+            extra = (kh, vh, kd, vd)
+            h2d += 2 * kh.numel() * 2
+        d2h = out_host.numel() * 2
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for k in range(K):
+            q_dev.copy_(q_host, non_blocking=True)
+            if extra:
+                extra[2].copy_(extra[0], non_blocking=True)
+                extra[3].copy_(extra[1], non_blocking=True)
+                step(k, q_=q_dev, kt_=extra[2], vt_=extra[3])
+            else:
+                step(k, q_=q_dev)
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+        e2e_s = (time.perf_counter() - t0) / K
+        errbits = int(err.item())
+        return dict(ms_step=ms_total / K, dec_ms=statistics.mean(dec_ms), dec_ms_med=statistics.median(dec_ms),
+                    e2e_s=e2e_s, h2d=h2d, d2h=d2h, bytes=cache_bytes_per_step(inp_), replicas=len(replicas),
+                    alloc=alloc, clocks=clk.summary(), launches=launches_per_step * K, err=errbits)
+
+    res = run_arm(inp, "quant")
+    peak, peak_kind = measured_peaks()
+
+    def allmax(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    ms_step = allmax(res["ms_step"])
+    e2e_s = allmax(res["e2e_s"])
+    bytes_step = res["bytes"]
+    value = world * bytes_step / (ms_step / 1e3) / 1e9
+    achieved = bytes_step / (res["dec_ms"] / 1e3) / 1e9
+
+    bf16 = None
+    if not args.no_bf16 and w.k_bits != 16:
+        wb = w.with_(k_bits=16, v_bits=16, window=0, channel_factor=False, name=w.name + "_bf16")
+        inb = make_inputs(wb)
+        rb = run_arm(inb, "bf16")
+        bf16 = {"workload": wb.name, "ms_per_step": rb["ms_step"], "decode_ms": rb["dec_ms"],
+                "bytes_per_step": rb["bytes"], "effective_gbs": rb["bytes"] / (rb["dec_ms"] / 1e3) / 1e9,
+                "frac_of_peak": rb["bytes"] / (rb["dec_ms"] / 1e3) / 1e9 / peak,
+                "speedup_quant_vs_bf16": rb["dec_ms"] / res["dec_ms"], "err_word": rb["err"]}
+        del inb
+
+    line = {
+        "metric": "quantized-KV decode attention: effective HBM GB/s (% of peak), steps/s",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_step, 6),
+        "steps_per_s": round(world * 1e3 / ms_step, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "s8/s4 codes, f16 mma, f32 accumulate" if w.k_bits != 16 else "bf16 mma, f32 accumulate",
+        "data": "synthetic (seeded), cache resident in HBM",
+        "config": {"workload": w.name, "description": w.description, "batch": w.batch, "q_heads": w.q_heads,
+                   "kv_heads": w.kv_heads, "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits,
+                   "window": w.window, "paged": w.paged, "append_one": w.append_one,
+                   "cache_bytes_per_step": bytes_step, "allocated_cache_bytes": res["alloc"],
+                   "l2": f"steps rotate over {res['replicas']} cache replicas "
+                         f"({res['replicas'] * bytes_step / 2**20:.0f} MiB >= 4x L2 or cache > L2)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(w.name, "decode"), "kernel": "kvq decode_kernel",
+                     "decode_ms_mean": round(res["dec_ms"], 6), "decode_ms_median": round(res["dec_ms_med"], 6)},
+        "e2e": {"value": round(world * bytes_step / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "ms_per_step": round(e2e_s * 1e3, 6)},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "bf16_same_design": bf16,
+        "device_err_word": res["err"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            d = run_cpu_sample(w.name, args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(d["bytes"] / d["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                    "kind": "oracle",
+                                    "sample": f"{d['units']} (sequence, kv_head) units of {w.name}, float64 "
+                                              f"dequantize + attention, single thread, "
+                                              f"{d['seconds']:.1f} s of CPU work"}
+        except Exception as e:  # reported, not fatal
+            line["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"failed: {e}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def reference_arm(args, rank, world):
+    """The float64 CPU oracle as the reference arm: rank 0 only."""
+    if rank != 0:
+        return
+    from synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    K = args.steps
+    # bounded: about 60 s of oracle work for the whole timed run, split over K steps
+    per_step_budget = min(60.0 / max(K, 1), 5.0)
+    d = run_cpu_sample(w.name, per_step_budget * K, steps=K)
+    gbs = d["bytes"] / d["seconds"] / 1e9
+    ms = d["seconds"] / K * 1e3
+    line = {
+        "impl": "reference",
+        "metric": "quantized-KV decode attention: effective HBM GB/s (% of peak), steps/s",
+        "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "description": w.description,
+                   "sample": "each step: a bounded sample of (sequence, kv_head) units"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{d['units']} units of {w.name} over {K} steps, {d['seconds']:.1f} s"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * kvq.h -- C ABI of the quantized-KV decode library (libkvq.so), sm_103a.
+ *
+ * Two operations make up the decode hot path:
+ *   kvq_append  quantize-on-write of new key/value vectors into a paged cache
+ *   kvq_decode  fused dequantize-on-load split attention for one decode step
+ * plus kvq_dequant (reads the stored cache back for tests) and a few helpers.
+ *
+ * Sources (page title, section):
+ *   [P1] "KV Cache Quantization Perturbs Attention Through Stored Keys and Values"
+ *   [P2] "KV Cache Quantization Reduces Cache Bytes with Separate Accuracy and Kernel Costs"
+ *   [P3] "KV Cache Quantization and Per-Token Scale Placement"
+ *
+ * Conventions shared by every entry point
+ *   - All buffers are caller-owned.  "device" pointers must be CUDA device
+ *     memory of the current device; "host" pointers are plain host memory.
+ *   - Calls are stream-ordered and asynchronous on `stream` (a cudaStream_t
+ *     passed as void*; NULL = legacy default stream).  The library never
+ *     allocates, frees or synchronizes.
+ *   - Arguments are validated on the host; a bad argument returns a status and
+ *     launches nothing.  Problems that only the device can see (a block-table
+ *     entry out of range, a length beyond the table's capacity, a pipeline wait
+ *     that gave up) set bits in the caller's device word *err_word (nullable)
+ *     with atomicOr and skip the offending item: kernels never trap.
+ *   - Head dimension D = 128 and block size 16 tokens are fixed.
+ *
+ * Cache layout (device memory, all pools 16-byte aligned)
+ *   Codes pool  : [num_blocks][num_kv_heads][block_bytes] with
+ *                 block_bytes = 16 * 128 * bits / 8 (int4 1024, int8 2048, bf16 4096).
+ *                 Inside a block the bytes are ordered so that each lane of a
+ *                 warp reads its tensor-core operand with one 16-byte load per
+ *                 512-byte chunk ("fragment-native" order).  Let lane = 4*g + t.
+ *     Keys, element (token i in block, dim d):
+ *         g = i & 7, hi = i >> 3, t = d >> 5, e = d & 31
+ *         int8 : chunk = 2*hi + (e >> 4), byte = e & 15
+ *         int4 : chunk = hi, word = e >> 3, nibble = ((e & 7) >> 1) + 4*(e & 1)
+ *         bf16 : chunk = 4*hi + (e >> 3), element = e & 7 (2 bytes each)
+ *     Values, element (token i, dim d):
+ *         mt = d >> 4, r = d & 15, g = r & 7, hi = r >> 3,
+ *         t = (i & 7) >> 1, j = 2*(i & 1) + (i >> 3)
+ *         int8 : chunk = mt >> 1, word = 2*(mt & 1) + hi, byte j of the word
+ *         int4 : chunk = mt >> 2, word = mt & 3, nibble = 2*hi + (j >> 1) + 4*(j & 1)
+ *         bf16 : chunk = mt, word = 2*hi + (j >> 1), element j & 1 of the word
+ *     Byte offset = chunk*512 + lane*16 + word*4 + (byte or nibble/2 or 2*element);
+ *     for int8 keys "byte" is the offset inside the lane's 16 bytes.  Nibble n
+ *     of a little-endian 32-bit word occupies bits 4n..4n+3.  Codes are two's
+ *     complement: int8 in [-127,127], int4 in [-8,7] (-8 never produced).
+ *   Scale pool  : float [num_blocks][num_kv_heads][16], natural token order
+ *                 (absent for a bf16 cache).
+ *   Window ring : bf16 [window_batch][num_kv_heads][window][128], plain order;
+ *                 position p of sequence b lives in slot p % window.
+ *   Block table : int32 [batch][max_blocks_per_seq]; logical block j of
+ *                 sequence b is physical block block_table[b*max_blocks_per_seq+j].
+ *                 Position p of a sequence is token p % 16 of logical block p / 16.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,  /* null / negative / inconsistent argument            */
+  KVQ_ERR_UNSUPPORTED = 2,  /* valid but not implemented (D != 128, G > 8, ...)    */
+  KVQ_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned                      */
+  KVQ_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required            */
+  KVQ_ERR_CUDA = 5          /* a CUDA runtime call or launch failed                  */
+} kvq_status;
+
+/* Bits of the device error word. */
+#define KVQ_DEVERR_BLOCK_ID 1u  /* block-table entry outside [0, num_blocks)        */
+#define KVQ_DEVERR_SEQ_LEN 2u   /* length < 0 or beyond the block table's capacity  */
+#define KVQ_DEVERR_TIMEOUT 4u   /* a pipeline wait gave up (the CTA skipped work)   */
+#define KVQ_DEVERR_RANGE 8u     /* a value scale above 65504 (fp16 operand range)   */
+#define KVQ_DEVERR_POSITION 16u /* append: sequence index or position out of range  */
+
+/* kvq_append modes */
+#define KVQ_APPEND_QUANT 0 /* quantize the new vectors into the block store at pos      */
+#define KVQ_APPEND_RING 1  /* copy the new bf16 vectors into window slot pos % window   */
+#define KVQ_APPEND_STEP 2  /* decode step with a window: the token at pos - window (if  */
+                           /* pos >= window) leaves the ring and is quantized into the  */
+                           /* block store, then the new token enters the ring           */
+
+/* Description of one layer's cache.  Every pointer is caller-owned device memory. */
+typedef struct {
+  int32_t num_kv_heads;   /* H_kv >= 1                                              */
+  int32_t head_dim;       /* must be 128                                            */
+  int32_t block_size;     /* must be 16                                             */
+  int32_t num_blocks;     /* physical blocks in each pool                           */
+  int32_t k_bits;         /* 8 or 4 (quantized), or 16 together with v_bits = 16    */
+  int32_t v_bits;         /* 8 or 4, or 16                                          */
+  void* k_codes;          /* codes pool for keys (see layout above)                 */
+  void* v_codes;          /* codes pool for values                                  */
+  float* k_scales;        /* per-token key scales; NULL for a bf16 cache            */
+  float* v_scales;        /* per-token value scales; NULL for a bf16 cache          */
+  const float* k_channel_factor; /* [num_kv_heads][128] positive, or NULL           */
+  int32_t window;         /* recent-token bf16 window W (0 = none, 1..128)          */
+  int32_t window_batch;   /* first dimension of the ring buffers (sequences)        */
+  void* k_window;         /* bf16 [window_batch][H_kv][W][128] or NULL if W == 0    */
+  void* v_window;
+} kvq_cache_desc;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kvq_status_string(kvq_status status);
+
+/* Bytes of one 16-token block of one KV head for a code width (4, 8 or 16). */
+kvq_status kvq_block_bytes(int32_t bits, size_t* bytes);
+
+/*
+ * kvq_append -- quantize-on-write.
+ * [P3] "Per-token scales and where they can live": the scale is computed from
+ * the vector being written, at write time, and stored alongside it, one scale
+ * per token per head.  [P2] "Quantization needs a scale convention" and the
+ * listing in [P3] "The axis choice is a kernel decision": s = max|x| / qmax
+ * (stored as float32, RN), code = clamp(round_half_even(x / s)), all-zero
+ * vector -> codes 0 and s = 1.  qmax = 127 (int8) or 7 (int4).  With a
+ * per-channel key factor c, keys are first divided by c (float32, RN) and then
+ * quantized per token ([P3] "The axis choice is a kernel decision").  Codes are
+ * the correctly rounded quotient of the exact x / s.
+ *   k_new, v_new : device bf16 [n][num_kv_heads][128]
+ *   n            : number of new tokens (0 is a no-op)
+ *   seq_idx, pos : device int32 [n]; token r belongs to sequence seq_idx[r] at
+ *                  position pos[r].  Within one call the positions of one
+ *                  sequence must be distinct, and in KVQ_APPEND_STEP mode they
+ *                  must span fewer than `window` positions.
+ *   mode         : KVQ_APPEND_QUANT / RING / STEP (RING and STEP need window > 0)
+ *   block_table  : device int32 [batch][max_blocks_per_seq] (unused by RING)
+ *   err_word     : device uint32 or NULL (POSITION / BLOCK_ID bits)
+ */
+kvq_status kvq_append(const kvq_cache_desc* cache, const void* k_new, const void* v_new, int32_t n,
+                      const int32_t* seq_idx, const int32_t* pos, int32_t mode,
+                      const int32_t* block_table, int32_t batch, int32_t max_blocks_per_seq,
+                      uint32_t* err_word, void* stream);
+
+/* Work decomposition of kvq_decode (host-only arithmetic, no CUDA calls). */
+typedef struct {
+  int32_t stream_ctas;    /* CTAs sharing the token blocks of all (seq, kv_head) units */
+  int32_t window_ctas;    /* one CTA per unit for the bf16 window (0 without a window) */
+  int32_t units;          /* batch * num_kv_heads                                       */
+  int32_t partial_slots;  /* partial-result records in the workspace                    */
+  size_t workspace_bytes; /* bytes kvq_decode needs for this plan                       */
+} kvq_decode_plan;
+
+/* Plan for `num_sms` SMs with `ctas_per_sm` resident decode CTAs each, or an
+ * explicit `stream_ctas` (> 0 overrides the SM-based count). */
+kvq_status kvq_make_decode_plan(int32_t batch, int32_t q_heads, int32_t num_kv_heads, int32_t window,
+                                int32_t num_sms, int32_t ctas_per_sm, int32_t stream_ctas,
+                                kvq_decode_plan* plan);
+
+/* Workspace bytes kvq_decode needs on the current device (stream_ctas 0 = automatic). */
+kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t batch, int32_t q_heads,
+                                     int32_t stream_ctas, size_t* bytes);
+
+/* Zero a decode workspace (its merge counters must start at zero; every
+ * kvq_decode leaves them at zero again).  Call once after allocating it. */
+kvq_status kvq_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * kvq_decode -- one decode step of attention over the quantized cache.
+ * [P1] "Key error acts before the softmax" and [P2] "Keys and values need not
+ * have identical error sensitivity": score_i = q . k_hat_i / sqrt(D),
+ * o = sum_i softmax(score)_i v_hat_i.  [P3] "The axis choice is a kernel
+ * decision": the per-token key scale multiplies the score after the integer
+ * dot product; the per-channel key factor is applied to the query once.
+ * [P3] "Per-token scales and where they can live": dequantization happens as
+ * the kernel loads (codes and scales are two read streams).  [P1] "Cache growth
+ * changes the serving trade": the last min(W, L) positions are read from the
+ * bf16 window, older ones from the quantized blocks.  Query head hq reads KV
+ * head hq / (q_heads / num_kv_heads).
+ *   q          : device bf16 [batch][q_heads][128]
+ *   seq_lens   : device int32 [batch], tokens attended per sequence (0 allowed:
+ *                out = 0, lse = -inf)
+ *   out        : device [batch][q_heads][128], bf16 (out_fp32 = 0) or float32
+ *   lse        : device float [batch][q_heads] natural-log log-sum-exp of the
+ *                scores, or NULL
+ *   workspace  : device, >= kvq_decode_workspace_size bytes, zeroed once by
+ *                kvq_workspace_init; one workspace per concurrently running call
+ *   stream_ctas: 0 = one wave on all SMs, > 0 = explicit count (tests)
+ * Requirements: q_heads % num_kv_heads == 0, q_heads / num_kv_heads <= 8.
+ */
+kvq_status kvq_decode(const kvq_cache_desc* cache, const void* q, int32_t batch, int32_t q_heads,
+                      const int32_t* seq_lens, const int32_t* block_table, int32_t max_blocks_per_seq,
+                      void* out, int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes,
+                      int32_t stream_ctas, uint32_t* err_word, void* stream);
+
+/*
+ * kvq_dequant -- read the block store back: x_hat = RN32(code * s)
+ * ([P2] "Quantization needs a scale convention"), without the per-channel key
+ * factor.  For a bf16 cache the stored values are widened.  For tests.
+ *   slots : device int32 [n], physical slot = physical_block * 16 + token
+ *   k_out, v_out : device float [n][num_kv_heads][128]
+ */
+kvq_status kvq_dequant(const kvq_cache_desc* cache, const int32_t* slots, int32_t n, float* k_out,
+                       float* v_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

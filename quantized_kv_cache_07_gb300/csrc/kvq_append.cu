@@ -1,0 +1,246 @@
+// Quantize-on-write (kvq_append) and read-back (kvq_dequant) kernels.
+//
+// Quantizer: "KV Cache Quantization and Per-Token Scale Placement", sections
+// "Per-token scales and where they can live" (one scale per token per head,
+// computed at write time, stored alongside the codes) and "The axis choice is a
+// kernel decision" (listing: amax, zero vector -> scale 1, scale = amax/qmax,
+// clamp(round(x/scale))); "KV Cache Quantization Reduces Cache Bytes with
+// Separate Accuracy and Kernel Costs", section "Quantization needs a scale
+// convention" (q = clamp(round(x/s)), x_hat = q*s).
+//
+// One warp quantizes one 128-element vector; lane l owns dims 4l..4l+3.
+#include "kvq_device.cuh"
+#include "kvq_launch.h"
+
+namespace kvq {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// Round-half-even of the exact quotient x / s (s > 0, finite).  The float32
+// quotient decides unless it landed exactly on a half-integer; then the sign of
+// the exact residual x - q*s (computed exactly in double: q*s has at most 48
+// significant bits) tells which side the true quotient lies on.
+__device__ __forceinline__ float round_quotient(float x, float s) {
+  const float q = __fdiv_rn(x, s);
+  const float fl = floorf(q);
+  if (q - fl == 0.5f) {
+    const double res = double(x) - double(q) * double(s);
+    if (res > 0.0) return fl + 1.0f;
+    if (res < 0.0) return fl;
+  }
+  return rintf(q);
+}
+
+// Warp-cooperative per-vector quantization.
+__device__ __forceinline__ void quantize_warp(const float (&x)[4], int bits, int (&code)[4], float& s) {
+  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFull, a, o));
+  const int qmax = bits == 8 ? 127 : 7;
+  const int lo = bits == 8 ? -127 : -8;
+  if (a == 0.0f) {
+    s = 1.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) code[j] = 0;
+    return;
+  }
+  s = __fdiv_rn(a, float(qmax));
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int c = int(round_quotient(x[j], s));
+    code[j] = min(qmax, max(lo, c));
+  }
+}
+
+// Store the codes of one quantized vector (token `tok`) into its block.
+__device__ void store_codes(bool is_key, int bits, uint8_t* blk, int tok, const int (&code)[4], int lane) {
+  if (bits == 8) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int d = 4 * lane + j;
+      const Loc L = is_key ? key_loc(8, tok, d) : value_loc(8, tok, d);
+      blk[L.byte] = uint8_t(int8_t(code[j]));
+    }
+    return;
+  }
+  // 4-bit
+  if (is_key) {
+    // Lanes l and l^1 own the 8 nibbles of one 32-bit word of this token.
+    uint32_t part = 0;
+    int word_off = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int d = 4 * lane + j;
+      const Loc L = key_loc(4, tok, d);
+      const int nib = ((L.byte & 3) << 1) | (L.shift >> 2);
+      part |= (uint32_t(code[j]) & 0xFu) << (4 * nib);
+      word_off = L.byte & ~3;
+    }
+    const uint32_t word = part | __shfl_xor_sync(kFull, part, 1);
+    if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(blk + word_off) = word;
+    return;
+  }
+  // 4-bit values: a word mixes four tokens, so update only this token's nibbles.
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int d = 4 * lane + j;
+    const Loc L = value_loc(4, tok, d);
+    const int nib = ((L.byte & 3) << 1) | (L.shift >> 2);
+    uint32_t* w = reinterpret_cast<uint32_t*>(blk + (L.byte & ~3));
+    atomicAnd(w, ~(0xFu << (4 * nib)));
+    atomicOr(w, (uint32_t(code[j]) & 0xFu) << (4 * nib));
+  }
+}
+
+__device__ void store_bf16(bool is_key, uint8_t* blk, int tok, const uint16_t (&xb)[4], int lane) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int d = 4 * lane + j;
+    const Loc L = is_key ? key_loc(16, tok, d) : value_loc(16, tok, d);
+    *reinterpret_cast<uint16_t*>(blk + L.byte) = xb[j];
+  }
+}
+
+// Quantize (or copy, for a bf16 cache) one vector into the block store at
+// position p of sequence b.
+__device__ void write_block_store(const AppendArgs& a, bool is_key, int b, int p, int h, const uint16_t (&xb)[4],
+                                  int lane) {
+  const CacheView& c = a.c;
+  if (p >= a.mbps * kBlock) {
+    if (lane == 0) flag(a.err, KVQ_DEVERR_POSITION);
+    return;
+  }
+  const int phys = a.table[size_t(b) * a.mbps + p / kBlock];
+  if (phys < 0 || phys >= c.num_blocks) {
+    if (lane == 0) flag(a.err, KVQ_DEVERR_BLOCK_ID);
+    return;
+  }
+  const int tok = p % kBlock;
+  const int bits = is_key ? c.k_bits : c.v_bits;
+  uint8_t* pool = is_key ? c.k_codes : c.v_codes;
+  uint8_t* blk = pool + (size_t(phys) * c.H + h) * block_bytes(bits);
+  if (bits == 16) {
+    store_bf16(is_key, blk, tok, xb, lane);
+    return;
+  }
+  float x[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[j] = bf16_bits_to_f32(xb[j]);
+    if (is_key && c.factor) x[j] = __fdiv_rn(x[j], c.factor[h * kHeadDim + 4 * lane + j]);
+  }
+  int code[4];
+  float s;
+  quantize_warp(x, bits, code, s);
+  store_codes(is_key, bits, blk, tok, code, lane);
+  if (lane == 0) {
+    float* sc = is_key ? c.k_scales : c.v_scales;
+    sc[(size_t(phys) * c.H + h) * kBlock + tok] = s;
+  }
+}
+
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long vec = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int H = a.c.H;
+  if (vec >= (long long)a.n * 2 * H) return;
+  const int r = int(vec / (2 * H));
+  const int kv = int((vec / H) % 2);
+  const int h = int(vec % H);
+  const bool is_key = kv == 0;
+  const int b = a.seq_idx[r];
+  const int p = a.pos[r];
+  if (b < 0 || b >= a.batch || p < 0 ||
+      (a.mode != KVQ_APPEND_QUANT && b >= a.c.window_batch)) {
+    if (lane == 0) flag(a.err, KVQ_DEVERR_POSITION);
+    return;
+  }
+  const uint16_t* src = (is_key ? a.k_new : a.v_new) + (size_t(r) * H + h) * kHeadDim + 4 * lane;
+  uint16_t xb[4];
+  {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    xb[0] = uint16_t(v.x & 0xFFFF);
+    xb[1] = uint16_t(v.x >> 16);
+    xb[2] = uint16_t(v.y & 0xFFFF);
+    xb[3] = uint16_t(v.y >> 16);
+  }
+  if (a.mode == KVQ_APPEND_QUANT) {
+    write_block_store(a, is_key, b, p, h, xb, lane);
+    return;
+  }
+  const int W = a.c.window;
+  uint16_t* ring = (is_key ? a.c.k_win : a.c.v_win) + ((size_t(b) * H + h) * W + (p % W)) * kHeadDim + 4 * lane;
+  if (a.mode == KVQ_APPEND_STEP && p >= W) {
+    // the token at p - W occupies this ring slot: it leaves the window now
+    const uint2 ov = *reinterpret_cast<const uint2*>(ring);
+    uint16_t ob[4] = {uint16_t(ov.x & 0xFFFF), uint16_t(ov.x >> 16), uint16_t(ov.y & 0xFFFF),
+                      uint16_t(ov.y >> 16)};
+    write_block_store(a, is_key, b, p - W, h, ob, lane);
+    __syncwarp();
+  }
+  *reinterpret_cast<uint2*>(ring) = make_uint2(uint32_t(xb[0]) | (uint32_t(xb[1]) << 16),
+                                               uint32_t(xb[2]) | (uint32_t(xb[3]) << 16));
+}
+
+__global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long vec = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int H = a.c.H;
+  if (vec >= (long long)a.n * 2 * H) return;
+  const int r = int(vec / (2 * H));
+  const bool is_key = ((vec / H) % 2) == 0;
+  const int h = int(vec % H);
+  const int slot = a.slots[r];
+  const int phys = slot / kBlock, tok = slot % kBlock;
+  float* out = (is_key ? a.k_out : a.v_out) + (size_t(r) * H + h) * kHeadDim + 4 * lane;
+  if (slot < 0 || phys >= a.c.num_blocks) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[j] = 0.0f;
+    return;
+  }
+  const int bits = is_key ? a.c.k_bits : a.c.v_bits;
+  const uint8_t* blk = (is_key ? a.c.k_codes : a.c.v_codes) + (size_t(phys) * H + h) * block_bytes(bits);
+  float s = 1.0f;
+  if (bits != 16) s = (is_key ? a.c.k_scales : a.c.v_scales)[(size_t(phys) * H + h) * kBlock + tok];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int d = 4 * lane + j;
+    const Loc L = is_key ? key_loc(bits, tok, d) : value_loc(bits, tok, d);
+    float v;
+    if (bits == 16) {
+      v = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(blk + L.byte));
+    } else if (bits == 8) {
+      v = __fmul_rn(float(int8_t(blk[L.byte])), s);
+    } else {
+      int nib = (blk[L.byte] >> L.shift) & 0xF;
+      nib = nib >= 8 ? nib - 16 : nib;
+      v = __fmul_rn(float(nib), s);
+    }
+    out[j] = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+  const long long vecs = (long long)a.n * 2 * a.c.H;
+  if (vecs == 0) return cudaSuccess;
+  const int warps = 8;
+  const long long grid = (vecs + warps - 1) / warps;
+  append_kernel<<<unsigned(grid), warps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s) {
+  const long long vecs = (long long)a.n * 2 * a.c.H;
+  if (vecs == 0) return cudaSuccess;
+  const int warps = 8;
+  const long long grid = (vecs + warps - 1) / warps;
+  dequant_kernel<<<unsigned(grid), warps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,836 @@
+// Fused dequantize-on-load decode attention (kvq_decode), sm_103a.
+//
+// What is computed, per query head of every sequence (one decode step):
+//   score_i = q . k_hat_i / sqrt(D),  o = sum_i softmax(score)_i v_hat_i
+//   ("KV Cache Quantization Perturbs Attention Through Stored Keys and Values",
+//   section "Key error acts before the softmax"; "KV Cache Quantization Reduces
+//   Cache Bytes with Separate Accuracy and Kernel Costs", section "Keys and
+//   values need not have identical error sensitivity").
+// How ("KV Cache Quantization and Per-Token Scale Placement"):
+//   - the key dot product runs on the integer codes and the per-token key scale
+//     multiplies the scalar score afterwards (section "The axis choice is a
+//     kernel decision");
+//   - a per-channel key factor is multiplied onto the query once (same section);
+//   - codes and scales are two read streams, dequantized as they are loaded
+//     (section "Per-token scales and where they can live");
+//   - the value scale is folded into the attention weight, so the value loop is
+//     a pure code contraction.
+// The most recent W tokens may sit in a bf16 ring ("KV Cache Quantization
+// Perturbs Attention ...", section "Cache growth changes the serving trade").
+//
+// GB300 mapping
+//   * Stream-K decomposition: all (sequence, kv_head) units' 16-token blocks form
+//     one global range that is cut evenly over one wave of CTAs (SMs x resident
+//     CTAs).  A CTA walks its range, keeps online-softmax state per unit segment
+//     and writes one partial (m, l, o) per segment; the last CTA to finish a
+//     unit (atomic ticket, no spinning) merges its partials with a log-sum-exp
+//     reduce.  A unit held by a single CTA is normalised in place.
+//   * One producer warp streams whole 16-token blocks (codes of K and V plus
+//     their scales) with cp.async.bulk into a ring of shared-memory stages
+//     guarded by mbarriers; four consumer warps each take one block per stage.
+//   * The GQA group (G <= 8 query heads sharing the KV head) makes the two small
+//     contractions dense: S^T = Kcodes . Q^T and O^T += V^T . (p*s_v)^T run on
+//     mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens/dims on M, the query
+//     group on N.  Codes are converted exactly to fp16 in registers; the cache
+//     is stored in the fragment order so every lane reads 16 contiguous bytes.
+//   * The query is scaled by an exact power of two into fp16's range; the score
+//     scale s_k * 2^-e * log2(e) / sqrt(D) is applied per score in fp32.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <map>
+#include <tuple>
+
+#include "kvq_device.cuh"
+#include "kvq_launch.h"
+
+namespace kvq {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kInvSqrtD = 0.08838834764831845f;  // 1/sqrt(128)
+#define kNegInf (-__int_as_float(0x7f800000))
+
+template <int KB, int VB>
+struct Fmt {
+  static constexpr bool kBf16 = (KB == 16);
+  static constexpr int kKBB = block_bytes(KB);
+  static constexpr int kVBB = block_bytes(VB);
+  static constexpr int kSCB = kBf16 ? 0 : kBlock * 4;  // scale bytes per block per tensor
+  static constexpr int kPerBlock = kKBB + kVBB + 2 * kSCB;
+  static constexpr int kStageBytes = kConsumerWarps * kPerBlock;
+  static constexpr int kStagesRaw = 65536 / kStageBytes;
+  static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+  // stage sub-buffers
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kConsumerWarps * kKBB;
+  static constexpr int kOffKS = kOffV + kConsumerWarps * kVBB;
+  static constexpr int kOffVS = kOffKS + kConsumerWarps * kSCB;
+};
+
+// Shared-memory map after the stage ring (all offsets 16-byte aligned).
+struct SmemMap {
+  int merge_o;   // float [4 warps][8 q][128]
+  int merge_ml;  // float m[4][8], l[4][8]
+  int qh;        // 16-bit [8][128]
+  int qs;        // float [8]
+  int hdr;       // int4 [stages]
+  int bars;      // uint64 full[stages], empty[stages], cbar
+  int misc;      // int [4]
+  int len;       // int [B]
+  int pre;       // int [B+1]
+  int total;
+};
+
+__host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, int B) {
+  SmemMap m;
+  int o = stage_bytes_total;
+  m.merge_o = o;  o += kConsumerWarps * kMaxGroup * kHeadDim * 4;
+  m.merge_ml = o; o += 2 * kConsumerWarps * kMaxGroup * 4;
+  m.qh = o;       o += kMaxGroup * kHeadDim * 2;
+  m.qs = o;       o += kMaxGroup * 4 + 32;
+  m.hdr = o;      o += stages * 16;
+  m.bars = o;     o += (2 * stages + 2) * 8;
+  m.misc = o;     o += 16;
+  m.len = o;      o += ((B * 4 + 15) / 16) * 16;
+  m.pre = o;      o += (((B + 1) * 4 + 15) / 16) * 16;
+  m.total = o;
+  return m;
+}
+
+// ------------------------------------------------------------------ score / value contractions
+template <int KB>
+__device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&qf)[16], float (&acc)[4],
+                                            int lane) {
+  const uint4* p = reinterpret_cast<const uint4*>(kb) + lane;
+  if constexpr (KB == 8) {
+    const uint4 r0a = p[0], r0b = p[32], r1a = p[64], r1b = p[96];
+    const uint32_t g0[8] = {r0a.x, r0a.y, r0a.z, r0a.w, r0b.x, r0b.y, r0b.z, r0b.w};
+    const uint32_t g8[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      s8x4_to_f16(g0[kk], a0, a2);
+      s8x4_to_f16(g8[kk], a1, a3);
+      mma_f16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+    }
+  } else if constexpr (KB == 4) {
+    const uint4 r0 = p[0], r1 = p[32];
+    const uint32_t g0[4] = {r0.x, r0.y, r0.z, r0.w};
+    const uint32_t g8[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+      s4x8_to_f16(g0[wi], x0, x1, x2, x3);
+      s4x8_to_f16(g8[wi], y0, y1, y2, y3);
+      mma_f16(acc, x0, y0, x1, y1, qf[4 * wi], qf[4 * wi + 1]);
+      mma_f16(acc, x2, y2, x3, y3, qf[4 * wi + 2], qf[4 * wi + 3]);
+    }
+  } else {
+    uint4 c[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) c[h] = p[h * 32];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint4 lo = c[kk >> 1], hi = c[4 + (kk >> 1)];
+      const uint32_t a0 = (kk & 1) ? lo.z : lo.x, a2 = (kk & 1) ? lo.w : lo.y;
+      const uint32_t a1 = (kk & 1) ? hi.z : hi.x, a3 = (kk & 1) ? hi.w : hi.y;
+      mma_bf16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+    }
+  }
+}
+
+template <int VB>
+__device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint32_t b1, uint32_t b0lo,
+                                            uint32_t b1lo, float (&O)[8][4], int lane) {
+  const uint4* p = reinterpret_cast<const uint4*>(vb) + lane;
+  if constexpr (VB == 8) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint4 c = p[h * 32];
+      uint32_t a0, a1, a2, a3;
+      s8x4_to_f16(c.x, a0, a2);
+      s8x4_to_f16(c.y, a1, a3);
+      mma_f16(O[2 * h], a0, a1, a2, a3, b0, b1);
+      s8x4_to_f16(c.z, a0, a2);
+      s8x4_to_f16(c.w, a1, a3);
+      mma_f16(O[2 * h + 1], a0, a1, a2, a3, b0, b1);
+    }
+  } else if constexpr (VB == 4) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 c = p[h * 32];
+      const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t x0, x1, x2, x3;
+        s4x8_to_f16(w[k], x0, x1, x2, x3);
+        mma_f16(O[4 * h + k], x0, x2, x1, x3, b0, b1);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const uint4 c = p[mt * 32];
+      mma_bf16(O[mt], c.x, c.z, c.y, c.w, b0, b1);
+      mma_bf16(O[mt], c.x, c.z, c.y, c.w, b0lo, b1lo);
+    }
+  }
+}
+
+struct Params {
+  DecodeArgs a;
+  int P;  // stream CTAs
+};
+
+// CTA-consumer barrier on an mbarrier (count = kConsumers), bounded wait.
+__device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase) {
+  mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, phase);
+  phase ^= 1u;
+  return ok;
+}
+
+__device__ __forceinline__ long long cta_of(long long x, long long T, int P) {
+  return ((x + 1) * (long long)P - 1) / T;
+}
+
+// Write the final normalised output of query row hq.
+__device__ __forceinline__ void write_out(const DecodeArgs& a, int b, int hq, int d, float o, float l, float M) {
+  const size_t idx = (size_t(b) * a.Hq + hq) * kHeadDim + d;
+  const float v = o / l;
+  if (a.out_fp32) reinterpret_cast<float*>(a.out)[idx] = v;
+  else reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(v);
+  if (d == 0 && a.lse) a.lse[size_t(b) * a.Hq + hq] = (M + log2f(l)) * kLn2;
+}
+
+// Merge every partial record of unit u (run by the last CTA to finish it).
+__device__ void merge_unit(const DecodeArgs& a, int u, long long c0, long long c1, bool has_win, int P, int tid,
+                           int nthreads) {
+  // P: launched stream CTAs (the window records sit after P + units slots)
+  const int b = u / a.c.H, h = u % a.c.H;
+  const float* pm = reinterpret_cast<const float*>(a.ws + a.lay.off_m);
+  const float* pl = reinterpret_cast<const float*>(a.ws + a.lay.off_l);
+  const float* po = reinterpret_cast<const float*>(a.ws + a.lay.off_o);
+  const int wslot = P + a.lay.units + u;
+  for (int e = tid; e < a.G * kHeadDim; e += nthreads) {
+    const int q = e / kHeadDim, d = e % kHeadDim;
+    float M = kNegInf;
+    for (long long j = c0; j <= c1; ++j) M = fmaxf(M, __ldcg(pm + (j + u) * kMaxGroup + q));
+    if (has_win) M = fmaxf(M, __ldcg(pm + size_t(wslot) * kMaxGroup + q));
+    float l = 0.f, o = 0.f;
+    for (long long j = c0; j <= c1; ++j) {
+      const size_t s = size_t(j + u);
+      const float w = exp2f(__ldcg(pm + s * kMaxGroup + q) - M);
+      l += w * __ldcg(pl + s * kMaxGroup + q);
+      o += w * __ldcg(po + (s * kMaxGroup + q) * kHeadDim + d);
+    }
+    if (has_win) {
+      const size_t s = size_t(wslot);
+      const float w = exp2f(__ldcg(pm + s * kMaxGroup + q) - M);
+      l += w * __ldcg(pl + s * kMaxGroup + q);
+      o += w * __ldcg(po + (s * kMaxGroup + q) * kHeadDim + d);
+    }
+    write_out(a, b, h * a.G + q, d, o, l, M);
+  }
+}
+
+// Number of partial records unit u has (stream segments + window).
+__device__ __forceinline__ void unit_segments(const DecodeArgs& a, const int* len_s, const int* pre_s, int u,
+                                              long long T, int P, long long& c0, long long& c1, int& nseg,
+                                              bool& has_win) {
+  const int H = a.c.H, b = u / H, h = u % H;
+  const int nblk = pre_s[b + 1] - pre_s[b];
+  const long long start = (long long)H * pre_s[b] + (long long)h * nblk;
+  nseg = 0;
+  c0 = 0;
+  c1 = -1;
+  if (nblk > 0) {
+    c0 = cta_of(start, T, P);
+    c1 = cta_of(start + nblk - 1, T, P);
+    nseg = int(c1 - c0 + 1);
+  }
+  has_win = a.c.window > 0 && len_s[b] > 0;
+  nseg += has_win ? 1 : 0;
+}
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
+  using F = Fmt<KB, VB>;
+  constexpr int S = F::kStages;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const DecodeArgs& a = prm.a;
+  const int P = prm.P;
+  const int H = a.c.H, G = a.G, B = a.B;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const SmemMap mp = smem_map(S * F::kStageBytes, S, B);
+  float* merge_o = reinterpret_cast<float*>(smem + mp.merge_o);
+  float* merge_m = reinterpret_cast<float*>(smem + mp.merge_ml);
+  float* merge_l = merge_m + kConsumerWarps * kMaxGroup;
+  uint16_t* qh = reinterpret_cast<uint16_t*>(smem + mp.qh);
+  float* qs = reinterpret_cast<float*>(smem + mp.qs);
+  int4* hdr = reinterpret_cast<int4*>(smem + mp.hdr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + mp.bars);
+  uint64_t* empty = full + S;
+  uint64_t* cbar = empty + S;
+  int* misc = reinterpret_cast<int*>(smem + mp.misc);
+  int* len_s = reinterpret_cast<int*>(smem + mp.len);
+  int* pre_s = reinterpret_cast<int*>(smem + mp.pre);
+
+  // ---- sequence geometry: clamped lengths and block prefix sums
+  const int W = a.c.window;
+  const int cap = a.mbps * kBlock;
+  for (int b = tid; b < B; b += kThreads) {
+    int L = a.seq_lens[b];
+    if (L < 0) {
+      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
+      L = 0;
+    }
+    int Lq = W > 0 ? max(L - W, 0) : L;
+    if (Lq > cap) {
+      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
+      Lq = cap;
+      L = W > 0 ? cap + W : cap;
+    }
+    len_s[b] = L;
+    pre_s[b + 1] = (Lq + kBlock - 1) / kBlock;  // block count, scanned below
+  }
+  if (tid == 0) {
+    pre_s[0] = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    mbar_init(cbar, kConsumers);
+    misc[0] = 0;  // ticket result
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < B; base += 32) {
+      const int i = base + lane;
+      int v = i < B ? pre_s[i + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += n;
+      }
+      if (i < B) pre_s[i + 1] = v + carry;
+      carry += __shfl_sync(kFull, v, 31);
+    }
+  }
+  __syncthreads();
+  const long long T = (long long)H * pre_s[B];
+  const int U = B * H;
+  // Effective stream split: never more CTAs than blocks, so every CTA below Pe
+  // owns at least one block and a unit's owners are exactly the CTAs c0..c1.
+  const int Pe = int(T < (long long)P ? T : (long long)P);
+  const float* pfac = a.c.factor;
+
+  // ==================================================================== window CTAs
+  if (blockIdx.x >= P) {
+    const int u = blockIdx.x - P;
+    const int b = u / H, h = u % H;
+    const int L = len_s[b];
+    if (L <= 0) return;
+    const int nw = min(L, W);
+    float* qf = merge_o;                      // [8][128] fp32 query
+    float* sc = merge_o + kMaxGroup * kHeadDim;  // [8][128] scores -> weights
+    for (int e = tid; e < G * kHeadDim; e += kThreads) {
+      const int q = e / kHeadDim, d = e % kHeadDim;
+      qf[e] = __uint_as_float(uint32_t(a.q[(size_t(b) * a.Hq + h * G + q) * kHeadDim + d]) << 16);
+    }
+    __syncthreads();
+    const uint16_t* kw = a.c.k_win + (size_t(b) * H + h) * W * kHeadDim;
+    const uint16_t* vw = a.c.v_win + (size_t(b) * H + h) * W * kHeadDim;
+    if (tid < nw) {
+      float dot[kMaxGroup];
+#pragma unroll
+      for (int q = 0; q < kMaxGroup; ++q) dot[q] = 0.f;
+      const uint4* kr = reinterpret_cast<const uint4*>(kw + size_t(tid) * kHeadDim);
+      for (int c = 0; c < kHeadDim / 8; ++c) {
+        const uint4 v = kr[c];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+          const int d = c * 8 + 2 * k;
+#pragma unroll
+          for (int q = 0; q < kMaxGroup; ++q)
+            if (q < G) dot[q] = fmaf(qf[q * kHeadDim + d + 1], hi, fmaf(qf[q * kHeadDim + d], lo, dot[q]));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kMaxGroup; ++q)
+        if (q < G) sc[q * kHeadDim + tid] = dot[q] * (kLog2e * kInvSqrtD);
+    }
+    __syncthreads();
+    float* wm = merge_m;  // [8]
+    float* wl = merge_l;
+    for (int q = warp; q < G; q += kThreads / 32) {
+      float m = kNegInf;
+      for (int i = lane; i < nw; i += 32) m = fmaxf(m, sc[q * kHeadDim + i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      float l = 0.f;
+      for (int i = lane; i < nw; i += 32) {
+        const float p = exp2f(sc[q * kHeadDim + i] - m);
+        sc[q * kHeadDim + i] = p;
+        l += p;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+      if (lane == 0) {
+        wm[q] = m;
+        wl[q] = l;
+      }
+    }
+    __syncthreads();
+    long long c0, c1;
+    int nseg;
+    bool has_win;
+    unit_segments(a, len_s, pre_s, u, T, Pe, c0, c1, nseg, has_win);
+    float* pm = reinterpret_cast<float*>(a.ws + a.lay.off_m);
+    float* pl = reinterpret_cast<float*>(a.ws + a.lay.off_l);
+    float* po = reinterpret_cast<float*>(a.ws + a.lay.off_o);
+    const size_t slot = size_t(P) + U + u;
+    if (tid < kHeadDim) {
+      const int d = tid;
+      for (int q = 0; q < G; ++q) {
+        float o = 0.f;
+        for (int i = 0; i < nw; ++i)
+          o = fmaf(sc[q * kHeadDim + i], __uint_as_float(uint32_t(vw[size_t(i) * kHeadDim + d]) << 16), o);
+        if (nseg == 1) {
+          write_out(a, b, h * G + q, d, o, wl[q], wm[q]);
+        } else {
+          po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
+          if (d == 0) {
+            pm[slot * kMaxGroup + q] = wm[q];
+            pl[slot * kMaxGroup + q] = wl[q];
+          }
+        }
+      }
+    }
+    if (nseg > 1) {
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        int* cnt = reinterpret_cast<int*>(a.ws + a.lay.off_counter);
+        const int t = atomicAdd(&cnt[u], 1);
+        misc[0] = (t == nseg - 1);
+      }
+      __syncthreads();
+      if (misc[0]) {
+        __threadfence();
+        merge_unit(a, u, c0, c1, has_win, P, tid, kThreads);
+        if (tid == 0) reinterpret_cast<int*>(a.ws + a.lay.off_counter)[u] = 0;
+      }
+    }
+    return;
+  }
+
+  // ==================================================================== stream CTAs
+  // units with no tokens at all: out = 0, lse = -inf
+  for (int u = blockIdx.x; u < U; u += P) {
+    const int b = u / H, h = u % H;
+    if (len_s[b] != 0) continue;
+    for (int e = tid; e < G * kHeadDim; e += kThreads) {
+      const int q = e / kHeadDim, d = e % kHeadDim;
+      const size_t idx = (size_t(b) * a.Hq + h * G + q) * kHeadDim + d;
+      if (a.out_fp32) reinterpret_cast<float*>(a.out)[idx] = 0.f;
+      else reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(0.f);
+      if (d == 0 && a.lse) a.lse[size_t(b) * a.Hq + h * G + q] = kNegInf;
+    }
+  }
+  if (blockIdx.x >= Pe) return;
+  const long long x0 = (long long)blockIdx.x * T / Pe;
+  const long long x1 = (long long)(blockIdx.x + 1) * T / Pe;
+  if (x0 >= x1) return;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint64_t pol = l2_evict_first_policy();
+    // locate the unit holding x0: largest b with H*pre[b] <= x0 and blocks > 0
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)H * pre_s[mid] <= x0) lo = mid;
+      else hi = mid - 1;
+    }
+    int b = lo;
+    while (pre_s[b + 1] == pre_s[b]) ++b;  // skip empty sequences (x0 lies in a non-empty one)
+    int nblk = pre_s[b + 1] - pre_s[b];
+    int h = int((x0 - (long long)H * pre_s[b]) / nblk);
+    long long ustart = (long long)H * pre_s[b] + (long long)h * nblk;
+    long long x = x0;
+    int it = 0;
+    bool ok = true;
+    while (x < x1) {
+      if (x >= ustart + nblk) {
+        ++h;
+        if (h == H) {
+          h = 0;
+          do { ++b; } while (pre_s[b + 1] == pre_s[b]);
+          nblk = pre_s[b + 1] - pre_s[b];
+        }
+        ustart = (long long)H * pre_s[b] + (long long)h * nblk;
+      }
+      const long long rem = (x1 - x) < (ustart + nblk - x) ? (x1 - x) : (ustart + nblk - x);
+      const int n = int(rem < kConsumerWarps ? rem : kConsumerWarps);
+      const int s = it % S;
+      if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1)) {
+        flag(a.err, KVQ_DEVERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+      const int local = int(x - ustart);
+      hdr[s] = make_int4(b * H + h, local, n, 0);
+      mbar_arrive_expect_tx(&full[s], uint32_t(n * F::kPerBlock));
+      uint8_t* st = smem + s * F::kStageBytes;
+      for (int j = 0; j < n; ++j) {
+        int phys = a.table[size_t(b) * a.mbps + local + j];
+        if (phys < 0 || phys >= a.c.num_blocks) {
+          flag(a.err, KVQ_DEVERR_BLOCK_ID);
+          phys = 0;
+        }
+        const size_t bh = size_t(phys) * H + h;
+        bulk_g2s(st + F::kOffK + j * F::kKBB, a.c.k_codes + bh * F::kKBB, F::kKBB, &full[s], pol);
+        bulk_g2s(st + F::kOffV + j * F::kVBB, a.c.v_codes + bh * F::kVBB, F::kVBB, &full[s], pol);
+        if constexpr (!F::kBf16) {
+          bulk_g2s(st + F::kOffKS + j * F::kSCB, a.c.k_scales + bh * kBlock, F::kSCB, &full[s], pol);
+          bulk_g2s(st + F::kOffVS + j * F::kSCB, a.c.v_scales + bh * kBlock, F::kSCB, &full[s], pol);
+        }
+      }
+      x += n;
+      ++it;
+    }
+    if (ok) {  // terminator stage
+      const int s = it % S;
+      if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1)) {
+        flag(a.err, KVQ_DEVERR_TIMEOUT);
+      } else {
+        hdr[s] = make_int4(-1, 0, 0, 0);
+        mbar_arrive(&full[s]);
+        ++it;
+      }
+    }
+    // drain: the most recent use of every stage must have landed before exit
+    for (int k = max(0, it - S); k < it; ++k)
+      if (!mbar_wait(&full[k % S], (k / S) & 1)) flag(a.err, KVQ_DEVERR_TIMEOUT);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, t = lane & 3;
+  float O[8][4];
+  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+  uint32_t qf[16];
+  float qs0 = 0.f, qs1 = 0.f;
+  uint32_t cphase = 0;
+  int cur = -1;
+  int cur_b = 0, cur_lq = 0;
+  int* cnt = reinterpret_cast<int*>(a.ws + a.lay.off_counter);
+  float* pm = reinterpret_cast<float*>(a.ws + a.lay.off_m);
+  float* pl = reinterpret_cast<float*>(a.ws + a.lay.off_l);
+  float* po = reinterpret_cast<float*>(a.ws + a.lay.off_o);
+
+  for (int it = 0;; ++it) {
+    const int s = it % S;
+    if (!mbar_wait(&full[s], (it / S) & 1)) {
+      flag(a.err, KVQ_DEVERR_TIMEOUT);
+      return;
+    }
+    const int4 hd = hdr[s];
+    if (hd.x != cur) {
+      if (cur >= 0) {
+        // ---------------- flush the finished unit segment
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          l0 += __shfl_xor_sync(kFull, l0, o);
+          l1 += __shfl_xor_sync(kFull, l1, o);
+        }
+        if (g == 0) {
+          merge_m[warp * kMaxGroup + 2 * t] = m0;
+          merge_m[warp * kMaxGroup + 2 * t + 1] = m1;
+          merge_l[warp * kMaxGroup + 2 * t] = l0;
+          merge_l[warp * kMaxGroup + 2 * t + 1] = l1;
+        }
+        float* ow = merge_o + warp * kMaxGroup * kHeadDim;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          ow[(2 * t) * kHeadDim + 16 * mt + g] = O[mt][0];
+          ow[(2 * t + 1) * kHeadDim + 16 * mt + g] = O[mt][1];
+          ow[(2 * t) * kHeadDim + 16 * mt + g + 8] = O[mt][2];
+          ow[(2 * t + 1) * kHeadDim + 16 * mt + g + 8] = O[mt][3];
+        }
+        if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
+        const int ub = cur / H, uh = cur % H;
+        long long c0, c1;
+        int nseg;
+        bool has_win;
+        unit_segments(a, len_s, pre_s, cur, T, Pe, c0, c1, nseg, has_win);
+        const size_t slot = size_t(blockIdx.x) + cur;
+        {
+          const int d = tid;
+          for (int q = 0; q < G; ++q) {
+            float M = kNegInf;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * kMaxGroup + q]);
+            float l = 0.f, o = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+              const float mw = merge_m[w * kMaxGroup + q];
+              const float al = (mw == kNegInf) ? 0.f : exp2f(mw - M);
+              l += al * merge_l[w * kMaxGroup + q];
+              o += al * merge_o[(w * kMaxGroup + q) * kHeadDim + d];
+            }
+            if (nseg == 1) {
+              write_out(a, ub, uh * G + q, d, o, l, M);
+            } else {
+              po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
+              if (d == 0) {
+                pm[slot * kMaxGroup + q] = M;
+                pl[slot * kMaxGroup + q] = l;
+              }
+            }
+          }
+        }
+        if (nseg > 1) {
+          __threadfence();
+          if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
+          if (tid == 0) {
+            const int tk = atomicAdd(&cnt[cur], 1);
+            misc[0] = (tk == nseg - 1);
+          }
+          if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
+          if (misc[0]) {
+            __threadfence();
+            merge_unit(a, cur, c0, c1, has_win, P, tid, kConsumers);
+            if (tid == 0) cnt[cur] = 0;
+          }
+        }
+        if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
+      }
+      if (hd.x < 0) break;  // terminator
+      // ---------------- start a new unit: prepare the query group in fp16 / bf16
+      cur = hd.x;
+      cur_b = cur / H;
+      const int uh = cur % H;
+      cur_lq = W > 0 ? max(len_s[cur_b] - W, 0) : len_s[cur_b];
+      for (int q = warp; q < kMaxGroup; q += kConsumerWarps) {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (q < G) {
+          const uint2 raw =
+              *reinterpret_cast<const uint2*>(a.q + (size_t(cur_b) * a.Hq + uh * G + q) * kHeadDim + 4 * lane);
+          x[0] = __uint_as_float(raw.x << 16);
+          x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+          x[2] = __uint_as_float(raw.y << 16);
+          x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+        }
+        if constexpr (F::kBf16) {
+          uint2 packed;
+          packed.x = pack_bf162(x[0], x[1]);
+          packed.y = pack_bf162(x[2], x[3]);
+          *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
+          if (lane == 0) qs[q] = kLog2e * kInvSqrtD;
+        } else {
+          if (pfac) {
+            const float4 c = *reinterpret_cast<const float4*>(pfac + uh * kHeadDim + 4 * lane);
+            x[0] *= c.x;
+            x[1] *= c.y;
+            x[2] *= c.z;
+            x[3] *= c.w;
+          }
+          float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
+          int e = 0;
+          if (am > 0.f) {
+            int ex;
+            frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
+            e = 15 - ex;      // am * 2^e in [2^14, 2^15)
+          }
+          uint2 packed;
+          packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
+          packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+          *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
+          if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
+        }
+      }
+      if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
+      {
+        const uint4* qp = reinterpret_cast<const uint4*>(qh + g * kHeadDim + 32 * t);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = qp[i];
+          qf[4 * i] = v.x;
+          qf[4 * i + 1] = v.y;
+          qf[4 * i + 2] = v.z;
+          qf[4 * i + 3] = v.w;
+        }
+        qs0 = qs[2 * t];
+        qs1 = qs[2 * t + 1];
+      }
+      m0 = m1 = kNegInf;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+    }
+
+    // ---------------- one 16-token block per consumer warp
+    if (warp < hd.z) {
+      const uint8_t* st = smem + s * F::kStageBytes;
+      const int valid = min(kBlock, cur_lq - (hd.y + warp) * kBlock);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      score_block<KB>(st + F::kOffK + warp * F::kKBB, qf, acc, lane);
+      float sk0 = 1.f, sk1 = 1.f, sv0 = 1.f, sv1 = 1.f;
+      if constexpr (!F::kBf16) {
+        const float* ks = reinterpret_cast<const float*>(st + F::kOffKS + warp * F::kSCB);
+        const float* vs = reinterpret_cast<const float*>(st + F::kOffVS + warp * F::kSCB);
+        sk0 = ks[g];
+        sk1 = ks[g + 8];
+        sv0 = vs[g];
+        sv1 = vs[g + 8];
+      }
+      const bool v0 = g < valid, v1 = g + 8 < valid;
+      const float x00 = v0 ? acc[0] * (sk0 * qs0) : kNegInf;
+      const float x01 = v0 ? acc[1] * (sk0 * qs1) : kNegInf;
+      const float x10 = v1 ? acc[2] * (sk1 * qs0) : kNegInf;
+      const float x11 = v1 ? acc[3] * (sk1 * qs1) : kNegInf;
+      float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      if (__any_sync(kFull, (mn0 > m0) || (mn1 > m1))) {
+        const float al0 = (mn0 == kNegInf) ? 1.f : exp2f(m0 - mn0);
+        const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(m1 - mn1);
+        l0 *= al0;
+        l1 *= al1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          O[i][0] *= al0;
+          O[i][2] *= al0;
+          O[i][1] *= al1;
+          O[i][3] *= al1;
+        }
+        m0 = mn0;
+        m1 = mn1;
+      }
+      const float base0 = (m0 == kNegInf) ? 0.f : m0, base1 = (m1 == kNegInf) ? 0.f : m1;
+      const float p00 = exp2f(x00 - base0), p10 = exp2f(x10 - base0);
+      const float p01 = exp2f(x01 - base1), p11 = exp2f(x11 - base1);
+      l0 += p00 + p10;
+      l1 += p01 + p11;
+      uint32_t pk0, pk1, pk0lo = 0, pk1lo = 0;
+      if constexpr (F::kBf16) {
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(p00, p10), h1 = __floats2bfloat162_rn(p01, p11);
+        pk0 = *reinterpret_cast<const uint32_t*>(&h0);
+        pk1 = *reinterpret_cast<const uint32_t*>(&h1);
+        pk0lo = pack_bf162(p00 - __low2float(h0), p10 - __high2float(h0));
+        pk1lo = pack_bf162(p01 - __low2float(h1), p11 - __high2float(h1));
+      } else {
+        if ((v0 && sv0 > 65504.f) || (v1 && sv1 > 65504.f)) flag(a.err, KVQ_DEVERR_RANGE);
+        pk0 = pack_half2(v0 ? p00 * sv0 : 0.f, v1 ? p10 * sv1 : 0.f);
+        pk1 = pack_half2(v0 ? p01 * sv0 : 0.f, v1 ? p11 * sv1 : 0.f);
+      }
+      // transpose the weights from the score accumulator layout (token rows,
+      // query columns) to the B-operand layout of the value contraction
+      const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
+      const uint32_t r00 = __shfl_sync(kFull, pk0, src0), r01 = __shfl_sync(kFull, pk1, src0);
+      const uint32_t r10 = __shfl_sync(kFull, pk0, src1), r11 = __shfl_sync(kFull, pk1, src1);
+      const uint32_t b0 = (g & 1) ? r01 : r00, b1 = (g & 1) ? r11 : r10;
+      uint32_t b0lo = 0, b1lo = 0;
+      if constexpr (F::kBf16) {
+        const uint32_t q00 = __shfl_sync(kFull, pk0lo, src0), q01 = __shfl_sync(kFull, pk1lo, src0);
+        const uint32_t q10 = __shfl_sync(kFull, pk0lo, src1), q11 = __shfl_sync(kFull, pk1lo, src1);
+        b0lo = (g & 1) ? q01 : q00;
+        b1lo = (g & 1) ? q11 : q10;
+      }
+      value_block<VB>(st + F::kOffV + warp * F::kVBB, b0, b1, b0lo, b1lo, O, lane);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+template <int KB, int VB>
+struct Kernel {
+  using F = Fmt<KB, VB>;
+  static int smem_bytes(int B) { return smem_map(F::kStages * F::kStageBytes, F::kStages, B).total; }
+  // Allow the largest opt-in dynamic shared memory once per device; the
+  // per-launch size (which depends on the batch) then always fits.
+  static void ensure_attribute(int dev) {
+    static std::mutex mu;
+    static std::map<int, bool> done;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count(dev)) return;
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncSetAttribute(decode_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    done[dev] = true;
+  }
+  static int ctas_per_sm(int B) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    ensure_attribute(dev);
+    const int smem = smem_bytes(B);
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(dev, smem);
+    auto itc = cache.find(key);
+    if (itc != cache.end()) return itc->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KB, VB>, kThreads, smem) != cudaSuccess)
+      n = 1;
+    n = n < 1 ? 1 : n;
+    cache[key] = n;
+    return n;
+  }
+  static cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
+    const int smem = smem_bytes(a.B);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    ensure_attribute(dev);
+    Params p{a, a.lay.stream_ctas};
+    const int grid = a.lay.stream_ctas + a.lay.window_ctas;
+    decode_kernel<KB, VB><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+};
+
+}  // namespace
+
+int decode_ctas_per_sm_for(int k_bits, int v_bits, int B) {
+  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8>::ctas_per_sm(B);
+  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4>::ctas_per_sm(B);
+  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8>::ctas_per_sm(B);
+  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4>::ctas_per_sm(B);
+  if (k_bits == 16 && v_bits == 16) return Kernel<16, 16>::ctas_per_sm(B);
+  return 0;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  const int kb = a.c.k_bits, vb = a.c.v_bits;
+  if (kb == 8 && vb == 8) return Kernel<8, 8>::launch(a, s);
+  if (kb == 4 && vb == 4) return Kernel<4, 4>::launch(a, s);
+  if (kb == 4 && vb == 8) return Kernel<4, 8>::launch(a, s);
+  if (kb == 8 && vb == 4) return Kernel<8, 4>::launch(a, s);
+  if (kb == 16 && vb == 16) return Kernel<16, 16>::launch(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

@@ -1,0 +1,189 @@
+// Device-side building blocks shared by the kvq kernels (sm_103a).
+//   - fragment-native cache layout offsets (see include/kvq.h for the spec)
+//   - exact integer-code -> fp16 conversions done in registers
+//   - mbarrier / bulk-copy (TMA, non-tensor) wrappers with bounded waits
+//   - warp-level mma.sync wrappers
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlock = 16;
+// Wall-clock limit of any device-side wait (ns).  A decode step takes well
+// under a millisecond; reaching this means the pipeline protocol broke.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__host__ __device__ constexpr int block_bytes(int bits) { return kBlock * kHeadDim * bits / 8; }
+
+// ------------------------------------------------------------------ layout
+// Byte offset (and nibble shift for 4-bit codes) of key element (token i, dim d)
+// inside one 16-token block of one head.
+struct Loc {
+  int byte;
+  int shift;  // 0 or 4 for nibbles, 0 otherwise
+};
+
+__host__ __device__ inline Loc key_loc(int bits, int i, int d) {
+  const int g = i & 7, hi = i >> 3, t = d >> 5, e = d & 31, lane = 4 * g + t;
+  if (bits == 8) return {(2 * hi + (e >> 4)) * 512 + lane * 16 + (e & 15), 0};
+  if (bits == 4) {
+    const int nib = ((e & 7) >> 1) + 4 * (e & 1);
+    return {hi * 512 + lane * 16 + (e >> 3) * 4 + (nib >> 1), (nib & 1) * 4};
+  }
+  return {(4 * hi + (e >> 3)) * 512 + lane * 16 + 2 * (e & 7), 0};  // bf16
+}
+
+__host__ __device__ inline Loc value_loc(int bits, int i, int d) {
+  const int mt = d >> 4, r = d & 15, g = r & 7, hi = r >> 3;
+  const int t = (i & 7) >> 1, j = 2 * (i & 1) + (i >> 3), lane = 4 * g + t;
+  if (bits == 8) return {(mt >> 1) * 512 + lane * 16 + (2 * (mt & 1) + hi) * 4 + j, 0};
+  if (bits == 4) {
+    const int nib = 2 * hi + (j >> 1) + 4 * (j & 1);
+    return {(mt >> 2) * 512 + lane * 16 + (mt & 3) * 4 + (nib >> 1), (nib & 1) * 4};
+  }
+  return {mt * 512 + lane * 16 + (2 * hi + (j >> 1)) * 4 + 2 * (j & 1), 0};  // bf16
+}
+
+// ------------------------------------------------------------------ error word
+__device__ __forceinline__ void flag(uint32_t* err, uint32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ conversions
+// Four int8 codes (two's complement, bytes b0..b3 of w) -> fp16 pairs
+// lo = (b0, b1), hi = (b2, b3), exact: 1024 + (code + 128) is built by placing
+// the biased byte into the mantissa of 1024.0 (0x6400), then 1152 is subtracted.
+__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+  uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+  const uint32_t bias = 0x64806480u;  // (1152, 1152)
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
+// Eight int4 codes (nibbles n0..n7 of w) -> fp16 pairs (n0,n4) (n1,n5) (n2,n6) (n3,n7), exact.
+__device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
+                                            uint32_t& p3) {
+  const uint32_t u = w ^ 0x88888888u;  // two's complement nibble -> nibble + 8
+  const uint32_t s = u >> 8;
+  const uint32_t a = (u & 0x000F000Fu) | 0x64006400u;  // 1024 + n0, 1024 + n4
+  const uint32_t b = (u & 0x00F000F0u) | 0x64006400u;  // 1024 + 16 n1, 1024 + 16 n5
+  const uint32_t c = (s & 0x000F000Fu) | 0x64006400u;
+  const uint32_t d = (s & 0x00F000F0u) | 0x64006400u;
+  const uint32_t bias = 0x64086408u;   // 1032
+  const uint32_t sixteenth = 0x2C002C00u;  // 1/16
+  const uint32_t m72 = 0xD480D480u;    // -72 = -(1024/16 + 8)
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(p0) : "r"(a), "r"(bias));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p1) : "r"(b), "r"(sixteenth), "r"(m72));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(p2) : "r"(c), "r"(bias));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p3) : "r"(d), "r"(sixteenth), "r"(m72));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ------------------------------------------------------------------ mma.sync
+// D(16x8 f32) += A(16x16) * B(16x8), fp16 or bf16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------ mbarrier + bulk copy
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: true once the phase with `parity` has completed, false after
+// kWaitLimitNs of wall-clock time.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// One contiguous global -> shared bulk copy completing on `bar` (bytes: multiple
+// of 16; both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace kvq

@@ -1,0 +1,80 @@
+// Internal host-side interface between the C ABI (kvq_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvq {
+
+struct CacheView {
+  int H;            // KV heads
+  int num_blocks;
+  int k_bits, v_bits;
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  float* k_scales;
+  float* v_scales;
+  const float* factor;  // [H][128] or null
+  int window, window_batch;
+  uint16_t* k_win;  // bf16 ring, [window_batch][H][W][128]
+  uint16_t* v_win;
+};
+
+struct AppendArgs {
+  CacheView c;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int n;
+  const int* seq_idx;
+  const int* pos;
+  int mode;
+  const int* table;
+  int batch;
+  int mbps;
+  uint32_t* err;
+};
+
+struct DequantArgs {
+  CacheView c;
+  const int* slots;
+  int n;
+  float* k_out;
+  float* v_out;
+};
+
+// Workspace layout of a decode call (byte offsets from the workspace base).
+struct DecodeLayout {
+  int stream_ctas, window_ctas, units, slots;
+  size_t off_counter, off_m, off_l, off_o, total;
+};
+
+struct DecodeArgs {
+  CacheView c;
+  const uint16_t* q;  // bf16 [B][Hq][128]
+  int B, Hq, G;
+  const int* seq_lens;
+  const int* table;
+  int mbps;
+  void* out;
+  int out_fp32;
+  float* lse;
+  uint8_t* ws;
+  DecodeLayout lay;
+  uint32_t* err;
+};
+
+// Partial-result records hold this many query rows (G <= 8).
+constexpr int kMaxGroup = 8;
+
+DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas);
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
+// Resident decode CTAs per SM for this cache format and batch (occupancy
+// query on the current device, cached); 0 for an unsupported format.
+int decode_ctas_per_sm_for(int k_bits, int v_bits, int batch);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+}  // namespace kvq

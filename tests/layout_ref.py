@@ -1,0 +1,66 @@
+"""Test-side reader of the cache layouts, written from the layout text in
+include/kvq.h (independent of the CUDA sources): maps a stored block back to
+logical codes [token, dim] so stored codes can be compared with the oracle."""
+import numpy as np
+
+BLOCK = 16
+D = 128
+
+
+def block_bytes(bits: int) -> int:
+    return BLOCK * D * bits // 8
+
+
+def key_offsets(bits: int):
+    i = np.arange(BLOCK)[:, None]
+    d = np.arange(D)[None, :]
+    g, hi, t, e = i & 7, i >> 3, d >> 5, d & 31
+    lane = 4 * g + t
+    if bits == 8:
+        return (2 * hi + (e >> 4)) * 512 + lane * 16 + (e & 15), np.zeros((BLOCK, D), int)
+    if bits == 4:
+        nib = ((e & 7) >> 1) + 4 * (e & 1)
+        return hi * 512 + lane * 16 + (e >> 3) * 4 + nib // 2, (nib & 1) * 4
+    return (4 * hi + (e >> 3)) * 512 + lane * 16 + 2 * (e & 7), np.zeros((BLOCK, D), int)
+
+
+def value_offsets(bits: int):
+    i = np.arange(BLOCK)[:, None]
+    d = np.arange(D)[None, :]
+    mt, r = d >> 4, d & 15
+    g, hi = r & 7, r >> 3
+    t, j = (i & 7) >> 1, 2 * (i & 1) + (i >> 3)
+    lane = 4 * g + t
+    if bits == 8:
+        return (mt >> 1) * 512 + lane * 16 + (2 * (mt & 1) + hi) * 4 + j, np.zeros((BLOCK, D), int)
+    if bits == 4:
+        nib = 2 * hi + (j >> 1) + 4 * (j & 1)
+        return (mt >> 2) * 512 + lane * 16 + (mt & 3) * 4 + nib // 2, (nib & 1) * 4
+    return mt * 512 + lane * 16 + (2 * hi + (j >> 1)) * 4 + 2 * (j & 1), np.zeros((BLOCK, D), int)
+
+
+def unpack_blocks(pool: np.ndarray, bits: int, is_key: bool, heads: int) -> np.ndarray:
+    """pool: uint8 [num_blocks * heads * block_bytes] -> int32 codes
+    [num_blocks, heads, 16, 128] (two's complement), or uint16 bf16 bits for bits == 16."""
+    bb = block_bytes(bits)
+    blocks = pool.reshape(-1, heads, bb)
+    off, sh = (key_offsets if is_key else value_offsets)(bits)
+    if bits == 16:
+        lo = blocks[..., off].astype(np.uint16)
+        hi = blocks[..., off + 1].astype(np.uint16)
+        return lo | (hi << 8)
+    raw = blocks[..., off].astype(np.int32)
+    if bits == 8:
+        return np.where(raw >= 128, raw - 256, raw)
+    nib = (raw >> sh) & 0xF
+    return np.where(nib >= 8, nib - 16, nib)
+
+
+def offsets_are_a_permutation(bits: int, is_key: bool) -> bool:
+    off, sh = (key_offsets if is_key else value_offsets)(bits)
+    if bits == 16:
+        cells = np.concatenate([off.ravel(), off.ravel() + 1])
+        return np.array_equal(np.sort(cells), np.arange(block_bytes(16)))
+    cells = (off * 2 + sh // 4).ravel() if bits == 4 else off.ravel()
+    n = block_bytes(bits) * (2 if bits == 4 else 1)
+    return np.array_equal(np.sort(cells), np.arange(n))

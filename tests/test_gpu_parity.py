@@ -1,0 +1,274 @@
+"""Parity of the CUDA path (through the C ABI) against the float64 oracle.
+
+Stored codes and scales must match bit for bit; decode outputs must be within
+2e-3 max-abs (fp32 output), 2e-3 + half a bf16 ulp (bf16 output), and lse within
+2e-3.  Small cases span several 64-token stages and ragged tails; the five
+named workloads run at full size on sampled (sequence, kv head) units.
+"""
+import numpy as np
+import pytest
+
+from harness import GpuRun, compare_outputs, oracle_decode, oracle_state, small_workload
+from layout_ref import unpack_blocks
+from oracle import kvq_oracle as O
+from synth import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+SMALL = {
+    "int8_g4": small_workload("int8_g4"),
+    "int8_g1": small_workload("int8_g1", q_heads=4, kv_heads=4, len_range=(1, 200)),
+    "int4_factor_g8": small_workload("int4_factor_g8", batch=4, q_heads=16, kv_heads=2, k_bits=4, v_bits=4,
+                                     channel_factor=True),
+    "k4v8_g8_t3": small_workload("k4v8_g8_t3", batch=2, q_heads=16, kv_heads=2, k_bits=4, v_bits=8,
+                                 len_range=(100, 700), k_dist="t3"),
+    "k8v4_g2": small_workload("k8v4_g2", batch=3, q_heads=8, kv_heads=4, k_bits=8, v_bits=4),
+    "window32_int8": small_workload("window32_int8", batch=5, len_range=(1, 120), window=32,
+                                    outlier_channels=4),
+    "window128_int8": small_workload("window128_int8", batch=3, len_range=(100, 400), window=128),
+    "paged_append": small_workload("paged_append", batch=4, len_range=(1, 250), paged=True, append_one=True),
+    "bf16": small_workload("bf16", k_bits=16, v_bits=16, len_range=(1, 333)),
+    "bf16_g8": small_workload("bf16_g8", batch=2, q_heads=16, kv_heads=2, k_bits=16, v_bits=16,
+                              len_range=(50, 400), k_dist="t3"),
+}
+
+
+@pytest.fixture(scope="module")
+def runs():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            inp = make_inputs(SMALL[name])
+            cache[name] = (inp, GpuRun(inp))
+        return cache[name]
+    return get
+
+
+def check_stored_cache(inp, run, units=None, max_positions=None):
+    """Block-store codes/scales and window ring vs the oracle, bit for bit."""
+    w = inp.workload
+    pools = run.pools()
+    kc = unpack_blocks(pools["k_codes"], w.k_bits, True, w.kv_heads)
+    vc = unpack_blocks(pools["v_codes"], w.v_bits, False, w.kv_heads)
+    bs = sorted({b for b, _ in units}) if units else range(w.batch)
+    rng = np.random.default_rng(7)
+    checked = 0
+    for b in bs:
+        st = oracle_state(inp, b)
+        Lq = st["Lq"]
+        pos = np.arange(Lq)
+        if max_positions and Lq > max_positions:
+            pos = np.unique(np.concatenate([pos[:64], pos[-64:], rng.choice(Lq, max_positions, replace=False)]))
+        phys = inp.block_table[b, pos // 16]
+        tok = pos % 16
+        if w.k_bits == 16:
+            from synth import f32_to_bf16_bits
+            np.testing.assert_array_equal(kc[phys, :, tok], f32_to_bf16_bits(st["k_plain"][pos].astype(np.float32)))
+            np.testing.assert_array_equal(vc[phys, :, tok], f32_to_bf16_bits(st["v_plain"][pos].astype(np.float32)))
+        else:
+            np.testing.assert_array_equal(kc[phys, :, tok], st["k_codes"][pos])
+            np.testing.assert_array_equal(vc[phys, :, tok], st["v_codes"][pos])
+            ks = pools["k_scales"].reshape(-1, w.kv_heads, 16)[phys, :, tok]
+            vs = pools["v_scales"].reshape(-1, w.kv_heads, 16)[phys, :, tok]
+            np.testing.assert_array_equal(ks.view(np.uint32), st["k_scale"][pos].astype(np.float32).view(np.uint32))
+            np.testing.assert_array_equal(vs.view(np.uint32), st["v_scale"][pos].astype(np.float32).view(np.uint32))
+        checked += len(pos)
+        if w.window:
+            L = Lq + st["k_window"].shape[0]
+            wp = np.arange(Lq, L)
+            ring_k = pools["k_window"].reshape(w.batch, w.kv_heads, w.window, 128)[b][:, wp % w.window]
+            ring_v = pools["v_window"].reshape(w.batch, w.kv_heads, w.window, 128)[b][:, wp % w.window]
+            from synth import f32_to_bf16_bits
+            np.testing.assert_array_equal(ring_k.transpose(1, 0, 2), f32_to_bf16_bits(st["k_window"].astype(np.float32)))
+            np.testing.assert_array_equal(ring_v.transpose(1, 0, 2), f32_to_bf16_bits(st["v_window"].astype(np.float32)))
+    return checked
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_append_stores_bit_exact_codes_and_scales(runs, name):
+    inp, run = runs(name)
+    assert check_stored_cache(inp, run) > 0
+    assert run.err_bits() == 0
+
+
+@pytest.mark.parametrize("name", ["int8_g4", "int4_factor_g8", "k4v8_g8_t3", "bf16"])
+def test_dequant_returns_rn32_of_code_times_scale(runs, name):
+    inp, run = runs(name)
+    w = inp.workload
+    b = 0
+    st = oracle_state(inp, b)
+    pos = np.arange(st["Lq"])
+    slots = inp.block_table[b, pos // 16].astype(np.int64) * 16 + pos % 16
+    st_t = torch.from_numpy(slots.astype(np.int32)).cuda()
+    ko = torch.empty((len(pos), w.kv_heads, 128), dtype=torch.float32, device="cuda")
+    vo = torch.empty_like(ko)
+    run.lib.kvq_dequant(run.cache.desc, st_t, ko, vo)
+    torch.cuda.synchronize()
+    if w.k_bits == 16:
+        np.testing.assert_array_equal(ko.cpu().numpy(), st["k_plain"][pos].astype(np.float32))
+        return
+    ref_k = O.dequantize(st["k_codes"][pos], st["k_scale"][pos]).astype(np.float32)   # exact, then RN32
+    ref_v = O.dequantize(st["v_codes"][pos], st["v_scale"][pos]).astype(np.float32)
+    np.testing.assert_array_equal(ko.cpu().numpy().view(np.uint32), ref_k.view(np.uint32))
+    np.testing.assert_array_equal(vo.cpu().numpy().view(np.uint32), ref_v.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("out_fp32", [True, False])
+def test_decode_matches_oracle(runs, name, out_fp32):
+    inp, run = runs(name)
+    out, lse = run.decode(out_fp32=out_fp32)
+    ref = oracle_decode(inp)
+    worst = compare_outputs(inp, out, lse, ref, out_is_bf16=not out_fp32)
+    assert worst <= 1.0, f"max error ratio {worst:.3f}"
+    assert run.err_bits() == 0
+
+
+@pytest.mark.parametrize("name", ["int8_g4", "k4v8_g8_t3", "window32_int8", "bf16"])
+def test_decode_split_count_does_not_change_result(runs, name):
+    inp, run = runs(name)
+    base, base_lse = run.decode(out_fp32=True, stream_ctas=1)
+    for p in (2, 3, 7, 64, 0):
+        out, lse = run.decode(out_fp32=True, stream_ctas=p)
+        np.testing.assert_allclose(out, base, rtol=0, atol=2e-5)
+        np.testing.assert_allclose(lse, base_lse, rtol=0, atol=2e-5)
+
+
+@pytest.mark.parametrize("window", [0, 32])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_decode_edge_lengths(window, group):
+    lengths = np.array([0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 129], dtype=np.int32)
+    w = small_workload(f"edge_{window}_{group}", batch=len(lengths), q_heads=2 * group, kv_heads=2,
+                       seq_len=1, len_range=None, window=window)
+    inp = make_inputs(w)
+    # replace the lengths (and the matching packed K/V rows) by the edge set
+    rng = np.random.default_rng(3)
+    from synth import f32_to_bf16_bits
+    n = int(lengths.sum())
+    inp.lengths = lengths
+    inp.seq_offsets = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    inp.k = f32_to_bf16_bits(rng.standard_normal((n, 2, 128)).astype(np.float32))
+    inp.v = f32_to_bf16_bits(rng.standard_normal((n, 2, 128)).astype(np.float32))
+    nblk = np.maximum((lengths + 15) // 16, 1)
+    table = np.full((len(lengths), int(nblk.max())), -1, np.int32)
+    off = 0
+    for b, nb in enumerate(nblk):
+        table[b, :nb] = np.arange(off, off + nb)
+        off += nb
+    inp.block_table = table
+    inp.num_blocks = off
+    run = GpuRun(inp)
+    for out_fp32 in (True, False):
+        out, lse = run.decode(out_fp32=out_fp32)
+        ref = oracle_decode(inp)
+        assert compare_outputs(inp, out, lse, ref, out_is_bf16=not out_fp32) <= 1.0
+        assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert run.err_bits() == 0
+
+
+def test_step_append_equals_bulk_fill():
+    """Token-by-token window steps leave the same bytes as the bulk fill."""
+    from quantized_kv_cache_07_gb300 import _lib
+    from quantized_kv_cache_07_gb300.cache import cache_for_inputs
+    w = small_workload("step_vs_bulk", batch=3, len_range=(1, 90), window=32, k_bits=4, v_bits=4,
+                       channel_factor=True)
+    inp = make_inputs(w)
+    bulk = GpuRun(inp)
+    step_cache = cache_for_inputs(inp)
+    table = bulk.table
+    for p in range(int(inp.lengths.max())):
+        seqs = np.nonzero(inp.lengths > p)[0]
+        rows = inp.seq_offsets[seqs] + p
+        kt = torch.from_numpy(inp.k[rows].view(np.int16)).cuda().view(torch.bfloat16)
+        vt = torch.from_numpy(inp.v[rows].view(np.int16)).cuda().view(torch.bfloat16)
+        si = torch.from_numpy(seqs.astype(np.int32)).cuda()
+        po = torch.full((len(seqs),), p, dtype=torch.int32, device="cuda")
+        _lib.kvq_append(step_cache.desc, kt, vt, si, po, _lib.APPEND_STEP, table, w.batch, inp.max_blocks)
+    torch.cuda.synchronize()
+    a = bulk.pools()
+    for key in ("k_window", "v_window"):
+        np.testing.assert_array_equal(getattr(step_cache, key).view(torch.int16).cpu().numpy().view(np.uint16), a[key])
+    # block store: compare every position older than the window
+    kc_s = unpack_blocks(step_cache.k_codes.cpu().numpy(), 4, True, w.kv_heads)
+    kc_b = unpack_blocks(a["k_codes"], 4, True, w.kv_heads)
+    vc_s = unpack_blocks(step_cache.v_codes.cpu().numpy(), 4, False, w.kv_heads)
+    vc_b = unpack_blocks(a["v_codes"], 4, False, w.kv_heads)
+    ks_s = step_cache.k_scales.cpu().numpy().reshape(-1, w.kv_heads, 16)
+    ks_b = a["k_scales"].reshape(-1, w.kv_heads, 16)
+    for b in range(w.batch):
+        for p in range(max(int(inp.lengths[b]) - w.window, 0)):
+            ph, t = inp.block_table[b, p // 16], p % 16
+            np.testing.assert_array_equal(kc_s[ph, :, t], kc_b[ph, :, t])
+            np.testing.assert_array_equal(vc_s[ph, :, t], vc_b[ph, :, t])
+            np.testing.assert_array_equal(ks_s[ph, :, t], ks_b[ph, :, t])
+
+
+def test_device_errors_are_flagged_not_trapped():
+    inp = make_inputs(small_workload("errs", batch=2, len_range=(40, 80)))
+    run = GpuRun(inp)
+    bad = run.table.clone()
+    bad[1, 1] = inp.num_blocks + 5                 # block id out of range
+    from quantized_kv_cache_07_gb300.cache import DecodeWorkspace
+    w = inp.workload
+    out = torch.zeros((w.batch, w.q_heads, 128), dtype=torch.float32, device="cuda")
+    ws = DecodeWorkspace(run.cache, w.batch, w.q_heads)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run.lib.kvq_decode(run.cache.desc, run.q, w.batch, w.q_heads, run.lens, bad, inp.max_blocks, out,
+                       workspace=ws.buf, workspace_bytes=ws.nbytes, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & run.lib.KVQ_DEVERR_BLOCK_ID
+    # a length beyond the table's capacity is clamped and flagged
+    err.zero_()
+    long = run.lens.clone()
+    long[0] = inp.max_blocks * 16 + 100
+    run.lib.kvq_decode(run.cache.desc, run.q, w.batch, w.q_heads, long, run.table, inp.max_blocks, out,
+                       workspace=ws.buf, workspace_bytes=ws.nbytes, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & run.lib.KVQ_DEVERR_SEQ_LEN
+    # the workspace counters are back at zero: a normal call still matches the oracle
+    o2, l2 = run.decode(out_fp32=True)
+    assert compare_outputs(inp, o2, l2, oracle_decode(inp), out_is_bf16=False) <= 1.0
+
+
+def test_host_validation_errors():
+    inp = make_inputs(small_workload("val", batch=1, len_range=(10, 10)))
+    run = GpuRun(inp)
+    lib = run.lib
+    w = inp.workload
+    out = torch.zeros((1, w.q_heads, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(lib.KvqError) as e:
+        lib.kvq_decode(run.cache.desc, run.q, 1, w.q_heads, run.lens, run.table, inp.max_blocks, out,
+                       workspace=None, workspace_bytes=0)
+    assert e.value.status == lib.KVQ_ERR_WORKSPACE
+    with pytest.raises(lib.KvqError) as e:
+        lib.kvq_decode(run.cache.desc, run.q, 1, 3, run.lens, run.table, inp.max_blocks, out)
+    assert e.value.status == lib.KVQ_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- full-size named workloads
+def _sample_units(w, k, seed=11):
+    rng = np.random.default_rng(seed)
+    units = {(int(b), int(h)) for b, h in zip(rng.integers(0, w.batch, k), rng.integers(0, w.kv_heads, k))}
+    units.add((w.batch - 1, w.kv_heads - 1))
+    return units
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_full_size_workload(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    run = GpuRun(inp)
+    units = _sample_units(w, 6 if w.batch * w.kv_heads > 8 else 4)
+    assert check_stored_cache(inp, run, units=units, max_positions=2048) > 0
+    out, lse = run.decode(out_fp32=False)
+    ref = oracle_decode(inp, units)
+    worst = compare_outputs(inp, out, lse, ref, out_is_bf16=True)
+    assert worst <= 1.0, f"max error ratio {worst:.3f}"
+    # properties that hold for every unit: finite outputs, lse finite where L > 0
+    assert np.all(np.isfinite(out))
+    assert run.err_bits() == 0
