@@ -131,11 +131,17 @@ def test_decode_matches_oracle(runs, name, out_fp32):
 
 @pytest.mark.parametrize("name", ["int8_g4", "k4v8_g8_t3", "window32_int8", "bf16"])
 def test_decode_split_count_does_not_change_result(runs, name):
+    """Any split of the token range gives the same attention up to the rounding
+    of the fp16 value weights p*s_v, which are rounded relative to the running
+    maximum of each split: each weight moves by at most 2^-11 relative, so the
+    outputs of two splits differ by at most 2^-11 * max|v_hat| (+ fp32 noise)."""
     inp, run = runs(name)
+    vmax = float(np.abs(O.bf16_to_f64(inp.v)).max()) * (1 + 1 / 14)
+    atol = 2.0 ** -11 * vmax + 1e-5
     base, base_lse = run.decode(out_fp32=True, stream_ctas=1)
     for p in (2, 3, 7, 64, 0):
         out, lse = run.decode(out_fp32=True, stream_ctas=p)
-        np.testing.assert_allclose(out, base, rtol=0, atol=2e-5)
+        np.testing.assert_allclose(out, base, rtol=0, atol=atol)
         np.testing.assert_allclose(lse, base_lse, rtol=0, atol=2e-5)
 
 
