@@ -195,6 +195,8 @@ def main():
     ap.add_argument("--no-bf16", action="store_true", help="skip the same-design bf16-cache comparison run")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--stream-ctas", type=int, default=0)
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of untimed steps before the timed region (clock sampling, steady state)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -282,12 +284,14 @@ def main():
             step(k)
         torch.cuda.synchronize()
         # soak (untimed) so the clock sampler sees the load for >= ~1 s
-        t_est = time.perf_counter()
-        for k in range(20):
-            step(k)
-        torch.cuda.synchronize()
-        per = max((time.perf_counter() - t_est) / 20, 1e-6)
-        soak = int(min(max(1.0 / per, 0), 200000))
+        soak = 0
+        if args.soak > 0:
+            t_est = time.perf_counter()
+            for k in range(20):
+                step(k)
+            torch.cuda.synchronize()
+            per = max((time.perf_counter() - t_est) / 20, 1e-6)
+            soak = int(min(max(args.soak / per, 0), 200000))
         K = args.steps
         dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -47,8 +47,11 @@
  *     complement: int8 in [-127,127], int4 in [-8,7] (-8 never produced).
  *   Scale pool  : float [num_blocks][num_kv_heads][16], natural token order
  *                 (absent for a bf16 cache).
- *   Window ring : bf16 [window_batch][num_kv_heads][window][128], plain order;
- *                 position p of sequence b lives in slot p % window.
+ *   Window ring : bf16 [window_batch][num_kv_heads][window / 16][4096 bytes]:
+ *                 window / 16 blocks per (sequence, head) for keys and for
+ *                 values, each in the bf16 key / value block order above;
+ *                 position p of sequence b lives in slot p % window, which is
+ *                 token (slot % 16) of ring block slot / 16.
  *   Block table : int32 [batch][max_blocks_per_seq]; logical block j of
  *                 sequence b is physical block block_table[b*max_blocks_per_seq+j].
  *                 Position p of a sequence is token p % 16 of logical block p / 16.
@@ -99,9 +102,10 @@ typedef struct {
   float* k_scales;        /* per-token key scales; NULL for a bf16 cache            */
   float* v_scales;        /* per-token value scales; NULL for a bf16 cache          */
   const float* k_channel_factor; /* [num_kv_heads][128] positive, or NULL           */
-  int32_t window;         /* recent-token bf16 window W (0 = none, 1..128)          */
+  int32_t window;         /* recent-token bf16 window W: 0 = none, or 16..128 in    */
+                          /* steps of 16                                            */
   int32_t window_batch;   /* first dimension of the ring buffers (sequences)        */
-  void* k_window;         /* bf16 [window_batch][H_kv][W][128] or NULL if W == 0    */
+  void* k_window;         /* bf16 ring (layout above), or NULL if W == 0            */
   void* v_window;
 } kvq_cache_desc;
 

@@ -13,7 +13,7 @@ namespace {
 using kvq::kHeadDim;
 
 constexpr int kMaxBatch = 4096;  // sequence geometry is staged in shared memory
-constexpr int kMaxWindow = 128;  // one window token per thread of the window CTA
+constexpr int kMaxWindow = 128;  // window ring: at most 8 bf16 blocks per (sequence, kv head)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -39,7 +39,7 @@ kvq_status check_cache(const kvq_cache_desc* c) {
     if (!aligned16(c->k_channel_factor)) return KVQ_ERR_ALIGNMENT;
   }
   if (c->window < 0) return KVQ_ERR_INVALID_ARG;
-  if (c->window > kMaxWindow) return KVQ_ERR_UNSUPPORTED;
+  if (c->window > kMaxWindow || c->window % 16 != 0) return KVQ_ERR_UNSUPPORTED;
   if (c->window > 0) {
     if (!c->k_window || !c->v_window || c->window_batch < 1) return KVQ_ERR_INVALID_ARG;
     if (!aligned16(c->k_window) || !aligned16(c->v_window)) return KVQ_ERR_ALIGNMENT;
@@ -60,20 +60,27 @@ kvq::CacheView view(const kvq_cache_desc* c) {
   v.factor = c->k_channel_factor;
   v.window = c->window;
   v.window_batch = c->window_batch;
-  v.k_win = static_cast<uint16_t*>(c->k_window);
-  v.v_win = static_cast<uint16_t*>(c->v_window);
+  v.k_win = static_cast<uint8_t*>(c->k_window);
+  v.v_win = static_cast<uint8_t*>(c->v_window);
   return v;
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Stream CTAs for the current device: SMs x resident CTAs (0 on failure).
+// Stream CTAs for one wave of `slots` resident CTAs: the window CTAs (one per
+// unit, launched first) take their slots out of the wave, down to half of it.
+int stream_ctas_for(int slots, int window_ctas) {
+  const int left = slots - window_ctas;
+  return left > slots / 2 ? left : (slots / 2 > 0 ? slots / 2 : 1);
+}
+
+// Stream CTAs for the current device (0 on failure).
 int auto_stream_ctas(const kvq_cache_desc* c, int batch) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, batch);
-  return sms * per;
+  return stream_ctas_for(sms * per, c->window > 0 ? batch * c->num_kv_heads : 0);
 }
 
 kvq_status check_decode_shape(const kvq_cache_desc* c, int batch, int q_heads) {
@@ -171,7 +178,7 @@ kvq_status kvq_make_decode_plan(int32_t batch, int32_t q_heads, int32_t num_kv_h
   int P = stream_ctas;
   if (P <= 0) {
     if (num_sms < 1 || ctas_per_sm < 1) return KVQ_ERR_INVALID_ARG;
-    P = num_sms * ctas_per_sm;
+    P = stream_ctas_for(num_sms * ctas_per_sm, window > 0 ? batch * num_kv_heads : 0);
   }
   const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, num_kv_heads, window, P);
   plan->stream_ctas = L.stream_ctas;

@@ -171,18 +171,29 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     write_block_store(a, is_key, b, p, h, xb, lane);
     return;
   }
+  // window ring: slot p % W is token (slot % 16) of ring block slot / 16, stored
+  // in the fragment-native bf16 block layout
   const int W = a.c.window;
-  uint16_t* ring = (is_key ? a.c.k_win : a.c.v_win) + ((size_t(b) * H + h) * W + (p % W)) * kHeadDim + 4 * lane;
+  const int slot = p % W;
+  uint8_t* ring = (is_key ? a.c.k_win : a.c.v_win) +
+                  ((size_t(b) * H + h) * (W / kBlock) + slot / kBlock) * block_bytes(16);
+  const int tok = slot % kBlock;
+  int off[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const Loc L = is_key ? key_loc(16, tok, 4 * lane + j) : value_loc(16, tok, 4 * lane + j);
+    off[j] = L.byte;
+  }
   if (a.mode == KVQ_APPEND_STEP && p >= W) {
     // the token at p - W occupies this ring slot: it leaves the window now
-    const uint2 ov = *reinterpret_cast<const uint2*>(ring);
-    uint16_t ob[4] = {uint16_t(ov.x & 0xFFFF), uint16_t(ov.x >> 16), uint16_t(ov.y & 0xFFFF),
-                      uint16_t(ov.y >> 16)};
+    uint16_t ob[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ob[j] = *reinterpret_cast<const uint16_t*>(ring + off[j]);
     write_block_store(a, is_key, b, p - W, h, ob, lane);
     __syncwarp();
   }
-  *reinterpret_cast<uint2*>(ring) = make_uint2(uint32_t(xb[0]) | (uint32_t(xb[1]) << 16),
-                                               uint32_t(xb[2]) | (uint32_t(xb[3]) << 16));
+#pragma unroll
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint16_t*>(ring + off[j]) = xb[j];
 }
 
 __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {

@@ -64,7 +64,7 @@ struct Fmt {
   static constexpr int kSCB = kBf16 ? 0 : kBlock * 4;  // scale bytes per block per tensor
   static constexpr int kPerBlock = kKBB + kVBB + 2 * kSCB;
   static constexpr int kStageBytes = kConsumerWarps * kPerBlock;
-  static constexpr int kStagesRaw = 65536 / kStageBytes;
+  static constexpr int kStagesRaw = 53248 / kStageBytes;  // ~52 KB ring: 3 CTAs per SM
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   // stage sub-buffers
   static constexpr int kOffK = 0;
@@ -107,6 +107,8 @@ __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, i
 template <int KB>
 __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&qf)[16], float (&acc)[4],
                                             int lane) {
+  // two accumulators halve the dependent MMA chain; summed at the end
+  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
   const uint4* p = reinterpret_cast<const uint4*>(kb) + lane;
   if constexpr (KB == 8) {
     const uint4 r0a = p[0], r0b = p[32], r1a = p[64], r1b = p[96];
@@ -117,7 +119,8 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
       uint32_t a0, a1, a2, a3;
       s8x4_to_f16(g0[kk], a0, a2);
       s8x4_to_f16(g8[kk], a1, a3);
-      mma_f16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+      if (kk & 1) mma_f16(acc2, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+      else mma_f16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
     }
   } else if constexpr (KB == 4) {
     const uint4 r0 = p[0], r1 = p[32];
@@ -129,7 +132,7 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
       s4x8_to_f16(g0[wi], x0, x1, x2, x3);
       s4x8_to_f16(g8[wi], y0, y1, y2, y3);
       mma_f16(acc, x0, y0, x1, y1, qf[4 * wi], qf[4 * wi + 1]);
-      mma_f16(acc, x2, y2, x3, y3, qf[4 * wi + 2], qf[4 * wi + 3]);
+      mma_f16(acc2, x2, y2, x3, y3, qf[4 * wi + 2], qf[4 * wi + 3]);
     }
   } else {
     uint4 c[8];
@@ -140,9 +143,12 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
       const uint4 lo = c[kk >> 1], hi = c[4 + (kk >> 1)];
       const uint32_t a0 = (kk & 1) ? lo.z : lo.x, a2 = (kk & 1) ? lo.w : lo.y;
       const uint32_t a1 = (kk & 1) ? hi.z : hi.x, a3 = (kk & 1) ? hi.w : hi.y;
-      mma_bf16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+      if (kk & 1) mma_bf16(acc2, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+      else mma_bf16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
     }
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
 }
 
 template <int VB>
@@ -185,8 +191,12 @@ __device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint
 
 struct Params {
   DecodeArgs a;
-  int P;  // stream CTAs
+  int P;   // stream CTAs launched (after the window CTAs)
+  int Uw;  // window CTAs launched first in the grid (one per unit, 0 without a window)
 };
+
+// A stream CTA owns at least this many blocks (fewer, deeper splits for tiny problems).
+constexpr int kMinBlocksPerCta = 8;
 
 // CTA-consumer barrier on an mbarrier (count = kConsumers), bounded wait.
 __device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase) {
@@ -209,40 +219,10 @@ __device__ __forceinline__ void write_out(const DecodeArgs& a, int b, int hq, in
   if (d == 0 && a.lse) a.lse[size_t(b) * a.Hq + hq] = (M + log2f(l)) * kLn2;
 }
 
-// Merge every partial record of unit u (run by the last CTA to finish it).
-__device__ void merge_unit(const DecodeArgs& a, int u, long long c0, long long c1, bool has_win, int P, int tid,
-                           int nthreads) {
-  // P: launched stream CTAs (the window records sit after P + units slots)
-  const int b = u / a.c.H, h = u % a.c.H;
-  const float* pm = reinterpret_cast<const float*>(a.ws + a.lay.off_m);
-  const float* pl = reinterpret_cast<const float*>(a.ws + a.lay.off_l);
-  const float* po = reinterpret_cast<const float*>(a.ws + a.lay.off_o);
-  const int wslot = P + a.lay.units + u;
-  for (int e = tid; e < a.G * kHeadDim; e += nthreads) {
-    const int q = e / kHeadDim, d = e % kHeadDim;
-    float M = kNegInf;
-    for (long long j = c0; j <= c1; ++j) M = fmaxf(M, __ldcg(pm + (j + u) * kMaxGroup + q));
-    if (has_win) M = fmaxf(M, __ldcg(pm + size_t(wslot) * kMaxGroup + q));
-    float l = 0.f, o = 0.f;
-    for (long long j = c0; j <= c1; ++j) {
-      const size_t s = size_t(j + u);
-      const float w = exp2f(__ldcg(pm + s * kMaxGroup + q) - M);
-      l += w * __ldcg(pl + s * kMaxGroup + q);
-      o += w * __ldcg(po + (s * kMaxGroup + q) * kHeadDim + d);
-    }
-    if (has_win) {
-      const size_t s = size_t(wslot);
-      const float w = exp2f(__ldcg(pm + s * kMaxGroup + q) - M);
-      l += w * __ldcg(pl + s * kMaxGroup + q);
-      o += w * __ldcg(po + (s * kMaxGroup + q) * kHeadDim + d);
-    }
-    write_out(a, b, h * a.G + q, d, o, l, M);
-  }
-}
-
-// Number of partial records unit u has (stream segments + window).
+// Partial records of unit u: stream segments c0..c1 (slot j + u) and, with a
+// window, one window record (slot P + units + u).
 __device__ __forceinline__ void unit_segments(const DecodeArgs& a, const int* len_s, const int* pre_s, int u,
-                                              long long T, int P, long long& c0, long long& c1, int& nseg,
+                                              long long T, int Pe, long long& c0, long long& c1, int& nseg,
                                               bool& has_win) {
   const int H = a.c.H, b = u / H, h = u % H;
   const int nblk = pre_s[b + 1] - pre_s[b];
@@ -251,34 +231,362 @@ __device__ __forceinline__ void unit_segments(const DecodeArgs& a, const int* le
   c0 = 0;
   c1 = -1;
   if (nblk > 0) {
-    c0 = cta_of(start, T, P);
-    c1 = cta_of(start + nblk - 1, T, P);
+    c0 = cta_of(start, T, Pe);
+    c1 = cta_of(start + nblk - 1, T, Pe);
     nseg = int(c1 - c0 + 1);
   }
   has_win = a.c.window > 0 && len_s[b] > 0;
   nseg += has_win ? 1 : 0;
 }
 
+// Online-softmax state of one consumer warp; each thread holds queries 2t, 2t+1.
+struct WarpState {
+  float O[8][4];
+  float m0, m1, l0, l1;
+  __device__ __forceinline__ void reset() {
+    m0 = m1 = kNegInf;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+  }
+};
+
+// One 16-token block: scores on the codes, per-token key scale after the dot
+// product, online softmax, value scale folded into the weight, value MMA.
 template <int KB, int VB>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
+__device__ __forceinline__ void process_block(const uint8_t* kb, const uint8_t* vb, const float* ks, const float* vs,
+                                              int valid, const uint32_t (&qf)[16], float qs0, float qs1,
+                                              WarpState& st, int lane, uint32_t* err) {
+  constexpr bool kBf16 = (KB == 16);
+  const int g = lane >> 2, t = lane & 3;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  score_block<KB>(kb, qf, acc, lane);
+  float sk0 = 1.f, sk1 = 1.f, sv0 = 1.f, sv1 = 1.f;
+  if constexpr (!kBf16) {
+    sk0 = ks[g];
+    sk1 = ks[g + 8];
+    sv0 = vs[g];
+    sv1 = vs[g + 8];
+  }
+  const bool v0 = g < valid, v1 = g + 8 < valid;
+  const float x00 = v0 ? acc[0] * (sk0 * qs0) : kNegInf;
+  const float x01 = v0 ? acc[1] * (sk0 * qs1) : kNegInf;
+  const float x10 = v1 ? acc[2] * (sk1 * qs0) : kNegInf;
+  const float x11 = v1 ? acc[3] * (sk1 * qs1) : kNegInf;
+  float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+  }
+  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+  if (__any_sync(kFull, (mn0 > st.m0) || (mn1 > st.m1))) {
+    const float al0 = (mn0 == kNegInf) ? 1.f : exp2f(st.m0 - mn0);
+    const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(st.m1 - mn1);
+    st.l0 *= al0;
+    st.l1 *= al1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      st.O[i][0] *= al0;
+      st.O[i][2] *= al0;
+      st.O[i][1] *= al1;
+      st.O[i][3] *= al1;
+    }
+    st.m0 = mn0;
+    st.m1 = mn1;
+  }
+  const float base0 = (st.m0 == kNegInf) ? 0.f : st.m0, base1 = (st.m1 == kNegInf) ? 0.f : st.m1;
+  const float p00 = exp2f(x00 - base0), p10 = exp2f(x10 - base0);
+  const float p01 = exp2f(x01 - base1), p11 = exp2f(x11 - base1);
+  st.l0 += p00 + p10;
+  st.l1 += p01 + p11;
+  uint32_t pk0, pk1, pk0lo = 0, pk1lo = 0;
+  if constexpr (kBf16) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(p00, p10), h1 = __floats2bfloat162_rn(p01, p11);
+    pk0 = *reinterpret_cast<const uint32_t*>(&h0);
+    pk1 = *reinterpret_cast<const uint32_t*>(&h1);
+    pk0lo = pack_bf162(p00 - __low2float(h0), p10 - __high2float(h0));
+    pk1lo = pack_bf162(p01 - __low2float(h1), p11 - __high2float(h1));
+  } else {
+    if ((v0 && sv0 > 65504.f) || (v1 && sv1 > 65504.f)) flag(err, KVQ_DEVERR_RANGE);
+    pk0 = pack_half2(v0 ? p00 * sv0 : 0.f, v1 ? p10 * sv1 : 0.f);
+    pk1 = pack_half2(v0 ? p01 * sv0 : 0.f, v1 ? p11 * sv1 : 0.f);
+  }
+  // transpose the weights from the score accumulator layout (token rows, query
+  // columns) into the B-operand layout of the value contraction
+  const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
+  const uint32_t r00 = __shfl_sync(kFull, pk0, src0), r01 = __shfl_sync(kFull, pk1, src0);
+  const uint32_t r10 = __shfl_sync(kFull, pk0, src1), r11 = __shfl_sync(kFull, pk1, src1);
+  const uint32_t b0 = (g & 1) ? r01 : r00, b1 = (g & 1) ? r11 : r10;
+  uint32_t b0lo = 0, b1lo = 0;
+  if constexpr (kBf16) {
+    const uint32_t q00 = __shfl_sync(kFull, pk0lo, src0), q01 = __shfl_sync(kFull, pk1lo, src0);
+    const uint32_t q10 = __shfl_sync(kFull, pk0lo, src1), q11 = __shfl_sync(kFull, pk1lo, src1);
+    b0lo = (g & 1) ? q01 : q00;
+    b1lo = (g & 1) ? q11 : q10;
+  }
+  value_block<VB>(vb, b0, b1, b0lo, b1lo, st.O, lane);
+}
+
+// Consumer warps write the query group of unit (b, h) into shared memory as
+// B-operand rows: fp16 scaled by an exact power of two for code blocks (with
+// the per-channel key factor applied), or the raw bf16 values for bf16 blocks.
+template <bool kBf16Q>
+__device__ __forceinline__ void stage_query(const DecodeArgs& a, int b, int h, uint16_t* qh, float* qs, int warp,
+                                            int lane) {
+  for (int q = warp; q < kMaxGroup; q += kConsumerWarps) {
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (q < a.G) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(a.q + (size_t(b) * a.Hq + h * a.G + q) * kHeadDim + 4 * lane);
+      x[0] = __uint_as_float(raw.x << 16);
+      x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+      x[2] = __uint_as_float(raw.y << 16);
+      x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    }
+    uint2 packed;
+    if constexpr (kBf16Q) {
+      packed.x = pack_bf162(x[0], x[1]);
+      packed.y = pack_bf162(x[2], x[3]);
+      if (lane == 0) qs[q] = kLog2e * kInvSqrtD;
+    } else {
+      if (a.c.factor) {
+        const float4 c = *reinterpret_cast<const float4*>(a.c.factor + h * kHeadDim + 4 * lane);
+        x[0] *= c.x;
+        x[1] *= c.y;
+        x[2] *= c.z;
+        x[3] *= c.w;
+      }
+      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
+      int e = 0;
+      if (am > 0.f) {
+        int ex;
+        frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
+        e = 15 - ex;      // am * 2^e in [2^14, 2^15)
+      }
+      packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
+      packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+      if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
+    }
+    *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
+  }
+}
+
+__device__ __forceinline__ void load_query(const uint16_t* qh, const float* qs, uint32_t (&qf)[16], float& qs0,
+                                           float& qs1, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint4* qp = reinterpret_cast<const uint4*>(qh + g * kHeadDim + 32 * t);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = qp[i];
+    qf[4 * i] = v.x;
+    qf[4 * i + 1] = v.y;
+    qf[4 * i + 2] = v.z;
+    qf[4 * i + 3] = v.w;
+  }
+  qs0 = qs[2 * t];
+  qs1 = qs[2 * t + 1];
+}
+
+// Shared scratch used by the combine and the merge.
+struct Scratch {
+  float* merge_o;  // [4 warps][8][128]
+  float* merge_m;  // [4][8]
+  float* merge_l;  // [4][8]
+  int* misc;
+  uint64_t* cbar;
+};
+
+// Log-sum-exp merge of every partial record of unit u (run by the 128
+// consumer threads of the last CTA to finish the unit; thread = dim).
+__device__ __noinline__ bool merge_unit(const DecodeArgs& a, int u, long long c0, long long c1, bool has_win, int P,
+                           const Scratch& sc, uint32_t& cphase, int warp, int lane, int tid) {
+  const int G = a.G, H = a.c.H;
+  const int b = u / H, h = u % H;
+  const int ns = c1 >= c0 ? int(c1 - c0 + 1) : 0;
+  const int ntot = ns + (has_win ? 1 : 0);
+  const size_t wslot = size_t(P) + a.lay.units + u;
+  const float* pm = reinterpret_cast<const float*>(a.ws + a.lay.off_m);
+  const float* pl = reinterpret_cast<const float*>(a.ws + a.lay.off_l);
+  const float* po = reinterpret_cast<const float*>(a.ws + a.lay.off_o);
+  float* Ms = sc.merge_m;          // [8]
+  float* Ls = sc.merge_m + 8;      // [8]
+  float* Wt = sc.merge_o;          // [128][8] weights of one chunk of records
+  float* red = sc.merge_o + 1024;  // [4][8] cross-warp reduction
+  // pass 1: maximum of the record maxima per query
+  float mx[kMaxGroup];
+#pragma unroll
+  for (int q = 0; q < kMaxGroup; ++q) mx[q] = kNegInf;
+  for (int s = tid; s < ntot; s += kConsumers) {
+    const size_t slot = s < ns ? size_t(c0 + s + u) : wslot;
+#pragma unroll
+    for (int q = 0; q < kMaxGroup; ++q)
+      if (q < G) mx[q] = fmaxf(mx[q], __ldcg(pm + slot * kMaxGroup + q));
+  }
+#pragma unroll
+  for (int q = 0; q < kMaxGroup; ++q) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx[q] = fmaxf(mx[q], __shfl_xor_sync(kFull, mx[q], o));
+    if (lane == 0) red[warp * kMaxGroup + q] = mx[q];
+  }
+  if (!consumer_sync(sc.cbar, cphase)) return false;
+  if (tid < kMaxGroup) {
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red[w * kMaxGroup + tid]);
+    Ms[tid] = M;
+  }
+  if (!consumer_sync(sc.cbar, cphase)) return false;
+  // pass 2: weights 2^(m_r - M) per chunk of records, weighted sums
+  float o[kMaxGroup], lp[kMaxGroup];
+#pragma unroll
+  for (int q = 0; q < kMaxGroup; ++q) o[q] = lp[q] = 0.f;
+  for (int base = 0; base < ntot; base += kConsumers) {
+    const int s = base + tid;
+    if (s < ntot) {
+      const size_t slot = s < ns ? size_t(c0 + s + u) : wslot;
+#pragma unroll
+      for (int q = 0; q < kMaxGroup; ++q) {
+        float w = 0.f;
+        if (q < G) {
+          w = exp2f(__ldcg(pm + slot * kMaxGroup + q) - Ms[q]);
+          lp[q] += w * __ldcg(pl + slot * kMaxGroup + q);
+        }
+        Wt[tid * kMaxGroup + q] = w;
+      }
+    }
+    if (!consumer_sync(sc.cbar, cphase)) return false;
+    const int cnt = min(kConsumers, ntot - base);
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const int s2 = base + k;
+      const size_t slot = s2 < ns ? size_t(c0 + s2 + u) : wslot;
+#pragma unroll
+      for (int q = 0; q < kMaxGroup; ++q)
+        if (q < G) o[q] += Wt[k * kMaxGroup + q] * __ldcg(po + (slot * kMaxGroup + q) * kHeadDim + tid);
+    }
+    if (!consumer_sync(sc.cbar, cphase)) return false;
+  }
+#pragma unroll
+  for (int q = 0; q < kMaxGroup; ++q) {
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) lp[q] += __shfl_xor_sync(kFull, lp[q], o2);
+    if (lane == 0) red[warp * kMaxGroup + q] = lp[q];
+  }
+  if (!consumer_sync(sc.cbar, cphase)) return false;
+  if (tid < kMaxGroup) {
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) l += red[w * kMaxGroup + tid];
+    Ls[tid] = l;
+  }
+  if (!consumer_sync(sc.cbar, cphase)) return false;
+  for (int q = 0; q < G; ++q) write_out(a, b, h * G + q, tid, o[q], Ls[q], Ms[q]);
+  return true;
+}
+
+// Combine the four consumer warps' states of unit u and emit them: the final
+// output if this is the unit's only record, else a partial record in `slot`
+// followed by the arrival ticket; the last CTA to arrive merges the unit.
+__device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& st, int u, size_t slot, const int* len_s,
+                               const int* pre_s, long long T, int Pe, int P, const Scratch& sc, uint32_t& cphase,
+                               int warp, int lane, int tid) {
+  const int g = lane >> 2, t = lane & 3;
+  const int G = a.G, H = a.c.H;
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    st.l0 += __shfl_xor_sync(kFull, st.l0, o);
+    st.l1 += __shfl_xor_sync(kFull, st.l1, o);
+  }
+  if (g == 0) {
+    sc.merge_m[warp * kMaxGroup + 2 * t] = st.m0;
+    sc.merge_m[warp * kMaxGroup + 2 * t + 1] = st.m1;
+    sc.merge_l[warp * kMaxGroup + 2 * t] = st.l0;
+    sc.merge_l[warp * kMaxGroup + 2 * t + 1] = st.l1;
+  }
+  float* ow = sc.merge_o + warp * kMaxGroup * kHeadDim;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    ow[(2 * t) * kHeadDim + 16 * mt + g] = st.O[mt][0];
+    ow[(2 * t + 1) * kHeadDim + 16 * mt + g] = st.O[mt][1];
+    ow[(2 * t) * kHeadDim + 16 * mt + g + 8] = st.O[mt][2];
+    ow[(2 * t + 1) * kHeadDim + 16 * mt + g + 8] = st.O[mt][3];
+  }
+  if (!consumer_sync(sc.cbar, cphase)) return false;
+  long long c0, c1;
+  int nseg;
+  bool has_win;
+  unit_segments(a, len_s, pre_s, u, T, Pe, c0, c1, nseg, has_win);
+  const int b = u / H, h = u % H;
+  float* pm = reinterpret_cast<float*>(a.ws + a.lay.off_m);
+  float* pl = reinterpret_cast<float*>(a.ws + a.lay.off_l);
+  float* po = reinterpret_cast<float*>(a.ws + a.lay.off_o);
+  const int d = tid;
+  for (int q = 0; q < G; ++q) {
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sc.merge_m[w * kMaxGroup + q]);
+    float l = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = sc.merge_m[w * kMaxGroup + q];
+      const float al = (mw == kNegInf) ? 0.f : exp2f(mw - M);
+      l += al * sc.merge_l[w * kMaxGroup + q];
+      o += al * sc.merge_o[(w * kMaxGroup + q) * kHeadDim + d];
+    }
+    if (nseg == 1) {
+      write_out(a, b, h * G + q, d, o, l, M);
+    } else {
+      po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
+      if (d == 0) {
+        pm[slot * kMaxGroup + q] = M;
+        pl[slot * kMaxGroup + q] = l;
+      }
+    }
+  }
+  if (!consumer_sync(sc.cbar, cphase)) return false;  // merge_o free again
+  if (nseg > 1) {
+    __threadfence();
+    if (!consumer_sync(sc.cbar, cphase)) return false;
+    if (tid == 0) {
+      int* cnt = reinterpret_cast<int*>(a.ws + a.lay.off_counter);
+      const int tk = atomicAdd(&cnt[u], 1);
+      sc.misc[0] = (tk == nseg - 1);
+    }
+    if (!consumer_sync(sc.cbar, cphase)) return false;
+    const bool last = sc.misc[0] != 0;
+    if (!consumer_sync(sc.cbar, cphase)) return false;  // everyone has read misc[0]
+    if (last) {
+      __threadfence();
+      if (!merge_unit(a, u, c0, c1, has_win, P, sc, cphase, warp, lane, tid)) return false;
+      if (tid == 0) reinterpret_cast<int*>(a.ws + a.lay.off_counter)[u] = 0;
+    }
+  }
+  return true;
+}
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   using F = Fmt<KB, VB>;
   constexpr int S = F::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   const DecodeArgs& a = prm.a;
-  const int P = prm.P;
+  const int P = prm.P, Uw = prm.Uw;
   const int H = a.c.H, G = a.G, B = a.B;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const SmemMap mp = smem_map(S * F::kStageBytes, S, B);
-  float* merge_o = reinterpret_cast<float*>(smem + mp.merge_o);
-  float* merge_m = reinterpret_cast<float*>(smem + mp.merge_ml);
-  float* merge_l = merge_m + kConsumerWarps * kMaxGroup;
+  Scratch sc;
+  sc.merge_o = reinterpret_cast<float*>(smem + mp.merge_o);
+  sc.merge_m = reinterpret_cast<float*>(smem + mp.merge_ml);
+  sc.merge_l = sc.merge_m + kConsumerWarps * kMaxGroup;
   uint16_t* qh = reinterpret_cast<uint16_t*>(smem + mp.qh);
   float* qs = reinterpret_cast<float*>(smem + mp.qs);
   int4* hdr = reinterpret_cast<int4*>(smem + mp.hdr);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + mp.bars);
   uint64_t* empty = full + S;
-  uint64_t* cbar = empty + S;
-  int* misc = reinterpret_cast<int*>(smem + mp.misc);
+  sc.cbar = empty + S;
+  sc.misc = reinterpret_cast<int*>(smem + mp.misc);
   int* len_s = reinterpret_cast<int*>(smem + mp.len);
   int* pre_s = reinterpret_cast<int*>(smem + mp.pre);
 
@@ -306,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
-    mbar_init(cbar, kConsumers);
-    misc[0] = 0;  // ticket result
+    mbar_init(sc.cbar, kConsumers);
+    sc.misc[0] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -328,116 +636,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
   __syncthreads();
   const long long T = (long long)H * pre_s[B];
   const int U = B * H;
-  // Effective stream split: never more CTAs than blocks, so every CTA below Pe
-  // owns at least one block and a unit's owners are exactly the CTAs c0..c1.
-  const int Pe = int(T < (long long)P ? T : (long long)P);
-  const float* pfac = a.c.factor;
+  // Effective stream split: never more CTAs than blocks / kMinBlocksPerCta, so
+  // every CTA below Pe owns blocks and a unit's owners are exactly c0..c1.
+  const long long cap_ctas = (T + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
+  const int Pe = int(cap_ctas < (long long)P ? cap_ctas : (long long)P);
+  uint32_t cphase = 0;
 
   // ==================================================================== window CTAs
-  if (blockIdx.x >= P) {
-    const int u = blockIdx.x - P;
+  if ((int)blockIdx.x < Uw) {
+    const int u = blockIdx.x;
     const int b = u / H, h = u % H;
     const int L = len_s[b];
-    if (L <= 0) return;
+    if (L <= 0 || warp >= kConsumerWarps) return;  // the producer warp has no role here
     const int nw = min(L, W);
-    float* qf = merge_o;                      // [8][128] fp32 query
-    float* sc = merge_o + kMaxGroup * kHeadDim;  // [8][128] scores -> weights
-    for (int e = tid; e < G * kHeadDim; e += kThreads) {
-      const int q = e / kHeadDim, d = e % kHeadDim;
-      qf[e] = __uint_as_float(uint32_t(a.q[(size_t(b) * a.Hq + h * G + q) * kHeadDim + d]) << 16);
+    const int nwb = (nw + kBlock - 1) / kBlock;
+    stage_query<true>(a, b, h, qh, qs, warp, lane);
+    if (!consumer_sync(sc.cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
+    uint32_t qf[16];
+    float qs0, qs1;
+    load_query(qh, qs, qf, qs0, qs1, lane);
+    WarpState st;
+    st.reset();
+    const size_t ring0 = size_t(u) * (W / kBlock);
+    for (int j = warp; j < nwb; j += kConsumerWarps) {
+      const uint8_t* kb = a.c.k_win + (ring0 + j) * block_bytes(16);
+      const uint8_t* vb = a.c.v_win + (ring0 + j) * block_bytes(16);
+      process_block<16, 16>(kb, vb, nullptr, nullptr, min(kBlock, nw - j * kBlock), qf, qs0, qs1, st, lane, a.err);
     }
-    __syncthreads();
-    const uint16_t* kw = a.c.k_win + (size_t(b) * H + h) * W * kHeadDim;
-    const uint16_t* vw = a.c.v_win + (size_t(b) * H + h) * W * kHeadDim;
-    if (tid < nw) {
-      float dot[kMaxGroup];
-#pragma unroll
-      for (int q = 0; q < kMaxGroup; ++q) dot[q] = 0.f;
-      const uint4* kr = reinterpret_cast<const uint4*>(kw + size_t(tid) * kHeadDim);
-      for (int c = 0; c < kHeadDim / 8; ++c) {
-        const uint4 v = kr[c];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
-          const int d = c * 8 + 2 * k;
-#pragma unroll
-          for (int q = 0; q < kMaxGroup; ++q)
-            if (q < G) dot[q] = fmaf(qf[q * kHeadDim + d + 1], hi, fmaf(qf[q * kHeadDim + d], lo, dot[q]));
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kMaxGroup; ++q)
-        if (q < G) sc[q * kHeadDim + tid] = dot[q] * (kLog2e * kInvSqrtD);
-    }
-    __syncthreads();
-    float* wm = merge_m;  // [8]
-    float* wl = merge_l;
-    for (int q = warp; q < G; q += kThreads / 32) {
-      float m = kNegInf;
-      for (int i = lane; i < nw; i += 32) m = fmaxf(m, sc[q * kHeadDim + i]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-      float l = 0.f;
-      for (int i = lane; i < nw; i += 32) {
-        const float p = exp2f(sc[q * kHeadDim + i] - m);
-        sc[q * kHeadDim + i] = p;
-        l += p;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
-      if (lane == 0) {
-        wm[q] = m;
-        wl[q] = l;
-      }
-    }
-    __syncthreads();
-    long long c0, c1;
-    int nseg;
-    bool has_win;
-    unit_segments(a, len_s, pre_s, u, T, Pe, c0, c1, nseg, has_win);
-    float* pm = reinterpret_cast<float*>(a.ws + a.lay.off_m);
-    float* pl = reinterpret_cast<float*>(a.ws + a.lay.off_l);
-    float* po = reinterpret_cast<float*>(a.ws + a.lay.off_o);
     const size_t slot = size_t(P) + U + u;
-    if (tid < kHeadDim) {
-      const int d = tid;
-      for (int q = 0; q < G; ++q) {
-        float o = 0.f;
-        for (int i = 0; i < nw; ++i)
-          o = fmaf(sc[q * kHeadDim + i], __uint_as_float(uint32_t(vw[size_t(i) * kHeadDim + d]) << 16), o);
-        if (nseg == 1) {
-          write_out(a, b, h * G + q, d, o, wl[q], wm[q]);
-        } else {
-          po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
-          if (d == 0) {
-            pm[slot * kMaxGroup + q] = wm[q];
-            pl[slot * kMaxGroup + q] = wl[q];
-          }
-        }
-      }
-    }
-    if (nseg > 1) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        int* cnt = reinterpret_cast<int*>(a.ws + a.lay.off_counter);
-        const int t = atomicAdd(&cnt[u], 1);
-        misc[0] = (t == nseg - 1);
-      }
-      __syncthreads();
-      if (misc[0]) {
-        __threadfence();
-        merge_unit(a, u, c0, c1, has_win, P, tid, kThreads);
-        if (tid == 0) reinterpret_cast<int*>(a.ws + a.lay.off_counter)[u] = 0;
-      }
-    }
+    if (!finish_segment(a, st, u, slot, len_s, pre_s, T, Pe, P, sc, cphase, warp, lane, tid))
+      flag(a.err, KVQ_DEVERR_TIMEOUT);
     return;
   }
 
   // ==================================================================== stream CTAs
+  const int ci = blockIdx.x - Uw;  // stream CTA index
   // units with no tokens at all: out = 0, lse = -inf
-  for (int u = blockIdx.x; u < U; u += P) {
+  for (int u = ci; u < U; u += P) {
     const int b = u / H, h = u % H;
     if (len_s[b] != 0) continue;
     for (int e = tid; e < G * kHeadDim; e += kThreads) {
@@ -448,16 +683,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
       if (d == 0 && a.lse) a.lse[size_t(b) * a.Hq + h * G + q] = kNegInf;
     }
   }
-  if (blockIdx.x >= Pe) return;
-  const long long x0 = (long long)blockIdx.x * T / Pe;
-  const long long x1 = (long long)(blockIdx.x + 1) * T / Pe;
+  if (ci >= Pe) return;
+  const long long x0 = (long long)ci * T / Pe;
+  const long long x1 = (long long)(ci + 1) * T / Pe;
   if (x0 >= x1) return;
 
   if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane != 0) return;
+    // ------------------------------------------------------------ producer warp
     const uint64_t pol = l2_evict_first_policy();
-    // locate the unit holding x0: largest b with H*pre[b] <= x0 and blocks > 0
+    // locate the unit holding x0: largest b with H*pre[b] <= x0 (it has blocks)
     int lo = 0, hi = B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -465,13 +699,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
       else hi = mid - 1;
     }
     int b = lo;
-    while (pre_s[b + 1] == pre_s[b]) ++b;  // skip empty sequences (x0 lies in a non-empty one)
+    while (pre_s[b + 1] == pre_s[b]) ++b;
     int nblk = pre_s[b + 1] - pre_s[b];
     int h = int((x0 - (long long)H * pre_s[b]) / nblk);
     long long ustart = (long long)H * pre_s[b] + (long long)h * nblk;
     long long x = x0;
     int it = 0;
     bool ok = true;
+    // 32 block-table entries of sequence tc_b, logical blocks tc_base + lane
+    int tc_b = -1, tc_base = 0, tc_val = 0;
     while (x < x1) {
       if (x >= ustart + nblk) {
         ++h;
@@ -484,33 +720,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
       }
       const long long rem = (x1 - x) < (ustart + nblk - x) ? (x1 - x) : (ustart + nblk - x);
       const int n = int(rem < kConsumerWarps ? rem : kConsumerWarps);
-      const int s = it % S;
-      if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1)) {
-        flag(a.err, KVQ_DEVERR_TIMEOUT);
-        ok = false;
-        break;
-      }
       const int local = int(x - ustart);
-      hdr[s] = make_int4(b * H + h, local, n, 0);
-      mbar_arrive_expect_tx(&full[s], uint32_t(n * F::kPerBlock));
-      uint8_t* st = smem + s * F::kStageBytes;
-      for (int j = 0; j < n; ++j) {
-        int phys = a.table[size_t(b) * a.mbps + local + j];
-        if (phys < 0 || phys >= a.c.num_blocks) {
-          flag(a.err, KVQ_DEVERR_BLOCK_ID);
-          phys = 0;
+      if (tc_b != b || local < tc_base || local + n > tc_base + 32) {
+        tc_b = b;
+        tc_base = local;
+        const int idx = local + lane;
+        int v = 0;
+        if (idx < nblk) {
+          v = a.table[size_t(b) * a.mbps + idx];
+          if (v < 0 || v >= a.c.num_blocks) {
+            flag(a.err, KVQ_DEVERR_BLOCK_ID);
+            v = 0;
+          }
         }
+        tc_val = v;
+      }
+      const int s = it % S;
+      if (it >= S) {
+        bool w_ok = true;
+        if (lane == 0) w_ok = mbar_wait(&empty[s], ((it / S) - 1) & 1);
+        if (!__shfl_sync(kFull, w_ok ? 1 : 0, 0)) {
+          if (lane == 0) flag(a.err, KVQ_DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+      }
+      const int phys = __shfl_sync(kFull, tc_val, (local - tc_base) + min(lane, n - 1));
+      if (lane == 0) {
+        hdr[s] = make_int4(b * H + h, local, n, 0);
+        mbar_arrive_expect_tx(&full[s], uint32_t(n * F::kPerBlock));
+      }
+      __syncwarp();
+      if (lane < n) {
+        uint8_t* st = smem + s * F::kStageBytes;
         const size_t bh = size_t(phys) * H + h;
-        bulk_g2s(st + F::kOffK + j * F::kKBB, a.c.k_codes + bh * F::kKBB, F::kKBB, &full[s], pol);
-        bulk_g2s(st + F::kOffV + j * F::kVBB, a.c.v_codes + bh * F::kVBB, F::kVBB, &full[s], pol);
+        bulk_g2s(st + F::kOffK + lane * F::kKBB, a.c.k_codes + bh * F::kKBB, F::kKBB, &full[s], pol);
+        bulk_g2s(st + F::kOffV + lane * F::kVBB, a.c.v_codes + bh * F::kVBB, F::kVBB, &full[s], pol);
         if constexpr (!F::kBf16) {
-          bulk_g2s(st + F::kOffKS + j * F::kSCB, a.c.k_scales + bh * kBlock, F::kSCB, &full[s], pol);
-          bulk_g2s(st + F::kOffVS + j * F::kSCB, a.c.v_scales + bh * kBlock, F::kSCB, &full[s], pol);
+          bulk_g2s(st + F::kOffKS + lane * F::kSCB, a.c.k_scales + bh * kBlock, F::kSCB, &full[s], pol);
+          bulk_g2s(st + F::kOffVS + lane * F::kSCB, a.c.v_scales + bh * kBlock, F::kSCB, &full[s], pol);
         }
       }
       x += n;
       ++it;
     }
+    if (lane != 0) return;
     if (ok) {  // terminator stage
       const int s = it % S;
       if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1)) {
@@ -527,22 +781,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
     return;
   }
 
-  // -------------------------------------------------------------- consumers
-  const int g = lane >> 2, t = lane & 3;
-  float O[8][4];
-  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+  // -------------------------------------------------------------- consumer warps
+  WarpState st;
+  st.reset();
   uint32_t qf[16];
   float qs0 = 0.f, qs1 = 0.f;
-  uint32_t cphase = 0;
-  int cur = -1;
-  int cur_b = 0, cur_lq = 0;
-  int* cnt = reinterpret_cast<int*>(a.ws + a.lay.off_counter);
-  float* pm = reinterpret_cast<float*>(a.ws + a.lay.off_m);
-  float* pl = reinterpret_cast<float*>(a.ws + a.lay.off_l);
-  float* po = reinterpret_cast<float*>(a.ws + a.lay.off_o);
-
+  int cur = -1, cur_lq = 0;
   for (int it = 0;; ++it) {
     const int s = it % S;
     if (!mbar_wait(&full[s], (it / S) & 1)) {
@@ -551,214 +795,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params prm) {
     }
     const int4 hd = hdr[s];
     if (hd.x != cur) {
-      if (cur >= 0) {
-        // ---------------- flush the finished unit segment
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          l0 += __shfl_xor_sync(kFull, l0, o);
-          l1 += __shfl_xor_sync(kFull, l1, o);
-        }
-        if (g == 0) {
-          merge_m[warp * kMaxGroup + 2 * t] = m0;
-          merge_m[warp * kMaxGroup + 2 * t + 1] = m1;
-          merge_l[warp * kMaxGroup + 2 * t] = l0;
-          merge_l[warp * kMaxGroup + 2 * t + 1] = l1;
-        }
-        float* ow = merge_o + warp * kMaxGroup * kHeadDim;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          ow[(2 * t) * kHeadDim + 16 * mt + g] = O[mt][0];
-          ow[(2 * t + 1) * kHeadDim + 16 * mt + g] = O[mt][1];
-          ow[(2 * t) * kHeadDim + 16 * mt + g + 8] = O[mt][2];
-          ow[(2 * t + 1) * kHeadDim + 16 * mt + g + 8] = O[mt][3];
-        }
-        if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
-        const int ub = cur / H, uh = cur % H;
-        long long c0, c1;
-        int nseg;
-        bool has_win;
-        unit_segments(a, len_s, pre_s, cur, T, Pe, c0, c1, nseg, has_win);
-        const size_t slot = size_t(blockIdx.x) + cur;
-        {
-          const int d = tid;
-          for (int q = 0; q < G; ++q) {
-            float M = kNegInf;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * kMaxGroup + q]);
-            float l = 0.f, o = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              const float mw = merge_m[w * kMaxGroup + q];
-              const float al = (mw == kNegInf) ? 0.f : exp2f(mw - M);
-              l += al * merge_l[w * kMaxGroup + q];
-              o += al * merge_o[(w * kMaxGroup + q) * kHeadDim + d];
-            }
-            if (nseg == 1) {
-              write_out(a, ub, uh * G + q, d, o, l, M);
-            } else {
-              po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
-              if (d == 0) {
-                pm[slot * kMaxGroup + q] = M;
-                pl[slot * kMaxGroup + q] = l;
-              }
-            }
-          }
-        }
-        if (nseg > 1) {
-          __threadfence();
-          if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
-          if (tid == 0) {
-            const int tk = atomicAdd(&cnt[cur], 1);
-            misc[0] = (tk == nseg - 1);
-          }
-          if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
-          if (misc[0]) {
-            __threadfence();
-            merge_unit(a, cur, c0, c1, has_win, P, tid, kConsumers);
-            if (tid == 0) cnt[cur] = 0;
-          }
-        }
-        if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
+      if (cur >= 0 &&
+          !finish_segment(a, st, cur, size_t(ci) + cur, len_s, pre_s, T, Pe, P, sc, cphase, warp, lane, tid)) {
+        flag(a.err, KVQ_DEVERR_TIMEOUT);
+        return;
       }
       if (hd.x < 0) break;  // terminator
-      // ---------------- start a new unit: prepare the query group in fp16 / bf16
       cur = hd.x;
-      cur_b = cur / H;
-      const int uh = cur % H;
-      cur_lq = W > 0 ? max(len_s[cur_b] - W, 0) : len_s[cur_b];
-      for (int q = warp; q < kMaxGroup; q += kConsumerWarps) {
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (q < G) {
-          const uint2 raw =
-              *reinterpret_cast<const uint2*>(a.q + (size_t(cur_b) * a.Hq + uh * G + q) * kHeadDim + 4 * lane);
-          x[0] = __uint_as_float(raw.x << 16);
-          x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-          x[2] = __uint_as_float(raw.y << 16);
-          x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-        }
-        if constexpr (F::kBf16) {
-          uint2 packed;
-          packed.x = pack_bf162(x[0], x[1]);
-          packed.y = pack_bf162(x[2], x[3]);
-          *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
-          if (lane == 0) qs[q] = kLog2e * kInvSqrtD;
-        } else {
-          if (pfac) {
-            const float4 c = *reinterpret_cast<const float4*>(pfac + uh * kHeadDim + 4 * lane);
-            x[0] *= c.x;
-            x[1] *= c.y;
-            x[2] *= c.z;
-            x[3] *= c.w;
-          }
-          float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
-          int e = 0;
-          if (am > 0.f) {
-            int ex;
-            frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
-            e = 15 - ex;      // am * 2^e in [2^14, 2^15)
-          }
-          uint2 packed;
-          packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
-          packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
-          *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
-          if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
-        }
-      }
-      if (!consumer_sync(cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
-      {
-        const uint4* qp = reinterpret_cast<const uint4*>(qh + g * kHeadDim + 32 * t);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 v = qp[i];
-          qf[4 * i] = v.x;
-          qf[4 * i + 1] = v.y;
-          qf[4 * i + 2] = v.z;
-          qf[4 * i + 3] = v.w;
-        }
-        qs0 = qs[2 * t];
-        qs1 = qs[2 * t + 1];
-      }
-      m0 = m1 = kNegInf;
-      l0 = l1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+      const int cb = cur / H;
+      cur_lq = W > 0 ? max(len_s[cb] - W, 0) : len_s[cb];
+      stage_query<F::kBf16>(a, cb, cur % H, qh, qs, warp, lane);
+      if (!consumer_sync(sc.cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
+      load_query(qh, qs, qf, qs0, qs1, lane);
+      st.reset();
     }
-
-    // ---------------- one 16-token block per consumer warp
     if (warp < hd.z) {
-      const uint8_t* st = smem + s * F::kStageBytes;
-      const int valid = min(kBlock, cur_lq - (hd.y + warp) * kBlock);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      score_block<KB>(st + F::kOffK + warp * F::kKBB, qf, acc, lane);
-      float sk0 = 1.f, sk1 = 1.f, sv0 = 1.f, sv1 = 1.f;
-      if constexpr (!F::kBf16) {
-        const float* ks = reinterpret_cast<const float*>(st + F::kOffKS + warp * F::kSCB);
-        const float* vs = reinterpret_cast<const float*>(st + F::kOffVS + warp * F::kSCB);
-        sk0 = ks[g];
-        sk1 = ks[g + 8];
-        sv0 = vs[g];
-        sv1 = vs[g + 8];
-      }
-      const bool v0 = g < valid, v1 = g + 8 < valid;
-      const float x00 = v0 ? acc[0] * (sk0 * qs0) : kNegInf;
-      const float x01 = v0 ? acc[1] * (sk0 * qs1) : kNegInf;
-      const float x10 = v1 ? acc[2] * (sk1 * qs0) : kNegInf;
-      const float x11 = v1 ? acc[3] * (sk1 * qs1) : kNegInf;
-      float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      if (__any_sync(kFull, (mn0 > m0) || (mn1 > m1))) {
-        const float al0 = (mn0 == kNegInf) ? 1.f : exp2f(m0 - mn0);
-        const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(m1 - mn1);
-        l0 *= al0;
-        l1 *= al1;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          O[i][0] *= al0;
-          O[i][2] *= al0;
-          O[i][1] *= al1;
-          O[i][3] *= al1;
-        }
-        m0 = mn0;
-        m1 = mn1;
-      }
-      const float base0 = (m0 == kNegInf) ? 0.f : m0, base1 = (m1 == kNegInf) ? 0.f : m1;
-      const float p00 = exp2f(x00 - base0), p10 = exp2f(x10 - base0);
-      const float p01 = exp2f(x01 - base1), p11 = exp2f(x11 - base1);
-      l0 += p00 + p10;
-      l1 += p01 + p11;
-      uint32_t pk0, pk1, pk0lo = 0, pk1lo = 0;
-      if constexpr (F::kBf16) {
-        const __nv_bfloat162 h0 = __floats2bfloat162_rn(p00, p10), h1 = __floats2bfloat162_rn(p01, p11);
-        pk0 = *reinterpret_cast<const uint32_t*>(&h0);
-        pk1 = *reinterpret_cast<const uint32_t*>(&h1);
-        pk0lo = pack_bf162(p00 - __low2float(h0), p10 - __high2float(h0));
-        pk1lo = pack_bf162(p01 - __low2float(h1), p11 - __high2float(h1));
-      } else {
-        if ((v0 && sv0 > 65504.f) || (v1 && sv1 > 65504.f)) flag(a.err, KVQ_DEVERR_RANGE);
-        pk0 = pack_half2(v0 ? p00 * sv0 : 0.f, v1 ? p10 * sv1 : 0.f);
-        pk1 = pack_half2(v0 ? p01 * sv0 : 0.f, v1 ? p11 * sv1 : 0.f);
-      }
-      // transpose the weights from the score accumulator layout (token rows,
-      // query columns) to the B-operand layout of the value contraction
-      const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
-      const uint32_t r00 = __shfl_sync(kFull, pk0, src0), r01 = __shfl_sync(kFull, pk1, src0);
-      const uint32_t r10 = __shfl_sync(kFull, pk0, src1), r11 = __shfl_sync(kFull, pk1, src1);
-      const uint32_t b0 = (g & 1) ? r01 : r00, b1 = (g & 1) ? r11 : r10;
-      uint32_t b0lo = 0, b1lo = 0;
-      if constexpr (F::kBf16) {
-        const uint32_t q00 = __shfl_sync(kFull, pk0lo, src0), q01 = __shfl_sync(kFull, pk1lo, src0);
-        const uint32_t q10 = __shfl_sync(kFull, pk0lo, src1), q11 = __shfl_sync(kFull, pk1lo, src1);
-        b0lo = (g & 1) ? q01 : q00;
-        b1lo = (g & 1) ? q11 : q10;
-      }
-      value_block<VB>(st + F::kOffV + warp * F::kVBB, b0, b1, b0lo, b1lo, O, lane);
+      const uint8_t* stg = smem + s * F::kStageBytes;
+      const float* ks = F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffKS + warp * F::kSCB);
+      const float* vs = F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffVS + warp * F::kSCB);
+      process_block<KB, VB>(stg + F::kOffK + warp * F::kKBB, stg + F::kOffV + warp * F::kVBB, ks, vs,
+                            min(kBlock, cur_lq - (hd.y + warp) * kBlock), qf, qs0, qs1, st, lane, a.err);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -805,8 +861,8 @@ struct Kernel {
     int dev = 0;
     cudaGetDevice(&dev);
     ensure_attribute(dev);
-    Params p{a, a.lay.stream_ctas};
-    const int grid = a.lay.stream_ctas + a.lay.window_ctas;
+    Params p{a, a.lay.stream_ctas, a.lay.window_ctas};
+    const int grid = a.lay.window_ctas + a.lay.stream_ctas;
     decode_kernel<KB, VB><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
   }

@@ -18,8 +18,8 @@ struct CacheView {
   float* v_scales;
   const float* factor;  // [H][128] or null
   int window, window_batch;
-  uint16_t* k_win;  // bf16 ring, [window_batch][H][W][128]
-  uint16_t* v_win;
+  uint8_t* k_win;  // bf16 ring: [window_batch][H][W/16] fragment-native bf16 blocks
+  uint8_t* v_win;
 };
 
 struct AppendArgs {

@@ -56,7 +56,11 @@ def test_decode_plan_one_wave_of_ctas(lib):
     slots = p.partial_slots
     assert p.workspace_bytes >= slots * 8 * (128 + 2) * 4 + 512 * 4
     pw = lib.kvq_make_decode_plan(8, 32, 8, 128, num_sms=152, ctas_per_sm=3)
-    assert pw.window_ctas == 64 and pw.partial_slots == 456 + 64 + 64
+    # window CTAs (one per unit) run first and take their slots out of the wave
+    assert pw.window_ctas == 64 and pw.stream_ctas == 456 - 64
+    assert pw.partial_slots == pw.stream_ctas + 64 + 64
+    pbig = lib.kvq_make_decode_plan(64, 32, 8, 128, num_sms=152, ctas_per_sm=3)
+    assert pbig.window_ctas == 512 and pbig.stream_ctas == 228        # never below half a wave
     px = lib.kvq_make_decode_plan(1, 4, 4, 0, num_sms=152, ctas_per_sm=3, stream_ctas=5)
     assert px.stream_ctas == 5
     with pytest.raises(lib.KvqError):
@@ -73,7 +77,7 @@ def _fake_desc(lib, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=64), 2), (dict(block_size=32), 2), (dict(k_bits=2), 2), (dict(k_bits=16, v_bits=8), 2),
     (dict(k_codes=0x1004), 3), (dict(k_scales=None), 1), (dict(num_kv_heads=0), 1), (dict(window=256), 2),
-    (dict(window=16), 1),
+    (dict(window=16), 1), (dict(window=24), 2),
 ])
 def test_host_validation_without_a_gpu(lib, kw, status):
     desc = _fake_desc(lib, **kw)

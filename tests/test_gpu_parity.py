@@ -81,8 +81,8 @@ def check_stored_cache(inp, run, units=None, max_positions=None):
         if w.window:
             L = Lq + st["k_window"].shape[0]
             wp = np.arange(Lq, L)
-            ring_k = pools["k_window"].reshape(w.batch, w.kv_heads, w.window, 128)[b][:, wp % w.window]
-            ring_v = pools["v_window"].reshape(w.batch, w.kv_heads, w.window, 128)[b][:, wp % w.window]
+            ring_k = unpack_blocks(pools["k_window"], 16, True, 1).reshape(w.batch, w.kv_heads, w.window, 128)[b][:, wp % w.window]
+            ring_v = unpack_blocks(pools["v_window"], 16, False, 1).reshape(w.batch, w.kv_heads, w.window, 128)[b][:, wp % w.window]
             from synth import f32_to_bf16_bits
             np.testing.assert_array_equal(ring_k.transpose(1, 0, 2), f32_to_bf16_bits(st["k_window"].astype(np.float32)))
             np.testing.assert_array_equal(ring_v.transpose(1, 0, 2), f32_to_bf16_bits(st["v_window"].astype(np.float32)))
@@ -198,7 +198,7 @@ def test_step_append_equals_bulk_fill():
     torch.cuda.synchronize()
     a = bulk.pools()
     for key in ("k_window", "v_window"):
-        np.testing.assert_array_equal(getattr(step_cache, key).view(torch.int16).cpu().numpy().view(np.uint16), a[key])
+        np.testing.assert_array_equal(getattr(step_cache, key).view(torch.uint8).cpu().numpy(), a[key])
     # block store: compare every position older than the window
     kc_s = unpack_blocks(step_cache.k_codes.cpu().numpy(), 4, True, w.kv_heads)
     kc_b = unpack_blocks(a["k_codes"], 4, True, w.kv_heads)
