@@ -257,6 +257,7 @@ def main():
         out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
         ws = DecodeWorkspace(replicas[0], B, Hq, args.stream_ctas)
+        plan = _lib.kvq_decode_device_plan(replicas[0].desc, B, Hq, args.stream_ctas)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         dec_lens = torch.from_numpy(inp_.decode_lengths.astype(np.int32)).to(dev)
         if wl.append_one:
@@ -341,7 +342,9 @@ def main():
         errbits = int(err.item())
         return dict(ms_step=ms_total / K, dec_ms=statistics.mean(dec_ms), dec_ms_med=statistics.median(dec_ms),
                     e2e_s=e2e_s, h2d=h2d, d2h=d2h, bytes=cache_bytes_per_step(inp_), replicas=len(replicas),
-                    alloc=alloc, clocks=clk.summary(), launches=launches_per_step * K, err=errbits)
+                    alloc=alloc, clocks=clk.summary(), launches=launches_per_step * K, err=errbits,
+                    plan={"stream_ctas": plan.stream_ctas, "window_ctas": plan.window_ctas,
+                          "workspace_bytes": plan.workspace_bytes})
 
     res = run_arm(inp, "quant")
     peak, peak_kind = measured_peaks()
@@ -390,7 +393,7 @@ def main():
                    "cache_bytes_per_step": bytes_step, "allocated_cache_bytes": res["alloc"],
                    "l2": f"steps rotate over {res['replicas']} cache replicas "
                          f"({res['replicas'] * bytes_step / 2**20:.0f} MiB >= 4x L2 or cache > L2)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "decode_grid": res["plan"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": recorded_traffic(w.name, "decode"), "kernel": "kvq decode_kernel",

@@ -25,7 +25,8 @@
  *   - Head dimension D = 128 and block size 16 tokens are fixed.
  *
  * Cache layout (device memory, all pools 16-byte aligned)
- *   Codes pool  : [num_blocks][num_kv_heads][block_bytes] with
+ *   Codes pool  : [num_kv_heads][num_blocks][block_bytes] (head-major, so the
+ *                 consecutive blocks of one head are adjacent in memory), with
  *                 block_bytes = 16 * 128 * bits / 8 (int4 1024, int8 2048, bf16 4096).
  *                 Inside a block the bytes are ordered so that each lane of a
  *                 warp reads its tensor-core operand with one 16-byte load per
@@ -45,7 +46,7 @@
  *     for int8 keys "byte" is the offset inside the lane's 16 bytes.  Nibble n
  *     of a little-endian 32-bit word occupies bits 4n..4n+3.  Codes are two's
  *     complement: int8 in [-127,127], int4 in [-8,7] (-8 never produced).
- *   Scale pool  : float [num_blocks][num_kv_heads][16], natural token order
+ *   Scale pool  : float [num_kv_heads][num_blocks][16], natural token order
  *                 (absent for a bf16 cache).
  *   Window ring : bf16 [window_batch][num_kv_heads][window / 16][4096 bytes]:
  *                 window / 16 blocks per (sequence, head) for keys and for
@@ -155,6 +156,12 @@ typedef struct {
 kvq_status kvq_make_decode_plan(int32_t batch, int32_t q_heads, int32_t num_kv_heads, int32_t window,
                                 int32_t num_sms, int32_t ctas_per_sm, int32_t stream_ctas,
                                 kvq_decode_plan* plan);
+
+/* The plan kvq_decode uses on the current device: stream CTAs = SMs x resident
+ * decode CTAs per SM (occupancy of this cache format) minus the window CTAs,
+ * or the explicit stream_ctas (> 0). */
+kvq_status kvq_decode_device_plan(const kvq_cache_desc* cache, int32_t batch, int32_t q_heads,
+                                  int32_t stream_ctas, kvq_decode_plan* plan);
 
 /* Workspace bytes kvq_decode needs on the current device (stream_ctas 0 = automatic). */
 kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t batch, int32_t q_heads,

@@ -66,6 +66,7 @@ SIGNATURES = {
                              c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
     "kvq_make_decode_plan": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_int32,
                                        POINTER(DecodePlan)]),
+    "kvq_decode_device_plan": (c_int32, [POINTER(CacheDesc), c_int32, c_int32, c_int32, POINTER(DecodePlan)]),
     "kvq_decode_workspace_size": (c_int32, [POINTER(CacheDesc), c_int32, c_int32, c_int32, POINTER(c_size_t)]),
     "kvq_workspace_init": (c_int32, [c_void_p, c_size_t, c_void_p]),
     "kvq_decode": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32,
@@ -134,6 +135,13 @@ def kvq_make_decode_plan(batch: int, q_heads: int, kv_heads: int, window: int, n
     plan = DecodePlan()
     _check(load().kvq_make_decode_plan(batch, q_heads, kv_heads, window, num_sms, ctas_per_sm, stream_ctas,
                                        ctypes.byref(plan)), "kvq_make_decode_plan")
+    return plan
+
+
+def kvq_decode_device_plan(desc: CacheDesc, batch: int, q_heads: int, stream_ctas: int = 0) -> DecodePlan:
+    plan = DecodePlan()
+    _check(load().kvq_decode_device_plan(ctypes.byref(desc), batch, q_heads, stream_ctas, ctypes.byref(plan)),
+           "kvq_decode_device_plan")
     return plan
 
 

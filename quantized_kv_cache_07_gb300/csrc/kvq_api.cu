@@ -202,6 +202,24 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t batch,
   return KVQ_OK;
 }
 
+kvq_status kvq_decode_device_plan(const kvq_cache_desc* cache, int32_t batch, int32_t q_heads, int32_t stream_ctas,
+                                  kvq_decode_plan* plan) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!plan) return KVQ_ERR_INVALID_ARG;
+  st = check_decode_shape(cache, batch, q_heads);
+  if (st != KVQ_OK) return st;
+  const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, batch);
+  if (P <= 0) return KVQ_ERR_CUDA;
+  const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, cache->num_kv_heads, cache->window, P);
+  plan->stream_ctas = L.stream_ctas;
+  plan->window_ctas = L.window_ctas;
+  plan->units = L.units;
+  plan->partial_slots = L.slots;
+  plan->workspace_bytes = L.total;
+  return KVQ_OK;
+}
+
 kvq_status kvq_workspace_init(void* workspace, size_t bytes, void* stream) {
   if (!workspace && bytes) return KVQ_ERR_INVALID_ARG;
   if (!bytes) return KVQ_OK;

@@ -121,7 +121,7 @@ __device__ void write_block_store(const AppendArgs& a, bool is_key, int b, int p
   const int tok = p % kBlock;
   const int bits = is_key ? c.k_bits : c.v_bits;
   uint8_t* pool = is_key ? c.k_codes : c.v_codes;
-  uint8_t* blk = pool + (size_t(phys) * c.H + h) * block_bytes(bits);
+  uint8_t* blk = pool + (size_t(h) * c.num_blocks + phys) * block_bytes(bits);
   if (bits == 16) {
     store_bf16(is_key, blk, tok, xb, lane);
     return;
@@ -138,7 +138,7 @@ __device__ void write_block_store(const AppendArgs& a, bool is_key, int b, int p
   store_codes(is_key, bits, blk, tok, code, lane);
   if (lane == 0) {
     float* sc = is_key ? c.k_scales : c.v_scales;
-    sc[(size_t(phys) * c.H + h) * kBlock + tok] = s;
+    sc[(size_t(h) * c.num_blocks + phys) * kBlock + tok] = s;
   }
 }
 
@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
     return;
   }
   const int bits = is_key ? a.c.k_bits : a.c.v_bits;
-  const uint8_t* blk = (is_key ? a.c.k_codes : a.c.v_codes) + (size_t(phys) * H + h) * block_bytes(bits);
+  const uint8_t* blk = (is_key ? a.c.k_codes : a.c.v_codes) + (size_t(h) * a.c.num_blocks + phys) * block_bytes(bits);
   float s = 1.0f;
-  if (bits != 16) s = (is_key ? a.c.k_scales : a.c.v_scales)[(size_t(phys) * H + h) * kBlock + tok];
+  if (bits != 16) s = (is_key ? a.c.k_scales : a.c.v_scales)[(size_t(h) * a.c.num_blocks + phys) * kBlock + tok];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int d = 4 * lane + j;

@@ -75,10 +75,12 @@ struct Fmt {
 
 // Shared-memory map after the stage ring (all offsets 16-byte aligned).
 struct SmemMap {
-  int merge_o;   // float [4 warps][8 q][128]
+  int merge_o;   // float [4 warps][4 q][128] (combine, four queries per pass)
   int merge_ml;  // float m[4][8], l[4][8]
-  int qh;        // 16-bit [8][128]
+  int qh;        // 16-bit [8][128]: B-operand rows of the current query group
   int qs;        // float [8]
+  int qraw;      // bf16 [2][8][128]: prefetched raw query rows (double buffer)
+  int fraw;      // float [2][128]: prefetched per-channel key factor row
   int hdr;       // int4 [stages]
   int bars;      // uint64 full[stages], empty[stages], cbar
   int misc;      // int [4]
@@ -90,10 +92,12 @@ struct SmemMap {
 __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, int B) {
   SmemMap m;
   int o = stage_bytes_total;
-  m.merge_o = o;  o += kConsumerWarps * kMaxGroup * kHeadDim * 4;
+  m.merge_o = o;  o += kConsumerWarps * 4 * kHeadDim * 4;
   m.merge_ml = o; o += 2 * kConsumerWarps * kMaxGroup * 4;
   m.qh = o;       o += kMaxGroup * kHeadDim * 2;
   m.qs = o;       o += kMaxGroup * 4 + 32;
+  m.qraw = o;     o += 2 * kMaxGroup * kHeadDim * 2;
+  m.fraw = o;     o += 2 * kHeadDim * 4;
   m.hdr = o;      o += stages * 16;
   m.bars = o;     o += (2 * stages + 2) * 8;
   m.misc = o;     o += 16;
@@ -196,7 +200,7 @@ struct Params {
 };
 
 // A stream CTA owns at least this many blocks (fewer, deeper splits for tiny problems).
-constexpr int kMinBlocksPerCta = 8;
+constexpr int kMinBlocksPerCta = 16;
 
 // CTA-consumer barrier on an mbarrier (count = kConsumers), bounded wait.
 __device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase) {
@@ -389,19 +393,100 @@ __device__ __forceinline__ void load_query(const uint16_t* qh, const float* qs, 
   qs1 = qs[2 * t + 1];
 }
 
+// Consumer warps start asynchronous copies of unit u's raw query rows (and of
+// the per-channel key factor row) into prefetch buffer `buf`; one commit group.
+__device__ __forceinline__ void prefetch_query(const DecodeArgs& a, int u, int buf, uint16_t* qraw, float* fraw,
+                                               int warp, int lane) {
+  const int H = a.c.H, b = u / H, h = u % H;
+  uint16_t* raw = qraw + buf * kMaxGroup * kHeadDim;
+  for (int q = warp; q < kMaxGroup; q += kConsumerWarps)
+    if (q < a.G)
+      cp_async8(raw + q * kHeadDim + 4 * lane, a.q + (size_t(b) * a.Hq + h * a.G + q) * kHeadDim + 4 * lane);
+  if (a.c.factor && warp == 0) cp_async16(fraw + buf * kHeadDim + 4 * lane, a.c.factor + h * kHeadDim + 4 * lane);
+  cp_async_commit();
+}
+
+// Next unit of this CTA's block range after unit `cur`, or -1.
+__device__ __forceinline__ int next_unit_in_range(int cur, long long x1, const int* pre_s, int B, int H) {
+  const int b = cur / H, h = cur % H;
+  const int nblk = pre_s[b + 1] - pre_s[b];
+  const long long uend = (long long)H * pre_s[b] + (long long)(h + 1) * nblk;
+  if (uend >= x1) return -1;
+  int b2 = b;
+  while (pre_s[b2 + 1] == pre_s[b2] || (long long)H * pre_s[b2 + 1] <= uend) ++b2;
+  const int nb2 = pre_s[b2 + 1] - pre_s[b2];
+  return b2 * H + int((uend - (long long)H * pre_s[b2]) / nb2);
+}
+
 // Shared scratch used by the combine and the merge.
 struct Scratch {
-  float* merge_o;  // [4 warps][8][128]
+  float* merge_o;  // [4 warps][4][128]
   float* merge_m;  // [4][8]
   float* merge_l;  // [4][8]
   int* misc;
   uint64_t* cbar;
 };
 
-// Log-sum-exp merge of every partial record of unit u (run by the 128
-// consumer threads of the last CTA to finish the unit; thread = dim).
-__device__ __noinline__ bool merge_unit(const DecodeArgs& a, int u, long long c0, long long c1, bool has_win, int P,
-                           const Scratch& sc, uint32_t& cphase, int warp, int lane, int tid) {
+// Once the copies of prefetch buffer `buf` have landed (every consumer thread
+// has waited on its cp.async groups), turn the raw rows into B-operand rows:
+// fp16 scaled by an exact power of two with the per-channel key factor
+// applied, or the raw bf16 values for bf16 blocks; then load the fragments.
+template <bool kBf16Q>
+__device__ __forceinline__ bool convert_query(const DecodeArgs& a, int buf, const uint16_t* qraw, const float* fraw,
+                                              uint16_t* qh, float* qs, const Scratch& sc, uint32_t& cphase, int warp,
+                                              int lane, uint32_t (&qf)[16], float& qs0, float& qs1) {
+  if (!consumer_sync(sc.cbar, cphase)) return false;  // the factor row was copied by warp 0
+  const uint16_t* raw = qraw + buf * kMaxGroup * kHeadDim;
+  for (int q = warp; q < kMaxGroup; q += kConsumerWarps) {
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (q < a.G) {
+      const uint2 r = *reinterpret_cast<const uint2*>(raw + q * kHeadDim + 4 * lane);
+      x[0] = __uint_as_float(r.x << 16);
+      x[1] = __uint_as_float(r.x & 0xFFFF0000u);
+      x[2] = __uint_as_float(r.y << 16);
+      x[3] = __uint_as_float(r.y & 0xFFFF0000u);
+    }
+    uint2 packed;
+    if constexpr (kBf16Q) {
+      packed.x = pack_bf162(x[0], x[1]);
+      packed.y = pack_bf162(x[2], x[3]);
+      if (lane == 0) qs[q] = kLog2e * kInvSqrtD;
+    } else {
+      if (a.c.factor) {
+        const float4 c = *reinterpret_cast<const float4*>(fraw + buf * kHeadDim + 4 * lane);
+        x[0] *= c.x;
+        x[1] *= c.y;
+        x[2] *= c.z;
+        x[3] *= c.w;
+      }
+      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
+      int e = 0;
+      if (am > 0.f) {
+        int ex;
+        frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
+        e = 15 - ex;      // am * 2^e in [2^14, 2^15)
+      }
+      packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
+      packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+      if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
+    }
+    *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
+  }
+  if (!consumer_sync(sc.cbar, cphase)) return false;
+  load_query(qh, qs, qf, qs0, qs1, lane);
+  return true;
+}
+
+// Log-sum-exp merge of every partial record of unit u, run by the consumer
+// threads of the last CTA to finish the unit.  Thread f owns float4 f of the
+// G x 128 output and merges it on its own, without block synchronisation: the
+// (m, l, o) of eight records are loaded at once, then folded into a running
+// (M, l, o) with the usual rescaling by 2^(M_old - M_new).
+__device__ __noinline__ void merge_unit(const DecodeArgs& a, int u, long long c0, long long c1, bool has_win, int P,
+                                        int tid) {
+  constexpr int kR = 8;  // records in flight per thread
   const int G = a.G, H = a.c.H;
   const int b = u / H, h = u % H;
   const int ns = c1 >= c0 ? int(c1 - c0 + 1) : 0;
@@ -410,80 +495,62 @@ __device__ __noinline__ bool merge_unit(const DecodeArgs& a, int u, long long c0
   const float* pm = reinterpret_cast<const float*>(a.ws + a.lay.off_m);
   const float* pl = reinterpret_cast<const float*>(a.ws + a.lay.off_l);
   const float* po = reinterpret_cast<const float*>(a.ws + a.lay.off_o);
-  float* Ms = sc.merge_m;          // [8]
-  float* Ls = sc.merge_m + 8;      // [8]
-  float* Wt = sc.merge_o;          // [128][8] weights of one chunk of records
-  float* red = sc.merge_o + 1024;  // [4][8] cross-warp reduction
-  // pass 1: maximum of the record maxima per query
-  float mx[kMaxGroup];
+  const int nf = G * (kHeadDim / 4);
+  for (int f = tid; f < nf; f += kConsumers) {
+    const int q = f >> 5, d4 = f & 31;
+    float M = kNegInf, l = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = 0; base < ntot; base += kR) {
+      const int cnt = min(kR, ntot - base);
+      float mr[kR], lr[kR];
+      float4 orr[kR];
 #pragma unroll
-  for (int q = 0; q < kMaxGroup; ++q) mx[q] = kNegInf;
-  for (int s = tid; s < ntot; s += kConsumers) {
-    const size_t slot = s < ns ? size_t(c0 + s + u) : wslot;
-#pragma unroll
-    for (int q = 0; q < kMaxGroup; ++q)
-      if (q < G) mx[q] = fmaxf(mx[q], __ldcg(pm + slot * kMaxGroup + q));
-  }
-#pragma unroll
-  for (int q = 0; q < kMaxGroup; ++q) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx[q] = fmaxf(mx[q], __shfl_xor_sync(kFull, mx[q], o));
-    if (lane == 0) red[warp * kMaxGroup + q] = mx[q];
-  }
-  if (!consumer_sync(sc.cbar, cphase)) return false;
-  if (tid < kMaxGroup) {
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red[w * kMaxGroup + tid]);
-    Ms[tid] = M;
-  }
-  if (!consumer_sync(sc.cbar, cphase)) return false;
-  // pass 2: weights 2^(m_r - M) per chunk of records, weighted sums
-  float o[kMaxGroup], lp[kMaxGroup];
-#pragma unroll
-  for (int q = 0; q < kMaxGroup; ++q) o[q] = lp[q] = 0.f;
-  for (int base = 0; base < ntot; base += kConsumers) {
-    const int s = base + tid;
-    if (s < ntot) {
-      const size_t slot = s < ns ? size_t(c0 + s + u) : wslot;
-#pragma unroll
-      for (int q = 0; q < kMaxGroup; ++q) {
-        float w = 0.f;
-        if (q < G) {
-          w = exp2f(__ldcg(pm + slot * kMaxGroup + q) - Ms[q]);
-          lp[q] += w * __ldcg(pl + slot * kMaxGroup + q);
+      for (int j = 0; j < kR; ++j) {
+        if (j < cnt) {
+          const int r = base + j;
+          const size_t slot = r < ns ? size_t(c0 + r + u) : wslot;
+          mr[j] = __ldcg(pm + slot * kMaxGroup + q);
+          lr[j] = __ldcg(pl + slot * kMaxGroup + q);
+          orr[j] = __ldcg(reinterpret_cast<const float4*>(po + (slot * kMaxGroup + q) * kHeadDim) + d4);
+        } else {
+          mr[j] = kNegInf;
+          lr[j] = 0.f;
+          orr[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        Wt[tid * kMaxGroup + q] = w;
       }
+      float Mn = M;
+#pragma unroll
+      for (int j = 0; j < kR; ++j) Mn = fmaxf(Mn, mr[j]);
+      const float rs = (M == kNegInf) ? 0.f : exp2f(M - Mn);
+      l *= rs;
+      o.x *= rs;
+      o.y *= rs;
+      o.z *= rs;
+      o.w *= rs;
+#pragma unroll
+      for (int j = 0; j < kR; ++j) {
+        const float w = (mr[j] == kNegInf) ? 0.f : exp2f(mr[j] - Mn);
+        l = fmaf(w, lr[j], l);
+        o.x = fmaf(w, orr[j].x, o.x);
+        o.y = fmaf(w, orr[j].y, o.y);
+        o.z = fmaf(w, orr[j].z, o.z);
+        o.w = fmaf(w, orr[j].w, o.w);
+      }
+      M = Mn;
     }
-    if (!consumer_sync(sc.cbar, cphase)) return false;
-    const int cnt = min(kConsumers, ntot - base);
-#pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {
-      const int s2 = base + k;
-      const size_t slot = s2 < ns ? size_t(c0 + s2 + u) : wslot;
-#pragma unroll
-      for (int q = 0; q < kMaxGroup; ++q)
-        if (q < G) o[q] += Wt[k * kMaxGroup + q] * __ldcg(po + (slot * kMaxGroup + q) * kHeadDim + tid);
+    const float inv = 1.f / l;
+    const size_t idx = (size_t(b) * a.Hq + h * G + q) * kHeadDim + 4 * d4;
+    if (a.out_fp32) {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + idx) =
+          make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    } else {
+      uint2 pk;
+      pk.x = pack_bf162(o.x * inv, o.y * inv);
+      pk.y = pack_bf162(o.z * inv, o.w * inv);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + idx) = pk;
     }
-    if (!consumer_sync(sc.cbar, cphase)) return false;
+    if (d4 == 0 && a.lse) a.lse[size_t(b) * a.Hq + h * G + q] = (M + log2f(l)) * kLn2;
   }
-#pragma unroll
-  for (int q = 0; q < kMaxGroup; ++q) {
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) lp[q] += __shfl_xor_sync(kFull, lp[q], o2);
-    if (lane == 0) red[warp * kMaxGroup + q] = lp[q];
-  }
-  if (!consumer_sync(sc.cbar, cphase)) return false;
-  if (tid < kMaxGroup) {
-    float l = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) l += red[w * kMaxGroup + tid];
-    Ls[tid] = l;
-  }
-  if (!consumer_sync(sc.cbar, cphase)) return false;
-  for (int q = 0; q < G; ++q) write_out(a, b, h * G + q, tid, o[q], Ls[q], Ms[q]);
-  return true;
 }
 
 // Combine the four consumer warps' states of unit u and emit them: the final
@@ -505,15 +572,6 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
     sc.merge_l[warp * kMaxGroup + 2 * t] = st.l0;
     sc.merge_l[warp * kMaxGroup + 2 * t + 1] = st.l1;
   }
-  float* ow = sc.merge_o + warp * kMaxGroup * kHeadDim;
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    ow[(2 * t) * kHeadDim + 16 * mt + g] = st.O[mt][0];
-    ow[(2 * t + 1) * kHeadDim + 16 * mt + g] = st.O[mt][1];
-    ow[(2 * t) * kHeadDim + 16 * mt + g + 8] = st.O[mt][2];
-    ow[(2 * t + 1) * kHeadDim + 16 * mt + g + 8] = st.O[mt][3];
-  }
-  if (!consumer_sync(sc.cbar, cphase)) return false;
   long long c0, c1;
   int nseg;
   bool has_win;
@@ -523,30 +581,46 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
   float* pl = reinterpret_cast<float*>(a.ws + a.lay.off_l);
   float* po = reinterpret_cast<float*>(a.ws + a.lay.off_o);
   const int d = tid;
-  for (int q = 0; q < G; ++q) {
-    float M = kNegInf;
+  // combine the warps' O through shared memory, four queries per pass
+  for (int pass = 0; pass * 4 < G; ++pass) {
+    if (pass > 0 && !consumer_sync(sc.cbar, cphase)) return false;  // previous pass has read merge_o
+    if ((t >> 1) == pass) {
+      float* ow = sc.merge_o + warp * 4 * kHeadDim;
+      const int q0 = 2 * t - 4 * pass;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sc.merge_m[w * kMaxGroup + q]);
-    float l = 0.f, o = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float mw = sc.merge_m[w * kMaxGroup + q];
-      const float al = (mw == kNegInf) ? 0.f : exp2f(mw - M);
-      l += al * sc.merge_l[w * kMaxGroup + q];
-      o += al * sc.merge_o[(w * kMaxGroup + q) * kHeadDim + d];
+      for (int mt = 0; mt < 8; ++mt) {
+        ow[q0 * kHeadDim + 16 * mt + g] = st.O[mt][0];
+        ow[(q0 + 1) * kHeadDim + 16 * mt + g] = st.O[mt][1];
+        ow[q0 * kHeadDim + 16 * mt + g + 8] = st.O[mt][2];
+        ow[(q0 + 1) * kHeadDim + 16 * mt + g + 8] = st.O[mt][3];
+      }
     }
-    if (nseg == 1) {
-      write_out(a, b, h * G + q, d, o, l, M);
-    } else {
-      po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
-      if (d == 0) {
-        pm[slot * kMaxGroup + q] = M;
-        pl[slot * kMaxGroup + q] = l;
+    if (!consumer_sync(sc.cbar, cphase)) return false;
+    for (int q = 4 * pass; q < min(G, 4 * pass + 4); ++q) {
+      float M = kNegInf;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sc.merge_m[w * kMaxGroup + q]);
+      float l = 0.f, o = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = sc.merge_m[w * kMaxGroup + q];
+        const float al = (mw == kNegInf) ? 0.f : exp2f(mw - M);
+        l += al * sc.merge_l[w * kMaxGroup + q];
+        o += al * sc.merge_o[(w * 4 + (q - 4 * pass)) * kHeadDim + d];
+      }
+      if (nseg == 1) {
+        write_out(a, b, h * G + q, d, o, l, M);
+      } else {
+        po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
+        if (d == 0) {
+          pm[slot * kMaxGroup + q] = M;
+          pl[slot * kMaxGroup + q] = l;
+        }
       }
     }
   }
-  if (!consumer_sync(sc.cbar, cphase)) return false;  // merge_o free again
   if (nseg > 1) {
+    // partial record visible device-wide before the arrival ticket
     __threadfence();
     if (!consumer_sync(sc.cbar, cphase)) return false;
     if (tid == 0) {
@@ -555,15 +629,31 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
       sc.misc[0] = (tk == nseg - 1);
     }
     if (!consumer_sync(sc.cbar, cphase)) return false;
-    const bool last = sc.misc[0] != 0;
-    if (!consumer_sync(sc.cbar, cphase)) return false;  // everyone has read misc[0]
-    if (last) {
+    if (sc.misc[0]) {
       __threadfence();
-      if (!merge_unit(a, u, c0, c1, has_win, P, sc, cphase, warp, lane, tid)) return false;
+      merge_unit(a, u, c0, c1, has_win, P, tid);
       if (tid == 0) reinterpret_cast<int*>(a.ws + a.lay.off_counter)[u] = 0;
     }
   }
+  // merge_o / misc are written again only after the next query staging sync
   return true;
+}
+
+// Unit holding global block x (x < T): the largest b with H*pre[b] <= x has
+// blocks; the head follows from the offset inside that sequence's range.
+__device__ __forceinline__ void locate_unit(long long x, const int* pre_s, int B, int H, int& b, int& h, int& nblk,
+                                            long long& ustart) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)H * pre_s[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  b = lo;
+  while (pre_s[b + 1] == pre_s[b]) ++b;
+  nblk = pre_s[b + 1] - pre_s[b];
+  h = int((x - (long long)H * pre_s[b]) / nblk);
+  ustart = (long long)H * pre_s[b] + (long long)h * nblk;
 }
 
 template <int KB, int VB>
@@ -582,6 +672,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   sc.merge_l = sc.merge_m + kConsumerWarps * kMaxGroup;
   uint16_t* qh = reinterpret_cast<uint16_t*>(smem + mp.qh);
   float* qs = reinterpret_cast<float*>(smem + mp.qs);
+  uint16_t* qraw = reinterpret_cast<uint16_t*>(smem + mp.qraw);
+  float* fraw = reinterpret_cast<float*>(smem + mp.fraw);
   int4* hdr = reinterpret_cast<int4*>(smem + mp.hdr);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + mp.bars);
   uint64_t* empty = full + S;
@@ -691,18 +783,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer warp
     const uint64_t pol = l2_evict_first_policy();
-    // locate the unit holding x0: largest b with H*pre[b] <= x0 (it has blocks)
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((long long)H * pre_s[mid] <= x0) lo = mid;
-      else hi = mid - 1;
-    }
-    int b = lo;
-    while (pre_s[b + 1] == pre_s[b]) ++b;
-    int nblk = pre_s[b + 1] - pre_s[b];
-    int h = int((x0 - (long long)H * pre_s[b]) / nblk);
-    long long ustart = (long long)H * pre_s[b] + (long long)h * nblk;
+    int b, h, nblk;
+    long long ustart;
+    locate_unit(x0, pre_s, B, H, b, h, nblk, ustart);
     long long x = x0;
     int it = 0;
     bool ok = true;
@@ -745,20 +828,32 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
           break;
         }
       }
+      // physical ids of the stage's blocks on every lane; a lane whose block
+      // starts a run of consecutive ids issues one copy for the whole run
       const int phys = __shfl_sync(kFull, tc_val, (local - tc_base) + min(lane, n - 1));
+      const int prev = __shfl_up_sync(kFull, phys, 1);
+      const bool start = lane < n && (lane == 0 || prev + 1 != phys);
+      int run = 1;
+      bool contig = true;
+#pragma unroll
+      for (int j = 1; j < kConsumerWarps; ++j) {
+        const int nx = __shfl_down_sync(kFull, phys, j);
+        contig = contig && (lane + j < n) && (nx == phys + j);
+        run += contig ? 1 : 0;
+      }
       if (lane == 0) {
         hdr[s] = make_int4(b * H + h, local, n, 0);
         mbar_arrive_expect_tx(&full[s], uint32_t(n * F::kPerBlock));
       }
       __syncwarp();
-      if (lane < n) {
+      if (start) {
         uint8_t* st = smem + s * F::kStageBytes;
-        const size_t bh = size_t(phys) * H + h;
-        bulk_g2s(st + F::kOffK + lane * F::kKBB, a.c.k_codes + bh * F::kKBB, F::kKBB, &full[s], pol);
-        bulk_g2s(st + F::kOffV + lane * F::kVBB, a.c.v_codes + bh * F::kVBB, F::kVBB, &full[s], pol);
+        const size_t hb = size_t(h) * a.c.num_blocks + phys;  // head-major pools
+        bulk_g2s(st + F::kOffK + lane * F::kKBB, a.c.k_codes + hb * F::kKBB, run * F::kKBB, &full[s], pol);
+        bulk_g2s(st + F::kOffV + lane * F::kVBB, a.c.v_codes + hb * F::kVBB, run * F::kVBB, &full[s], pol);
         if constexpr (!F::kBf16) {
-          bulk_g2s(st + F::kOffKS + lane * F::kSCB, a.c.k_scales + bh * kBlock, F::kSCB, &full[s], pol);
-          bulk_g2s(st + F::kOffVS + lane * F::kSCB, a.c.v_scales + bh * kBlock, F::kSCB, &full[s], pol);
+          bulk_g2s(st + F::kOffKS + lane * F::kSCB, a.c.k_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
+          bulk_g2s(st + F::kOffVS + lane * F::kSCB, a.c.v_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
         }
       }
       x += n;
@@ -786,7 +881,28 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   st.reset();
   uint32_t qf[16];
   float qs0 = 0.f, qs1 = 0.f;
-  int cur = -1, cur_lq = 0;
+  int cur, cur_lq, qbuf = 0, nxt;
+  {
+    // the first unit is known from x0: fetch its query group (and the next
+    // unit's) while the first stage is still in flight
+    int b0, h0, nb0;
+    long long us0;
+    locate_unit(x0, pre_s, B, H, b0, h0, nb0, us0);
+    cur = b0 * H + h0;
+    cur_lq = W > 0 ? max(len_s[b0] - W, 0) : len_s[b0];
+    prefetch_query(a, cur, 0, qraw, fraw, warp, lane);
+    nxt = next_unit_in_range(cur, x1, pre_s, B, H);
+    if (nxt >= 0) {
+      prefetch_query(a, nxt, 1, qraw, fraw, warp, lane);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    if (!convert_query<F::kBf16>(a, 0, qraw, fraw, qh, qs, sc, cphase, warp, lane, qf, qs0, qs1)) {
+      flag(a.err, KVQ_DEVERR_TIMEOUT);
+      return;
+    }
+  }
   for (int it = 0;; ++it) {
     const int s = it % S;
     if (!mbar_wait(&full[s], (it / S) & 1)) {
@@ -801,12 +917,21 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         return;
       }
       if (hd.x < 0) break;  // terminator
+      if (hd.x != nxt) {  // not the predicted next unit: fetch its query group now
+        cp_async_wait<0>();
+        prefetch_query(a, hd.x, qbuf ^ 1, qraw, fraw, warp, lane);
+      }
       cur = hd.x;
+      qbuf ^= 1;
       const int cb = cur / H;
       cur_lq = W > 0 ? max(len_s[cb] - W, 0) : len_s[cb];
-      stage_query<F::kBf16>(a, cb, cur % H, qh, qs, warp, lane);
-      if (!consumer_sync(sc.cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
-      load_query(qh, qs, qf, qs0, qs1, lane);
+      cp_async_wait<0>();
+      if (!convert_query<F::kBf16>(a, qbuf, qraw, fraw, qh, qs, sc, cphase, warp, lane, qf, qs0, qs1)) {
+        flag(a.err, KVQ_DEVERR_TIMEOUT);
+        return;
+      }
+      nxt = next_unit_in_range(cur, x1, pre_s, B, H);
+      if (nxt >= 0) prefetch_query(a, nxt, qbuf ^ 1, qraw, fraw, warp, lane);
       st.reset();
     }
     if (warp < hd.z) {
@@ -836,6 +961,11 @@ struct Kernel {
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncSetAttribute(decode_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    // Ask for the largest shared-memory carveout: the occupancy used to size
+    // the single wave assumes it, and a smaller split (chosen by default)
+    // would fit one CTA fewer per SM and turn the wave into 1.5 waves.
+    cudaFuncSetAttribute(decode_kernel<KB, VB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
     done[dev] = true;
   }
   static int ctas_per_sm(int B) {

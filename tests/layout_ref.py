@@ -40,10 +40,10 @@ def value_offsets(bits: int):
 
 
 def unpack_blocks(pool: np.ndarray, bits: int, is_key: bool, heads: int) -> np.ndarray:
-    """pool: uint8 [num_blocks * heads * block_bytes] -> int32 codes
+    """pool: uint8 [heads * num_blocks * block_bytes] (head-major) -> int32 codes
     [num_blocks, heads, 16, 128] (two's complement), or uint16 bf16 bits for bits == 16."""
     bb = block_bytes(bits)
-    blocks = pool.reshape(-1, heads, bb)
+    blocks = pool.reshape(heads, -1, bb).transpose(1, 0, 2)
     off, sh = (key_offsets if is_key else value_offsets)(bits)
     if bits == 16:
         lo = blocks[..., off].astype(np.uint16)
@@ -64,3 +64,8 @@ def offsets_are_a_permutation(bits: int, is_key: bool) -> bool:
     cells = (off * 2 + sh // 4).ravel() if bits == 4 else off.ravel()
     n = block_bytes(bits) * (2 if bits == 4 else 1)
     return np.array_equal(np.sort(cells), np.arange(n))
+
+
+def scales_by_block(pool: np.ndarray, heads: int) -> np.ndarray:
+    """float [heads * num_blocks * 16] (head-major) -> [num_blocks, heads, 16]."""
+    return pool.reshape(heads, -1, BLOCK).transpose(1, 0, 2)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from harness import GpuRun, compare_outputs, oracle_decode, oracle_state, small_workload
-from layout_ref import unpack_blocks
+from layout_ref import scales_by_block, unpack_blocks
 from oracle import kvq_oracle as O
 from synth import WORKLOADS, make_inputs
 
@@ -73,8 +73,8 @@ def check_stored_cache(inp, run, units=None, max_positions=None):
         else:
             np.testing.assert_array_equal(kc[phys, :, tok], st["k_codes"][pos])
             np.testing.assert_array_equal(vc[phys, :, tok], st["v_codes"][pos])
-            ks = pools["k_scales"].reshape(-1, w.kv_heads, 16)[phys, :, tok]
-            vs = pools["v_scales"].reshape(-1, w.kv_heads, 16)[phys, :, tok]
+            ks = scales_by_block(pools["k_scales"], w.kv_heads)[phys, :, tok]
+            vs = scales_by_block(pools["v_scales"], w.kv_heads)[phys, :, tok]
             np.testing.assert_array_equal(ks.view(np.uint32), st["k_scale"][pos].astype(np.float32).view(np.uint32))
             np.testing.assert_array_equal(vs.view(np.uint32), st["v_scale"][pos].astype(np.float32).view(np.uint32))
         checked += len(pos)
@@ -204,8 +204,8 @@ def test_step_append_equals_bulk_fill():
     kc_b = unpack_blocks(a["k_codes"], 4, True, w.kv_heads)
     vc_s = unpack_blocks(step_cache.v_codes.cpu().numpy(), 4, False, w.kv_heads)
     vc_b = unpack_blocks(a["v_codes"], 4, False, w.kv_heads)
-    ks_s = step_cache.k_scales.cpu().numpy().reshape(-1, w.kv_heads, 16)
-    ks_b = a["k_scales"].reshape(-1, w.kv_heads, 16)
+    ks_s = scales_by_block(step_cache.k_scales.cpu().numpy(), w.kv_heads)
+    ks_b = scales_by_block(a["k_scales"], w.kv_heads)
     for b in range(w.batch):
         for p in range(max(int(inp.lengths[b]) - w.window, 0)):
             ph, t = inp.block_table[b, p // 16], p % 16
