@@ -44,8 +44,9 @@
  *         bf16 : chunk = mt, word = 2*hi + (j >> 1), element j & 1 of the word
  *     Byte offset = chunk*512 + lane*16 + word*4 + (byte or nibble/2 or 2*element);
  *     for int8 keys "byte" is the offset inside the lane's 16 bytes.  Nibble n
- *     of a little-endian 32-bit word occupies bits 4n..4n+3.  Codes are two's
- *     complement: int8 in [-127,127], int4 in [-8,7] (-8 never produced).
+ *     of a little-endian 32-bit word occupies bits 4n..4n+3.  Codes are stored
+ *     offset-binary: an int8 code c in [-127,127] is the byte c + 128, an int4
+ *     code c in [-8,7] (-8 never produced) is the nibble c + 8.
  *   Scale pool  : float [num_kv_heads][num_blocks][16], natural token order
  *                 (absent for a bf16 cache).
  *   Window ring : bf16 [window_batch][num_kv_heads][window / 16][4096 bytes]:
@@ -80,7 +81,7 @@ typedef enum {
 #define KVQ_DEVERR_BLOCK_ID 1u  /* block-table entry outside [0, num_blocks)        */
 #define KVQ_DEVERR_SEQ_LEN 2u   /* length < 0 or beyond the block table's capacity  */
 #define KVQ_DEVERR_TIMEOUT 4u   /* a pipeline wait gave up (the CTA skipped work)   */
-#define KVQ_DEVERR_RANGE 8u     /* a value scale above 65504 (fp16 operand range)   */
+#define KVQ_DEVERR_RANGE 8u     /* a value scale above 1023 (fp16 weight range)     */
 #define KVQ_DEVERR_POSITION 16u /* append: sequence index or position out of range  */
 
 /* kvq_append modes */

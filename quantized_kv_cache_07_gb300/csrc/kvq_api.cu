@@ -69,9 +69,14 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Stream CTAs for one wave of `slots` resident CTAs: the window CTAs (one per
 // unit, launched first) take their slots out of the wave, down to half of it.
-int stream_ctas_for(int slots, int window_ctas) {
-  const int left = slots - window_ctas;
-  return left > slots / 2 ? left : (slots / 2 > 0 ? slots / 2 : 1);
+// When the units fit in the wave and only a few CTAs would be lost, the count
+// is rounded down to a multiple of the unit count: with equal lengths every
+// stream CTA then holds one segment of one unit (no unit boundary inside).
+int stream_ctas_for(int slots, int window_ctas, int units) {
+  int left = slots - window_ctas;
+  left = left > slots / 2 ? left : (slots / 2 > 0 ? slots / 2 : 1);
+  if (units > 0 && units <= left && left % units <= left / 16) left -= left % units;
+  return left;
 }
 
 // Stream CTAs for the current device (0 on failure).
@@ -80,7 +85,7 @@ int auto_stream_ctas(const kvq_cache_desc* c, int batch) {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, batch);
-  return stream_ctas_for(sms * per, c->window > 0 ? batch * c->num_kv_heads : 0);
+  return stream_ctas_for(sms * per, c->window > 0 ? batch * c->num_kv_heads : 0, batch * c->num_kv_heads);
 }
 
 kvq_status check_decode_shape(const kvq_cache_desc* c, int batch, int q_heads) {
@@ -178,7 +183,7 @@ kvq_status kvq_make_decode_plan(int32_t batch, int32_t q_heads, int32_t num_kv_h
   int P = stream_ctas;
   if (P <= 0) {
     if (num_sms < 1 || ctas_per_sm < 1) return KVQ_ERR_INVALID_ARG;
-    P = stream_ctas_for(num_sms * ctas_per_sm, window > 0 ? batch * num_kv_heads : 0);
+    P = stream_ctas_for(num_sms * ctas_per_sm, window > 0 ? batch * num_kv_heads : 0, batch * num_kv_heads);
   }
   const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, num_kv_heads, window, P);
   plan->stream_ctas = L.stream_ctas;

@@ -62,7 +62,7 @@ __device__ void store_codes(bool is_key, int bits, uint8_t* blk, int tok, const 
     for (int j = 0; j < 4; ++j) {
       const int d = 4 * lane + j;
       const Loc L = is_key ? key_loc(8, tok, d) : value_loc(8, tok, d);
-      blk[L.byte] = uint8_t(int8_t(code[j]));
+      blk[L.byte] = uint8_t(code[j] + 128);  // offset binary
     }
     return;
   }
@@ -76,7 +76,7 @@ __device__ void store_codes(bool is_key, int bits, uint8_t* blk, int tok, const 
       const int d = 4 * lane + j;
       const Loc L = key_loc(4, tok, d);
       const int nib = ((L.byte & 3) << 1) | (L.shift >> 2);
-      part |= (uint32_t(code[j]) & 0xFu) << (4 * nib);
+      part |= uint32_t(code[j] + 8) << (4 * nib);  // offset binary
       word_off = L.byte & ~3;
     }
     const uint32_t word = part | __shfl_xor_sync(kFull, part, 1);
@@ -91,7 +91,7 @@ __device__ void store_codes(bool is_key, int bits, uint8_t* blk, int tok, const 
     const int nib = ((L.byte & 3) << 1) | (L.shift >> 2);
     uint32_t* w = reinterpret_cast<uint32_t*>(blk + (L.byte & ~3));
     atomicAnd(w, ~(0xFu << (4 * nib)));
-    atomicOr(w, (uint32_t(code[j]) & 0xFu) << (4 * nib));
+    atomicOr(w, uint32_t(code[j] + 8) << (4 * nib));  // offset binary
   }
 }
 
@@ -224,10 +224,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
     if (bits == 16) {
       v = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(blk + L.byte));
     } else if (bits == 8) {
-      v = __fmul_rn(float(int8_t(blk[L.byte])), s);
+      v = __fmul_rn(float(int(blk[L.byte]) - 128), s);
     } else {
-      int nib = (blk[L.byte] >> L.shift) & 0xF;
-      nib = nib >= 8 ? nib - 16 : nib;
+      const int nib = ((blk[L.byte] >> L.shift) & 0xF) - 8;
       v = __fmul_rn(float(nib), s);
     }
     out[j] = v;

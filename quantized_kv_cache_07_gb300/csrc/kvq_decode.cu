@@ -199,6 +199,11 @@ struct Params {
   int Uw;  // window CTAs launched first in the grid (one per unit, 0 without a window)
 };
 
+// Slack of the lazy running maximum (log2 units) and the largest value scale
+// whose fp16 weight p * s_v (p <= 2^kMaxSlack) stays below 65504.
+constexpr float kMaxSlack = 6.f;
+constexpr float kMaxValueScale = 1023.f;
+
 // A stream CTA owns at least this many blocks (fewer, deeper splits for tiny problems).
 constexpr int kMinBlocksPerCta = 16;
 
@@ -273,18 +278,27 @@ __device__ __forceinline__ void process_block(const uint8_t* kb, const uint8_t* 
     sv1 = vs[g + 8];
   }
   const bool v0 = g < valid, v1 = g + 8 < valid;
-  const float x00 = v0 ? acc[0] * (sk0 * qs0) : kNegInf;
-  const float x01 = v0 ? acc[1] * (sk0 * qs1) : kNegInf;
-  const float x10 = v1 ? acc[2] * (sk1 * qs0) : kNegInf;
-  const float x11 = v1 ? acc[3] * (sk1 * qs1) : kNegInf;
-  float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+  const float f0 = sk0 * qs0, f1 = sk0 * qs1, f2 = sk1 * qs0, f3 = sk1 * qs1;
+  float x00 = acc[0] * f0, x01 = acc[1] * f1, x10 = acc[2] * f2, x11 = acc[3] * f3;
+  if (valid < kBlock) {  // the last block of a unit may be partial
+    x00 = v0 ? x00 : kNegInf;
+    x01 = v0 ? x01 : kNegInf;
+    x10 = v1 ? x10 : kNegInf;
+    x11 = v1 ? x11 : kNegInf;
   }
-  const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-  if (__any_sync(kFull, (mn0 > st.m0) || (mn1 > st.m1))) {
+  // Lazy running maximum: the reference m only moves (with a full reduction
+  // and a rescale of l and O) when a score exceeds it by more than
+  // kMaxSlack; otherwise the weights 2^(x - m) stay below 2^kMaxSlack.
+  const bool over = (x00 > st.m0 + kMaxSlack) || (x10 > st.m0 + kMaxSlack) || (x01 > st.m1 + kMaxSlack) ||
+                    (x11 > st.m1 + kMaxSlack);
+  if (__any_sync(kFull, over)) {
+    float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+    }
+    const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
     const float al0 = (mn0 == kNegInf) ? 1.f : exp2f(st.m0 - mn0);
     const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(st.m1 - mn1);
     st.l0 *= al0;
@@ -312,7 +326,8 @@ __device__ __forceinline__ void process_block(const uint8_t* kb, const uint8_t* 
     pk0lo = pack_bf162(p00 - __low2float(h0), p10 - __high2float(h0));
     pk1lo = pack_bf162(p01 - __low2float(h1), p11 - __high2float(h1));
   } else {
-    if ((v0 && sv0 > 65504.f) || (v1 && sv1 > 65504.f)) flag(err, KVQ_DEVERR_RANGE);
+    // weights are at most 2^kMaxSlack, so p * s_v stays finite in fp16 while s_v <= kMaxValueScale
+    if ((v0 && sv0 > kMaxValueScale) || (v1 && sv1 > kMaxValueScale)) flag(err, KVQ_DEVERR_RANGE);
     pk0 = pack_half2(v0 ? p00 * sv0 : 0.f, v1 ? p10 * sv1 : 0.f);
     pk1 = pack_half2(v0 ? p01 * sv0 : 0.f, v1 ? p11 * sv1 : 0.f);
   }

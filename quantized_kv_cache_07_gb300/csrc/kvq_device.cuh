@@ -62,30 +62,32 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // ------------------------------------------------------------------ conversions
-// Four int8 codes (two's complement, bytes b0..b3 of w) -> fp16 pairs
-// lo = (b0, b1), hi = (b2, b3), exact: 1024 + (code + 128) is built by placing
-// the biased byte into the mantissa of 1024.0 (0x6400), then 1152 is subtracted.
+// Codes are stored offset-binary: an int8 code c is the byte c + 128, an int4
+// code c is the nibble c + 8.  Placing the biased value u in the mantissa of
+// 1024.0 (fp16 0x6400) gives 1024 + u exactly; one fp16 subtraction of
+// 1024 + bias then yields c exactly.
+
+// Four int8 codes (biased bytes b0..b3 of w) -> fp16 pairs lo = (c0, c1), hi = (c2, c3).
 __device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
-  uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
-  const uint32_t bias = 0x64806480u;  // (1152, 1152)
+  const uint32_t a = __byte_perm(w, 0x64646464u, 0x4140);
+  const uint32_t b = __byte_perm(w, 0x64646464u, 0x4342);
+  const uint32_t bias = 0x64806480u;  // (1152, 1152) = 1024 + 128
   asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
   asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
 }
 
-// Eight int4 codes (nibbles n0..n7 of w) -> fp16 pairs (n0,n4) (n1,n5) (n2,n6) (n3,n7), exact.
+// Eight int4 codes (biased nibbles n0..n7 of w) -> fp16 pairs (c0,c4) (c1,c5) (c2,c6) (c3,c7).
+// Odd nibbles land at 16 * u in the mantissa; a fused (x / 16 - 72) recovers c.
 __device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
                                             uint32_t& p3) {
-  const uint32_t u = w ^ 0x88888888u;  // two's complement nibble -> nibble + 8
-  const uint32_t s = u >> 8;
-  const uint32_t a = (u & 0x000F000Fu) | 0x64006400u;  // 1024 + n0, 1024 + n4
-  const uint32_t b = (u & 0x00F000F0u) | 0x64006400u;  // 1024 + 16 n1, 1024 + 16 n5
+  const uint32_t s = w >> 8;
+  const uint32_t a = (w & 0x000F000Fu) | 0x64006400u;  // 1024 + u0, 1024 + u4
+  const uint32_t b = (w & 0x00F000F0u) | 0x64006400u;  // 1024 + 16 u1, 1024 + 16 u5
   const uint32_t c = (s & 0x000F000Fu) | 0x64006400u;
   const uint32_t d = (s & 0x00F000F0u) | 0x64006400u;
-  const uint32_t bias = 0x64086408u;   // 1032
+  const uint32_t bias = 0x64086408u;       // 1032 = 1024 + 8
   const uint32_t sixteenth = 0x2C002C00u;  // 1/16
-  const uint32_t m72 = 0xD480D480u;    // -72 = -(1024/16 + 8)
+  const uint32_t m72 = 0xD480D480u;        // -72 = -(1024/16 + 8)
   asm("sub.f16x2 %0, %1, %2;" : "=r"(p0) : "r"(a), "r"(bias));
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p1) : "r"(b), "r"(sixteenth), "r"(m72));
   asm("sub.f16x2 %0, %1, %2;" : "=r"(p2) : "r"(c), "r"(bias));

@@ -41,7 +41,8 @@ def value_offsets(bits: int):
 
 def unpack_blocks(pool: np.ndarray, bits: int, is_key: bool, heads: int) -> np.ndarray:
     """pool: uint8 [heads * num_blocks * block_bytes] (head-major) -> int32 codes
-    [num_blocks, heads, 16, 128] (two's complement), or uint16 bf16 bits for bits == 16."""
+    [num_blocks, heads, 16, 128], or uint16 bf16 bits for bits == 16.  Codes are
+    stored offset-binary (byte = code + 128, nibble = code + 8)."""
     bb = block_bytes(bits)
     blocks = pool.reshape(heads, -1, bb).transpose(1, 0, 2)
     off, sh = (key_offsets if is_key else value_offsets)(bits)
@@ -51,9 +52,8 @@ def unpack_blocks(pool: np.ndarray, bits: int, is_key: bool, heads: int) -> np.n
         return lo | (hi << 8)
     raw = blocks[..., off].astype(np.int32)
     if bits == 8:
-        return np.where(raw >= 128, raw - 256, raw)
-    nib = (raw >> sh) & 0xF
-    return np.where(nib >= 8, nib - 16, nib)
+        return raw - 128
+    return ((raw >> sh) & 0xF) - 8
 
 
 def offsets_are_a_permutation(bits: int, is_key: bool) -> bool:

@@ -51,13 +51,17 @@ def test_status_strings_and_block_bytes(lib):
 
 def test_decode_plan_one_wave_of_ctas(lib):
     p = lib.kvq_make_decode_plan(64, 32, 8, 0, num_sms=152, ctas_per_sm=3)
-    assert p.stream_ctas == 456 and p.window_ctas == 0 and p.units == 512
+    assert p.stream_ctas == 456 and p.window_ctas == 0 and p.units == 512      # units > CTAs: no rounding
+    p5 = lib.kvq_make_decode_plan(4, 64, 8, 0, num_sms=152, ctas_per_sm=3)
+    assert p5.stream_ctas == 448                                               # 14 CTAs per unit
+    p3 = lib.kvq_make_decode_plan(32, 32, 8, 0, num_sms=152, ctas_per_sm=3)
+    assert p3.stream_ctas == 456                                               # 456 % 256 too large to drop
     assert p.partial_slots == 456 + 512
     slots = p.partial_slots
     assert p.workspace_bytes >= slots * 8 * (128 + 2) * 4 + 512 * 4
     pw = lib.kvq_make_decode_plan(8, 32, 8, 128, num_sms=152, ctas_per_sm=3)
     # window CTAs (one per unit) run first and take their slots out of the wave
-    assert pw.window_ctas == 64 and pw.stream_ctas == 456 - 64
+    assert pw.window_ctas == 64 and pw.stream_ctas == 384        # 456 - 64 = 392, rounded to 6 x 64 units
     assert pw.partial_slots == pw.stream_ctas + 64 + 64
     pbig = lib.kvq_make_decode_plan(64, 32, 8, 128, num_sms=152, ctas_per_sm=3)
     assert pbig.window_ctas == 512 and pbig.stream_ctas == 228        # never below half a wave
