@@ -63,14 +63,18 @@ struct Fmt {
   static constexpr int kVBB = block_bytes(VB);
   static constexpr int kSCB = kBf16 ? 0 : kBlock * 4;  // scale bytes per block per tensor
   static constexpr int kPerBlock = kKBB + kVBB + 2 * kSCB;
-  static constexpr int kStageBytes = kConsumerWarps * kPerBlock;
+  // 4-bit keys: each consumer warp takes two blocks per stage (two independent
+  // dependency chains, one softmax reduction per 32 tokens)
+  static constexpr int kBPW = (KB == 4) ? 2 : 1;
+  static constexpr int kBlocksPerStage = kConsumerWarps * kBPW;
+  static constexpr int kStageBytes = kBlocksPerStage * kPerBlock;
   static constexpr int kStagesRaw = 53248 / kStageBytes;  // ~52 KB ring: 3 CTAs per SM
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   // stage sub-buffers
   static constexpr int kOffK = 0;
-  static constexpr int kOffV = kConsumerWarps * kKBB;
-  static constexpr int kOffKS = kOffV + kConsumerWarps * kVBB;
-  static constexpr int kOffVS = kOffKS + kConsumerWarps * kSCB;
+  static constexpr int kOffV = kBlocksPerStage * kKBB;
+  static constexpr int kOffKS = kOffV + kBlocksPerStage * kVBB;
+  static constexpr int kOffVS = kOffKS + kBlocksPerStage * kSCB;
 };
 
 // Shared-memory map after the stage ring (all offsets 16-byte aligned).
@@ -199,6 +203,14 @@ struct Params {
   int Uw;  // window CTAs launched first in the grid (one per unit, 0 without a window)
 };
 
+// Base-2 exponential: the PTX ex2.approx.f32 instruction (max relative error
+// about 2^-22 per the PTX ISA; ex2(-inf) = +0, subnormal results kept).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Slack of the lazy running maximum (log2 units) and the largest value scale
 // whose fp16 weight p * s_v (p <= 2^kMaxSlack) stays below 65504.
 constexpr float kMaxSlack = 6.f;
@@ -260,47 +272,61 @@ struct WarpState {
   }
 };
 
-// One 16-token block: scores on the codes, per-token key scale after the dot
-// product, online softmax, value scale folded into the weight, value MMA.
-template <int KB, int VB>
-__device__ __forceinline__ void process_block(const uint8_t* kb, const uint8_t* vb, const float* ks, const float* vs,
-                                              int valid, const uint32_t (&qf)[16], float qs0, float qs1,
-                                              WarpState& st, int lane, uint32_t* err) {
+// NB (1 or 2) 16-token blocks of one warp: scores on the codes, per-token key
+// scale after the dot product, online softmax, value scale folded into the
+// weight, value MMA.  With NB = 2 the two blocks' chains interleave and share
+// one lazy-maximum test and reduction.
+template <int KB, int VB, int NB>
+__device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], const uint8_t* const (&vb)[NB],
+                                               const float* const (&ks)[NB], const float* const (&vs)[NB],
+                                               const int (&valid)[NB], const uint32_t (&qf)[16], float qs0,
+                                               float qs1, WarpState& st, int lane, uint32_t* err) {
   constexpr bool kBf16 = (KB == 16);
   const int g = lane >> 2, t = lane & 3;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  score_block<KB>(kb, qf, acc, lane);
-  float sk0 = 1.f, sk1 = 1.f, sv0 = 1.f, sv1 = 1.f;
-  if constexpr (!kBf16) {
-    sk0 = ks[g];
-    sk1 = ks[g + 8];
-    sv0 = vs[g];
-    sv1 = vs[g + 8];
-  }
-  const bool v0 = g < valid, v1 = g + 8 < valid;
-  const float f0 = sk0 * qs0, f1 = sk0 * qs1, f2 = sk1 * qs0, f3 = sk1 * qs1;
-  float x00 = acc[0] * f0, x01 = acc[1] * f1, x10 = acc[2] * f2, x11 = acc[3] * f3;
-  if (valid < kBlock) {  // the last block of a unit may be partial
-    x00 = v0 ? x00 : kNegInf;
-    x01 = v0 ? x01 : kNegInf;
-    x10 = v1 ? x10 : kNegInf;
-    x11 = v1 ? x11 : kNegInf;
+  float x[NB][4];
+  float sv[NB][2];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    score_block<KB>(kb[j], qf, acc, lane);
+    float sk0 = 1.f, sk1 = 1.f;
+    sv[j][0] = sv[j][1] = 1.f;
+    if constexpr (!kBf16) {
+      sk0 = ks[j][g];
+      sk1 = ks[j][g + 8];
+      sv[j][0] = vs[j][g];
+      sv[j][1] = vs[j][g + 8];
+    }
+    x[j][0] = acc[0] * (sk0 * qs0);  // token g, query 2t
+    x[j][1] = acc[1] * (sk0 * qs1);  // token g, query 2t+1
+    x[j][2] = acc[2] * (sk1 * qs0);  // token g+8, query 2t
+    x[j][3] = acc[3] * (sk1 * qs1);  // token g+8, query 2t+1
+    if (valid[j] < kBlock) {  // the last block of a unit may be partial
+      const bool v0 = g < valid[j], v1 = g + 8 < valid[j];
+      x[j][0] = v0 ? x[j][0] : kNegInf;
+      x[j][1] = v0 ? x[j][1] : kNegInf;
+      x[j][2] = v1 ? x[j][2] : kNegInf;
+      x[j][3] = v1 ? x[j][3] : kNegInf;
+    }
   }
   // Lazy running maximum: the reference m only moves (with a full reduction
   // and a rescale of l and O) when a score exceeds it by more than
   // kMaxSlack; otherwise the weights 2^(x - m) stay below 2^kMaxSlack.
-  const bool over = (x00 > st.m0 + kMaxSlack) || (x10 > st.m0 + kMaxSlack) || (x01 > st.m1 + kMaxSlack) ||
-                    (x11 > st.m1 + kMaxSlack);
-  if (__any_sync(kFull, over)) {
-    float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+  float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+  for (int j = 1; j < NB; ++j) {
+    mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
+    mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
+  }
+  if (__any_sync(kFull, (mx0 > st.m0 + kMaxSlack) || (mx1 > st.m1 + kMaxSlack))) {
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
       mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
     }
     const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-    const float al0 = (mn0 == kNegInf) ? 1.f : exp2f(st.m0 - mn0);
-    const float al1 = (mn1 == kNegInf) ? 1.f : exp2f(st.m1 - mn1);
+    const float al0 = (mn0 == kNegInf) ? 1.f : ex2(st.m0 - mn0);
+    const float al1 = (mn1 == kNegInf) ? 1.f : ex2(st.m1 - mn1);
     st.l0 *= al0;
     st.l1 *= al1;
 #pragma unroll
@@ -314,37 +340,50 @@ __device__ __forceinline__ void process_block(const uint8_t* kb, const uint8_t* 
     st.m1 = mn1;
   }
   const float base0 = (st.m0 == kNegInf) ? 0.f : st.m0, base1 = (st.m1 == kNegInf) ? 0.f : st.m1;
-  const float p00 = exp2f(x00 - base0), p10 = exp2f(x10 - base0);
-  const float p01 = exp2f(x01 - base1), p11 = exp2f(x11 - base1);
-  st.l0 += p00 + p10;
-  st.l1 += p01 + p11;
-  uint32_t pk0, pk1, pk0lo = 0, pk1lo = 0;
-  if constexpr (kBf16) {
-    const __nv_bfloat162 h0 = __floats2bfloat162_rn(p00, p10), h1 = __floats2bfloat162_rn(p01, p11);
-    pk0 = *reinterpret_cast<const uint32_t*>(&h0);
-    pk1 = *reinterpret_cast<const uint32_t*>(&h1);
-    pk0lo = pack_bf162(p00 - __low2float(h0), p10 - __high2float(h0));
-    pk1lo = pack_bf162(p01 - __low2float(h1), p11 - __high2float(h1));
-  } else {
-    // weights are at most 2^kMaxSlack, so p * s_v stays finite in fp16 while s_v <= kMaxValueScale
-    if ((v0 && sv0 > kMaxValueScale) || (v1 && sv1 > kMaxValueScale)) flag(err, KVQ_DEVERR_RANGE);
-    pk0 = pack_half2(v0 ? p00 * sv0 : 0.f, v1 ? p10 * sv1 : 0.f);
-    pk1 = pack_half2(v0 ? p01 * sv0 : 0.f, v1 ? p11 * sv1 : 0.f);
-  }
-  // transpose the weights from the score accumulator layout (token rows, query
-  // columns) into the B-operand layout of the value contraction
   const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
-  const uint32_t r00 = __shfl_sync(kFull, pk0, src0), r01 = __shfl_sync(kFull, pk1, src0);
-  const uint32_t r10 = __shfl_sync(kFull, pk0, src1), r11 = __shfl_sync(kFull, pk1, src1);
-  const uint32_t b0 = (g & 1) ? r01 : r00, b1 = (g & 1) ? r11 : r10;
-  uint32_t b0lo = 0, b1lo = 0;
-  if constexpr (kBf16) {
-    const uint32_t q00 = __shfl_sync(kFull, pk0lo, src0), q01 = __shfl_sync(kFull, pk1lo, src0);
-    const uint32_t q10 = __shfl_sync(kFull, pk0lo, src1), q11 = __shfl_sync(kFull, pk1lo, src1);
-    b0lo = (g & 1) ? q01 : q00;
-    b1lo = (g & 1) ? q11 : q10;
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    const float p00 = ex2(x[j][0] - base0), p10 = ex2(x[j][2] - base0);
+    const float p01 = ex2(x[j][1] - base1), p11 = ex2(x[j][3] - base1);
+    st.l0 += p00 + p10;
+    st.l1 += p01 + p11;
+    uint32_t pk0, pk1, pk0lo = 0, pk1lo = 0;
+    if constexpr (kBf16) {
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(p00, p10), h1 = __floats2bfloat162_rn(p01, p11);
+      pk0 = *reinterpret_cast<const uint32_t*>(&h0);
+      pk1 = *reinterpret_cast<const uint32_t*>(&h1);
+      pk0lo = pack_bf162(p00 - __low2float(h0), p10 - __high2float(h0));
+      pk1lo = pack_bf162(p01 - __low2float(h1), p11 - __high2float(h1));
+    } else {
+      // weights are at most 2^kMaxSlack, so p * s_v stays finite in fp16 while s_v <= kMaxValueScale
+      float w00 = p00 * sv[j][0], w10 = p10 * sv[j][1], w01 = p01 * sv[j][0], w11 = p11 * sv[j][1];
+      float svmax = fmaxf(sv[j][0], sv[j][1]);
+      if (valid[j] < kBlock) {  // scales of empty slots of a partial block are not data
+        const bool v0 = g < valid[j], v1 = g + 8 < valid[j];
+        w00 = v0 ? w00 : 0.f;
+        w01 = v0 ? w01 : 0.f;
+        w10 = v1 ? w10 : 0.f;
+        w11 = v1 ? w11 : 0.f;
+        svmax = fmaxf(v0 ? sv[j][0] : 0.f, v1 ? sv[j][1] : 0.f);
+      }
+      if (svmax > kMaxValueScale) flag(err, KVQ_DEVERR_RANGE);
+      pk0 = pack_half2(w00, w10);
+      pk1 = pack_half2(w01, w11);
+    }
+    // transpose the weights from the score accumulator layout (token rows,
+    // query columns) into the B-operand layout of the value contraction
+    const uint32_t r00 = __shfl_sync(kFull, pk0, src0), r01 = __shfl_sync(kFull, pk1, src0);
+    const uint32_t r10 = __shfl_sync(kFull, pk0, src1), r11 = __shfl_sync(kFull, pk1, src1);
+    const uint32_t b0 = (g & 1) ? r01 : r00, b1 = (g & 1) ? r11 : r10;
+    uint32_t b0lo = 0, b1lo = 0;
+    if constexpr (kBf16) {
+      const uint32_t q00 = __shfl_sync(kFull, pk0lo, src0), q01 = __shfl_sync(kFull, pk1lo, src0);
+      const uint32_t q10 = __shfl_sync(kFull, pk0lo, src1), q11 = __shfl_sync(kFull, pk1lo, src1);
+      b0lo = (g & 1) ? q01 : q00;
+      b1lo = (g & 1) ? q11 : q10;
+    }
+    value_block<VB>(vb[j], b0, b1, b0lo, b1lo, st.O, lane);
   }
-  value_block<VB>(vb, b0, b1, b0lo, b1lo, st.O, lane);
 }
 
 // Consumer warps write the query group of unit (b, h) into shared memory as
@@ -768,7 +807,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     for (int j = warp; j < nwb; j += kConsumerWarps) {
       const uint8_t* kb = a.c.k_win + (ring0 + j) * block_bytes(16);
       const uint8_t* vb = a.c.v_win + (ring0 + j) * block_bytes(16);
-      process_block<16, 16>(kb, vb, nullptr, nullptr, min(kBlock, nw - j * kBlock), qf, qs0, qs1, st, lane, a.err);
+      const uint8_t* const kbs[1] = {kb};
+      const uint8_t* const vbs[1] = {vb};
+      const float* const nos[1] = {nullptr};
+      const int val[1] = {min(kBlock, nw - j * kBlock)};
+      process_blocks<16, 16, 1>(kbs, vbs, nos, nos, val, qf, qs0, qs1, st, lane, a.err);
     }
     const size_t slot = size_t(P) + U + u;
     if (!finish_segment(a, st, u, slot, len_s, pre_s, T, Pe, P, sc, cphase, warp, lane, tid))
@@ -802,7 +845,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     long long ustart;
     locate_unit(x0, pre_s, B, H, b, h, nblk, ustart);
     long long x = x0;
-    int it = 0;
+    int it = 0, s = 0;
+    uint32_t ph = 0;  // stage index and the parity of its current use
     bool ok = true;
     // 32 block-table entries of sequence tc_b, logical blocks tc_base + lane
     int tc_b = -1, tc_base = 0, tc_val = 0;
@@ -817,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         ustart = (long long)H * pre_s[b] + (long long)h * nblk;
       }
       const long long rem = (x1 - x) < (ustart + nblk - x) ? (x1 - x) : (ustart + nblk - x);
-      const int n = int(rem < kConsumerWarps ? rem : kConsumerWarps);
+      const int n = int(rem < F::kBlocksPerStage ? rem : F::kBlocksPerStage);
       const int local = int(x - ustart);
       if (tc_b != b || local < tc_base || local + n > tc_base + 32) {
         tc_b = b;
@@ -833,10 +877,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         }
         tc_val = v;
       }
-      const int s = it % S;
       if (it >= S) {
         bool w_ok = true;
-        if (lane == 0) w_ok = mbar_wait(&empty[s], ((it / S) - 1) & 1);
+        if (lane == 0) w_ok = mbar_wait(&empty[s], ph ^ 1u);
         if (!__shfl_sync(kFull, w_ok ? 1 : 0, 0)) {
           if (lane == 0) flag(a.err, KVQ_DEVERR_TIMEOUT);
           ok = false;
@@ -851,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       int run = 1;
       bool contig = true;
 #pragma unroll
-      for (int j = 1; j < kConsumerWarps; ++j) {
+      for (int j = 1; j < F::kBlocksPerStage; ++j) {
         const int nx = __shfl_down_sync(kFull, phys, j);
         contig = contig && (lane + j < n) && (nx == phys + j);
         run += contig ? 1 : 0;
@@ -873,11 +916,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       }
       x += n;
       ++it;
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     if (lane != 0) return;
     if (ok) {  // terminator stage
-      const int s = it % S;
-      if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1)) {
+      if (it >= S && !mbar_wait(&empty[s], ph ^ 1u)) {
         flag(a.err, KVQ_DEVERR_TIMEOUT);
       } else {
         hdr[s] = make_int4(-1, 0, 0, 0);
@@ -918,9 +964,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       return;
     }
   }
-  for (int it = 0;; ++it) {
-    const int s = it % S;
-    if (!mbar_wait(&full[s], (it / S) & 1)) {
+  int s = 0;
+  uint32_t ph = 0;  // stage index and the parity of its current use
+  for (;;) {
+    if (!mbar_wait(&full[s], ph)) {
       flag(a.err, KVQ_DEVERR_TIMEOUT);
       return;
     }
@@ -951,13 +998,38 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     }
     if (warp < hd.z) {
       const uint8_t* stg = smem + s * F::kStageBytes;
-      const float* ks = F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffKS + warp * F::kSCB);
-      const float* vs = F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffVS + warp * F::kSCB);
-      process_block<KB, VB>(stg + F::kOffK + warp * F::kKBB, stg + F::kOffV + warp * F::kVBB, ks, vs,
-                            min(kBlock, cur_lq - (hd.y + warp) * kBlock), qf, qs0, qs1, st, lane, a.err);
+      auto kp = [&](int j) { return stg + F::kOffK + j * F::kKBB; };
+      auto vp = [&](int j) { return stg + F::kOffV + j * F::kVBB; };
+      auto ksp = [&](int j) {
+        return F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffKS + j * F::kSCB);
+      };
+      auto vsp = [&](int j) {
+        return F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffVS + j * F::kSCB);
+      };
+      auto val = [&](int j) { return min(kBlock, cur_lq - (hd.y + j) * kBlock); };
+      const int j0 = warp, j1 = warp + kConsumerWarps;
+      if (F::kBPW == 2 && j1 < hd.z) {
+        const uint8_t* const kbs[2] = {kp(j0), kp(j1)};
+        const uint8_t* const vbs[2] = {vp(j0), vp(j1)};
+        const float* const kss[2] = {ksp(j0), ksp(j1)};
+        const float* const vss[2] = {vsp(j0), vsp(j1)};
+        const int vals[2] = {val(j0), val(j1)};
+        process_blocks<KB, VB, 2>(kbs, vbs, kss, vss, vals, qf, qs0, qs1, st, lane, a.err);
+      } else {
+        const uint8_t* const kbs[1] = {kp(j0)};
+        const uint8_t* const vbs[1] = {vp(j0)};
+        const float* const kss[1] = {ksp(j0)};
+        const float* const vss[1] = {vsp(j0)};
+        const int vals[1] = {val(j0)};
+        process_blocks<KB, VB, 1>(kbs, vbs, kss, vss, vals, qf, qs0, qs1, st, lane, a.err);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
   }
 }
 
