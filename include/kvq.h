@@ -200,6 +200,38 @@ kvq_status kvq_decode(const kvq_cache_desc* cache, const void* q, int32_t batch,
                       void* out, int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes,
                       int32_t stream_ctas, uint32_t* err_word, void* stream);
 
+/* Size of the fixed device scratch behind kvq_decode_static_scratch (bytes). */
+#define KVQ_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * kvq_decode_static_scratch -- kvq_decode for callers that cannot allocate.
+ * The pages have no counterpart to this entry point: it is a library
+ * integration variant of kvq_decode with identical arguments and results,
+ * minus the workspace.
+ * Some callers cannot call cudaMalloc on their decode path: code embedded in a
+ * host runtime that owns every device allocation (a plugin or custom operator
+ * given only input and output buffers), or loops that must not pay the
+ * implicit device synchronisation and allocator locking of cudaMalloc.  For
+ * them the split-attention scratch (partial records and merge counters) lives
+ * in one file-scope device array of KVQ_STATIC_SCRATCH_BYTES that every GPU
+ * loading the library holds until the process exits.  The caller still passes
+ * all inputs and outputs.
+ *   - A call whose plan (kvq_decode_device_plan) needs more than
+ *     KVQ_STATIC_SCRATCH_BYTES returns KVQ_ERR_WORKSPACE and launches nothing.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call clears the merge counters with cudaMemsetAsync on `stream`
+ *     (no allocation) and then runs kvq_decode on the shared array.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents: calls that overlap on the GPU (different streams, or several
+ *     host threads) race and corrupt each other's results.  Serialise them.
+ */
+kvq_status kvq_decode_static_scratch(const kvq_cache_desc* cache, const void* q, int32_t batch, int32_t q_heads,
+                                     const int32_t* seq_lens, const int32_t* block_table,
+                                     int32_t max_blocks_per_seq, void* out, int32_t out_fp32, float* lse,
+                                     int32_t stream_ctas, uint32_t* err_word, void* stream);
+
 /*
  * kvq_dequant -- read the block store back: x_hat = RN32(code * s)
  * ([P2] "Quantization needs a scale convention"), without the per-channel key

@@ -72,7 +72,11 @@ SIGNATURES = {
     "kvq_decode": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32,
                              c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_int32, c_void_p, c_void_p]),
     "kvq_dequant": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
+    "kvq_decode_static_scratch": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p,
+                                            c_int32, c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_void_p]),
 }
+
+STATIC_SCRATCH_BYTES = 8 << 20
 
 
 def load() -> ctypes.CDLL:
@@ -171,3 +175,17 @@ def kvq_dequant(desc: CacheDesc, slots, k_out, v_out, stream=None, n: int | None
     n = int(slots.shape[0]) if n is None else n
     _check(load().kvq_dequant(ctypes.byref(desc), _ptr(slots), n, _ptr(k_out), _ptr(v_out), _stream(stream)),
            "kvq_dequant")
+
+
+def kvq_decode_static_scratch(desc: CacheDesc, q, batch: int, q_heads: int, seq_lens, block_table,
+                              max_blocks_per_seq: int, out, lse=None, stream_ctas: int = 0, err_word=None,
+                              stream=None, out_fp32: bool | None = None):
+    """kvq_decode without a caller workspace (fixed device scratch inside the
+    library; see include/kvq.h for the size limit and the sharing rules)."""
+    if out_fp32 is None:
+        import torch
+        out_fp32 = out.dtype == torch.float32
+    _check(load().kvq_decode_static_scratch(ctypes.byref(desc), _ptr(q), batch, q_heads, _ptr(seq_lens),
+                                            _ptr(block_table), max_blocks_per_seq, _ptr(out), int(bool(out_fp32)),
+                                            _ptr(lse), stream_ctas, _ptr(err_word), _stream(stream)),
+           "kvq_decode_static_scratch")
