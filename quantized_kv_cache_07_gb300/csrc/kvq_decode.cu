@@ -736,6 +736,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   int* len_s = reinterpret_cast<int*>(smem + mp.len);
   int* pre_s = reinterpret_cast<int*>(smem + mp.pre);
 
+  // Programmatic dependent launch: this grid may be launched while the
+  // previous kernel on the stream is still finishing; wait here until it has
+  // completed (its writes visible) before touching any memory, then let the
+  // next kernel on the stream be launched early in turn.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---- sequence geometry: clamped lengths and block prefix sums
   const int W = a.c.window;
   const int cap = a.mbps * kBlock;
@@ -1080,7 +1087,18 @@ struct Kernel {
     ensure_attribute(dev);
     Params p{a, a.lay.stream_ctas, a.lay.window_ctas};
     const int grid = a.lay.window_ctas + a.lay.stream_ctas;
-    decode_kernel<KB, VB><<<grid, kThreads, smem, s>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<KB, VB>, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
 };
