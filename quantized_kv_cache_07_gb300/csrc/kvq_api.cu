@@ -108,6 +108,12 @@ DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas) {
   L.units = B * H;
   L.window_ctas = window > 0 ? L.units : 0;
   L.slots = stream_ctas + L.units + L.window_ctas;
+  // When the stream CTAs are a multiple of the units (equal lengths split
+  // unit-aligned) every CTA starts exactly one unit: no start cost needed.
+  // Otherwise starting a unit (query staging, record, ticket) is charged as
+  // kSwitchBlocks blocks of work so the split balances time, not blocks.
+  constexpr int kSwitchBlocks = 16;
+  L.switch_blocks = (L.units > 0 && L.units <= stream_ctas && stream_ctas % L.units == 0) ? 0 : kSwitchBlocks;
   size_t o = 0;
   L.off_counter = o;
   o = round_up(o + size_t(L.units) * 4, 256);

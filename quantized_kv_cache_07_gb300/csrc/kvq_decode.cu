@@ -90,6 +90,7 @@ struct SmemMap {
   int misc;      // int [4]
   int len;       // int [B]
   int pre;       // int [B+1]
+  int vpre;      // int [B+1]
   int total;
 };
 
@@ -107,6 +108,7 @@ __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, i
   m.misc = o;     o += 16;
   m.len = o;      o += ((B * 4 + 15) / 16) * 16;
   m.pre = o;      o += (((B + 1) * 4 + 15) / 16) * 16;
+  m.vpre = o;     o += (((B + 1) * 4 + 15) / 16) * 16;
   m.total = o;
   return m;
 }
@@ -203,6 +205,37 @@ struct Params {
   int Uw;  // window CTAs launched first in the grid (one per unit, 0 without a window)
 };
 
+// Geometry of the work split.  Every (sequence, kv_head) unit with data owns
+// a range of "virtual blocks" in one global order: X leading virtual blocks
+// that stand for the cost of starting the unit (query staging, flush of the
+// previous unit, its record), then its data blocks.  The stream CTAs cut the
+// virtual range evenly, so a CTA that starts more units gets fewer blocks.
+struct Geo {
+  const int* pre;   // [B+1] prefix sums of data blocks per sequence (one head)
+  const int* vpre;  // [B+1] prefix sums of virtual blocks per sequence (one head)
+  int B, H, X;
+};
+
+__device__ __forceinline__ int geo_nblk(const Geo& g, int b) { return g.pre[b + 1] - g.pre[b]; }
+__device__ __forceinline__ int geo_vlen(const Geo& g, int b) { return g.vpre[b + 1] - g.vpre[b]; }
+__device__ __forceinline__ long long geo_vstart(const Geo& g, int b, int h) {
+  return (long long)g.H * g.vpre[b] + (long long)h * geo_vlen(g, b);
+}
+
+// Unit holding virtual block x (x < total): the largest b with H*vpre[b] <= x
+// has blocks; the head follows from the offset inside that sequence's range.
+__device__ __forceinline__ void locate_unit(const Geo& g, long long x, int& b, int& h) {
+  int lo = 0, hi = g.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)g.H * g.vpre[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  b = lo;
+  while (geo_vlen(g, b) == 0) ++b;
+  h = int((x - (long long)g.H * g.vpre[b]) / geo_vlen(g, b));
+}
+
 // Base-2 exponential: the PTX ex2.approx.f32 instruction (max relative error
 // about 2^-22 per the PTX ISA; ex2(-inf) = +0, subnormal results kept).
 __device__ __forceinline__ float ex2(float x) {
@@ -240,20 +273,20 @@ __device__ __forceinline__ void write_out(const DecodeArgs& a, int b, int hq, in
   if (d == 0 && a.lse) a.lse[size_t(b) * a.Hq + hq] = (M + log2f(l)) * kLn2;
 }
 
-// Partial records of unit u: stream segments c0..c1 (slot j + u) and, with a
-// window, one window record (slot P + units + u).
-__device__ __forceinline__ void unit_segments(const DecodeArgs& a, const int* len_s, const int* pre_s, int u,
-                                              long long T, int Pe, long long& c0, long long& c1, int& nseg,
+// Partial records of unit u: stream segments c0..c1 (the CTAs owning its data
+// blocks, slot j + u) and, with a window, one window record (slot P + units + u).
+__device__ __forceinline__ void unit_segments(const DecodeArgs& a, const int* len_s, const Geo& g, int u,
+                                              long long Tv, int Pe, long long& c0, long long& c1, int& nseg,
                                               bool& has_win) {
-  const int H = a.c.H, b = u / H, h = u % H;
-  const int nblk = pre_s[b + 1] - pre_s[b];
-  const long long start = (long long)H * pre_s[b] + (long long)h * nblk;
+  const int b = u / g.H, h = u % g.H;
+  const int nblk = geo_nblk(g, b);
   nseg = 0;
   c0 = 0;
   c1 = -1;
   if (nblk > 0) {
-    c0 = cta_of(start, T, Pe);
-    c1 = cta_of(start + nblk - 1, T, Pe);
+    const long long d0 = geo_vstart(g, b, h) + g.X;
+    c0 = cta_of(d0, Tv, Pe);
+    c1 = cta_of(d0 + nblk - 1, Tv, Pe);
     nseg = int(c1 - c0 + 1);
   }
   has_win = a.c.window > 0 && len_s[b] > 0;
@@ -460,16 +493,15 @@ __device__ __forceinline__ void prefetch_query(const DecodeArgs& a, int u, int b
   cp_async_commit();
 }
 
-// Next unit of this CTA's block range after unit `cur`, or -1.
-__device__ __forceinline__ int next_unit_in_range(int cur, long long x1, const int* pre_s, int B, int H) {
-  const int b = cur / H, h = cur % H;
-  const int nblk = pre_s[b + 1] - pre_s[b];
-  const long long uend = (long long)H * pre_s[b] + (long long)(h + 1) * nblk;
-  if (uend >= x1) return -1;
-  int b2 = b;
-  while (pre_s[b2 + 1] == pre_s[b2] || (long long)H * pre_s[b2 + 1] <= uend) ++b2;
-  const int nb2 = pre_s[b2 + 1] - pre_s[b2];
-  return b2 * H + int((uend - (long long)H * pre_s[b2]) / nb2);
+// Next unit with data blocks in this CTA's virtual range [.., x1) after unit
+// `cur`, or -1.
+__device__ __forceinline__ int next_unit_in_range(const Geo& g, int cur, long long x1) {
+  const int b = cur / g.H, h = cur % g.H;
+  const long long vend = geo_vstart(g, b, h) + geo_vlen(g, b);
+  if (vend >= x1) return -1;
+  int b2, h2;
+  locate_unit(g, vend, b2, h2);
+  return (geo_vstart(g, b2, h2) + g.X < x1) ? b2 * g.H + h2 : -1;
 }
 
 // Shared scratch used by the combine and the merge.
@@ -611,8 +643,8 @@ __device__ __noinline__ void merge_unit(const DecodeArgs& a, int u, long long c0
 // output if this is the unit's only record, else a partial record in `slot`
 // followed by the arrival ticket; the last CTA to arrive merges the unit.
 __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& st, int u, size_t slot, const int* len_s,
-                               const int* pre_s, long long T, int Pe, int P, const Scratch& sc, uint32_t& cphase,
-                               int warp, int lane, int tid) {
+                                              const Geo& geo, long long Tv, int Pe, int P, const Scratch& sc,
+                                              uint32_t& cphase, int warp, int lane, int tid) {
   const int g = lane >> 2, t = lane & 3;
   const int G = a.G, H = a.c.H;
 #pragma unroll
@@ -629,7 +661,7 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
   long long c0, c1;
   int nseg;
   bool has_win;
-  unit_segments(a, len_s, pre_s, u, T, Pe, c0, c1, nseg, has_win);
+  unit_segments(a, len_s, geo, u, Tv, Pe, c0, c1, nseg, has_win);
   const int b = u / H, h = u % H;
   float* pm = reinterpret_cast<float*>(a.ws + a.lay.off_m);
   float* pl = reinterpret_cast<float*>(a.ws + a.lay.off_l);
@@ -674,10 +706,12 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
     }
   }
   if (nseg > 1) {
-    // partial record visible device-wide before the arrival ticket
-    __threadfence();
+    // The block barrier orders every thread's record stores before thread 0,
+    // whose device-scope fence then publishes them ahead of the ticket
+    // (barrier + single-thread fence + atomic, as in a semaphore release).
     if (!consumer_sync(sc.cbar, cphase)) return false;
     if (tid == 0) {
+      __threadfence();
       int* cnt = reinterpret_cast<int*>(a.ws + a.lay.off_counter);
       const int tk = atomicAdd(&cnt[u], 1);
       sc.misc[0] = (tk == nseg - 1);
@@ -691,23 +725,6 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
   }
   // merge_o / misc are written again only after the next query staging sync
   return true;
-}
-
-// Unit holding global block x (x < T): the largest b with H*pre[b] <= x has
-// blocks; the head follows from the offset inside that sequence's range.
-__device__ __forceinline__ void locate_unit(long long x, const int* pre_s, int B, int H, int& b, int& h, int& nblk,
-                                            long long& ustart) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)H * pre_s[mid] <= x) lo = mid;
-    else hi = mid - 1;
-  }
-  b = lo;
-  while (pre_s[b + 1] == pre_s[b]) ++b;
-  nblk = pre_s[b + 1] - pre_s[b];
-  h = int((x - (long long)H * pre_s[b]) / nblk);
-  ustart = (long long)H * pre_s[b] + (long long)h * nblk;
 }
 
 template <int KB, int VB>
@@ -735,6 +752,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   sc.misc = reinterpret_cast<int*>(smem + mp.misc);
   int* len_s = reinterpret_cast<int*>(smem + mp.len);
   int* pre_s = reinterpret_cast<int*>(smem + mp.pre);
+  int* vpre_s = reinterpret_cast<int*>(smem + mp.vpre);
+  const int X = a.lay.switch_blocks;
 
   // Programmatic dependent launch: this grid may be launched while the
   // previous kernel on the stream is still finishing; wait here until it has
@@ -759,10 +778,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       L = W > 0 ? cap + W : cap;
     }
     len_s[b] = L;
-    pre_s[b + 1] = (Lq + kBlock - 1) / kBlock;  // block count, scanned below
+    const int nb = (Lq + kBlock - 1) / kBlock;
+    pre_s[b + 1] = nb;                    // block count, scanned below
+    vpre_s[b + 1] = nb > 0 ? nb + X : 0;  // virtual blocks: start cost + data
   }
   if (tid == 0) {
     pre_s[0] = 0;
+    vpre_s[0] = 0;
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
@@ -772,22 +794,24 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     fence_mbar_init();
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp < 2) {  // warp 0 scans the data blocks, warp 1 the virtual blocks
+    int* arr = warp == 0 ? pre_s : vpre_s;
     int carry = 0;
     for (int base = 0; base < B; base += 32) {
       const int i = base + lane;
-      int v = i < B ? pre_s[i + 1] : 0;
+      int v = i < B ? arr[i + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(kFull, v, o);
         if (lane >= o) v += n;
       }
-      if (i < B) pre_s[i + 1] = v + carry;
+      if (i < B) arr[i + 1] = v + carry;
       carry += __shfl_sync(kFull, v, 31);
     }
   }
   __syncthreads();
-  const long long T = (long long)H * pre_s[B];
+  const Geo geo{pre_s, vpre_s, B, H, X};
+  const long long T = (long long)H * vpre_s[B];  // virtual blocks in total
   const int U = B * H;
   // Effective stream split: never more CTAs than blocks / kMinBlocksPerCta, so
   // every CTA below Pe owns blocks and a unit's owners are exactly c0..c1.
@@ -821,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       process_blocks<16, 16, 1>(kbs, vbs, nos, nos, val, qf, qs0, qs1, st, lane, a.err);
     }
     const size_t slot = size_t(P) + U + u;
-    if (!finish_segment(a, st, u, slot, len_s, pre_s, T, Pe, P, sc, cphase, warp, lane, tid))
+    if (!finish_segment(a, st, u, slot, len_s, geo, T, Pe, P, sc, cphase, warp, lane, tid))
       flag(a.err, KVQ_DEVERR_TIMEOUT);
     return;
   }
@@ -844,32 +868,38 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   const long long x0 = (long long)ci * T / Pe;
   const long long x1 = (long long)(ci + 1) * T / Pe;
   if (x0 >= x1) return;
+  int b_first, h_first;
+  locate_unit(geo, x0, b_first, h_first);
+  const long long xs = max(x0, geo_vstart(geo, b_first, h_first) + X);  // first data block of the range
+  if (xs >= x1) return;  // the range holds only unit-start cost: no data, no record
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer warp
     const uint64_t pol = l2_evict_first_policy();
-    int b, h, nblk;
-    long long ustart;
-    locate_unit(x0, pre_s, B, H, b, h, nblk, ustart);
-    long long x = x0;
+    int b = b_first, h = h_first;
+    int nblk = geo_nblk(geo, b);
+    long long dstart = geo_vstart(geo, b, h) + X;  // virtual index of the unit's first data block
+    long long x = xs;
     int it = 0, s = 0;
     uint32_t ph = 0;  // stage index and the parity of its current use
     bool ok = true;
     // 32 block-table entries of sequence tc_b, logical blocks tc_base + lane
     int tc_b = -1, tc_base = 0, tc_val = 0;
     while (x < x1) {
-      if (x >= ustart + nblk) {
+      if (x >= dstart + nblk) {  // next unit: skip its start cost
         ++h;
         if (h == H) {
           h = 0;
-          do { ++b; } while (pre_s[b + 1] == pre_s[b]);
-          nblk = pre_s[b + 1] - pre_s[b];
+          do { ++b; } while (geo_vlen(geo, b) == 0);
+          nblk = geo_nblk(geo, b);
         }
-        ustart = (long long)H * pre_s[b] + (long long)h * nblk;
+        dstart = geo_vstart(geo, b, h) + X;
+        x = max(x, dstart);
+        if (x >= x1) break;
       }
-      const long long rem = (x1 - x) < (ustart + nblk - x) ? (x1 - x) : (ustart + nblk - x);
+      const long long rem = (x1 - x) < (dstart + nblk - x) ? (x1 - x) : (dstart + nblk - x);
       const int n = int(rem < F::kBlocksPerStage ? rem : F::kBlocksPerStage);
-      const int local = int(x - ustart);
+      const int local = int(x - dstart);
       if (tc_b != b || local < tc_base || local + n > tc_base + 32) {
         tc_b = b;
         tc_base = local;
@@ -953,13 +983,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   {
     // the first unit is known from x0: fetch its query group (and the next
     // unit's) while the first stage is still in flight
-    int b0, h0, nb0;
-    long long us0;
-    locate_unit(x0, pre_s, B, H, b0, h0, nb0, us0);
+    const int b0 = b_first, h0 = h_first;
     cur = b0 * H + h0;
     cur_lq = W > 0 ? max(len_s[b0] - W, 0) : len_s[b0];
     prefetch_query(a, cur, 0, qraw, fraw, warp, lane);
-    nxt = next_unit_in_range(cur, x1, pre_s, B, H);
+    nxt = next_unit_in_range(geo, cur, x1);
     if (nxt >= 0) {
       prefetch_query(a, nxt, 1, qraw, fraw, warp, lane);
       cp_async_wait<1>();
@@ -981,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     const int4 hd = hdr[s];
     if (hd.x != cur) {
       if (cur >= 0 &&
-          !finish_segment(a, st, cur, size_t(ci) + cur, len_s, pre_s, T, Pe, P, sc, cphase, warp, lane, tid)) {
+          !finish_segment(a, st, cur, size_t(ci) + cur, len_s, geo, T, Pe, P, sc, cphase, warp, lane, tid)) {
         flag(a.err, KVQ_DEVERR_TIMEOUT);
         return;
       }
@@ -999,7 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         flag(a.err, KVQ_DEVERR_TIMEOUT);
         return;
       }
-      nxt = next_unit_in_range(cur, x1, pre_s, B, H);
+      nxt = next_unit_in_range(geo, cur, x1);
       if (nxt >= 0) prefetch_query(a, nxt, qbuf ^ 1, qraw, fraw, warp, lane);
       st.reset();
     }

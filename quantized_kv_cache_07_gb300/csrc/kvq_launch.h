@@ -47,6 +47,7 @@ struct DequantArgs {
 // Workspace layout of a decode call (byte offsets from the workspace base).
 struct DecodeLayout {
   int stream_ctas, window_ctas, units, slots;
+  int switch_blocks;  // virtual blocks charged for starting a unit (0: unit-aligned split)
   size_t off_counter, off_m, off_l, off_o, total;
 };
 
