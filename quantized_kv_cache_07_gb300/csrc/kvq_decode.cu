@@ -706,19 +706,20 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
     }
   }
   if (nseg > 1) {
-    // The block barrier orders every thread's record stores before thread 0,
-    // whose device-scope fence then publishes them ahead of the ticket
-    // (barrier + single-thread fence + atomic, as in a semaphore release).
+    // The block barrier (release/acquire at CTA scope) orders every thread's
+    // record stores before thread 0; its acquire-release atomic at GPU scope
+    // publishes them with the ticket and, for the last CTA to arrive, makes
+    // the other CTAs' records visible; the next block barrier extends that to
+    // all threads of this CTA.
     if (!consumer_sync(sc.cbar, cphase)) return false;
     if (tid == 0) {
-      __threadfence();
       int* cnt = reinterpret_cast<int*>(a.ws + a.lay.off_counter);
-      const int tk = atomicAdd(&cnt[u], 1);
+      int tk;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(tk) : "l"(cnt + u) : "memory");
       sc.misc[0] = (tk == nseg - 1);
     }
     if (!consumer_sync(sc.cbar, cphase)) return false;
     if (sc.misc[0]) {
-      __threadfence();
       merge_unit(a, u, c0, c1, has_win, P, tid);
       if (tid == 0) reinterpret_cast<int*>(a.ws + a.lay.off_counter)[u] = 0;
     }
