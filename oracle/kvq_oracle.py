@@ -29,6 +29,14 @@ Readings taken where the pages leave a step open:
   * with a recent-token window of W tokens, the last min(W, L) positions are
     kept as their bf16 values and only older positions are quantized;
   * the log-sum-exp is in natural-log units of the score q.k/sqrt(D).
+  * asymmetric format (scale and zero point, [P1] "Quantization granularity
+    defines which values share a scale": a scale and, depending on the scheme,
+    a zero point or another offset convention; [P3] "Per-token scales and
+    where they can live": "a scale and zero point add 6 percent"): per token
+    per head the offset is the vector minimum m, s = RN32((max - min) / qmaxu)
+    with qmaxu = 2^bits - 1, u = clamp(rint((x - m) / s), 0, qmaxu) with the
+    difference and the quotient evaluated in float64, x_hat = u * s + m; a
+    constant vector stores s = 1, u = 0 and m = its value.
 Every function below is pinned by tests/test_oracle_pins.py.
 """
 from __future__ import annotations
@@ -69,6 +77,34 @@ def quantize(x: np.ndarray, bits: int):
     quotient = x / s.astype(np.float64)[..., None]
     codes = np.clip(np.rint(quotient), lo, hi).astype(np.int16)   # rint: half to even
     return codes, s
+
+
+QMAXU = {8: 255, 4: 15}
+
+
+def quantize_asym(x: np.ndarray, bits: int):
+    """Asymmetric per-vector quantization along the last axis (scale and zero
+    point; see the module notes for the reading).
+
+    Returns (codes uint16 [..., D] in [0, 2^bits - 1], scale float32 [...],
+    offset float32 [...]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    qmaxu = QMAXU[bits]
+    lo = np.min(x, axis=-1)
+    hi = np.max(x, axis=-1)
+    rng = hi - lo                                   # float64 difference of float32 values
+    s = (rng / qmaxu).astype(np.float32)
+    s = np.where(rng == 0.0, np.float32(1.0), s).astype(np.float32)
+    quotient = (x - lo[..., None]) / s.astype(np.float64)[..., None]
+    codes = np.clip(np.rint(quotient), 0, qmaxu).astype(np.uint16)
+    return codes, s, lo.astype(np.float32)
+
+
+def dequantize_asym(codes: np.ndarray, scale: np.ndarray, offset: np.ndarray) -> np.ndarray:
+    """x_hat = u * s + m, exact in float64."""
+    return (np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[..., None]
+            + np.asarray(offset, np.float64)[..., None])
 
 
 def dequantize(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
@@ -154,7 +190,7 @@ def window_split(length: int, window: int) -> int:
     return max(length - window, 0)
 
 
-def quantize_sequence(k, v, k_bits: int, v_bits: int, window: int = 0, c=None):
+def quantize_sequence(k, v, k_bits: int, v_bits: int, window: int = 0, c=None, asym: bool = False):
     """Store one sequence: k, v float64 [L, H, D] (exact bf16 values).
 
     Returns a dict with the quantized prefix (codes/scales for K and V) and the
@@ -162,13 +198,18 @@ def quantize_sequence(k, v, k_bits: int, v_bits: int, window: int = 0, c=None):
     """
     L = k.shape[0]
     Lq = window_split(L, window)
-    st = {"Lq": Lq, "k_bits": k_bits, "v_bits": v_bits, "c": c}
+    st = {"Lq": Lq, "k_bits": k_bits, "v_bits": v_bits, "c": c, "asym": asym}
     if k_bits == 16:
         st["k_plain"] = k[:Lq]
+    elif asym:
+        kx = k[:Lq] if c is None else divide_by_channel_factor(k[:Lq], c)
+        st["k_codes"], st["k_scale"], st["k_offset"] = quantize_asym(kx, k_bits)
     else:
         st["k_codes"], st["k_scale"] = quantize_keys(k[:Lq], k_bits, c)
     if v_bits == 16:
         st["v_plain"] = v[:Lq]
+    elif asym:
+        st["v_codes"], st["v_scale"], st["v_offset"] = quantize_asym(v[:Lq], v_bits)
     else:
         st["v_codes"], st["v_scale"] = quantize(v[:Lq], v_bits)
     st["k_window"] = k[Lq:]
@@ -181,11 +222,16 @@ def reconstruct_sequence(st, head: int):
     c = st["c"]
     if st["k_bits"] == 16:
         kq = st["k_plain"][:, head]
+    elif st.get("asym"):
+        kq = dequantize_asym(st["k_codes"][:, head], st["k_scale"][:, head], st["k_offset"][:, head])
+        kq = kq if c is None else kq * np.asarray(c[head], np.float64)
     else:
         kq = reconstruct_keys(st["k_codes"][:, head], st["k_scale"][:, head],
                               None if c is None else c[head])
     if st["v_bits"] == 16:
         vq = st["v_plain"][:, head]
+    elif st.get("asym"):
+        vq = dequantize_asym(st["v_codes"][:, head], st["v_scale"][:, head], st["v_offset"][:, head])
     else:
         vq = dequantize(st["v_codes"][:, head], st["v_scale"][:, head])
     k_hat = np.concatenate([kq, st["k_window"][:, head]], axis=0)
@@ -223,9 +269,12 @@ def metadata_fraction(head_dim: int, bits: int, metadata_bytes: int) -> float:
     return metadata_bytes / (head_dim * bits / 8)
 
 
-def cache_bytes_per_token_head(head_dim: int, k_bits: int, v_bits: int, scale_bytes: int = 4) -> int:
-    """Bytes read per cached token per KV head: codes plus one scale for each of
-    K and V (no scale for a 16-bit cache)."""
-    kb = head_dim * k_bits // 8 + (0 if k_bits == 16 else scale_bytes)
-    vb = head_dim * v_bits // 8 + (0 if v_bits == 16 else scale_bytes)
+def cache_bytes_per_token_head(head_dim: int, k_bits: int, v_bits: int, scale_bytes: int = 4,
+                               asym: bool = False) -> int:
+    """Bytes read per cached token per KV head: codes plus one scale (and, for
+    the asymmetric format, one offset) for each of K and V (no metadata for a
+    16-bit cache)."""
+    meta = scale_bytes * (2 if asym else 1)
+    kb = head_dim * k_bits // 8 + (0 if k_bits == 16 else meta)
+    vb = head_dim * v_bits // 8 + (0 if v_bits == 16 else meta)
     return kb + vb

@@ -435,3 +435,71 @@ def test_pins_catch_a_planted_missing_sqrt_d(monkeypatch):
     assert np.max(np.abs(o_bad - ref)) > 1e-3
     o_good, _ = O.attention(q, k, v)
     assert np.max(np.abs(o_good - ref)) < 1e-13
+
+
+# ---------------------------------------------------------------- asymmetric format (scale + zero point)
+def exact_quantize_asym(xs, bits):
+    """Exact rational restatement: offset = min, s = RN32((max - min)/qmaxu),
+    u = clamp(RNE((x - min)/s), 0, qmaxu)."""
+    qmaxu = {8: 255, 4: 15}[bits]
+    fr = [Fraction(float(x)) for x in xs]
+    lo, hi = min(fr), max(fr)
+    if hi == lo:
+        return [0] * len(fr), Fraction(1), lo
+    s = rn_float32((hi - lo) / qmaxu)
+    return [min(qmaxu, max(0, rne_int((f - lo) / s))) for f in fr], s, lo
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_asym_quantizer_matches_exact_rational_brute_force(bits):
+    for trial in range(300):
+        n = int(RNG.integers(2, 40))
+        dist = "t3" if trial % 3 == 0 else "normal"
+        x = bf16_vec(n, scale=float(2.0 ** RNG.integers(-10, 10)), dist=dist)
+        if trial % 5 == 0:
+            x = np.abs(x)                                   # one-signed vectors: min far from 0
+        codes, s, m = O.quantize_asym(x, bits)
+        ref_codes, ref_s, ref_m = exact_quantize_asym(x, bits)
+        assert Fraction(float(s)) == ref_s and Fraction(float(m)) == ref_m
+        assert list(map(int, codes)) == ref_codes
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_asym_quantizer_invariants(bits):
+    qmaxu = O.QMAXU[bits]
+    x = O.bf16_to_f64(f32_to_bf16_bits(RNG.standard_normal((400, 128)).astype(np.float32) + 1.5))
+    codes, s, m = O.quantize_asym(x, bits)
+    xh = O.dequantize_asym(codes, s, m)
+    assert np.all(np.abs(x - xh) <= s.astype(np.float64)[:, None] / 2 * (1 + 1e-12))
+    assert np.all(codes.min(axis=1) == 0) and np.all(codes.max(axis=1) == qmaxu)   # min -> 0, max -> top
+    assert np.array_equal(m, x.min(axis=1).astype(np.float32))
+
+
+def test_asym_quantizer_constant_and_tie_cases():
+    c = np.full(16, 0.75)
+    codes, s, m = O.quantize_asym(c, 8)
+    assert np.all(codes == 0) and float(s) == 1.0 and float(m) == 0.75
+    assert np.array_equal(O.dequantize_asym(codes, s, m), c)
+    # (x - min) / s on exact half-integers rounds to even: s = 2^-4, min = -1
+    x = np.array([-1.0, -1.0 + 15 * 2.0 ** -4, -1.0 + 2.5 * 2.0 ** -4, -1.0 + 3.5 * 2.0 ** -4])
+    codes, s, m = O.quantize_asym(x, 4)
+    assert float(s) == 2.0 ** -4 and float(m) == -1.0
+    assert list(map(int, codes)) == [0, 15, 2, 4]
+
+
+def test_asym_score_fold_is_exact_in_rationals():
+    """q . (u*s + m) == s*(q . u) + m*(sum q): the offset moves out of the dot."""
+    q = bf16_vec(128)
+    k = bf16_vec(128) + 0.5
+    u, s, m = O.quantize_asym(k, 8)
+    qf = [Fraction(float(a)) for a in q]
+    lhs = sum(a * (int(c) * Fraction(float(s)) + Fraction(float(m))) for a, c in zip(qf, u))
+    rhs = Fraction(float(s)) * sum(a * int(c) for a, c in zip(qf, u)) + Fraction(float(m)) * sum(qf)
+    assert lhs == rhs
+    assert abs(float(q @ O.dequantize_asym(u, s, m)) - float(lhs)) <= 1e-12 * max(1.0, abs(float(lhs)))
+
+
+def test_asym_metadata_fraction_is_the_printed_six_percent(golden_dir):
+    # scale + zero point over 128 int8 codes: the page's "add 6 percent" row
+    assert O.metadata_fraction(128, 8, 8) == 0.0625
+    assert O.cache_bytes_per_token_head(128, 8, 8, asym=True) == 2 * (128 + 8)
