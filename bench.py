@@ -46,7 +46,7 @@ def measured_peaks():
 
 def decode_kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("kvq_decode.cu", "kvq_device.cuh"):
+    for f in ("kvq_decode_impl.cuh", "kvq_decode.cu", "kvq_device.cuh"):
         h.update(open(os.path.join(ROOT, "quantized_kv_cache_07_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 
@@ -126,7 +126,7 @@ def cache_bytes_per_step(inp) -> int:
     w = inp.workload
     L = inp.decode_lengths.astype(int)
     D = w.head_dim
-    per_q = D * w.k_bits // 8 + D * w.v_bits // 8 + (0 if w.k_bits == 16 else 8)
+    per_q = D * w.k_bits // 8 + D * w.v_bits // 8 + (0 if w.k_bits == 16 else (16 if w.asym else 8))
     if w.window:
         lq = [max(int(l) - w.window, 0) for l in L]
         lw = [int(l) - x for l, x in zip(L, lq)]
@@ -144,12 +144,14 @@ from oracle import kvq_oracle as O
 w = WORKLOADS[{name!r}]
 if {bf16}:
     w = w.with_(k_bits=16, v_bits=16, window=0, channel_factor=False)
+if {asym}:
+    w = w.with_(asym=True)
 inp = make_inputs(w)
 G = w.group
 budget = {budget}
 rng = np.random.default_rng(5)
 units = [(int(b), int(h)) for b in rng.permutation(w.batch) for h in range(w.kv_heads)]
-per_tok = 128 * w.k_bits // 8 + 128 * w.v_bits // 8 + (0 if w.k_bits == 16 else 8)
+per_tok = 128 * w.k_bits // 8 + 128 * w.v_bits // 8 + (0 if w.k_bits == 16 else (16 if w.asym else 8))
 tot_t, tot_b, n, i = 0.0, 0, 0, 0
 while tot_t < budget or n == 0:
     b, h = units[i % len(units)]; i += 1
@@ -159,7 +161,7 @@ while tot_t < budget or n == 0:
         k = np.concatenate([k, O.bf16_to_f64(inp.k_new[b:b+1, h:h+1])])
         v = np.concatenate([v, O.bf16_to_f64(inp.v_new[b:b+1, h:h+1])])
     c = None if inp.channel_factor is None else inp.channel_factor[h:h+1].astype(np.float64)
-    st = O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c)   # the stored cache: untimed
+    st = O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c, asym=w.asym)   # untimed
     t1 = time.perf_counter()
     kh, vh = O.reconstruct_sequence(st, 0)
     O.attention(O.bf16_to_f64(inp.q[b, h*G:(h+1)*G]), kh, vh)
@@ -170,12 +172,12 @@ print(json.dumps({{"seconds": tot_t, "bytes": tot_b, "units": n}}))
 """
 
 
-def run_cpu_sample(name: str, budget_s: float, steps: int = 1, bf16: bool = False):
+def run_cpu_sample(name: str, budget_s: float, steps: int = 1, bf16: bool = False, asym: bool = False):
     """Time the oracle's decode (dequantize + attention, float64) on a bounded
     sample of the workload's units, in a fresh single-threaded process."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    code = CPU_SAMPLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, bf16=bf16)
+    code = CPU_SAMPLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, bf16=bf16, asym=asym)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
     if res.returncode != 0:
         raise RuntimeError("oracle sample failed: " + res.stderr[-2000:])
@@ -204,6 +206,10 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true", help="skip the same-design bf16-cache comparison run")
+    ap.add_argument("--no-asym", action="store_true",
+                    help="skip the same-shape run in the asymmetric (scale + zero point) format")
+    ap.add_argument("--asym", action="store_true",
+                    help="time the workload in the asymmetric (scale + zero point) format")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--stream-ctas", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0,
@@ -238,6 +244,8 @@ def main():
     _lib.load()
 
     w = WORKLOADS[args.workload]
+    if args.asym:
+        w = w.with_(asym=True)
     inp = make_inputs(w)
     dev = torch.device("cuda", local)
     props = torch.cuda.get_device_properties(dev)
@@ -252,7 +260,8 @@ def main():
         replicas = [base]
         for _ in range(reps - 1):
             c = cache_for_inputs(inp_, dev)
-            for name in ("k_codes", "v_codes", "k_scales", "v_scales", "k_window", "v_window"):
+            for name in ("k_codes", "v_codes", "k_scales", "v_scales", "k_offsets", "v_offsets", "k_window",
+                         "v_window"):
                 src, dst = getattr(base, name), getattr(c, name)
                 if src is not None:
                     dst.copy_(src)
@@ -402,6 +411,18 @@ def main():
                 "speedup_quant_vs_bf16": rb["dec_ms"] / res["dec_ms"], "err_word": rb["err"]}
         del inb
 
+    asym = None
+    if not args.no_asym and w.k_bits != 16 and not w.asym:
+        wa = w.with_(asym=True, name=w.name + "_asym")
+        ina = make_inputs(wa)
+        ra = run_arm(ina, "asym")
+        asym = {"workload": wa.name, "ms_per_step": ra["ms_step"], "decode_ms": ra["dec_ms"],
+                "decode_ms_isolated_launch": ra["dec_ms_iso"], "bytes_per_step": ra["bytes"],
+                "effective_gbs": ra["bytes"] / (ra["dec_ms"] / 1e3) / 1e9,
+                "frac_of_peak": ra["bytes"] / (ra["dec_ms"] / 1e3) / 1e9 / peak,
+                "time_vs_symmetric": ra["dec_ms"] / res["dec_ms"], "err_word": ra["err"]}
+        del ina
+
     line = {
         "metric": "quantized-KV decode attention: effective HBM GB/s (% of peak), steps/s",
         "value": round(value, 2),
@@ -419,6 +440,7 @@ def main():
         "config": {"workload": w.name, "description": w.description, "batch": w.batch, "q_heads": w.q_heads,
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits,
                    "window": w.window, "paged": w.paged, "append_one": w.append_one,
+                   "format": "asymmetric (scale + zero point)" if w.asym else "symmetric (scale)",
                    "cache_bytes_per_step": bytes_step, "allocated_cache_bytes": res["alloc"],
                    "l2": f"steps rotate over {res['replicas']} cache replicas "
                          f"({res['replicas'] * bytes_step / 2**20:.0f} MiB >= 4x L2 or cache > L2)",
@@ -435,11 +457,12 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "bf16_same_design": bf16,
+        "asym_same_shape": asym,
         "device_err_word": res["err"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            d = run_cpu_sample(w.name, args.cpu_budget)
+            d = run_cpu_sample(args.workload, args.cpu_budget, asym=w.asym)
             line["cpu_baseline"] = {"value": round(d["bytes"] / d["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
                                     "kind": "oracle",
                                     "sample": f"{d['units']} (sequence, kv_head) units of {w.name}, float64 "

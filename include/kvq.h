@@ -46,9 +46,13 @@
  *     for int8 keys "byte" is the offset inside the lane's 16 bytes.  Nibble n
  *     of a little-endian 32-bit word occupies bits 4n..4n+3.  Codes are stored
  *     offset-binary: an int8 code c in [-127,127] is the byte c + 128, an int4
- *     code c in [-8,7] (-8 never produced) is the nibble c + 8.
+ *     code c in [-8,7] (-8 never produced) is the nibble c + 8.  In the
+ *     asymmetric format the unsigned code u (int8: 0..255, int4: 0..15) is
+ *     stored as the byte or nibble u itself.
  *   Scale pool  : float [num_kv_heads][num_blocks][16], natural token order
  *                 (absent for a bf16 cache).
+ *   Offset pool : asymmetric format only: the per-token zero point m, same
+ *                 layout as the scale pool.
  *   Window ring : bf16 [window_batch][num_kv_heads][window / 16][4096 bytes]:
  *                 window / 16 blocks per (sequence, head) for keys and for
  *                 values, each in the bf16 key / value block order above;
@@ -109,6 +113,16 @@ typedef struct {
   int32_t window_batch;   /* first dimension of the ring buffers (sequences)        */
   void* k_window;         /* bf16 ring (layout above), or NULL if W == 0            */
   void* v_window;
+  /* Asymmetric format ([P1] "Quantization granularity defines which values
+   * share a scale": a scale and, depending on the scheme, a zero point; [P3]
+   * "Per-token scales and where they can live": a scale and zero point cost
+   * twice the metadata).  Both NULL: symmetric codes.  Both set (8- or 4-bit
+   * blocks only): per token per head m = min(x), s = RN32((max(x) - min(x)) /
+   * (2^bits - 1)) (difference and quotient in double; a constant vector stores
+   * s = 1), u = clamp(round_half_even((x - m) / s), 0, 2^bits - 1) with the
+   * difference and quotient in double, x_hat = u * s + m. */
+  float* k_offsets;       /* per-token key zero points (offset pool), or NULL      */
+  float* v_offsets;       /* per-token value zero points, or NULL                  */
 } kvq_cache_desc;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -127,7 +141,9 @@ kvq_status kvq_block_bytes(int32_t bits, size_t* bytes);
  * vector -> codes 0 and s = 1.  qmax = 127 (int8) or 7 (int4).  With a
  * per-channel key factor c, keys are first divided by c (float32, RN) and then
  * quantized per token ([P3] "The axis choice is a kernel decision").  Codes are
- * the correctly rounded quotient of the exact x / s.
+ * the correctly rounded quotient of the exact x / s.  With k_offsets/v_offsets
+ * set, the asymmetric quantizer of kvq_cache_desc is used instead and the zero
+ * point is stored beside the scale.
  *   k_new, v_new : device bf16 [n][num_kv_heads][128]
  *   n            : number of new tokens (0 is a no-op)
  *   seq_idx, pos : device int32 [n]; token r belongs to sequence seq_idx[r] at
@@ -183,7 +199,9 @@ kvq_status kvq_workspace_init(void* workspace, size_t bytes, void* stream);
  * the kernel loads (codes and scales are two read streams).  [P1] "Cache growth
  * changes the serving trade": the last min(W, L) positions are read from the
  * bf16 window, older ones from the quantized blocks.  Query head hq reads KV
- * head hq / (q_heads / num_kv_heads).
+ * head hq / (q_heads / num_kv_heads).  In the asymmetric format the scores and
+ * outputs use x_hat = u * s + m (the zero-point terms are added to the code
+ * contractions: m * sum(q) per score, sum(p * m) per output).
  *   q          : device bf16 [batch][q_heads][128]
  *   seq_lens   : device int32 [batch], tokens attended per sequence (0 allowed:
  *                out = 0, lse = -inf)
@@ -235,7 +253,8 @@ kvq_status kvq_decode_static_scratch(const kvq_cache_desc* cache, const void* q,
 /*
  * kvq_dequant -- read the block store back: x_hat = RN32(code * s)
  * ([P2] "Quantization needs a scale convention"), without the per-channel key
- * factor.  For a bf16 cache the stored values are widened.  For tests.
+ * factor; in the asymmetric format x_hat = RN32(u * s + m) (one fused
+ * multiply-add).  For a bf16 cache the stored values are widened.  For tests.
  *   slots : device int32 [n], physical slot = physical_block * 16 + token
  *   k_out, v_out : device float [n][num_kv_heads][128]
  */

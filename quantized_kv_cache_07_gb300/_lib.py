@@ -47,6 +47,7 @@ class CacheDesc(ctypes.Structure):
         ("k_channel_factor", c_void_p),
         ("window", c_int32), ("window_batch", c_int32),
         ("k_window", c_void_p), ("v_window", c_void_p),
+        ("k_offsets", c_void_p), ("v_offsets", c_void_p),
     ]
 
 

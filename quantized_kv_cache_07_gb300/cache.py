@@ -21,10 +21,14 @@ def _require_cuda():
 
 
 class KVCache:
-    """Block pools (+ optional bf16 window ring) of one attention layer."""
+    """Block pools (+ optional bf16 window ring) of one attention layer.
+
+    ``asym=True`` selects the asymmetric format: a per-token zero point is
+    stored beside each scale (offset pools of the same shape).
+    """
 
     def __init__(self, num_blocks: int, kv_heads: int, k_bits: int, v_bits: int, window: int = 0,
-                 window_batch: int = 0, channel_factor=None, device="cuda"):
+                 window_batch: int = 0, channel_factor=None, asym: bool = False, device="cuda"):
         _require_cuda()
         self.num_blocks, self.kv_heads = int(num_blocks), int(kv_heads)
         self.k_bits, self.v_bits = int(k_bits), int(v_bits)
@@ -37,6 +41,11 @@ class KVCache:
         n_sc = self.num_blocks * kv_heads * BLOCK_SIZE
         self.k_scales = torch.zeros(n_sc, dtype=torch.float32, device=device) if quant else None
         self.v_scales = torch.zeros(n_sc, dtype=torch.float32, device=device) if quant else None
+        self.asym = bool(asym)
+        if self.asym and not quant:
+            raise ValueError("the asymmetric format needs 8- or 4-bit blocks")
+        self.k_offsets = torch.zeros(n_sc, dtype=torch.float32, device=device) if self.asym else None
+        self.v_offsets = torch.zeros(n_sc, dtype=torch.float32, device=device) if self.asym else None
         self.channel_factor = None
         if channel_factor is not None:
             self.channel_factor = torch.as_tensor(np.ascontiguousarray(channel_factor, dtype=np.float32)
@@ -55,16 +64,20 @@ class KVCache:
             k_channel_factor=self.channel_factor.data_ptr() if self.channel_factor is not None else None,
             window=self.window, window_batch=max(window_batch, 1) if window > 0 else 0,
             k_window=self.k_window.data_ptr() if self.k_window is not None else None,
-            v_window=self.v_window.data_ptr() if self.v_window is not None else None)
+            v_window=self.v_window.data_ptr() if self.v_window is not None else None,
+            k_offsets=self.k_offsets.data_ptr() if self.asym else None,
+            v_offsets=self.v_offsets.data_ptr() if self.asym else None)
 
-    # bytes the decode reads per cached token per KV head (codes + scales)
+    # bytes the decode reads per cached token per KV head (codes + scales + zero points)
     def bytes_per_token_head(self) -> int:
-        kb = HEAD_DIM * self.k_bits // 8 + (0 if self.k_bits == 16 else 4)
-        vb = HEAD_DIM * self.v_bits // 8 + (0 if self.v_bits == 16 else 4)
+        meta = 8 if self.asym else 4
+        kb = HEAD_DIM * self.k_bits // 8 + (0 if self.k_bits == 16 else meta)
+        vb = HEAD_DIM * self.v_bits // 8 + (0 if self.v_bits == 16 else meta)
         return kb + vb
 
     def allocated_bytes(self) -> int:
-        ts = [self.k_codes, self.v_codes, self.k_scales, self.v_scales, self.k_window, self.v_window]
+        ts = [self.k_codes, self.v_codes, self.k_scales, self.v_scales, self.k_offsets, self.v_offsets,
+              self.k_window, self.v_window]
         return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
 
@@ -124,4 +137,5 @@ def fill_from_inputs(cache: KVCache, inp, device="cuda", chunk_tokens: int = 1 <
 def cache_for_inputs(inp, device="cuda") -> KVCache:
     w = inp.workload
     return KVCache(inp.num_blocks, w.kv_heads, w.k_bits, w.v_bits, window=w.window,
-                   window_batch=w.batch if w.window else 0, channel_factor=inp.channel_factor, device=device)
+                   window_batch=w.batch if w.window else 0, channel_factor=inp.channel_factor,
+                   asym=getattr(w, "asym", False), device=device)

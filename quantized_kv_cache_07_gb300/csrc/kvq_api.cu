@@ -34,6 +34,12 @@ kvq_status check_cache(const kvq_cache_desc* c) {
     if (!c->k_scales || !c->v_scales) return KVQ_ERR_INVALID_ARG;
     if (!aligned16(c->k_scales) || !aligned16(c->v_scales)) return KVQ_ERR_ALIGNMENT;
   }
+  // zero points: both tensors or neither, and only on quantized blocks
+  if ((c->k_offsets != nullptr) != (c->v_offsets != nullptr)) return KVQ_ERR_INVALID_ARG;
+  if (c->k_offsets) {
+    if (!quant) return KVQ_ERR_UNSUPPORTED;
+    if (!aligned16(c->k_offsets) || !aligned16(c->v_offsets)) return KVQ_ERR_ALIGNMENT;
+  }
   if (c->k_channel_factor) {
     if (!quant) return KVQ_ERR_UNSUPPORTED;
     if (!aligned16(c->k_channel_factor)) return KVQ_ERR_ALIGNMENT;
@@ -57,6 +63,8 @@ kvq::CacheView view(const kvq_cache_desc* c) {
   v.v_codes = static_cast<uint8_t*>(c->v_codes);
   v.k_scales = c->k_scales;
   v.v_scales = c->v_scales;
+  v.k_offsets = c->k_offsets;
+  v.v_offsets = c->v_offsets;
   v.factor = c->k_channel_factor;
   v.window = c->window;
   v.window_batch = c->window_batch;
@@ -84,7 +92,7 @@ int auto_stream_ctas(const kvq_cache_desc* c, int batch) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, batch);
+  const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, c->k_offsets != nullptr, batch);
   return stream_ctas_for(sms * per, c->window > 0 ? batch * c->num_kv_heads : 0, batch * c->num_kv_heads);
 }
 

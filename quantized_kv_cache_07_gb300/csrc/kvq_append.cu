@@ -6,7 +6,10 @@
 // kernel decision" (listing: amax, zero vector -> scale 1, scale = amax/qmax,
 // clamp(round(x/scale))); "KV Cache Quantization Reduces Cache Bytes with
 // Separate Accuracy and Kernel Costs", section "Quantization needs a scale
-// convention" (q = clamp(round(x/s)), x_hat = q*s).
+// convention" (q = clamp(round(x/s)), x_hat = q*s).  Asymmetric format: "KV
+// Cache Quantization Perturbs Attention Through Stored Keys and Values",
+// section "Quantization granularity defines which values share a scale" (a
+// scale and a zero point per group; here per token per head).
 //
 // One warp quantizes one 128-element vector; lane l owns dims 4l..4l+3.
 #include "kvq_device.cuh"
@@ -55,14 +58,39 @@ __device__ __forceinline__ void quantize_warp(const float (&x)[4], int bits, int
   }
 }
 
-// Store the codes of one quantized vector (token `tok`) into its block.
+// Warp-cooperative asymmetric quantization: m = min(x), s = RN32((max - min) /
+// (2^bits - 1)) with the difference and the quotient in double (a constant
+// vector gets s = 1), u = clamp(rint((x - m) / s), 0, 2^bits - 1) with the
+// difference and the quotient in double (rint: half to even).
+__device__ __forceinline__ void quantize_asym_warp(const float (&x)[4], int bits, int (&u)[4], float& s, float& m) {
+  float lo = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float hi = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(kFull, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(kFull, hi, o));
+  }
+  const int qmaxu = bits == 8 ? 255 : 15;
+  const double rng = __dsub_rn(double(hi), double(lo));
+  s = rng == 0.0 ? 1.0f : __double2float_rn(__ddiv_rn(rng, double(qmaxu)));
+  m = lo;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const double r = rint(__ddiv_rn(__dsub_rn(double(x[j]), double(lo)), double(s)));
+    u[j] = r >= double(qmaxu) ? qmaxu : (r > 0.0 ? int(r) : 0);  // clamp before the conversion
+  }
+}
+
+// Store the codes of one quantized vector (token `tok`) into its block.  The
+// values given are the stored bytes / nibbles (offset-binary for symmetric
+// codes, the unsigned code itself for the asymmetric format).
 __device__ void store_codes(bool is_key, int bits, uint8_t* blk, int tok, const int (&code)[4], int lane) {
   if (bits == 8) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int d = 4 * lane + j;
       const Loc L = is_key ? key_loc(8, tok, d) : value_loc(8, tok, d);
-      blk[L.byte] = uint8_t(code[j] + 128);  // offset binary
+      blk[L.byte] = uint8_t(code[j]);
     }
     return;
   }
@@ -76,7 +104,7 @@ __device__ void store_codes(bool is_key, int bits, uint8_t* blk, int tok, const 
       const int d = 4 * lane + j;
       const Loc L = key_loc(4, tok, d);
       const int nib = ((L.byte & 3) << 1) | (L.shift >> 2);
-      part |= uint32_t(code[j] + 8) << (4 * nib);  // offset binary
+      part |= uint32_t(code[j]) << (4 * nib);
       word_off = L.byte & ~3;
     }
     const uint32_t word = part | __shfl_xor_sync(kFull, part, 1);
@@ -91,7 +119,7 @@ __device__ void store_codes(bool is_key, int bits, uint8_t* blk, int tok, const 
     const int nib = ((L.byte & 3) << 1) | (L.shift >> 2);
     uint32_t* w = reinterpret_cast<uint32_t*>(blk + (L.byte & ~3));
     atomicAnd(w, ~(0xFu << (4 * nib)));
-    atomicOr(w, uint32_t(code[j] + 8) << (4 * nib));  // offset binary
+    atomicOr(w, uint32_t(code[j]) << (4 * nib));
   }
 }
 
@@ -133,12 +161,21 @@ __device__ void write_block_store(const AppendArgs& a, bool is_key, int b, int p
     if (is_key && c.factor) x[j] = __fdiv_rn(x[j], c.factor[h * kHeadDim + 4 * lane + j]);
   }
   int code[4];
-  float s;
-  quantize_warp(x, bits, code, s);
+  float s, m = 0.f;
+  const bool asym = c.k_offsets != nullptr;
+  if (asym) {
+    quantize_asym_warp(x, bits, code, s, m);
+  } else {
+    quantize_warp(x, bits, code, s);
+    const int bias = bits == 8 ? 128 : 8;  // offset binary
+#pragma unroll
+    for (int j = 0; j < 4; ++j) code[j] += bias;
+  }
   store_codes(is_key, bits, blk, tok, code, lane);
   if (lane == 0) {
-    float* sc = is_key ? c.k_scales : c.v_scales;
-    sc[(size_t(h) * c.num_blocks + phys) * kBlock + tok] = s;
+    const size_t e = (size_t(h) * c.num_blocks + phys) * kBlock + tok;
+    (is_key ? c.k_scales : c.v_scales)[e] = s;
+    if (asym) (is_key ? c.k_offsets : c.v_offsets)[e] = m;
   }
 }
 
@@ -214,8 +251,14 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
   }
   const int bits = is_key ? a.c.k_bits : a.c.v_bits;
   const uint8_t* blk = (is_key ? a.c.k_codes : a.c.v_codes) + (size_t(h) * a.c.num_blocks + phys) * block_bytes(bits);
-  float s = 1.0f;
-  if (bits != 16) s = (is_key ? a.c.k_scales : a.c.v_scales)[(size_t(h) * a.c.num_blocks + phys) * kBlock + tok];
+  float s = 1.0f, m = 0.0f;
+  const bool asym = a.c.k_offsets != nullptr;
+  if (bits != 16) {
+    const size_t e = (size_t(h) * a.c.num_blocks + phys) * kBlock + tok;
+    s = (is_key ? a.c.k_scales : a.c.v_scales)[e];
+    if (asym) m = (is_key ? a.c.k_offsets : a.c.v_offsets)[e];
+  }
+  const int bias = asym ? 0 : (bits == 8 ? 128 : 8);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int d = 4 * lane + j;
@@ -223,11 +266,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
     float v;
     if (bits == 16) {
       v = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(blk + L.byte));
-    } else if (bits == 8) {
-      v = __fmul_rn(float(int(blk[L.byte]) - 128), s);
     } else {
-      const int nib = ((blk[L.byte] >> L.shift) & 0xF) - 8;
-      v = __fmul_rn(float(nib), s);
+      const int raw = bits == 8 ? int(blk[L.byte]) : int((blk[L.byte] >> L.shift) & 0xF);
+      v = asym ? __fmaf_rn(float(raw), s, m) : __fmul_rn(float(raw - bias), s);
     }
     out[j] = v;
   }

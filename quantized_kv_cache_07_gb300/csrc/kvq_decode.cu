@@ -1,1155 +1,28 @@
-// Fused dequantize-on-load decode attention (kvq_decode), sm_103a.
-//
-// What is computed, per query head of every sequence (one decode step):
-//   score_i = q . k_hat_i / sqrt(D),  o = sum_i softmax(score)_i v_hat_i
-//   ("KV Cache Quantization Perturbs Attention Through Stored Keys and Values",
-//   section "Key error acts before the softmax"; "KV Cache Quantization Reduces
-//   Cache Bytes with Separate Accuracy and Kernel Costs", section "Keys and
-//   values need not have identical error sensitivity").
-// How ("KV Cache Quantization and Per-Token Scale Placement"):
-//   - the key dot product runs on the integer codes and the per-token key scale
-//     multiplies the scalar score afterwards (section "The axis choice is a
-//     kernel decision");
-//   - a per-channel key factor is multiplied onto the query once (same section);
-//   - codes and scales are two read streams, dequantized as they are loaded
-//     (section "Per-token scales and where they can live");
-//   - the value scale is folded into the attention weight, so the value loop is
-//     a pure code contraction.
-// The most recent W tokens may sit in a bf16 ring ("KV Cache Quantization
-// Perturbs Attention ...", section "Cache growth changes the serving trade").
-//
-// GB300 mapping
-//   * Stream-K decomposition: all (sequence, kv_head) units' 16-token blocks form
-//     one global range that is cut evenly over one wave of CTAs (SMs x resident
-//     CTAs).  A CTA walks its range, keeps online-softmax state per unit segment
-//     and writes one partial (m, l, o) per segment; the last CTA to finish a
-//     unit (atomic ticket, no spinning) merges its partials with a log-sum-exp
-//     reduce.  A unit held by a single CTA is normalised in place.
-//   * One producer warp streams whole 16-token blocks (codes of K and V plus
-//     their scales) with cp.async.bulk into a ring of shared-memory stages
-//     guarded by mbarriers; four consumer warps each take one block per stage.
-//   * The GQA group (G <= 8 query heads sharing the KV head) makes the two small
-//     contractions dense: S^T = Kcodes . Q^T and O^T += V^T . (p*s_v)^T run on
-//     mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens/dims on M, the query
-//     group on N.  Codes are converted exactly to fp16 in registers; the cache
-//     is stored in the fragment order so every lane reads 16 contiguous bytes.
-//   * The query is scaled by an exact power of two into fp16's range; the score
-//     scale s_k * 2^-e * log2(e) / sqrt(D) is applied per score in fp32.
-#include <cuda_runtime.h>
-
-#include <mutex>
-#include <map>
-#include <tuple>
-
-#include "kvq_device.cuh"
-#include "kvq_launch.h"
+// Decode kernels for the symmetric formats (scale only) and bf16 blocks.  The
+// kernel template lives in kvq_decode_impl.cuh; the asymmetric formats are
+// instantiated in kvq_decode_asym.cu so the two compile in parallel.
+#include "kvq_decode_impl.cuh"
 
 namespace kvq {
-namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
-constexpr int kConsumerWarps = 4;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kInvSqrtD = 0.08838834764831845f;  // 1/sqrt(128)
-#define kNegInf (-__int_as_float(0x7f800000))
-
-template <int KB, int VB>
-struct Fmt {
-  static constexpr bool kBf16 = (KB == 16);
-  static constexpr int kKBB = block_bytes(KB);
-  static constexpr int kVBB = block_bytes(VB);
-  static constexpr int kSCB = kBf16 ? 0 : kBlock * 4;  // scale bytes per block per tensor
-  static constexpr int kPerBlock = kKBB + kVBB + 2 * kSCB;
-  // 4-bit keys: each consumer warp takes two blocks per stage (two independent
-  // dependency chains, one softmax reduction per 32 tokens)
-  static constexpr int kBPW = (KB == 4) ? 2 : 1;
-  static constexpr int kBlocksPerStage = kConsumerWarps * kBPW;
-  static constexpr int kStageBytes = kBlocksPerStage * kPerBlock;
-  static constexpr int kStagesRaw = 53248 / kStageBytes;  // ~52 KB ring: 3 CTAs per SM
-  static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
-  // stage sub-buffers
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kBlocksPerStage * kKBB;
-  static constexpr int kOffKS = kOffV + kBlocksPerStage * kVBB;
-  static constexpr int kOffVS = kOffKS + kBlocksPerStage * kSCB;
-};
-
-// Shared-memory map after the stage ring (all offsets 16-byte aligned).
-struct SmemMap {
-  int merge_o;   // float [4 warps][4 q][128] (combine, four queries per pass)
-  int merge_ml;  // float m[4][8], l[4][8]
-  int qh;        // 16-bit [8][128]: B-operand rows of the current query group
-  int qs;        // float [8]
-  int qraw;      // bf16 [2][8][128]: prefetched raw query rows (double buffer)
-  int fraw;      // float [2][128]: prefetched per-channel key factor row
-  int hdr;       // int4 [stages]
-  int bars;      // uint64 full[stages], empty[stages], cbar
-  int misc;      // int [4]
-  int len;       // int [B]
-  int pre;       // int [B+1]
-  int vpre;      // int [B+1]
-  int total;
-};
-
-__host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, int B) {
-  SmemMap m;
-  int o = stage_bytes_total;
-  m.merge_o = o;  o += kConsumerWarps * 4 * kHeadDim * 4;
-  m.merge_ml = o; o += 2 * kConsumerWarps * kMaxGroup * 4;
-  m.qh = o;       o += kMaxGroup * kHeadDim * 2;
-  m.qs = o;       o += kMaxGroup * 4 + 32;
-  m.qraw = o;     o += 2 * kMaxGroup * kHeadDim * 2;
-  m.fraw = o;     o += 2 * kHeadDim * 4;
-  m.hdr = o;      o += stages * 16;
-  m.bars = o;     o += (2 * stages + 2) * 8;
-  m.misc = o;     o += 16;
-  m.len = o;      o += ((B * 4 + 15) / 16) * 16;
-  m.pre = o;      o += (((B + 1) * 4 + 15) / 16) * 16;
-  m.vpre = o;     o += (((B + 1) * 4 + 15) / 16) * 16;
-  m.total = o;
-  return m;
-}
-
-// ------------------------------------------------------------------ score / value contractions
-template <int KB>
-__device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&qf)[16], float (&acc)[4],
-                                            int lane) {
-  // two accumulators halve the dependent MMA chain; summed at the end
-  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-  const uint4* p = reinterpret_cast<const uint4*>(kb) + lane;
-  if constexpr (KB == 8) {
-    const uint4 r0a = p[0], r0b = p[32], r1a = p[64], r1b = p[96];
-    const uint32_t g0[8] = {r0a.x, r0a.y, r0a.z, r0a.w, r0b.x, r0b.y, r0b.z, r0b.w};
-    const uint32_t g8[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      s8x4_to_f16(g0[kk], a0, a2);
-      s8x4_to_f16(g8[kk], a1, a3);
-      if (kk & 1) mma_f16(acc2, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
-      else mma_f16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
-    }
-  } else if constexpr (KB == 4) {
-    const uint4 r0 = p[0], r1 = p[32];
-    const uint32_t g0[4] = {r0.x, r0.y, r0.z, r0.w};
-    const uint32_t g8[4] = {r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-    for (int wi = 0; wi < 4; ++wi) {
-      uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-      s4x8_to_f16(g0[wi], x0, x1, x2, x3);
-      s4x8_to_f16(g8[wi], y0, y1, y2, y3);
-      mma_f16(acc, x0, y0, x1, y1, qf[4 * wi], qf[4 * wi + 1]);
-      mma_f16(acc2, x2, y2, x3, y3, qf[4 * wi + 2], qf[4 * wi + 3]);
-    }
-  } else {
-    uint4 c[8];
-#pragma unroll
-    for (int h = 0; h < 8; ++h) c[h] = p[h * 32];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint4 lo = c[kk >> 1], hi = c[4 + (kk >> 1)];
-      const uint32_t a0 = (kk & 1) ? lo.z : lo.x, a2 = (kk & 1) ? lo.w : lo.y;
-      const uint32_t a1 = (kk & 1) ? hi.z : hi.x, a3 = (kk & 1) ? hi.w : hi.y;
-      if (kk & 1) mma_bf16(acc2, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
-      else mma_bf16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
-}
-
-template <int VB>
-__device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint32_t b1, uint32_t b0lo,
-                                            uint32_t b1lo, float (&O)[8][4], int lane) {
-  const uint4* p = reinterpret_cast<const uint4*>(vb) + lane;
-  if constexpr (VB == 8) {
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const uint4 c = p[h * 32];
-      uint32_t a0, a1, a2, a3;
-      s8x4_to_f16(c.x, a0, a2);
-      s8x4_to_f16(c.y, a1, a3);
-      mma_f16(O[2 * h], a0, a1, a2, a3, b0, b1);
-      s8x4_to_f16(c.z, a0, a2);
-      s8x4_to_f16(c.w, a1, a3);
-      mma_f16(O[2 * h + 1], a0, a1, a2, a3, b0, b1);
-    }
-  } else if constexpr (VB == 4) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 c = p[h * 32];
-      const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t x0, x1, x2, x3;
-        s4x8_to_f16(w[k], x0, x1, x2, x3);
-        mma_f16(O[4 * h + k], x0, x2, x1, x3, b0, b1);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const uint4 c = p[mt * 32];
-      mma_bf16(O[mt], c.x, c.z, c.y, c.w, b0, b1);
-      mma_bf16(O[mt], c.x, c.z, c.y, c.w, b0lo, b1lo);
-    }
-  }
-}
-
-struct Params {
-  DecodeArgs a;
-  int P;   // stream CTAs launched (after the window CTAs)
-  int Uw;  // window CTAs launched first in the grid (one per unit, 0 without a window)
-};
-
-// Geometry of the work split.  Every (sequence, kv_head) unit with data owns
-// a range of "virtual blocks" in one global order: X leading virtual blocks
-// that stand for the cost of starting the unit (query staging, flush of the
-// previous unit, its record), then its data blocks.  The stream CTAs cut the
-// virtual range evenly, so a CTA that starts more units gets fewer blocks.
-struct Geo {
-  const int* pre;   // [B+1] prefix sums of data blocks per sequence (one head)
-  const int* vpre;  // [B+1] prefix sums of virtual blocks per sequence (one head)
-  int B, H, X;
-};
-
-__device__ __forceinline__ int geo_nblk(const Geo& g, int b) { return g.pre[b + 1] - g.pre[b]; }
-__device__ __forceinline__ int geo_vlen(const Geo& g, int b) { return g.vpre[b + 1] - g.vpre[b]; }
-__device__ __forceinline__ long long geo_vstart(const Geo& g, int b, int h) {
-  return (long long)g.H * g.vpre[b] + (long long)h * geo_vlen(g, b);
-}
-
-// Unit holding virtual block x (x < total): the largest b with H*vpre[b] <= x
-// has blocks; the head follows from the offset inside that sequence's range.
-__device__ __forceinline__ void locate_unit(const Geo& g, long long x, int& b, int& h) {
-  int lo = 0, hi = g.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)g.H * g.vpre[mid] <= x) lo = mid;
-    else hi = mid - 1;
-  }
-  b = lo;
-  while (geo_vlen(g, b) == 0) ++b;
-  h = int((x - (long long)g.H * g.vpre[b]) / geo_vlen(g, b));
-}
-
-// Base-2 exponential: the PTX ex2.approx.f32 instruction (max relative error
-// about 2^-22 per the PTX ISA; ex2(-inf) = +0, subnormal results kept).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Slack of the lazy running maximum (log2 units) and the largest value scale
-// whose fp16 weight p * s_v (p <= 2^kMaxSlack) stays below 65504.
-constexpr float kMaxSlack = 6.f;
-constexpr float kMaxValueScale = 1023.f;
-
-// A stream CTA owns at least this many blocks (fewer, deeper splits for tiny problems).
-constexpr int kMinBlocksPerCta = 16;
-
-// CTA-consumer barrier on an mbarrier (count = kConsumers), bounded wait.
-__device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase) {
-  mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, phase);
-  phase ^= 1u;
-  return ok;
-}
-
-__device__ __forceinline__ long long cta_of(long long x, long long T, int P) {
-  return ((x + 1) * (long long)P - 1) / T;
-}
-
-// Write the final normalised output of query row hq.
-__device__ __forceinline__ void write_out(const DecodeArgs& a, int b, int hq, int d, float o, float l, float M) {
-  const size_t idx = (size_t(b) * a.Hq + hq) * kHeadDim + d;
-  const float v = o / l;
-  if (a.out_fp32) reinterpret_cast<float*>(a.out)[idx] = v;
-  else reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(v);
-  if (d == 0 && a.lse) a.lse[size_t(b) * a.Hq + hq] = (M + log2f(l)) * kLn2;
-}
-
-// Partial records of unit u: stream segments c0..c1 (the CTAs owning its data
-// blocks, slot j + u) and, with a window, one window record (slot P + units + u).
-__device__ __forceinline__ void unit_segments(const DecodeArgs& a, const int* len_s, const Geo& g, int u,
-                                              long long Tv, int Pe, long long& c0, long long& c1, int& nseg,
-                                              bool& has_win) {
-  const int b = u / g.H, h = u % g.H;
-  const int nblk = geo_nblk(g, b);
-  nseg = 0;
-  c0 = 0;
-  c1 = -1;
-  if (nblk > 0) {
-    const long long d0 = geo_vstart(g, b, h) + g.X;
-    c0 = cta_of(d0, Tv, Pe);
-    c1 = cta_of(d0 + nblk - 1, Tv, Pe);
-    nseg = int(c1 - c0 + 1);
-  }
-  has_win = a.c.window > 0 && len_s[b] > 0;
-  nseg += has_win ? 1 : 0;
-}
-
-// Online-softmax state of one consumer warp; each thread holds queries 2t, 2t+1.
-struct WarpState {
-  float O[8][4];
-  float m0, m1, l0, l1;
-  __device__ __forceinline__ void reset() {
-    m0 = m1 = kNegInf;
-    l0 = l1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
-  }
-};
-
-// NB (1 or 2) 16-token blocks of one warp: scores on the codes, per-token key
-// scale after the dot product, online softmax, value scale folded into the
-// weight, value MMA.  With NB = 2 the two blocks' chains interleave and share
-// one lazy-maximum test and reduction.
-template <int KB, int VB, int NB>
-__device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], const uint8_t* const (&vb)[NB],
-                                               const float* const (&ks)[NB], const float* const (&vs)[NB],
-                                               const int (&valid)[NB], const uint32_t (&qf)[16], float qs0,
-                                               float qs1, WarpState& st, int lane, uint32_t* err) {
-  constexpr bool kBf16 = (KB == 16);
-  const int g = lane >> 2, t = lane & 3;
-  float x[NB][4];
-  float sv[NB][2];
-#pragma unroll
-  for (int j = 0; j < NB; ++j) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    score_block<KB>(kb[j], qf, acc, lane);
-    float sk0 = 1.f, sk1 = 1.f;
-    sv[j][0] = sv[j][1] = 1.f;
-    if constexpr (!kBf16) {
-      sk0 = ks[j][g];
-      sk1 = ks[j][g + 8];
-      sv[j][0] = vs[j][g];
-      sv[j][1] = vs[j][g + 8];
-    }
-    x[j][0] = acc[0] * (sk0 * qs0);  // token g, query 2t
-    x[j][1] = acc[1] * (sk0 * qs1);  // token g, query 2t+1
-    x[j][2] = acc[2] * (sk1 * qs0);  // token g+8, query 2t
-    x[j][3] = acc[3] * (sk1 * qs1);  // token g+8, query 2t+1
-    if (valid[j] < kBlock) {  // the last block of a unit may be partial
-      const bool v0 = g < valid[j], v1 = g + 8 < valid[j];
-      x[j][0] = v0 ? x[j][0] : kNegInf;
-      x[j][1] = v0 ? x[j][1] : kNegInf;
-      x[j][2] = v1 ? x[j][2] : kNegInf;
-      x[j][3] = v1 ? x[j][3] : kNegInf;
-    }
-  }
-  // Lazy running maximum: the reference m only moves (with a full reduction
-  // and a rescale of l and O) when a score exceeds it by more than
-  // kMaxSlack; otherwise the weights 2^(x - m) stay below 2^kMaxSlack.
-  float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
-#pragma unroll
-  for (int j = 1; j < NB; ++j) {
-    mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
-    mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
-  }
-  if (__any_sync(kFull, (mx0 > st.m0 + kMaxSlack) || (mx1 > st.m1 + kMaxSlack))) {
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-    }
-    const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-    const float al0 = (mn0 == kNegInf) ? 1.f : ex2(st.m0 - mn0);
-    const float al1 = (mn1 == kNegInf) ? 1.f : ex2(st.m1 - mn1);
-    st.l0 *= al0;
-    st.l1 *= al1;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      st.O[i][0] *= al0;
-      st.O[i][2] *= al0;
-      st.O[i][1] *= al1;
-      st.O[i][3] *= al1;
-    }
-    st.m0 = mn0;
-    st.m1 = mn1;
-  }
-  const float base0 = (st.m0 == kNegInf) ? 0.f : st.m0, base1 = (st.m1 == kNegInf) ? 0.f : st.m1;
-  const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
-#pragma unroll
-  for (int j = 0; j < NB; ++j) {
-    const float p00 = ex2(x[j][0] - base0), p10 = ex2(x[j][2] - base0);
-    const float p01 = ex2(x[j][1] - base1), p11 = ex2(x[j][3] - base1);
-    st.l0 += p00 + p10;
-    st.l1 += p01 + p11;
-    uint32_t pk0, pk1, pk0lo = 0, pk1lo = 0;
-    if constexpr (kBf16) {
-      const __nv_bfloat162 h0 = __floats2bfloat162_rn(p00, p10), h1 = __floats2bfloat162_rn(p01, p11);
-      pk0 = *reinterpret_cast<const uint32_t*>(&h0);
-      pk1 = *reinterpret_cast<const uint32_t*>(&h1);
-      pk0lo = pack_bf162(p00 - __low2float(h0), p10 - __high2float(h0));
-      pk1lo = pack_bf162(p01 - __low2float(h1), p11 - __high2float(h1));
-    } else {
-      // weights are at most 2^kMaxSlack, so p * s_v stays finite in fp16 while s_v <= kMaxValueScale
-      float w00 = p00 * sv[j][0], w10 = p10 * sv[j][1], w01 = p01 * sv[j][0], w11 = p11 * sv[j][1];
-      float svmax = fmaxf(sv[j][0], sv[j][1]);
-      if (valid[j] < kBlock) {  // scales of empty slots of a partial block are not data
-        const bool v0 = g < valid[j], v1 = g + 8 < valid[j];
-        w00 = v0 ? w00 : 0.f;
-        w01 = v0 ? w01 : 0.f;
-        w10 = v1 ? w10 : 0.f;
-        w11 = v1 ? w11 : 0.f;
-        svmax = fmaxf(v0 ? sv[j][0] : 0.f, v1 ? sv[j][1] : 0.f);
-      }
-      if (svmax > kMaxValueScale) flag(err, KVQ_DEVERR_RANGE);
-      pk0 = pack_half2(w00, w10);
-      pk1 = pack_half2(w01, w11);
-    }
-    // transpose the weights from the score accumulator layout (token rows,
-    // query columns) into the B-operand layout of the value contraction
-    const uint32_t r00 = __shfl_sync(kFull, pk0, src0), r01 = __shfl_sync(kFull, pk1, src0);
-    const uint32_t r10 = __shfl_sync(kFull, pk0, src1), r11 = __shfl_sync(kFull, pk1, src1);
-    const uint32_t b0 = (g & 1) ? r01 : r00, b1 = (g & 1) ? r11 : r10;
-    uint32_t b0lo = 0, b1lo = 0;
-    if constexpr (kBf16) {
-      const uint32_t q00 = __shfl_sync(kFull, pk0lo, src0), q01 = __shfl_sync(kFull, pk1lo, src0);
-      const uint32_t q10 = __shfl_sync(kFull, pk0lo, src1), q11 = __shfl_sync(kFull, pk1lo, src1);
-      b0lo = (g & 1) ? q01 : q00;
-      b1lo = (g & 1) ? q11 : q10;
-    }
-    value_block<VB>(vb[j], b0, b1, b0lo, b1lo, st.O, lane);
-  }
-}
-
-// Consumer warps write the query group of unit (b, h) into shared memory as
-// B-operand rows: fp16 scaled by an exact power of two for code blocks (with
-// the per-channel key factor applied), or the raw bf16 values for bf16 blocks.
-template <bool kBf16Q>
-__device__ __forceinline__ void stage_query(const DecodeArgs& a, int b, int h, uint16_t* qh, float* qs, int warp,
-                                            int lane) {
-  for (int q = warp; q < kMaxGroup; q += kConsumerWarps) {
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
-    if (q < a.G) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(a.q + (size_t(b) * a.Hq + h * a.G + q) * kHeadDim + 4 * lane);
-      x[0] = __uint_as_float(raw.x << 16);
-      x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-      x[2] = __uint_as_float(raw.y << 16);
-      x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-    }
-    uint2 packed;
-    if constexpr (kBf16Q) {
-      packed.x = pack_bf162(x[0], x[1]);
-      packed.y = pack_bf162(x[2], x[3]);
-      if (lane == 0) qs[q] = kLog2e * kInvSqrtD;
-    } else {
-      if (a.c.factor) {
-        const float4 c = *reinterpret_cast<const float4*>(a.c.factor + h * kHeadDim + 4 * lane);
-        x[0] *= c.x;
-        x[1] *= c.y;
-        x[2] *= c.z;
-        x[3] *= c.w;
-      }
-      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
-      int e = 0;
-      if (am > 0.f) {
-        int ex;
-        frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
-        e = 15 - ex;      // am * 2^e in [2^14, 2^15)
-      }
-      packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
-      packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
-      if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
-    }
-    *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
-  }
-}
-
-__device__ __forceinline__ void load_query(const uint16_t* qh, const float* qs, uint32_t (&qf)[16], float& qs0,
-                                           float& qs1, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  const uint4* qp = reinterpret_cast<const uint4*>(qh + g * kHeadDim + 32 * t);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 v = qp[i];
-    qf[4 * i] = v.x;
-    qf[4 * i + 1] = v.y;
-    qf[4 * i + 2] = v.z;
-    qf[4 * i + 3] = v.w;
-  }
-  qs0 = qs[2 * t];
-  qs1 = qs[2 * t + 1];
-}
-
-// Consumer warps start asynchronous copies of unit u's raw query rows (and of
-// the per-channel key factor row) into prefetch buffer `buf`; one commit group.
-__device__ __forceinline__ void prefetch_query(const DecodeArgs& a, int u, int buf, uint16_t* qraw, float* fraw,
-                                               int warp, int lane) {
-  const int H = a.c.H, b = u / H, h = u % H;
-  uint16_t* raw = qraw + buf * kMaxGroup * kHeadDim;
-  for (int q = warp; q < kMaxGroup; q += kConsumerWarps)
-    if (q < a.G)
-      cp_async8(raw + q * kHeadDim + 4 * lane, a.q + (size_t(b) * a.Hq + h * a.G + q) * kHeadDim + 4 * lane);
-  if (a.c.factor && warp == 0) cp_async16(fraw + buf * kHeadDim + 4 * lane, a.c.factor + h * kHeadDim + 4 * lane);
-  cp_async_commit();
-}
-
-// Next unit with data blocks in this CTA's virtual range [.., x1) after unit
-// `cur`, or -1.
-__device__ __forceinline__ int next_unit_in_range(const Geo& g, int cur, long long x1) {
-  const int b = cur / g.H, h = cur % g.H;
-  const long long vend = geo_vstart(g, b, h) + geo_vlen(g, b);
-  if (vend >= x1) return -1;
-  int b2, h2;
-  locate_unit(g, vend, b2, h2);
-  return (geo_vstart(g, b2, h2) + g.X < x1) ? b2 * g.H + h2 : -1;
-}
-
-// Shared scratch used by the combine and the merge.
-struct Scratch {
-  float* merge_o;  // [4 warps][4][128]
-  float* merge_m;  // [4][8]
-  float* merge_l;  // [4][8]
-  int* misc;
-  uint64_t* cbar;
-};
-
-// Once the copies of prefetch buffer `buf` have landed (every consumer thread
-// has waited on its cp.async groups), turn the raw rows into B-operand rows:
-// fp16 scaled by an exact power of two with the per-channel key factor
-// applied, or the raw bf16 values for bf16 blocks; then load the fragments.
-template <bool kBf16Q>
-__device__ __forceinline__ bool convert_query(const DecodeArgs& a, int buf, const uint16_t* qraw, const float* fraw,
-                                              uint16_t* qh, float* qs, const Scratch& sc, uint32_t& cphase, int warp,
-                                              int lane, uint32_t (&qf)[16], float& qs0, float& qs1) {
-  if (!consumer_sync(sc.cbar, cphase)) return false;  // the factor row was copied by warp 0
-  const uint16_t* raw = qraw + buf * kMaxGroup * kHeadDim;
-  for (int q = warp; q < kMaxGroup; q += kConsumerWarps) {
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
-    if (q < a.G) {
-      const uint2 r = *reinterpret_cast<const uint2*>(raw + q * kHeadDim + 4 * lane);
-      x[0] = __uint_as_float(r.x << 16);
-      x[1] = __uint_as_float(r.x & 0xFFFF0000u);
-      x[2] = __uint_as_float(r.y << 16);
-      x[3] = __uint_as_float(r.y & 0xFFFF0000u);
-    }
-    uint2 packed;
-    if constexpr (kBf16Q) {
-      packed.x = pack_bf162(x[0], x[1]);
-      packed.y = pack_bf162(x[2], x[3]);
-      if (lane == 0) qs[q] = kLog2e * kInvSqrtD;
-    } else {
-      if (a.c.factor) {
-        const float4 c = *reinterpret_cast<const float4*>(fraw + buf * kHeadDim + 4 * lane);
-        x[0] *= c.x;
-        x[1] *= c.y;
-        x[2] *= c.z;
-        x[3] *= c.w;
-      }
-      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
-      int e = 0;
-      if (am > 0.f) {
-        int ex;
-        frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
-        e = 15 - ex;      // am * 2^e in [2^14, 2^15)
-      }
-      packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
-      packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
-      if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
-    }
-    *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
-  }
-  if (!consumer_sync(sc.cbar, cphase)) return false;
-  load_query(qh, qs, qf, qs0, qs1, lane);
-  return true;
-}
-
-// Log-sum-exp merge of every partial record of unit u, run by the consumer
-// threads of the last CTA to finish the unit.  Thread f owns float4 f of the
-// G x 128 output and merges it on its own, without block synchronisation: the
-// (m, l, o) of eight records are loaded at once, then folded into a running
-// (M, l, o) with the usual rescaling by 2^(M_old - M_new).
-__device__ __noinline__ void merge_unit(const DecodeArgs& a, int u, long long c0, long long c1, bool has_win, int P,
-                                        int tid) {
-  constexpr int kR = 8;  // records in flight per thread
-  const int G = a.G, H = a.c.H;
-  const int b = u / H, h = u % H;
-  const int ns = c1 >= c0 ? int(c1 - c0 + 1) : 0;
-  const int ntot = ns + (has_win ? 1 : 0);
-  const size_t wslot = size_t(P) + a.lay.units + u;
-  const float* pm = reinterpret_cast<const float*>(a.ws + a.lay.off_m);
-  const float* pl = reinterpret_cast<const float*>(a.ws + a.lay.off_l);
-  const float* po = reinterpret_cast<const float*>(a.ws + a.lay.off_o);
-  const int nf = G * (kHeadDim / 4);
-  for (int f = tid; f < nf; f += kConsumers) {
-    const int q = f >> 5, d4 = f & 31;
-    float M = kNegInf, l = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = 0; base < ntot; base += kR) {
-      const int cnt = min(kR, ntot - base);
-      float mr[kR], lr[kR];
-      float4 orr[kR];
-#pragma unroll
-      for (int j = 0; j < kR; ++j) {
-        if (j < cnt) {
-          const int r = base + j;
-          const size_t slot = r < ns ? size_t(c0 + r + u) : wslot;
-          mr[j] = __ldcg(pm + slot * kMaxGroup + q);
-          lr[j] = __ldcg(pl + slot * kMaxGroup + q);
-          orr[j] = __ldcg(reinterpret_cast<const float4*>(po + (slot * kMaxGroup + q) * kHeadDim) + d4);
-        } else {
-          mr[j] = kNegInf;
-          lr[j] = 0.f;
-          orr[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-      float Mn = M;
-#pragma unroll
-      for (int j = 0; j < kR; ++j) Mn = fmaxf(Mn, mr[j]);
-      const float rs = (M == kNegInf) ? 0.f : exp2f(M - Mn);
-      l *= rs;
-      o.x *= rs;
-      o.y *= rs;
-      o.z *= rs;
-      o.w *= rs;
-#pragma unroll
-      for (int j = 0; j < kR; ++j) {
-        const float w = (mr[j] == kNegInf) ? 0.f : exp2f(mr[j] - Mn);
-        l = fmaf(w, lr[j], l);
-        o.x = fmaf(w, orr[j].x, o.x);
-        o.y = fmaf(w, orr[j].y, o.y);
-        o.z = fmaf(w, orr[j].z, o.z);
-        o.w = fmaf(w, orr[j].w, o.w);
-      }
-      M = Mn;
-    }
-    const float inv = 1.f / l;
-    const size_t idx = (size_t(b) * a.Hq + h * G + q) * kHeadDim + 4 * d4;
-    if (a.out_fp32) {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + idx) =
-          make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-    } else {
-      uint2 pk;
-      pk.x = pack_bf162(o.x * inv, o.y * inv);
-      pk.y = pack_bf162(o.z * inv, o.w * inv);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + idx) = pk;
-    }
-    if (d4 == 0 && a.lse) a.lse[size_t(b) * a.Hq + h * G + q] = (M + log2f(l)) * kLn2;
-  }
-}
-
-// Combine the four consumer warps' states of unit u and emit them: the final
-// output if this is the unit's only record, else a partial record in `slot`
-// followed by the arrival ticket; the last CTA to arrive merges the unit.
-__device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& st, int u, size_t slot, const int* len_s,
-                                              const Geo& geo, long long Tv, int Pe, int P, const Scratch& sc,
-                                              uint32_t& cphase, int warp, int lane, int tid) {
-  const int g = lane >> 2, t = lane & 3;
-  const int G = a.G, H = a.c.H;
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    st.l0 += __shfl_xor_sync(kFull, st.l0, o);
-    st.l1 += __shfl_xor_sync(kFull, st.l1, o);
-  }
-  if (g == 0) {
-    sc.merge_m[warp * kMaxGroup + 2 * t] = st.m0;
-    sc.merge_m[warp * kMaxGroup + 2 * t + 1] = st.m1;
-    sc.merge_l[warp * kMaxGroup + 2 * t] = st.l0;
-    sc.merge_l[warp * kMaxGroup + 2 * t + 1] = st.l1;
-  }
-  long long c0, c1;
-  int nseg;
-  bool has_win;
-  unit_segments(a, len_s, geo, u, Tv, Pe, c0, c1, nseg, has_win);
-  const int b = u / H, h = u % H;
-  float* pm = reinterpret_cast<float*>(a.ws + a.lay.off_m);
-  float* pl = reinterpret_cast<float*>(a.ws + a.lay.off_l);
-  float* po = reinterpret_cast<float*>(a.ws + a.lay.off_o);
-  const int d = tid;
-  // combine the warps' O through shared memory, four queries per pass
-  for (int pass = 0; pass * 4 < G; ++pass) {
-    if (pass > 0 && !consumer_sync(sc.cbar, cphase)) return false;  // previous pass has read merge_o
-    if ((t >> 1) == pass) {
-      float* ow = sc.merge_o + warp * 4 * kHeadDim;
-      const int q0 = 2 * t - 4 * pass;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        ow[q0 * kHeadDim + 16 * mt + g] = st.O[mt][0];
-        ow[(q0 + 1) * kHeadDim + 16 * mt + g] = st.O[mt][1];
-        ow[q0 * kHeadDim + 16 * mt + g + 8] = st.O[mt][2];
-        ow[(q0 + 1) * kHeadDim + 16 * mt + g + 8] = st.O[mt][3];
-      }
-    }
-    if (!consumer_sync(sc.cbar, cphase)) return false;
-    for (int q = 4 * pass; q < min(G, 4 * pass + 4); ++q) {
-      float M = kNegInf;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sc.merge_m[w * kMaxGroup + q]);
-      float l = 0.f, o = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = sc.merge_m[w * kMaxGroup + q];
-        const float al = (mw == kNegInf) ? 0.f : exp2f(mw - M);
-        l += al * sc.merge_l[w * kMaxGroup + q];
-        o += al * sc.merge_o[(w * 4 + (q - 4 * pass)) * kHeadDim + d];
-      }
-      if (nseg == 1) {
-        write_out(a, b, h * G + q, d, o, l, M);
-      } else {
-        po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
-        if (d == 0) {
-          pm[slot * kMaxGroup + q] = M;
-          pl[slot * kMaxGroup + q] = l;
-        }
-      }
-    }
-  }
-  if (nseg > 1) {
-    // The block barrier (release/acquire at CTA scope) orders every thread's
-    // record stores before thread 0; its acquire-release atomic at GPU scope
-    // publishes them with the ticket and, for the last CTA to arrive, makes
-    // the other CTAs' records visible; the next block barrier extends that to
-    // all threads of this CTA.
-    if (!consumer_sync(sc.cbar, cphase)) return false;
-    if (tid == 0) {
-      int* cnt = reinterpret_cast<int*>(a.ws + a.lay.off_counter);
-      int tk;
-      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(tk) : "l"(cnt + u) : "memory");
-      sc.misc[0] = (tk == nseg - 1);
-    }
-    if (!consumer_sync(sc.cbar, cphase)) return false;
-    if (sc.misc[0]) {
-      merge_unit(a, u, c0, c1, has_win, P, tid);
-      if (tid == 0) reinterpret_cast<int*>(a.ws + a.lay.off_counter)[u] = 0;
-    }
-  }
-  // merge_o / misc are written again only after the next query staging sync
-  return true;
-}
-
-template <int KB, int VB>
-__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
-  using F = Fmt<KB, VB>;
-  constexpr int S = F::kStages;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const DecodeArgs& a = prm.a;
-  const int P = prm.P, Uw = prm.Uw;
-  const int H = a.c.H, G = a.G, B = a.B;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const SmemMap mp = smem_map(S * F::kStageBytes, S, B);
-  Scratch sc;
-  sc.merge_o = reinterpret_cast<float*>(smem + mp.merge_o);
-  sc.merge_m = reinterpret_cast<float*>(smem + mp.merge_ml);
-  sc.merge_l = sc.merge_m + kConsumerWarps * kMaxGroup;
-  uint16_t* qh = reinterpret_cast<uint16_t*>(smem + mp.qh);
-  float* qs = reinterpret_cast<float*>(smem + mp.qs);
-  uint16_t* qraw = reinterpret_cast<uint16_t*>(smem + mp.qraw);
-  float* fraw = reinterpret_cast<float*>(smem + mp.fraw);
-  int4* hdr = reinterpret_cast<int4*>(smem + mp.hdr);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + mp.bars);
-  uint64_t* empty = full + S;
-  sc.cbar = empty + S;
-  sc.misc = reinterpret_cast<int*>(smem + mp.misc);
-  int* len_s = reinterpret_cast<int*>(smem + mp.len);
-  int* pre_s = reinterpret_cast<int*>(smem + mp.pre);
-  int* vpre_s = reinterpret_cast<int*>(smem + mp.vpre);
-  const int X = a.lay.switch_blocks;
-
-  // Programmatic dependent launch: this grid may be launched while the
-  // previous kernel on the stream is still finishing; wait here until it has
-  // completed (its writes visible) before touching any memory, then let the
-  // next kernel on the stream be launched early in turn.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  // ---- sequence geometry: clamped lengths and block prefix sums
-  const int W = a.c.window;
-  const int cap = a.mbps * kBlock;
-  for (int b = tid; b < B; b += kThreads) {
-    int L = a.seq_lens[b];
-    if (L < 0) {
-      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
-      L = 0;
-    }
-    int Lq = W > 0 ? max(L - W, 0) : L;
-    if (Lq > cap) {
-      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
-      Lq = cap;
-      L = W > 0 ? cap + W : cap;
-    }
-    len_s[b] = L;
-    const int nb = (Lq + kBlock - 1) / kBlock;
-    pre_s[b + 1] = nb;                    // block count, scanned below
-    vpre_s[b + 1] = nb > 0 ? nb + X : 0;  // virtual blocks: start cost + data
-  }
-  if (tid == 0) {
-    pre_s[0] = 0;
-    vpre_s[0] = 0;
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
-    }
-    mbar_init(sc.cbar, kConsumers);
-    sc.misc[0] = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (warp < 2) {  // warp 0 scans the data blocks, warp 1 the virtual blocks
-    int* arr = warp == 0 ? pre_s : vpre_s;
-    int carry = 0;
-    for (int base = 0; base < B; base += 32) {
-      const int i = base + lane;
-      int v = i < B ? arr[i + 1] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(kFull, v, o);
-        if (lane >= o) v += n;
-      }
-      if (i < B) arr[i + 1] = v + carry;
-      carry += __shfl_sync(kFull, v, 31);
-    }
-  }
-  __syncthreads();
-  const Geo geo{pre_s, vpre_s, B, H, X};
-  const long long T = (long long)H * vpre_s[B];  // virtual blocks in total
-  const int U = B * H;
-  // Effective stream split: never more CTAs than blocks / kMinBlocksPerCta, so
-  // every CTA below Pe owns blocks and a unit's owners are exactly c0..c1.
-  const long long cap_ctas = (T + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
-  const int Pe = int(cap_ctas < (long long)P ? cap_ctas : (long long)P);
-  uint32_t cphase = 0;
-
-  // ==================================================================== window CTAs
-  if ((int)blockIdx.x < Uw) {
-    const int u = blockIdx.x;
-    const int b = u / H, h = u % H;
-    const int L = len_s[b];
-    if (L <= 0 || warp >= kConsumerWarps) return;  // the producer warp has no role here
-    const int nw = min(L, W);
-    const int nwb = (nw + kBlock - 1) / kBlock;
-    stage_query<true>(a, b, h, qh, qs, warp, lane);
-    if (!consumer_sync(sc.cbar, cphase)) { flag(a.err, KVQ_DEVERR_TIMEOUT); return; }
-    uint32_t qf[16];
-    float qs0, qs1;
-    load_query(qh, qs, qf, qs0, qs1, lane);
-    WarpState st;
-    st.reset();
-    const size_t ring0 = size_t(u) * (W / kBlock);
-    for (int j = warp; j < nwb; j += kConsumerWarps) {
-      const uint8_t* kb = a.c.k_win + (ring0 + j) * block_bytes(16);
-      const uint8_t* vb = a.c.v_win + (ring0 + j) * block_bytes(16);
-      const uint8_t* const kbs[1] = {kb};
-      const uint8_t* const vbs[1] = {vb};
-      const float* const nos[1] = {nullptr};
-      const int val[1] = {min(kBlock, nw - j * kBlock)};
-      process_blocks<16, 16, 1>(kbs, vbs, nos, nos, val, qf, qs0, qs1, st, lane, a.err);
-    }
-    const size_t slot = size_t(P) + U + u;
-    if (!finish_segment(a, st, u, slot, len_s, geo, T, Pe, P, sc, cphase, warp, lane, tid))
-      flag(a.err, KVQ_DEVERR_TIMEOUT);
-    return;
-  }
-
-  // ==================================================================== stream CTAs
-  const int ci = blockIdx.x - Uw;  // stream CTA index
-  // units with no tokens at all: out = 0, lse = -inf
-  for (int u = ci; u < U; u += P) {
-    const int b = u / H, h = u % H;
-    if (len_s[b] != 0) continue;
-    for (int e = tid; e < G * kHeadDim; e += kThreads) {
-      const int q = e / kHeadDim, d = e % kHeadDim;
-      const size_t idx = (size_t(b) * a.Hq + h * G + q) * kHeadDim + d;
-      if (a.out_fp32) reinterpret_cast<float*>(a.out)[idx] = 0.f;
-      else reinterpret_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(0.f);
-      if (d == 0 && a.lse) a.lse[size_t(b) * a.Hq + h * G + q] = kNegInf;
-    }
-  }
-  if (ci >= Pe) return;
-  const long long x0 = (long long)ci * T / Pe;
-  const long long x1 = (long long)(ci + 1) * T / Pe;
-  if (x0 >= x1) return;
-  int b_first, h_first;
-  locate_unit(geo, x0, b_first, h_first);
-  const long long xs = max(x0, geo_vstart(geo, b_first, h_first) + X);  // first data block of the range
-  if (xs >= x1) return;  // the range holds only unit-start cost: no data, no record
-
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer warp
-    const uint64_t pol = l2_evict_first_policy();
-    int b = b_first, h = h_first;
-    int nblk = geo_nblk(geo, b);
-    long long dstart = geo_vstart(geo, b, h) + X;  // virtual index of the unit's first data block
-    long long x = xs;
-    int it = 0, s = 0;
-    uint32_t ph = 0;  // stage index and the parity of its current use
-    bool ok = true;
-    // 32 block-table entries of sequence tc_b, logical blocks tc_base + lane
-    int tc_b = -1, tc_base = 0, tc_val = 0;
-    while (x < x1) {
-      if (x >= dstart + nblk) {  // next unit: skip its start cost
-        ++h;
-        if (h == H) {
-          h = 0;
-          do { ++b; } while (geo_vlen(geo, b) == 0);
-          nblk = geo_nblk(geo, b);
-        }
-        dstart = geo_vstart(geo, b, h) + X;
-        x = max(x, dstart);
-        if (x >= x1) break;
-      }
-      const long long rem = (x1 - x) < (dstart + nblk - x) ? (x1 - x) : (dstart + nblk - x);
-      const int n = int(rem < F::kBlocksPerStage ? rem : F::kBlocksPerStage);
-      const int local = int(x - dstart);
-      if (tc_b != b || local < tc_base || local + n > tc_base + 32) {
-        tc_b = b;
-        tc_base = local;
-        const int idx = local + lane;
-        int v = 0;
-        if (idx < nblk) {
-          v = a.table[size_t(b) * a.mbps + idx];
-          if (v < 0 || v >= a.c.num_blocks) {
-            flag(a.err, KVQ_DEVERR_BLOCK_ID);
-            v = 0;
-          }
-        }
-        tc_val = v;
-      }
-      if (it >= S) {
-        bool w_ok = true;
-        if (lane == 0) w_ok = mbar_wait(&empty[s], ph ^ 1u);
-        if (!__shfl_sync(kFull, w_ok ? 1 : 0, 0)) {
-          if (lane == 0) flag(a.err, KVQ_DEVERR_TIMEOUT);
-          ok = false;
-          break;
-        }
-      }
-      // physical ids of the stage's blocks on every lane; a lane whose block
-      // starts a run of consecutive ids issues one copy for the whole run
-      const int phys = __shfl_sync(kFull, tc_val, (local - tc_base) + min(lane, n - 1));
-      const int prev = __shfl_up_sync(kFull, phys, 1);
-      const bool start = lane < n && (lane == 0 || prev + 1 != phys);
-      int run = 1;
-      bool contig = true;
-#pragma unroll
-      for (int j = 1; j < F::kBlocksPerStage; ++j) {
-        const int nx = __shfl_down_sync(kFull, phys, j);
-        contig = contig && (lane + j < n) && (nx == phys + j);
-        run += contig ? 1 : 0;
-      }
-      if (lane == 0) {
-        hdr[s] = make_int4(b * H + h, local, n, 0);
-        mbar_arrive_expect_tx(&full[s], uint32_t(n * F::kPerBlock));
-      }
-      __syncwarp();
-      if (start) {
-        uint8_t* st = smem + s * F::kStageBytes;
-        const size_t hb = size_t(h) * a.c.num_blocks + phys;  // head-major pools
-        bulk_g2s(st + F::kOffK + lane * F::kKBB, a.c.k_codes + hb * F::kKBB, run * F::kKBB, &full[s], pol);
-        bulk_g2s(st + F::kOffV + lane * F::kVBB, a.c.v_codes + hb * F::kVBB, run * F::kVBB, &full[s], pol);
-        if constexpr (!F::kBf16) {
-          bulk_g2s(st + F::kOffKS + lane * F::kSCB, a.c.k_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
-          bulk_g2s(st + F::kOffVS + lane * F::kSCB, a.c.v_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
-        }
-      }
-      x += n;
-      ++it;
-      if (++s == S) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-    if (lane != 0) return;
-    if (ok) {  // terminator stage
-      if (it >= S && !mbar_wait(&empty[s], ph ^ 1u)) {
-        flag(a.err, KVQ_DEVERR_TIMEOUT);
-      } else {
-        hdr[s] = make_int4(-1, 0, 0, 0);
-        mbar_arrive(&full[s]);
-        ++it;
-      }
-    }
-    // drain: the most recent use of every stage must have landed before exit
-    for (int k = max(0, it - S); k < it; ++k)
-      if (!mbar_wait(&full[k % S], (k / S) & 1)) flag(a.err, KVQ_DEVERR_TIMEOUT);
-    return;
-  }
-
-  // -------------------------------------------------------------- consumer warps
-  WarpState st;
-  st.reset();
-  uint32_t qf[16];
-  float qs0 = 0.f, qs1 = 0.f;
-  int cur, cur_lq, qbuf = 0, nxt;
-  {
-    // the first unit is known from x0: fetch its query group (and the next
-    // unit's) while the first stage is still in flight
-    const int b0 = b_first, h0 = h_first;
-    cur = b0 * H + h0;
-    cur_lq = W > 0 ? max(len_s[b0] - W, 0) : len_s[b0];
-    prefetch_query(a, cur, 0, qraw, fraw, warp, lane);
-    nxt = next_unit_in_range(geo, cur, x1);
-    if (nxt >= 0) {
-      prefetch_query(a, nxt, 1, qraw, fraw, warp, lane);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    if (!convert_query<F::kBf16>(a, 0, qraw, fraw, qh, qs, sc, cphase, warp, lane, qf, qs0, qs1)) {
-      flag(a.err, KVQ_DEVERR_TIMEOUT);
-      return;
-    }
-  }
-  int s = 0;
-  uint32_t ph = 0;  // stage index and the parity of its current use
-  for (;;) {
-    if (!mbar_wait(&full[s], ph)) {
-      flag(a.err, KVQ_DEVERR_TIMEOUT);
-      return;
-    }
-    const int4 hd = hdr[s];
-    if (hd.x != cur) {
-      if (cur >= 0 &&
-          !finish_segment(a, st, cur, size_t(ci) + cur, len_s, geo, T, Pe, P, sc, cphase, warp, lane, tid)) {
-        flag(a.err, KVQ_DEVERR_TIMEOUT);
-        return;
-      }
-      if (hd.x < 0) break;  // terminator
-      if (hd.x != nxt) {  // not the predicted next unit: fetch its query group now
-        cp_async_wait<0>();
-        prefetch_query(a, hd.x, qbuf ^ 1, qraw, fraw, warp, lane);
-      }
-      cur = hd.x;
-      qbuf ^= 1;
-      const int cb = cur / H;
-      cur_lq = W > 0 ? max(len_s[cb] - W, 0) : len_s[cb];
-      cp_async_wait<0>();
-      if (!convert_query<F::kBf16>(a, qbuf, qraw, fraw, qh, qs, sc, cphase, warp, lane, qf, qs0, qs1)) {
-        flag(a.err, KVQ_DEVERR_TIMEOUT);
-        return;
-      }
-      nxt = next_unit_in_range(geo, cur, x1);
-      if (nxt >= 0) prefetch_query(a, nxt, qbuf ^ 1, qraw, fraw, warp, lane);
-      st.reset();
-    }
-    if (warp < hd.z) {
-      const uint8_t* stg = smem + s * F::kStageBytes;
-      auto kp = [&](int j) { return stg + F::kOffK + j * F::kKBB; };
-      auto vp = [&](int j) { return stg + F::kOffV + j * F::kVBB; };
-      auto ksp = [&](int j) {
-        return F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffKS + j * F::kSCB);
-      };
-      auto vsp = [&](int j) {
-        return F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffVS + j * F::kSCB);
-      };
-      auto val = [&](int j) { return min(kBlock, cur_lq - (hd.y + j) * kBlock); };
-      const int j0 = warp, j1 = warp + kConsumerWarps;
-      if (F::kBPW == 2 && j1 < hd.z) {
-        const uint8_t* const kbs[2] = {kp(j0), kp(j1)};
-        const uint8_t* const vbs[2] = {vp(j0), vp(j1)};
-        const float* const kss[2] = {ksp(j0), ksp(j1)};
-        const float* const vss[2] = {vsp(j0), vsp(j1)};
-        const int vals[2] = {val(j0), val(j1)};
-        process_blocks<KB, VB, 2>(kbs, vbs, kss, vss, vals, qf, qs0, qs1, st, lane, a.err);
-      } else {
-        const uint8_t* const kbs[1] = {kp(j0)};
-        const uint8_t* const vbs[1] = {vp(j0)};
-        const float* const kss[1] = {ksp(j0)};
-        const float* const vss[1] = {vsp(j0)};
-        const int vals[1] = {val(j0)};
-        process_blocks<KB, VB, 1>(kbs, vbs, kss, vss, vals, qf, qs0, qs1, st, lane, a.err);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (++s == S) {
-      s = 0;
-      ph ^= 1u;
-    }
-  }
-}
-
-// ------------------------------------------------------------------ host side
-template <int KB, int VB>
-struct Kernel {
-  using F = Fmt<KB, VB>;
-  static int smem_bytes(int B) { return smem_map(F::kStages * F::kStageBytes, F::kStages, B).total; }
-  // Allow the largest opt-in dynamic shared memory once per device; the
-  // per-launch size (which depends on the batch) then always fits.
-  static void ensure_attribute(int dev) {
-    static std::mutex mu;
-    static std::map<int, bool> done;
-    std::lock_guard<std::mutex> lk(mu);
-    if (done.count(dev)) return;
-    int optin = 0;
-    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    cudaFuncSetAttribute(decode_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    // Ask for the largest shared-memory carveout: the occupancy used to size
-    // the single wave assumes it, and a smaller split (chosen by default)
-    // would fit one CTA fewer per SM and turn the wave into 1.5 waves.
-    cudaFuncSetAttribute(decode_kernel<KB, VB>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    done[dev] = true;
-  }
-  static int ctas_per_sm(int B) {
-    static std::mutex mu;
-    static std::map<std::pair<int, int>, int> cache;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    ensure_attribute(dev);
-    const int smem = smem_bytes(B);
-    std::lock_guard<std::mutex> lk(mu);
-    auto key = std::make_pair(dev, smem);
-    auto itc = cache.find(key);
-    if (itc != cache.end()) return itc->second;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KB, VB>, kThreads, smem) != cudaSuccess)
-      n = 1;
-    n = n < 1 ? 1 : n;
-    cache[key] = n;
-    return n;
-  }
-  static cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
-    const int smem = smem_bytes(a.B);
-    int dev = 0;
-    cudaGetDevice(&dev);
-    ensure_attribute(dev);
-    Params p{a, a.lay.stream_ctas, a.lay.window_ctas};
-    const int grid = a.lay.window_ctas + a.lay.stream_ctas;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<KB, VB>, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-  }
-};
-
-}  // namespace
-
-int decode_ctas_per_sm_for(int k_bits, int v_bits, int B) {
-  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8>::ctas_per_sm(B);
-  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4>::ctas_per_sm(B);
-  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8>::ctas_per_sm(B);
-  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4>::ctas_per_sm(B);
-  if (k_bits == 16 && v_bits == 16) return Kernel<16, 16>::ctas_per_sm(B);
+int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int B) {
+  if (asym) return decode_ctas_per_sm_asym(k_bits, v_bits, B);
+  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, false>::ctas_per_sm(B);
+  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, false>::ctas_per_sm(B);
+  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, false>::ctas_per_sm(B);
+  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, false>::ctas_per_sm(B);
+  if (k_bits == 16 && v_bits == 16) return Kernel<16, 16, false>::ctas_per_sm(B);
   return 0;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  if (a.c.k_offsets) return launch_decode_asym(a, s);
   const int kb = a.c.k_bits, vb = a.c.v_bits;
-  if (kb == 8 && vb == 8) return Kernel<8, 8>::launch(a, s);
-  if (kb == 4 && vb == 4) return Kernel<4, 4>::launch(a, s);
-  if (kb == 4 && vb == 8) return Kernel<4, 8>::launch(a, s);
-  if (kb == 8 && vb == 4) return Kernel<8, 4>::launch(a, s);
-  if (kb == 16 && vb == 16) return Kernel<16, 16>::launch(a, s);
+  if (kb == 8 && vb == 8) return Kernel<8, 8, false>::launch(a, s);
+  if (kb == 4 && vb == 4) return Kernel<4, 4, false>::launch(a, s);
+  if (kb == 4 && vb == 8) return Kernel<4, 8, false>::launch(a, s);
+  if (kb == 8 && vb == 4) return Kernel<8, 4, false>::launch(a, s);
+  if (kb == 16 && vb == 16) return Kernel<16, 16, false>::launch(a, s);
   return cudaErrorInvalidValue;
 }
 

@@ -16,6 +16,8 @@ struct CacheView {
   uint8_t* v_codes;
   float* k_scales;
   float* v_scales;
+  float* k_offsets;  // zero points, same layout as the scales; null: symmetric format
+  float* v_offsets;
   const float* factor;  // [H][128] or null
   int window, window_batch;
   uint8_t* k_win;  // bf16 ring: [window_batch][H][W/16] fragment-native bf16 blocks
@@ -75,7 +77,10 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 // Resident decode CTAs per SM for this cache format and batch (occupancy
 // query on the current device, cached); 0 for an unsupported format.
-int decode_ctas_per_sm_for(int k_bits, int v_bits, int batch);
+int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int batch);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// The asymmetric instantiations (kvq_decode_asym.cu).
+int decode_ctas_per_sm_asym(int k_bits, int v_bits, int batch);
+cudaError_t launch_decode_asym(const DecodeArgs& a, cudaStream_t s);
 
 }  // namespace kvq

@@ -55,6 +55,7 @@ class Workload:
     k_dist: str = "normal"           # "normal" or "t3" (Student-t, nu = 3)
     outlier_channels: int = 0        # number of key channels scaled by outlier_mult
     outlier_mult: float = 10.0
+    asym: bool = False               # asymmetric format: per-token scale and zero point
     head_dim: int = HEAD_DIM
     block_size: int = BLOCK_SIZE
     seed: int = 0

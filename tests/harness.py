@@ -31,7 +31,7 @@ def oracle_state(inp, b):
     w = inp.workload
     k, v = seq_kv(inp, b)
     c = None if inp.channel_factor is None else inp.channel_factor.astype(np.float64)
-    return O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c)
+    return O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c, asym=w.asym)
 
 
 def oracle_decode(inp, units=None):
@@ -127,6 +127,6 @@ class GpuRun:
         c = self.cache
         get = lambda t: None if t is None else t.cpu().numpy()
         return dict(k_codes=get(c.k_codes), v_codes=get(c.v_codes), k_scales=get(c.k_scales),
-                    v_scales=get(c.v_scales),
+                    v_scales=get(c.v_scales), k_offsets=get(c.k_offsets), v_offsets=get(c.v_offsets),
                     k_window=None if c.k_window is None else c.k_window.view(self.torch.uint8).cpu().numpy(),
                     v_window=None if c.v_window is None else c.v_window.view(self.torch.uint8).cpu().numpy())

@@ -39,10 +39,11 @@ def value_offsets(bits: int):
     return mt * 512 + lane * 16 + (2 * hi + (j >> 1)) * 4 + 2 * (j & 1), np.zeros((BLOCK, D), int)
 
 
-def unpack_blocks(pool: np.ndarray, bits: int, is_key: bool, heads: int) -> np.ndarray:
+def unpack_blocks(pool: np.ndarray, bits: int, is_key: bool, heads: int, asym: bool = False) -> np.ndarray:
     """pool: uint8 [heads * num_blocks * block_bytes] (head-major) -> int32 codes
-    [num_blocks, heads, 16, 128], or uint16 bf16 bits for bits == 16.  Codes are
-    stored offset-binary (byte = code + 128, nibble = code + 8)."""
+    [num_blocks, heads, 16, 128], or uint16 bf16 bits for bits == 16.  Symmetric
+    codes are stored offset-binary (byte = code + 128, nibble = code + 8);
+    asymmetric codes are the stored byte / nibble itself."""
     bb = block_bytes(bits)
     blocks = pool.reshape(heads, -1, bb).transpose(1, 0, 2)
     off, sh = (key_offsets if is_key else value_offsets)(bits)
@@ -52,8 +53,8 @@ def unpack_blocks(pool: np.ndarray, bits: int, is_key: bool, heads: int) -> np.n
         return lo | (hi << 8)
     raw = blocks[..., off].astype(np.int32)
     if bits == 8:
-        return raw - 128
-    return ((raw >> sh) & 0xF) - 8
+        return raw if asym else raw - 128
+    return ((raw >> sh) & 0xF) - (0 if asym else 8)
 
 
 def offsets_are_a_permutation(bits: int, is_key: bool) -> bool:

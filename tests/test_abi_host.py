@@ -82,6 +82,9 @@ def _fake_desc(lib, **kw):
     (dict(head_dim=64), 2), (dict(block_size=32), 2), (dict(k_bits=2), 2), (dict(k_bits=16, v_bits=8), 2),
     (dict(k_codes=0x1004), 3), (dict(k_scales=None), 1), (dict(num_kv_heads=0), 1), (dict(window=256), 2),
     (dict(window=16), 1), (dict(window=24), 2),
+    # zero points: both or neither, 16-byte aligned, only on quantized blocks
+    (dict(k_offsets=0xA000), 1), (dict(v_offsets=0xA000), 1), (dict(k_offsets=0xA000, v_offsets=0xB008), 3),
+    (dict(k_bits=16, v_bits=16, k_scales=None, v_scales=None, k_offsets=0xA000, v_offsets=0xB000), 2),
 ])
 def test_host_validation_without_a_gpu(lib, kw, status):
     desc = _fake_desc(lib, **kw)

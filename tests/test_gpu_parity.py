@@ -34,6 +34,15 @@ SMALL = {
     "bf16": small_workload("bf16", k_bits=16, v_bits=16, len_range=(1, 333)),
     "bf16_g8": small_workload("bf16_g8", batch=2, q_heads=16, kv_heads=2, k_bits=16, v_bits=16,
                               len_range=(50, 400), k_dist="t3"),
+    # asymmetric format (per-token scale and zero point)
+    "asym_int8_g4": small_workload("asym_int8_g4", asym=True, outlier_channels=4),
+    "asym_int4_factor_g8": small_workload("asym_int4_factor_g8", batch=4, q_heads=16, kv_heads=2, k_bits=4,
+                                          v_bits=4, channel_factor=True, asym=True),
+    "asym_k4v8_window32_t3": small_workload("asym_k4v8_window32_t3", batch=3, q_heads=16, kv_heads=2, k_bits=4,
+                                            v_bits=8, len_range=(1, 500), window=32, k_dist="t3", asym=True),
+    "asym_k8v4_paged_append": small_workload("asym_k8v4_paged_append", batch=4, q_heads=4, kv_heads=4, k_bits=8,
+                                             v_bits=4, len_range=(1, 250), paged=True, append_one=True,
+                                             asym=True),
 }
 
 
@@ -53,8 +62,8 @@ def check_stored_cache(inp, run, units=None, max_positions=None):
     """Block-store codes/scales and window ring vs the oracle, bit for bit."""
     w = inp.workload
     pools = run.pools()
-    kc = unpack_blocks(pools["k_codes"], w.k_bits, True, w.kv_heads)
-    vc = unpack_blocks(pools["v_codes"], w.v_bits, False, w.kv_heads)
+    kc = unpack_blocks(pools["k_codes"], w.k_bits, True, w.kv_heads, asym=w.asym)
+    vc = unpack_blocks(pools["v_codes"], w.v_bits, False, w.kv_heads, asym=w.asym)
     bs = sorted({b for b, _ in units}) if units else range(w.batch)
     rng = np.random.default_rng(7)
     checked = 0
@@ -77,6 +86,13 @@ def check_stored_cache(inp, run, units=None, max_positions=None):
             vs = scales_by_block(pools["v_scales"], w.kv_heads)[phys, :, tok]
             np.testing.assert_array_equal(ks.view(np.uint32), st["k_scale"][pos].astype(np.float32).view(np.uint32))
             np.testing.assert_array_equal(vs.view(np.uint32), st["v_scale"][pos].astype(np.float32).view(np.uint32))
+            if w.asym:
+                ko = scales_by_block(pools["k_offsets"], w.kv_heads)[phys, :, tok]
+                vo = scales_by_block(pools["v_offsets"], w.kv_heads)[phys, :, tok]
+                np.testing.assert_array_equal(ko.view(np.uint32),
+                                              st["k_offset"][pos].astype(np.float32).view(np.uint32))
+                np.testing.assert_array_equal(vo.view(np.uint32),
+                                              st["v_offset"][pos].astype(np.float32).view(np.uint32))
         checked += len(pos)
         if w.window:
             L = Lq + st["k_window"].shape[0]
@@ -94,6 +110,39 @@ def test_append_stores_bit_exact_codes_and_scales(runs, name):
     inp, run = runs(name)
     assert check_stored_cache(inp, run) > 0
     assert run.err_bits() == 0
+
+
+def _exact_rn32(a, b):
+    """RN32(a + b) for float64 a, b whose float64 sum is exact (checked with the
+    error term of Knuth's TwoSum), so one rounding to float32 is the correctly
+    rounded result."""
+    s = a + b
+    bb = s - a
+    err = (a - (s - bb)) + (b - bb)
+    assert np.all(err == 0.0), "float64 sum not exact: the reference would round twice"
+    return s.astype(np.float32)
+
+
+@pytest.mark.parametrize("name", ["asym_int8_g4", "asym_int4_factor_g8", "asym_k4v8_window32_t3"])
+def test_dequant_asym_returns_rn32_of_code_times_scale_plus_offset(runs, name):
+    inp, run = runs(name)
+    w = inp.workload
+    b = 0
+    st = oracle_state(inp, b)
+    pos = np.arange(st["Lq"])
+    if pos.size == 0:
+        pytest.skip("sequence 0 lies entirely in the window")
+    slots = inp.block_table[b, pos // 16].astype(np.int64) * 16 + pos % 16
+    st_t = torch.from_numpy(slots.astype(np.int32)).cuda()
+    ko = torch.empty((len(pos), w.kv_heads, 128), dtype=torch.float32, device="cuda")
+    vo = torch.empty_like(ko)
+    run.lib.kvq_dequant(run.cache.desc, st_t, ko, vo)
+    torch.cuda.synchronize()
+    for got, tag in ((ko, "k"), (vo, "v")):
+        u = st[f"{tag}_codes"][pos].astype(np.float64)
+        prod = u * st[f"{tag}_scale"][pos].astype(np.float64)[..., None]          # exact: <= 32 significant bits
+        ref = _exact_rn32(prod, np.broadcast_to(st[f"{tag}_offset"][pos].astype(np.float64)[..., None], prod.shape))
+        np.testing.assert_array_equal(got.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
 @pytest.mark.parametrize("name", ["int8_g4", "int4_factor_g8", "k4v8_g8_t3", "bf16"])
@@ -129,7 +178,7 @@ def test_decode_matches_oracle(runs, name, out_fp32):
     assert run.err_bits() == 0
 
 
-@pytest.mark.parametrize("name", ["int8_g4", "k4v8_g8_t3", "window32_int8", "bf16"])
+@pytest.mark.parametrize("name", ["int8_g4", "k4v8_g8_t3", "window32_int8", "bf16", "asym_k4v8_window32_t3"])
 def test_decode_split_count_does_not_change_result(runs, name):
     """Any split of the token range gives the same attention up to the rounding
     of the fp16 value weights p*s_v, which are rounded relative to the running
@@ -264,9 +313,17 @@ def _sample_units(w, k, seed=11):
     return units
 
 
-@pytest.mark.parametrize("name", list(WORKLOADS))
+FULL = dict(WORKLOADS)
+# the asymmetric format on two of the named shapes
+FULL["asym_gqa_int8_window128_b8_t4096"] = WORKLOADS["gqa_int8_window128_b8_t4096"].with_(
+    name="asym_gqa_int8_window128_b8_t4096", asym=True)
+FULL["asym_long_k4v8_b4_t131072"] = WORKLOADS["long_k4v8_b4_t131072"].with_(name="asym_long_k4v8_b4_t131072",
+                                                                          asym=True)
+
+
+@pytest.mark.parametrize("name", list(FULL))
 def test_full_size_workload(name):
-    w = WORKLOADS[name]
+    w = FULL[name]
     inp = make_inputs(w)
     run = GpuRun(inp)
     units = _sample_units(w, 6 if w.batch * w.kv_heads > 8 else 4)
