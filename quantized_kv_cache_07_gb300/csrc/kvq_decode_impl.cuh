@@ -806,6 +806,53 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
   return true;
 }
 
+// Clamped lengths and the two block prefix sums of every sequence, in shared
+// memory (all threads; ends with a block barrier).  `load` reads a length;
+// block 0 reports lengths that are negative or beyond the table's capacity.
+template <typename LoadLen>
+__device__ __forceinline__ void scan_geometry(const DecodeArgs& a, int B, int W, int X, int* len_s, int* pre_s,
+                                              int* vpre_s, LoadLen load, int tid, int warp, int lane) {
+  const int cap = a.mbps * kBlock;
+  for (int b = tid; b < B; b += kThreads) {
+    int L = load(b);
+    if (L < 0) {
+      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
+      L = 0;
+    }
+    int Lq = W > 0 ? max(L - W, 0) : L;
+    if (Lq > cap) {
+      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
+      Lq = cap;
+      L = W > 0 ? cap + W : cap;
+    }
+    len_s[b] = L;
+    const int nb = (Lq + kBlock - 1) / kBlock;
+    pre_s[b + 1] = nb;                    // block count, scanned below
+    vpre_s[b + 1] = nb > 0 ? nb + X : 0;  // virtual blocks: start cost + data
+  }
+  if (tid == 0) {
+    pre_s[0] = 0;
+    vpre_s[0] = 0;
+  }
+  __syncthreads();
+  if (warp < 2) {  // warp 0 scans the data blocks, warp 1 the virtual blocks
+    int* arr = warp == 0 ? pre_s : vpre_s;
+    int carry = 0;
+    for (int base = 0; base < B; base += 32) {
+      const int i = base + lane;
+      int v = i < B ? arr[i + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += n;
+      }
+      if (i < B) arr[i + 1] = v + carry;
+      carry += __shfl_sync(kFull, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
 template <int KB, int VB, bool ASYM>
 __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   using F = Fmt<KB, VB, ASYM>;
@@ -834,36 +881,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   int* vpre_s = reinterpret_cast<int*>(smem + mp.vpre);
   const int X = a.lay.switch_blocks;
 
-  // Programmatic dependent launch: this grid may be launched while the
-  // previous kernel on the stream is still finishing; wait here until it has
-  // completed (its writes visible) before touching any memory, then let the
-  // next kernel on the stream be launched early in turn.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  // ---- sequence geometry: clamped lengths and block prefix sums
   const int W = a.c.window;
-  const int cap = a.mbps * kBlock;
-  for (int b = tid; b < B; b += kThreads) {
-    int L = a.seq_lens[b];
-    if (L < 0) {
-      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
-      L = 0;
-    }
-    int Lq = W > 0 ? max(L - W, 0) : L;
-    if (Lq > cap) {
-      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
-      Lq = cap;
-      L = W > 0 ? cap + W : cap;
-    }
-    len_s[b] = L;
-    const int nb = (Lq + kBlock - 1) / kBlock;
-    pre_s[b + 1] = nb;                    // block count, scanned below
-    vpre_s[b + 1] = nb > 0 ? nb + X : 0;  // virtual blocks: start cost + data
-  }
   if (tid == 0) {
-    pre_s[0] = 0;
-    vpre_s[0] = 0;
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
@@ -872,23 +891,15 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     sc.misc[0] = 0;
     fence_mbar_init();
   }
-  __syncthreads();
-  if (warp < 2) {  // warp 0 scans the data blocks, warp 1 the virtual blocks
-    int* arr = warp == 0 ? pre_s : vpre_s;
-    int carry = 0;
-    for (int base = 0; base < B; base += 32) {
-      const int i = base + lane;
-      int v = i < B ? arr[i + 1] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(kFull, v, o);
-        if (lane >= o) v += n;
-      }
-      if (i < B) arr[i + 1] = v + carry;
-      carry += __shfl_sync(kFull, v, 31);
-    }
-  }
-  __syncthreads();
+  // Programmatic dependent launch: this grid may start while the previous
+  // kernel on the stream is still finishing.  Let the next kernel launch
+  // early in turn, then wait until the previous kernel has completed (its
+  // writes visible) before reading any memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- sequence geometry: clamped lengths and block prefix sums
+  scan_geometry(a, B, W, X, len_s, pre_s, vpre_s, [&](int b) { return a.seq_lens[b]; }, tid, warp, lane);
   const Geo geo{pre_s, vpre_s, B, H, X};
   const long long T = (long long)H * vpre_s[B];  // virtual blocks in total
   const int U = B * H;
