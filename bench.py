@@ -447,7 +447,7 @@ def main():
                    "parallelism": f"replicas x{world}", "decode_grid": res["plan"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": recorded_traffic(w.name, "decode"), "kernel": "kvq decode_kernel",
+                     "traffic": recorded_traffic(w.name, "decode_asym" if w.asym else "decode"), "kernel": "kvq decode_kernel",
                      "decode_ms_in_timed_region": round(res["dec_ms"], 6),
                      "append_ms_per_step": round(res["app_ms"], 6),
                      "decode_ms_isolated_launch": round(res["dec_ms_iso"], 6)},
