@@ -37,6 +37,15 @@ Readings taken where the pages leave a step open:
     with qmaxu = 2^bits - 1, u = clamp(rint((x - m) / s), 0, qmaxu) with the
     difference and the quotient evaluated in float64, x_hat = u * s + m; a
     constant vector stores s = 1, u = 0 and m = its value.
+  * quantized query ([P3] "Precision floors and mixed cache formats": an 8-bit
+    query meets the integer key codes, the dot product accumulates in integers
+    and is converted to floating point before the exponential): the query row,
+    after the per-channel key factor is moved onto it, is quantized by the same
+    symmetric int8 rule as the cache, s_q = RN32(max|x| / 127), q_int =
+    clamp(rint(x / s_q)); the folded row q * c is formed in float32, the
+    kernel's precision, because it decides integer codes.  The score is
+    s_q * s_k * (q_int . k_int) / sqrt(D); against bf16 window keys the query
+    is q_int * s_q / c (q_int * s_q without a factor).
 Every function below is pinned by tests/test_oracle_pins.py.
 """
 from __future__ import annotations
@@ -110,6 +119,23 @@ def dequantize_asym(codes: np.ndarray, scale: np.ndarray, offset: np.ndarray) ->
 def dequantize(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
     """x_hat = q * s ([P2] "Quantization needs a scale convention"), exact in float64."""
     return np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[..., None]
+
+
+def quantize_query(q: np.ndarray, c: np.ndarray | None = None):
+    """Integer query of the quantized-query mode (see the module notes):
+    (codes int16 [..., D] in [-127, 127], scale float32 [...])."""
+    x = np.asarray(q, np.float64)
+    if c is not None:
+        x = (x * np.asarray(c, np.float64)).astype(np.float32).astype(np.float64)
+    return quantize(x, 8)
+
+
+def effective_query(q: np.ndarray, c: np.ndarray | None = None) -> np.ndarray:
+    """The float query whose dot product with the reconstructed keys c * k'_hat
+    equals s_q * (q_int . k'_hat): q_int * s_q / c (float64)."""
+    codes, s = quantize_query(q, c)
+    qe = dequantize(codes, s)
+    return qe if c is None else qe / np.asarray(c, np.float64)
 
 
 def divide_by_channel_factor(k: np.ndarray, c: np.ndarray) -> np.ndarray:
@@ -239,20 +265,25 @@ def reconstruct_sequence(st, head: int):
     return k_hat, v_hat
 
 
-def decode_sequence(q_bits, st, kv_heads: int):
+def decode_sequence(q_bits, st, kv_heads: int, query_bits: int = 16):
     """One decode step of one sequence: q_bits [H_q, D] bf16 bits.
 
     Query head h reads KV head h // (H_q / H_kv) (grouped-query sharing; the
-    pages' one-head formulas applied per head).  Returns (o [H_q, D], lse [H_q]).
+    pages' one-head formulas applied per head).  query_bits = 8 selects the
+    quantized-query mode (effective_query).  Returns (o [H_q, D], lse [H_q]).
     """
     q = bf16_to_f64(q_bits)
     H_q, D = q.shape
     G = H_q // kv_heads
     o = np.zeros((H_q, D))
     lse = np.zeros(H_q)
+    c = st["c"]
     for h in range(kv_heads):
         k_hat, v_hat = reconstruct_sequence(st, h)
-        o[h * G:(h + 1) * G], lse[h * G:(h + 1) * G] = attention(q[h * G:(h + 1) * G], k_hat, v_hat)
+        qh = q[h * G:(h + 1) * G]
+        if query_bits == 8:
+            qh = effective_query(qh, None if c is None else c[h])
+        o[h * G:(h + 1) * G], lse[h * G:(h + 1) * G] = attention(qh, k_hat, v_hat)
     return o, lse
 
 

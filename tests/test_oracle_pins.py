@@ -503,3 +503,89 @@ def test_asym_metadata_fraction_is_the_printed_six_percent(golden_dir):
     # scale + zero point over 128 int8 codes: the page's "add 6 percent" row
     assert O.metadata_fraction(128, 8, 8) == 0.0625
     assert O.cache_bytes_per_token_head(128, 8, 8, asym=True) == 2 * (128 + 8)
+
+
+# ---------------------------------------------------------------- quantized query (integer dot)
+def test_query_quantizer_is_the_cache_rule_on_the_folded_query():
+    """q_int / s_q are the exact symmetric int8 rule applied to q, or to the
+    float32 product q * c when a per-channel key factor is folded onto q."""
+    for trial in range(100):
+        q = bf16_vec(128, scale=float(2.0 ** RNG.integers(-6, 6)))
+        codes, s = O.quantize_query(q)
+        ref_codes, ref_s = exact_quantize(q, 8)
+        assert Fraction(float(s)) == ref_s and list(map(int, codes)) == ref_codes
+        c = (np.abs(bf16_vec(128)) + 0.1).astype(np.float32).astype(np.float64)
+        codes, s = O.quantize_query(q, c)
+        folded = (q * c).astype(np.float32)                         # one float32 rounding per element
+        ref_codes, ref_s = exact_quantize(folded, 8)
+        assert Fraction(float(s)) == ref_s and list(map(int, codes)) == ref_codes
+
+
+@pytest.mark.parametrize("k_bits", [8, 4])
+@pytest.mark.parametrize("factor", [False, True])
+def test_quantized_query_score_is_the_scaled_integer_dot(k_bits, factor):
+    """The oracle's score with the effective query equals s_q * s_k *
+    (q_int . k_int) / sqrt(D) computed with exact integers, with or without a
+    per-channel key factor (which cancels between query and keys)."""
+    D = 128
+    c = (np.abs(bf16_vec(D)) + 0.25).astype(np.float32).astype(np.float64) if factor else None
+    for _ in range(20):
+        q = bf16_vec(D)
+        k = bf16_vec(D, dist="t3")
+        q_int, s_q = O.quantize_query(q, c)
+        k_int, s_k = O.quantize_keys(k, k_bits, c)
+        acc = sum(int(a) * int(b) for a, b in zip(q_int, k_int))            # integer accumulator
+        exact = Fraction(float(s_q)) * Fraction(float(s_k)) * acc
+        k_hat = O.reconstruct_keys(k_int, s_k, c)
+        oracle_dot = float(O.effective_query(q, c) @ k_hat)
+        assert abs(oracle_dot - float(exact)) <= 1e-12 * max(1.0, abs(float(exact)))
+
+
+def test_integer_accumulator_width_matches_the_page():
+    """[P3] "Precision floors and mixed cache formats": a 4-bit key times an
+    8-bit query fits easily in 16 bits, the sum over 128 dims needs a few more
+    bits.  The extreme codes the two quantizers can produce bear this out."""
+    q_int, _ = O.quantize_query(np.ones(128))
+    k_int, _ = O.quantize_keys(-np.ones(128), 4)
+    assert int(q_int.max()) == 127 and int(k_int.min()) == -7          # -8 is unreachable
+    prods = q_int.astype(np.int64) * k_int.astype(np.int64)
+    assert np.abs(prods).max() < 2 ** 15                                 # a signed 16-bit product
+    acc = int(prods.sum())
+    assert 2 ** 15 <= abs(acc) < 2 ** 17                                 # the sum needs 17-18 bits
+
+
+def test_quantized_query_error_is_bounded_by_half_its_scale():
+    """|score(q_int s_q) - score(q)| <= (s_q / 2) * sum|k_hat| / sqrt(D): the
+    query quantizer's round-trip bound carried through the dot product (a
+    wrong query scale breaks it)."""
+    D = 128
+    for _ in range(50):
+        q = bf16_vec(D)
+        k_hat = bf16_vec(D)
+        _, s_q = O.quantize_query(q)
+        s_exact = float(q @ k_hat) / math.sqrt(D)
+        s_quant = float(O.effective_query(q) @ k_hat) / math.sqrt(D)
+        bound = float(s_q) / 2 * float(np.abs(k_hat).sum()) / math.sqrt(D)
+        assert abs(s_quant - s_exact) <= bound * (1 + 1e-12)
+        assert abs(s_quant - s_exact) > 0 or bound == 0
+
+
+def test_decode_sequence_quantized_query_mode_uses_each_heads_factor():
+    """GQA: the quantized-query decode of a sequence equals attention of each
+    query group's effective query over its own KV head (factor row h)."""
+    H, G, D, L = 2, 3, 128, 40
+    rng = np.random.default_rng(5)
+    k = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    v = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    qb = f32_to_bf16_bits(rng.standard_normal((H * G, D)).astype(np.float32))
+    c = (np.abs(rng.standard_normal((H, D))) + 0.5).astype(np.float32).astype(np.float64)
+    st = O.quantize_sequence(k, v, 8, 8, c=c)
+    o, lse = O.decode_sequence(qb, st, H, query_bits=8)
+    q = O.bf16_to_f64(qb)
+    for h in range(H):
+        k_hat, v_hat = O.reconstruct_sequence(st, h)
+        ref_o, ref_l = O.attention(O.effective_query(q[h * G:(h + 1) * G], c[h]), k_hat, v_hat)
+        np.testing.assert_allclose(o[h * G:(h + 1) * G], ref_o, rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse[h * G:(h + 1) * G], ref_l, rtol=0, atol=1e-15)
+    o16, _ = O.decode_sequence(qb, st, H)
+    assert not np.array_equal(o, o16)                                    # the mode changes the numerics
