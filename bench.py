@@ -146,6 +146,7 @@ if {bf16}:
     w = w.with_(k_bits=16, v_bits=16, window=0, channel_factor=False)
 if {asym}:
     w = w.with_(asym=True)
+QBITS = {qbits}
 inp = make_inputs(w)
 G = w.group
 budget = {budget}
@@ -164,7 +165,10 @@ while tot_t < budget or n == 0:
     st = O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c, asym=w.asym)   # untimed
     t1 = time.perf_counter()
     kh, vh = O.reconstruct_sequence(st, 0)
-    O.attention(O.bf16_to_f64(inp.q[b, h*G:(h+1)*G]), kh, vh)
+    qv = O.bf16_to_f64(inp.q[b, h*G:(h+1)*G])
+    if QBITS == 8:
+        qv = O.effective_query(qv, None if c is None else c[0])
+    O.attention(qv, kh, vh)
     tot_t += time.perf_counter() - t1
     L = k.shape[0]; Lq = st["Lq"]
     tot_b += per_tok * Lq + 512 * (L - Lq); n += 1
@@ -172,12 +176,13 @@ print(json.dumps({{"seconds": tot_t, "bytes": tot_b, "units": n}}))
 """
 
 
-def run_cpu_sample(name: str, budget_s: float, steps: int = 1, bf16: bool = False, asym: bool = False):
+def run_cpu_sample(name: str, budget_s: float, steps: int = 1, bf16: bool = False, asym: bool = False,
+                   qbits: int = 16):
     """Time the oracle's decode (dequantize + attention, float64) on a bounded
     sample of the workload's units, in a fresh single-threaded process."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    code = CPU_SAMPLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, bf16=bf16, asym=asym)
+    code = CPU_SAMPLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, bf16=bf16, asym=asym, qbits=qbits)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
     if res.returncode != 0:
         raise RuntimeError("oracle sample failed: " + res.stderr[-2000:])
@@ -210,6 +215,10 @@ def main():
                     help="skip the same-shape run in the asymmetric (scale + zero point) format")
     ap.add_argument("--asym", action="store_true",
                     help="time the workload in the asymmetric (scale + zero point) format")
+    ap.add_argument("--q-bits", type=int, default=16, choices=[8, 16],
+                    help="8: decode with int8-quantized query rows (integer dot product)")
+    ap.add_argument("--no-qint8", action="store_true",
+                    help="skip the same-shape run with int8-quantized query rows")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--stream-ctas", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0,
@@ -246,6 +255,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.asym:
         w = w.with_(asym=True)
+    if args.q_bits == 8:
+        w = w.with_(q_bits=8)
     inp = make_inputs(w)
     dev = torch.device("cuda", local)
     props = torch.cuda.get_device_properties(dev)
@@ -423,6 +434,17 @@ def main():
                 "time_vs_symmetric": ra["dec_ms"] / res["dec_ms"], "err_word": ra["err"]}
         del ina
 
+    qint8 = None
+    if not args.no_qint8 and w.k_bits != 16 and w.q_bits != 8 and not (w.channel_factor and w.window):
+        wq = w.with_(q_bits=8, name=w.name + "_qint8")
+        inq = make_inputs(wq)
+        rq = run_arm(inq, "qint8")
+        qint8 = {"workload": wq.name, "ms_per_step": rq["ms_step"], "decode_ms": rq["dec_ms"],
+                 "bytes_per_step": rq["bytes"], "effective_gbs": rq["bytes"] / (rq["dec_ms"] / 1e3) / 1e9,
+                 "frac_of_peak": rq["bytes"] / (rq["dec_ms"] / 1e3) / 1e9 / peak,
+                 "time_vs_bf16_query": rq["dec_ms"] / res["dec_ms"], "err_word": rq["err"]}
+        del inq
+
     line = {
         "metric": "quantized-KV decode attention: effective HBM GB/s (% of peak), steps/s",
         "value": round(value, 2),
@@ -441,6 +463,7 @@ def main():
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits,
                    "window": w.window, "paged": w.paged, "append_one": w.append_one,
                    "format": "asymmetric (scale + zero point)" if w.asym else "symmetric (scale)",
+                   "query": "int8 rows, integer dot" if w.q_bits == 8 else "bf16",
                    "cache_bytes_per_step": bytes_step, "allocated_cache_bytes": res["alloc"],
                    "l2": f"steps rotate over {res['replicas']} cache replicas "
                          f"({res['replicas'] * bytes_step / 2**20:.0f} MiB >= 4x L2 or cache > L2)",
@@ -458,11 +481,12 @@ def main():
         "clocks": res["clocks"],
         "bf16_same_design": bf16,
         "asym_same_shape": asym,
+        "qint8_same_shape": qint8,
         "device_err_word": res["err"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            d = run_cpu_sample(args.workload, args.cpu_budget, asym=w.asym)
+            d = run_cpu_sample(args.workload, args.cpu_budget, asym=w.asym, qbits=w.q_bits)
             line["cpu_baseline"] = {"value": round(d["bytes"] / d["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
                                     "kind": "oracle",
                                     "sample": f"{d['units']} (sequence, kv_head) units of {w.name}, float64 "

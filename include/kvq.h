@@ -123,6 +123,17 @@ typedef struct {
    * difference and quotient in double, x_hat = u * s + m. */
   float* k_offsets;       /* per-token key zero points (offset pool), or NULL      */
   float* v_offsets;       /* per-token value zero points, or NULL                  */
+  /* Query format of kvq_decode against this cache ([P3] "Precision floors and
+   * mixed cache formats": an 8-bit query meets the integer key codes, the dot
+   * product accumulates in integers and is converted to float before the
+   * exponential).  0 or 16: the bf16 query (default).  8: each query row, after
+   * the per-channel key factor is multiplied onto it in float32, is quantized
+   * per row with the symmetric int8 rule of kvq_append (s_q = RN32(max|x| /
+   * 127), q_int = clamp(round_half_even(x / s_q))) and the score is
+   * s_q * s_k * (q_int . k_int) / sqrt(D), the integer dot exact; bf16 window
+   * keys see q_int * s_q.  Needs 8- or 4-bit blocks; not combined with both a
+   * per-channel key factor and a window (KVQ_ERR_UNSUPPORTED). */
+  int32_t q_bits;
 } kvq_cache_desc;
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -24,11 +24,13 @@ class KVCache:
     """Block pools (+ optional bf16 window ring) of one attention layer.
 
     ``asym=True`` selects the asymmetric format: a per-token zero point is
-    stored beside each scale (offset pools of the same shape).
+    stored beside each scale (offset pools of the same shape).  ``q_bits=8``
+    makes kvq_decode quantize each query row to int8 (integer dot product).
     """
 
     def __init__(self, num_blocks: int, kv_heads: int, k_bits: int, v_bits: int, window: int = 0,
-                 window_batch: int = 0, channel_factor=None, asym: bool = False, device="cuda"):
+                 window_batch: int = 0, channel_factor=None, asym: bool = False, q_bits: int = 16,
+                 device="cuda"):
         _require_cuda()
         self.num_blocks, self.kv_heads = int(num_blocks), int(kv_heads)
         self.k_bits, self.v_bits = int(k_bits), int(v_bits)
@@ -66,7 +68,8 @@ class KVCache:
             k_window=self.k_window.data_ptr() if self.k_window is not None else None,
             v_window=self.v_window.data_ptr() if self.v_window is not None else None,
             k_offsets=self.k_offsets.data_ptr() if self.asym else None,
-            v_offsets=self.v_offsets.data_ptr() if self.asym else None)
+            v_offsets=self.v_offsets.data_ptr() if self.asym else None,
+            q_bits=int(q_bits))
 
     # bytes the decode reads per cached token per KV head (codes + scales + zero points)
     def bytes_per_token_head(self) -> int:
@@ -138,4 +141,4 @@ def cache_for_inputs(inp, device="cuda") -> KVCache:
     w = inp.workload
     return KVCache(inp.num_blocks, w.kv_heads, w.k_bits, w.v_bits, window=w.window,
                    window_batch=w.batch if w.window else 0, channel_factor=inp.channel_factor,
-                   asym=getattr(w, "asym", False), device=device)
+                   asym=getattr(w, "asym", False), q_bits=getattr(w, "q_bits", 16), device=device)

@@ -44,6 +44,8 @@ kvq_status check_cache(const kvq_cache_desc* c) {
     if (!quant) return KVQ_ERR_UNSUPPORTED;
     if (!aligned16(c->k_channel_factor)) return KVQ_ERR_ALIGNMENT;
   }
+  if (c->q_bits != 0 && c->q_bits != 16 && c->q_bits != 8) return KVQ_ERR_UNSUPPORTED;
+  if (c->q_bits == 8 && (!quant || (c->k_channel_factor && c->window > 0))) return KVQ_ERR_UNSUPPORTED;
   if (c->window < 0) return KVQ_ERR_INVALID_ARG;
   if (c->window > kMaxWindow || c->window % 16 != 0) return KVQ_ERR_UNSUPPORTED;
   if (c->window > 0) {
@@ -68,6 +70,7 @@ kvq::CacheView view(const kvq_cache_desc* c) {
   v.factor = c->k_channel_factor;
   v.window = c->window;
   v.window_batch = c->window_batch;
+  v.q_bits = c->q_bits == 8 ? 8 : 16;
   v.k_win = static_cast<uint8_t*>(c->k_window);
   v.v_win = static_cast<uint8_t*>(c->v_window);
   return v;

@@ -22,21 +22,6 @@ constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
-// Round-half-even of the exact quotient x / s (s > 0, finite).  The float32
-// quotient decides unless it landed exactly on a half-integer; then the sign of
-// the exact residual x - q*s (computed exactly in double: q*s has at most 48
-// significant bits) tells which side the true quotient lies on.
-__device__ __forceinline__ float round_quotient(float x, float s) {
-  const float q = __fdiv_rn(x, s);
-  const float fl = floorf(q);
-  if (q - fl == 0.5f) {
-    const double res = double(x) - double(q) * double(s);
-    if (res > 0.0) return fl + 1.0f;
-    if (res < 0.0) return fl;
-  }
-  return rintf(q);
-}
-
 // Warp-cooperative per-vector quantization.
 __device__ __forceinline__ void quantize_warp(const float (&x)[4], int bits, int (&code)[4], float& s) {
   float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));

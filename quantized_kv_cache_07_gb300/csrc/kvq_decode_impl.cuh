@@ -483,9 +483,22 @@ __device__ __forceinline__ void stage_query(const DecodeArgs& a, int b, int h, u
     }
     uint2 packed;
     if constexpr (kBf16Q) {
-      packed.x = pack_bf162(x[0], x[1]);
-      packed.y = pack_bf162(x[2], x[3]);
-      if (lane == 0) qs[q] = kLog2e * kInvSqrtD;
+      if (a.c.q_bits == 8) {
+        // quantized query against bf16 window keys: q_int (exact in bf16) and
+        // s_q in the score scale (no per-channel factor with a window here)
+        float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
+        float cq[4];
+        const float sq = quantize_int8_row(x, am, cq);
+        packed.x = pack_bf162(cq[0], cq[1]);
+        packed.y = pack_bf162(cq[2], cq[3]);
+        if (lane == 0) qs[q] = sq * (kLog2e * kInvSqrtD);
+      } else {
+        packed.x = pack_bf162(x[0], x[1]);
+        packed.y = pack_bf162(x[2], x[3]);
+        if (lane == 0) qs[q] = kLog2e * kInvSqrtD;
+      }
     } else {
       if (a.c.factor) {
         const float4 c = *reinterpret_cast<const float4*>(a.c.factor + h * kHeadDim + 4 * lane);
@@ -596,15 +609,25 @@ __device__ __forceinline__ bool convert_query(const DecodeArgs& a, int buf, cons
       float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
-      int e = 0;
-      if (am > 0.f) {
-        int ex;
-        frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
-        e = 15 - ex;      // am * 2^e in [2^14, 2^15)
+      if (a.c.q_bits == 8) {
+        // quantized query: int8 codes (exact in fp16) and s_q folded into the
+        // score scale; the MMA then forms the integer dot exactly
+        float cq[4];
+        const float sq = quantize_int8_row(x, am, cq);
+        packed.x = pack_half2(cq[0], cq[1]);
+        packed.y = pack_half2(cq[2], cq[3]);
+        if (lane == 0) qs[q] = sq * (kLog2e * kInvSqrtD);
+      } else {
+        int e = 0;
+        if (am > 0.f) {
+          int ex;
+          frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
+          e = 15 - ex;      // am * 2^e in [2^14, 2^15)
+        }
+        packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
+        packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+        if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
       }
-      packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
-      packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
-      if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
       if constexpr (ASYM) {
         // sum of the fp16 row exactly as the MMA sees it (zero-point term)
         const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));

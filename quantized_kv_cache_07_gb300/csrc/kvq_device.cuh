@@ -61,6 +61,34 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// Round-half-even of the exact quotient x / s (s > 0, finite).  The float32
+// quotient decides unless it landed exactly on a half-integer; then the sign of
+// the exact residual x - q*s (computed exactly in double: q*s has at most 48
+// significant bits) tells which side the true quotient lies on.
+__device__ __forceinline__ float round_quotient(float x, float s) {
+  const float q = __fdiv_rn(x, s);
+  const float fl = floorf(q);
+  if (q - fl == 0.5f) {
+    const double res = double(x) - double(q) * double(s);
+    if (res > 0.0) return fl + 1.0f;
+    if (res < 0.0) return fl;
+  }
+  return rintf(q);
+}
+
+// Symmetric int8 codes of four values of a warp-wide 128-vector whose max|x| is
+// amax: s = RN32(amax / 127) (1 for a zero vector), c = clamp(rint(x / s)).
+__device__ __forceinline__ float quantize_int8_row(const float (&x)[4], float amax, float (&c)[4]) {
+  if (amax == 0.f) {
+    c[0] = c[1] = c[2] = c[3] = 0.f;
+    return 1.f;
+  }
+  const float s = __fdiv_rn(amax, 127.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) c[j] = fminf(127.f, fmaxf(-127.f, round_quotient(x[j], s)));
+  return s;
+}
+
 // ------------------------------------------------------------------ conversions
 // Codes are stored offset-binary: an int8 code c is the byte c + 128, an int4
 // code c is the nibble c + 8.  Placing the biased value u in the mantissa of

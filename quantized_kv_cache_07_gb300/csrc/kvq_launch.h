@@ -20,6 +20,7 @@ struct CacheView {
   float* v_offsets;
   const float* factor;  // [H][128] or null
   int window, window_batch;
+  int q_bits;      // 8: int8-quantized query rows (integer dot), else the bf16 query
   uint8_t* k_win;  // bf16 ring: [window_batch][H][W/16] fragment-native bf16 blocks
   uint8_t* v_win;
 };

@@ -56,6 +56,7 @@ class Workload:
     outlier_channels: int = 0        # number of key channels scaled by outlier_mult
     outlier_mult: float = 10.0
     asym: bool = False               # asymmetric format: per-token scale and zero point
+    q_bits: int = 16                 # 8: int8-quantized query rows (integer dot)
     head_dim: int = HEAD_DIM
     block_size: int = BLOCK_SIZE
     seed: int = 0

@@ -47,7 +47,10 @@ def oracle_decode(inp, units=None):
             if units is not None and (b, h) not in units:
                 continue
             k_hat, v_hat = O.reconstruct_sequence(st, h)
-            res[(b, h)] = O.attention(q[h * G:(h + 1) * G], k_hat, v_hat)
+            qh = q[h * G:(h + 1) * G]
+            if w.q_bits == 8:
+                qh = O.effective_query(qh, None if st["c"] is None else st["c"][h])
+            res[(b, h)] = O.attention(qh, k_hat, v_hat)
     return res
 
 

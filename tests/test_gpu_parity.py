@@ -43,6 +43,14 @@ SMALL = {
     "asym_k8v4_paged_append": small_workload("asym_k8v4_paged_append", batch=4, q_heads=4, kv_heads=4, k_bits=8,
                                              v_bits=4, len_range=(1, 250), paged=True, append_one=True,
                                              asym=True),
+    # quantized query (int8 query rows, integer dot product)
+    "qint8_int8_g4": small_workload("qint8_int8_g4", q_bits=8, outlier_channels=4),
+    "qint8_int4_factor_g8": small_workload("qint8_int4_factor_g8", batch=4, q_heads=16, kv_heads=2, k_bits=4,
+                                           v_bits=4, channel_factor=True, q_bits=8),
+    "qint8_k4v8_window32_t3": small_workload("qint8_k4v8_window32_t3", batch=3, q_heads=16, kv_heads=2, k_bits=4,
+                                             v_bits=8, len_range=(1, 500), window=32, k_dist="t3", q_bits=8),
+    "qint8_asym_k8v4_g1": small_workload("qint8_asym_k8v4_g1", batch=3, q_heads=4, kv_heads=4, k_bits=8, v_bits=4,
+                                         len_range=(1, 300), asym=True, q_bits=8),
 }
 
 
@@ -178,7 +186,8 @@ def test_decode_matches_oracle(runs, name, out_fp32):
     assert run.err_bits() == 0
 
 
-@pytest.mark.parametrize("name", ["int8_g4", "k4v8_g8_t3", "window32_int8", "bf16", "asym_k4v8_window32_t3"])
+@pytest.mark.parametrize("name", ["int8_g4", "k4v8_g8_t3", "window32_int8", "bf16", "asym_k4v8_window32_t3",
+                                  "qint8_k4v8_window32_t3"])
 def test_decode_split_count_does_not_change_result(runs, name):
     """Any split of the token range gives the same attention up to the rounding
     of the fp16 value weights p*s_v, which are rounded relative to the running
@@ -319,6 +328,9 @@ FULL["asym_gqa_int8_window128_b8_t4096"] = WORKLOADS["gqa_int8_window128_b8_t409
     name="asym_gqa_int8_window128_b8_t4096", asym=True)
 FULL["asym_long_k4v8_b4_t131072"] = WORKLOADS["long_k4v8_b4_t131072"].with_(name="asym_long_k4v8_b4_t131072",
                                                                           asym=True)
+# the quantized-query mode on the int4 / per-channel factor shape
+FULL["qint8_int4_factor_b32_len1k_8k"] = WORKLOADS["int4_factor_b32_len1k_8k"].with_(
+    name="qint8_int4_factor_b32_len1k_8k", q_bits=8)
 
 
 @pytest.mark.parametrize("name", list(FULL))
