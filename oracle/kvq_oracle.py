@@ -37,6 +37,13 @@ Readings taken where the pages leave a step open:
     with qmaxu = 2^bits - 1, u = clamp(rint((x - m) / s), 0, qmaxu) with the
     difference and the quotient evaluated in float64, x_hat = u * s + m; a
     constant vector stores s = 1, u = 0 and m = its value.
+  * per-channel key scales only ([P3] "The axis choice is a kernel decision":
+    schemes with per-channel key scales move them onto the query; read here as
+    the variant where the keys carry no per-token scale at all): code_j =
+    clamp(rint(k_j / c_j)) with c_j the caller's per-channel scale (the clamp
+    binds for values outside the calibrated range), k_hat_j = c_j * code_j; the
+    decode multiplies the query by c once.  The default per-channel factor
+    reading divides by c and then quantizes per token (quantize_keys).
   * quantized query ([P3] "Precision floors and mixed cache formats": an 8-bit
     query meets the integer key codes, the dot product accumulates in integers
     and is converted to floating point before the exponential): the query row,
@@ -151,6 +158,15 @@ def quantize_keys(k: np.ndarray, bits: int, c: np.ndarray | None = None):
     return quantize(x, bits)
 
 
+def quantize_keys_per_channel(k: np.ndarray, bits: int, c: np.ndarray) -> np.ndarray:
+    """Key codes under per-channel scales only: clamp(rint(k / c)) with the
+    float64 quotient of float32 operands (equal to rounding the exact quotient,
+    as in quantize); int16 [..., D]."""
+    lo, hi = CLAMP[bits]
+    x = np.asarray(k, np.float64) / np.asarray(c, np.float64)
+    return np.clip(np.rint(x), lo, hi).astype(np.int16)
+
+
 def reconstruct_keys(codes, scale, c=None) -> np.ndarray:
     """k_hat = c * (q * s); without a factor, k_hat = q * s."""
     kh = dequantize(codes, scale)
@@ -216,17 +232,23 @@ def window_split(length: int, window: int) -> int:
     return max(length - window, 0)
 
 
-def quantize_sequence(k, v, k_bits: int, v_bits: int, window: int = 0, c=None, asym: bool = False):
+def quantize_sequence(k, v, k_bits: int, v_bits: int, window: int = 0, c=None, asym: bool = False,
+                      k_per_channel: bool = False):
     """Store one sequence: k, v float64 [L, H, D] (exact bf16 values).
 
     Returns a dict with the quantized prefix (codes/scales for K and V) and the
     bf16 window values (float64).  16-bit formats store the values unchanged.
+    k_per_channel: keys carry the per-channel scales c only (no per-token scale).
     """
     L = k.shape[0]
     Lq = window_split(L, window)
-    st = {"Lq": Lq, "k_bits": k_bits, "v_bits": v_bits, "c": c, "asym": asym}
+    st = {"Lq": Lq, "k_bits": k_bits, "v_bits": v_bits, "c": c, "asym": asym, "k_per_channel": k_per_channel}
+    if k_per_channel and (c is None or asym or k_bits == 16):
+        raise ValueError("per-channel-only key scales need c, symmetric codes and 8- or 4-bit keys")
     if k_bits == 16:
         st["k_plain"] = k[:Lq]
+    elif k_per_channel:
+        st["k_codes"] = quantize_keys_per_channel(k[:Lq], k_bits, c)
     elif asym:
         kx = k[:Lq] if c is None else divide_by_channel_factor(k[:Lq], c)
         st["k_codes"], st["k_scale"], st["k_offset"] = quantize_asym(kx, k_bits)
@@ -248,6 +270,8 @@ def reconstruct_sequence(st, head: int):
     c = st["c"]
     if st["k_bits"] == 16:
         kq = st["k_plain"][:, head]
+    elif st.get("k_per_channel"):
+        kq = np.asarray(st["k_codes"][:, head], np.float64) * np.asarray(c[head], np.float64)
     elif st.get("asym"):
         kq = dequantize_asym(st["k_codes"][:, head], st["k_scale"][:, head], st["k_offset"][:, head])
         kq = kq if c is None else kq * np.asarray(c[head], np.float64)
@@ -301,11 +325,11 @@ def metadata_fraction(head_dim: int, bits: int, metadata_bytes: int) -> float:
 
 
 def cache_bytes_per_token_head(head_dim: int, k_bits: int, v_bits: int, scale_bytes: int = 4,
-                               asym: bool = False) -> int:
+                               asym: bool = False, k_per_channel: bool = False) -> int:
     """Bytes read per cached token per KV head: codes plus one scale (and, for
     the asymmetric format, one offset) for each of K and V (no metadata for a
-    16-bit cache)."""
+    16-bit cache, none for keys under per-channel scales only)."""
     meta = scale_bytes * (2 if asym else 1)
-    kb = head_dim * k_bits // 8 + (0 if k_bits == 16 else meta)
+    kb = head_dim * k_bits // 8 + (0 if (k_bits == 16 or k_per_channel) else meta)
     vb = head_dim * v_bits // 8 + (0 if v_bits == 16 else meta)
     return kb + vb

@@ -589,3 +589,54 @@ def test_decode_sequence_quantized_query_mode_uses_each_heads_factor():
         np.testing.assert_allclose(lse[h * G:(h + 1) * G], ref_l, rtol=0, atol=1e-15)
     o16, _ = O.decode_sequence(qb, st, H)
     assert not np.array_equal(o, o16)                                    # the mode changes the numerics
+
+
+# ---------------------------------------------------------------- per-channel key scales only
+def exact_quantize_per_channel(ks, cs, bits):
+    lo, hi = {8: (-127, 127), 4: (-8, 7)}[bits]
+    return [min(hi, max(lo, rne_int(Fraction(float(k)) / Fraction(float(c))))) for k, c in zip(ks, cs)]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_per_channel_key_codes_match_exact_rationals(bits):
+    for trial in range(60):
+        k = bf16_vec(128, dist="t3" if trial % 2 else "normal")
+        c = (np.abs(bf16_vec(128)) * (0.02 if bits == 8 else 0.3) + 1e-3).astype(np.float32).astype(np.float64)
+        codes = O.quantize_keys_per_channel(k, bits, c)
+        assert list(map(int, codes)) == exact_quantize_per_channel(k, c, bits)
+
+
+def test_per_channel_key_ties_and_clamp():
+    c = np.array([0.25, 0.25, 0.5, 0.5, 0.125, 1.0, 1.0, 1.0])
+    k = np.array([0.125, 0.375, 0.25, 0.75, -0.0625, 200.0, -200.0, -7.75])   # quotients .5 1.5 .5 1.5 -.5 200 -200 -7.75
+    assert list(map(int, O.quantize_keys_per_channel(k, 8, c))) == [0, 2, 0, 2, 0, 127, -127, -8]
+    assert list(map(int, O.quantize_keys_per_channel(k, 4, c))) == [0, 2, 0, 2, 0, 7, -8, -8]   # -8 reachable here
+
+
+def test_per_channel_keys_round_trip_and_query_fold():
+    """|k - code * c| <= c / 2 inside the calibrated range, and the fold onto the
+    query is exact: (q * c) . code == q . (c * code) in rationals."""
+    k = bf16_vec(128)
+    c = (np.abs(k) / 127 * 1.5 + 1e-4).astype(np.float32).astype(np.float64)   # |k / c| < 127
+    codes = O.quantize_keys_per_channel(k, 8, c)
+    assert np.all(np.abs(k - codes * c) <= c / 2 * (1 + 1e-12))
+    q = bf16_vec(128)
+    lhs = sum((Fraction(float(a)) * Fraction(float(cc))) * int(b) for a, cc, b in zip(q, c, codes))
+    rhs = sum(Fraction(float(a)) * (Fraction(float(cc)) * int(b)) for a, cc, b in zip(q, c, codes))
+    assert lhs == rhs
+
+
+def test_per_channel_sequence_reconstruction_and_bytes():
+    rng = np.random.default_rng(9)
+    L, H, D = 20, 2, 128
+    k = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    v = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    c = (np.abs(k).max(axis=0) / 7).astype(np.float32).astype(np.float64)     # per-channel absmax / qmax
+    st = O.quantize_sequence(k, v, 4, 8, window=4, c=c, k_per_channel=True)
+    assert "k_scale" not in st
+    k_hat, _ = O.reconstruct_sequence(st, 1)
+    assert np.array_equal(k_hat[:16], st["k_codes"][:, 1].astype(np.float64) * c[1])
+    assert np.array_equal(k_hat[16:], k[16:, 1])
+    assert O.cache_bytes_per_token_head(128, 8, 8, k_per_channel=True) == 128 + 128 + 4
+    with pytest.raises(ValueError):
+        O.quantize_sequence(k, v, 8, 8, c=None, k_per_channel=True)
