@@ -46,7 +46,7 @@ def measured_peaks():
 
 def decode_kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("kvq_decode_impl.cuh", "kvq_decode.cu", "kvq_device.cuh"):
+    for f in ("kvq_decode_impl.cuh", "kvq_decode.cu", "kvq_device.cuh"):  # the default-path kernels
         h.update(open(os.path.join(ROOT, "quantized_kv_cache_07_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 
@@ -126,7 +126,8 @@ def cache_bytes_per_step(inp) -> int:
     w = inp.workload
     L = inp.decode_lengths.astype(int)
     D = w.head_dim
-    per_q = D * w.k_bits // 8 + D * w.v_bits // 8 + (0 if w.k_bits == 16 else (16 if w.asym else 8))
+    per_q = (D * w.k_bits // 8 + D * w.v_bits // 8
+             + (0 if w.k_bits == 16 else (16 if w.asym else 8)) - (4 if w.k_per_channel else 0))
     if w.window:
         lq = [max(int(l) - w.window, 0) for l in L]
         lw = [int(l) - x for l, x in zip(L, lq)]
@@ -152,7 +153,8 @@ G = w.group
 budget = {budget}
 rng = np.random.default_rng(5)
 units = [(int(b), int(h)) for b in rng.permutation(w.batch) for h in range(w.kv_heads)]
-per_tok = 128 * w.k_bits // 8 + 128 * w.v_bits // 8 + (0 if w.k_bits == 16 else (16 if w.asym else 8))
+per_tok = (128 * w.k_bits // 8 + 128 * w.v_bits // 8 + (0 if w.k_bits == 16 else (16 if w.asym else 8))
+           - (4 if w.k_per_channel else 0))
 tot_t, tot_b, n, i = 0.0, 0, 0, 0
 while tot_t < budget or n == 0:
     b, h = units[i % len(units)]; i += 1
@@ -162,7 +164,8 @@ while tot_t < budget or n == 0:
         k = np.concatenate([k, O.bf16_to_f64(inp.k_new[b:b+1, h:h+1])])
         v = np.concatenate([v, O.bf16_to_f64(inp.v_new[b:b+1, h:h+1])])
     c = None if inp.channel_factor is None else inp.channel_factor[h:h+1].astype(np.float64)
-    st = O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c, asym=w.asym)   # untimed
+    st = O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c, asym=w.asym,
+                             k_per_channel=w.k_per_channel)   # untimed
     t1 = time.perf_counter()
     kh, vh = O.reconstruct_sequence(st, 0)
     qv = O.bf16_to_f64(inp.q[b, h*G:(h+1)*G])
@@ -215,8 +218,8 @@ def main():
                     help="skip the same-shape run in the asymmetric (scale + zero point) format")
     ap.add_argument("--asym", action="store_true",
                     help="time the workload in the asymmetric (scale + zero point) format")
-    ap.add_argument("--q-bits", type=int, default=16, choices=[8, 16],
-                    help="8: decode with int8-quantized query rows (integer dot product)")
+    ap.add_argument("--q-bits", type=int, default=16, choices=[8, 16, 32],
+                    help="query format: 8 int8 rows (integer dot), 16 fp16 (default), 32 fp16 hi + lo")
     ap.add_argument("--no-qint8", action="store_true",
                     help="skip the same-shape run with int8-quantized query rows")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
@@ -255,8 +258,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.asym:
         w = w.with_(asym=True)
-    if args.q_bits == 8:
-        w = w.with_(q_bits=8)
+    if args.q_bits != 16:
+        w = w.with_(q_bits=args.q_bits)
     inp = make_inputs(w)
     dev = torch.device("cuda", local)
     props = torch.cuda.get_device_properties(dev)
@@ -463,7 +466,7 @@ def main():
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits,
                    "window": w.window, "paged": w.paged, "append_one": w.append_one,
                    "format": "asymmetric (scale + zero point)" if w.asym else "symmetric (scale)",
-                   "query": "int8 rows, integer dot" if w.q_bits == 8 else "bf16",
+                   "query": {8: "int8 rows, integer dot", 16: "fp16", 32: "fp16 hi + lo"}[w.q_bits],
                    "cache_bytes_per_step": bytes_step, "allocated_cache_bytes": res["alloc"],
                    "l2": f"steps rotate over {res['replicas']} cache replicas "
                          f"({res['replicas'] * bytes_step / 2**20:.0f} MiB >= 4x L2 or cache > L2)",

@@ -126,7 +126,11 @@ typedef struct {
   /* Query format of kvq_decode against this cache ([P3] "Precision floors and
    * mixed cache formats": an 8-bit query meets the integer key codes, the dot
    * product accumulates in integers and is converted to float before the
-   * exponential).  0 or 16: the bf16 query (default).  8: each query row, after
+   * exponential).  0 or 16: the bf16 query, carried into the code contraction
+   * as fp16 scaled by a power of two (11 significant bits; default).  32: the
+   * same fp16 value plus an fp16 low part (about 22 significant bits, one more
+   * MMA per k-slice: 2-13 % more time), for scores large enough that 11 bits
+   * of query cost more than the output tolerance.  8: each query row, after
    * the per-channel key factor is multiplied onto it in float32, is quantized
    * per row with the symmetric int8 rule of kvq_append (s_q = RN32(max|x| /
    * 127), q_int = clamp(round_half_even(x / s_q))) and the score is
@@ -134,6 +138,14 @@ typedef struct {
    * keys see q_int * s_q.  Needs 8- or 4-bit blocks; not combined with both a
    * per-channel key factor and a window (KVQ_ERR_UNSUPPORTED). */
   int32_t q_bits;
+  /* Per-channel key scales only ([P3] "The axis choice is a kernel decision":
+   * per-channel key scales are moved onto the query).  0: the per-channel key
+   * factor (if any) divides the keys before the per-token quantizer.  1: the
+   * keys carry no per-token scale: code_j = clamp(round_half_even(k_j / c_j))
+   * with c = k_channel_factor as the per-channel scale (required; the clamp
+   * binds for values beyond qmax * c_j), k_hat_j = c_j * code_j; k_scales is
+   * not read or written and may be NULL.  Symmetric 8- or 4-bit keys only. */
+  int32_t k_per_channel;
 } kvq_cache_desc;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -265,7 +277,8 @@ kvq_status kvq_decode_static_scratch(const kvq_cache_desc* cache, const void* q,
  * kvq_dequant -- read the block store back: x_hat = RN32(code * s)
  * ([P2] "Quantization needs a scale convention"), without the per-channel key
  * factor; in the asymmetric format x_hat = RN32(u * s + m) (one fused
- * multiply-add).  For a bf16 cache the stored values are widened.  For tests.
+ * multiply-add); keys under per-channel scales only give RN32(code * c_j).
+ * For a bf16 cache the stored values are widened.  For tests.
  *   slots : device int32 [n], physical slot = physical_block * 16 + token
  *   k_out, v_out : device float [n][num_kv_heads][128]
  */

@@ -48,7 +48,7 @@ class CacheDesc(ctypes.Structure):
         ("window", c_int32), ("window_batch", c_int32),
         ("k_window", c_void_p), ("v_window", c_void_p),
         ("k_offsets", c_void_p), ("v_offsets", c_void_p),
-        ("q_bits", c_int32),
+        ("q_bits", c_int32), ("k_per_channel", c_int32),
     ]
 
 

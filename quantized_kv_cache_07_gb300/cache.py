@@ -30,7 +30,7 @@ class KVCache:
 
     def __init__(self, num_blocks: int, kv_heads: int, k_bits: int, v_bits: int, window: int = 0,
                  window_batch: int = 0, channel_factor=None, asym: bool = False, q_bits: int = 16,
-                 device="cuda"):
+                 k_per_channel: bool = False, device="cuda"):
         _require_cuda()
         self.num_blocks, self.kv_heads = int(num_blocks), int(kv_heads)
         self.k_bits, self.v_bits = int(k_bits), int(v_bits)
@@ -40,8 +40,10 @@ class KVCache:
         self.k_codes = torch.zeros(self.num_blocks * kv_heads * kbb, dtype=torch.uint8, device=device)
         self.v_codes = torch.zeros(self.num_blocks * kv_heads * vbb, dtype=torch.uint8, device=device)
         quant = k_bits != 16
+        self.k_per_channel = bool(k_per_channel)
         n_sc = self.num_blocks * kv_heads * BLOCK_SIZE
-        self.k_scales = torch.zeros(n_sc, dtype=torch.float32, device=device) if quant else None
+        self.k_scales = (torch.zeros(n_sc, dtype=torch.float32, device=device)
+                         if quant and not self.k_per_channel else None)
         self.v_scales = torch.zeros(n_sc, dtype=torch.float32, device=device) if quant else None
         self.asym = bool(asym)
         if self.asym and not quant:
@@ -61,7 +63,7 @@ class KVCache:
             num_kv_heads=kv_heads, head_dim=HEAD_DIM, block_size=BLOCK_SIZE, num_blocks=self.num_blocks,
             k_bits=k_bits, v_bits=v_bits,
             k_codes=self.k_codes.data_ptr(), v_codes=self.v_codes.data_ptr(),
-            k_scales=self.k_scales.data_ptr() if quant else None,
+            k_scales=self.k_scales.data_ptr() if self.k_scales is not None else None,
             v_scales=self.v_scales.data_ptr() if quant else None,
             k_channel_factor=self.channel_factor.data_ptr() if self.channel_factor is not None else None,
             window=self.window, window_batch=max(window_batch, 1) if window > 0 else 0,
@@ -69,12 +71,12 @@ class KVCache:
             v_window=self.v_window.data_ptr() if self.v_window is not None else None,
             k_offsets=self.k_offsets.data_ptr() if self.asym else None,
             v_offsets=self.v_offsets.data_ptr() if self.asym else None,
-            q_bits=int(q_bits))
+            q_bits=int(q_bits), k_per_channel=int(self.k_per_channel))
 
     # bytes the decode reads per cached token per KV head (codes + scales + zero points)
     def bytes_per_token_head(self) -> int:
         meta = 8 if self.asym else 4
-        kb = HEAD_DIM * self.k_bits // 8 + (0 if self.k_bits == 16 else meta)
+        kb = HEAD_DIM * self.k_bits // 8 + (0 if self.k_bits == 16 or self.k_per_channel else meta)
         vb = HEAD_DIM * self.v_bits // 8 + (0 if self.v_bits == 16 else meta)
         return kb + vb
 
@@ -141,4 +143,5 @@ def cache_for_inputs(inp, device="cuda") -> KVCache:
     w = inp.workload
     return KVCache(inp.num_blocks, w.kv_heads, w.k_bits, w.v_bits, window=w.window,
                    window_batch=w.batch if w.window else 0, channel_factor=inp.channel_factor,
-                   asym=getattr(w, "asym", False), q_bits=getattr(w, "q_bits", 16), device=device)
+                   asym=getattr(w, "asym", False), q_bits=getattr(w, "q_bits", 16),
+                   k_per_channel=getattr(w, "k_per_channel", False), device=device)

@@ -30,9 +30,12 @@ kvq_status check_cache(const kvq_cache_desc* c) {
   if (!c->k_codes || !c->v_codes) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(c->k_codes) || !aligned16(c->v_codes)) return KVQ_ERR_ALIGNMENT;
   const bool quant = c->k_bits != 16;
+  if (c->k_per_channel != 0 && c->k_per_channel != 1) return KVQ_ERR_INVALID_ARG;
+  if (c->k_per_channel && (!quant || c->k_offsets || c->v_offsets)) return KVQ_ERR_UNSUPPORTED;
+  if (c->k_per_channel && !c->k_channel_factor) return KVQ_ERR_INVALID_ARG;
   if (quant) {
-    if (!c->k_scales || !c->v_scales) return KVQ_ERR_INVALID_ARG;
-    if (!aligned16(c->k_scales) || !aligned16(c->v_scales)) return KVQ_ERR_ALIGNMENT;
+    if ((!c->k_scales && !c->k_per_channel) || !c->v_scales) return KVQ_ERR_INVALID_ARG;
+    if ((c->k_scales && !aligned16(c->k_scales)) || !aligned16(c->v_scales)) return KVQ_ERR_ALIGNMENT;
   }
   // zero points: both tensors or neither, and only on quantized blocks
   if ((c->k_offsets != nullptr) != (c->v_offsets != nullptr)) return KVQ_ERR_INVALID_ARG;
@@ -44,7 +47,7 @@ kvq_status check_cache(const kvq_cache_desc* c) {
     if (!quant) return KVQ_ERR_UNSUPPORTED;
     if (!aligned16(c->k_channel_factor)) return KVQ_ERR_ALIGNMENT;
   }
-  if (c->q_bits != 0 && c->q_bits != 16 && c->q_bits != 8) return KVQ_ERR_UNSUPPORTED;
+  if (c->q_bits != 0 && c->q_bits != 16 && c->q_bits != 8 && c->q_bits != 32) return KVQ_ERR_UNSUPPORTED;
   if (c->q_bits == 8 && (!quant || (c->k_channel_factor && c->window > 0))) return KVQ_ERR_UNSUPPORTED;
   if (c->window < 0) return KVQ_ERR_INVALID_ARG;
   if (c->window > kMaxWindow || c->window % 16 != 0) return KVQ_ERR_UNSUPPORTED;
@@ -70,7 +73,8 @@ kvq::CacheView view(const kvq_cache_desc* c) {
   v.factor = c->k_channel_factor;
   v.window = c->window;
   v.window_batch = c->window_batch;
-  v.q_bits = c->q_bits == 8 ? 8 : 16;
+  v.q_bits = c->q_bits == 0 ? 16 : c->q_bits;
+  v.k_chan = c->k_per_channel;
   v.k_win = static_cast<uint8_t*>(c->k_window);
   v.v_win = static_cast<uint8_t*>(c->v_window);
   return v;
@@ -95,7 +99,7 @@ int auto_stream_ctas(const kvq_cache_desc* c, int batch) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, c->k_offsets != nullptr, batch);
+  const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, c->k_offsets != nullptr, c->q_bits, batch);
   return stream_ctas_for(sms * per, c->window > 0 ? batch * c->num_kv_heads : 0, batch * c->num_kv_heads);
 }
 

@@ -140,6 +140,18 @@ __device__ void write_block_store(const AppendArgs& a, bool is_key, int b, int p
     return;
   }
   float x[4];
+  if (is_key && c.k_chan) {
+    // per-channel scales only: code = clamp(rint(k / c)) of the exact quotient, no per-token scale
+    const int lo = bits == 8 ? -127 : -8, hi = bits == 8 ? 127 : 7, bias = bits == 8 ? 128 : 8;
+    int code[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float q = round_quotient(bf16_bits_to_f32(xb[j]), c.factor[h * kHeadDim + 4 * lane + j]);
+      code[j] = int(fminf(float(hi), fmaxf(float(lo), q))) + bias;
+    }
+    store_codes(is_key, bits, blk, tok, code, lane);
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     x[j] = bf16_bits_to_f32(xb[j]);
@@ -238,7 +250,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
   const uint8_t* blk = (is_key ? a.c.k_codes : a.c.v_codes) + (size_t(h) * a.c.num_blocks + phys) * block_bytes(bits);
   float s = 1.0f, m = 0.0f;
   const bool asym = a.c.k_offsets != nullptr;
-  if (bits != 16) {
+  const bool chan = is_key && a.c.k_chan;  // per-channel key scale c_j instead of a per-token one
+  if (bits != 16 && !chan) {
     const size_t e = (size_t(h) * a.c.num_blocks + phys) * kBlock + tok;
     s = (is_key ? a.c.k_scales : a.c.v_scales)[e];
     if (asym) m = (is_key ? a.c.k_offsets : a.c.v_offsets)[e];
@@ -253,7 +266,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
       v = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(blk + L.byte));
     } else {
       const int raw = bits == 8 ? int(blk[L.byte]) : int((blk[L.byte] >> L.shift) & 0xF);
-      v = asym ? __fmaf_rn(float(raw), s, m) : __fmul_rn(float(raw - bias), s);
+      const float sd = chan ? a.c.factor[h * kHeadDim + d] : s;
+      v = asym ? __fmaf_rn(float(raw), s, m) : __fmul_rn(float(raw - bias), sd);
     }
     out[j] = v;
   }

@@ -97,6 +97,7 @@ struct SmemMap {
   int merge_o;   // float [4 warps][4 q][128] (combine, four queries per pass)
   int merge_ml;  // float m[4][8], l[4][8]
   int qh;        // 16-bit [8][128]: B-operand rows of the current query group
+  int qlo;       // fp16 [32 lanes x 16] low parts of the query fragments, in fragment order
   int qs;        // float [8] score scales, then float [8] sums of the fp16 query rows
   int qraw;      // bf16 [2][8][128]: prefetched raw query rows (double buffer)
   int fraw;      // float [2][128]: prefetched per-channel key factor row
@@ -109,12 +110,13 @@ struct SmemMap {
   int total;
 };
 
-__host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, int B) {
+__host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, int B, bool loq) {
   SmemMap m;
   int o = stage_bytes_total;
   m.merge_o = o;  o += kConsumerWarps * 4 * kHeadDim * 4;
   m.merge_ml = o; o += 2 * kConsumerWarps * kMaxGroup * 4;
   m.qh = o;       o += kMaxGroup * kHeadDim * 2;
+  m.qlo = o;      o += loq ? kMaxGroup * kHeadDim * 2 : 0;  // two-part query only
   m.qs = o;       o += kMaxGroup * 4 + 32;
   m.qraw = o;     o += 2 * kMaxGroup * kHeadDim * 2;
   m.fraw = o;     o += 2 * kHeadDim * 4;
@@ -129,9 +131,14 @@ __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, i
 }
 
 // ------------------------------------------------------------------ score / value contractions
-template <int KB>
-__device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&qf)[16], float (&acc)[4],
-                                            int lane) {
+// S^T of one 16-token block.  For code blocks the query is the fp16 pair
+// hi + lo (hi in registers, lo fragments from shared memory in the same order,
+// qlo = this lane's first uint4, null when lo is zero): every k-slice runs one
+// MMA with hi and one with lo into the same fp32 accumulator, so the score
+// carries about 22 significant bits of the query instead of 11.
+template <int KB, bool LOQ>
+__device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&qf)[16], const uint4* qlo,
+                                            float (&acc)[4], int lane) {
   // two accumulators halve the dependent MMA chain; summed at the end
   float acc2[4] = {0.f, 0.f, 0.f, 0.f};
   const uint4* p = reinterpret_cast<const uint4*>(kb) + lane;
@@ -140,12 +147,19 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
     const uint32_t g0[8] = {r0a.x, r0a.y, r0a.z, r0a.w, r0b.x, r0b.y, r0b.z, r0b.w};
     const uint32_t g8[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      s8x4_to_f16(g0[kk], a0, a2);
-      s8x4_to_f16(g8[kk], a1, a3);
-      if (kk & 1) mma_f16(acc2, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
-      else mma_f16(acc, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+    for (int i = 0; i < 4; ++i) {
+      uint4 lo = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (LOQ) lo = qlo[i * 32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kk = 2 * i + h;
+        uint32_t a0, a1, a2, a3;
+        s8x4_to_f16(g0[kk], a0, a2);
+        s8x4_to_f16(g8[kk], a1, a3);
+        float (&ac)[4] = h ? acc2 : acc;
+        mma_f16(ac, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
+        if constexpr (LOQ) mma_f16(ac, a0, a1, a2, a3, h ? lo.z : lo.x, h ? lo.w : lo.y);
+      }
     }
   } else if constexpr (KB == 4) {
     const uint4 r0 = p[0], r1 = p[32];
@@ -158,6 +172,11 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
       s4x8_to_f16(g8[wi], y0, y1, y2, y3);
       mma_f16(acc, x0, y0, x1, y1, qf[4 * wi], qf[4 * wi + 1]);
       mma_f16(acc2, x2, y2, x3, y3, qf[4 * wi + 2], qf[4 * wi + 3]);
+      if constexpr (LOQ) {
+        const uint4 lo = qlo[wi * 32];
+        mma_f16(acc, x0, y0, x1, y1, lo.x, lo.y);
+        mma_f16(acc2, x2, y2, x3, y3, lo.z, lo.w);
+      }
     }
   } else {
     uint4 c[8];
@@ -329,13 +348,13 @@ struct WarpState {
 //
 // Asymmetric blocks (ASYM) add the key zero-point term m'_k * sum(q) to each
 // score and accumulate the value zero-point term p * m'_v per query.
-template <int KB, int VB, int NB, bool ASYM>
+template <int KB, int VB, int NB, bool ASYM, bool LOQ>
 __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], const uint8_t* const (&vb)[NB],
                                                const float* const (&ks)[NB], const float* const (&vs)[NB],
                                                const float* const (&ko)[NB], const float* const (&vo)[NB],
-                                               const int (&valid)[NB], const uint32_t (&qf)[16], float qs0,
-                                               float qs1, float qz0, float qz1, WarpState& st, int lane,
-                                               uint32_t* err) {
+                                               const int (&valid)[NB], const uint32_t (&qf)[16],
+                                               const uint4* qlo, float qs0, float qs1, float qz0, float qz1,
+                                               WarpState& st, int lane, uint32_t* err) {
   constexpr bool kBf16 = (KB == 16);
   // offset-binary centre of the code conversion: c' = u - kKC
   constexpr float kKC = (KB == 8) ? 128.f : 8.f, kVC = (VB == 8) ? 128.f : 8.f;
@@ -346,11 +365,11 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
 #pragma unroll
   for (int j = 0; j < NB; ++j) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    score_block<KB>(kb[j], qf, acc, lane);
+    score_block<KB, LOQ>(kb[j], qf, qlo, acc, lane);
     float sk0 = 1.f, sk1 = 1.f;
     sv[j][0] = sv[j][1] = 1.f;
     if constexpr (!kBf16) {
-      sk0 = ks[j][g];
+      sk0 = ks[j][g];  // per-channel key scales only: the ring holds 1.0 here (never copied over)
       sk1 = ks[j][g + 8];
       sv[j][0] = vs[j][g];
       sv[j][1] = vs[j][g + 8];
@@ -573,16 +592,14 @@ struct Scratch {
   uint64_t* cbar;
 };
 
-// Once the copies of prefetch buffer `buf` have landed (every consumer thread
-// has waited on its cp.async groups), turn the raw rows into B-operand rows:
-// fp16 scaled by an exact power of two with the per-channel key factor
-// applied, or the raw bf16 values for bf16 blocks; then load the fragments.
+// The query rows of prefetch buffer `buf` as B-operand rows in shared memory
+// (fp16 scaled by a power of two, int8 codes, or raw bf16; plus the low parts
+// of the two-part query and the row sums of the asymmetric format).  Out of
+// line: it runs once per unit and keeps its rarely used branches out of the
+// consumers' block loop.
 template <bool kBf16Q, bool ASYM>
-__device__ __forceinline__ bool convert_query(const DecodeArgs& a, int buf, const uint16_t* qraw, const float* fraw,
-                                              uint16_t* qh, float* qs, const Scratch& sc, uint32_t& cphase, int warp,
-                                              int lane, uint32_t (&qf)[16], float& qs0, float& qs1, float& qz0,
-                                              float& qz1) {
-  if (!consumer_sync(sc.cbar, cphase)) return false;  // the factor row was copied by warp 0
+__device__ __noinline__ void write_query_rows(const DecodeArgs& a, int buf, const uint16_t* qraw, const float* fraw,
+                                              uint16_t* qh, uint32_t* qlo, float* qs, int warp, int lane) {
   const uint16_t* raw = qraw + buf * kMaxGroup * kHeadDim;
   for (int q = warp; q < kMaxGroup; q += kConsumerWarps) {
     float x[4] = {0.f, 0.f, 0.f, 0.f};
@@ -624,15 +641,35 @@ __device__ __forceinline__ bool convert_query(const DecodeArgs& a, int buf, cons
           frexpf(am, &ex);  // am = f * 2^ex, f in [0.5, 1)
           e = 15 - ex;      // am * 2^e in [2^14, 2^15)
         }
-        packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
-        packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+        const float y0 = ldexpf(x[0], e), y1 = ldexpf(x[1], e), y2 = ldexpf(x[2], e), y3 = ldexpf(x[3], e);
+        packed.x = pack_half2(y0, y1);
+        packed.y = pack_half2(y2, y3);
         if (lane == 0) qs[q] = ldexpf(kLog2e * kInvSqrtD, -e);
+        if (a.c.q_bits == 32) {
+          // two-part query: low parts y - hi (exact in fp32), stored in fragment
+          // order: lane 4q + t holds dims 32t + 8i + 2k, +1 of row q in uint32
+          // (i * 32 + lane) * 4 + k
+          const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));
+          const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&packed.y));
+          uint2 lo;
+          lo.x = pack_half2(y0 - h0.x, y1 - h0.y);
+          lo.y = pack_half2(y2 - h1.x, y3 - h1.y);
+          const int ft = lane >> 3, fi = (lane & 7) >> 1, fk = 2 * (lane & 1);
+          *reinterpret_cast<uint2*>(qlo + (fi * 32 + 4 * q + ft) * 4 + fk) = lo;
+        }
       }
       if constexpr (ASYM) {
         // sum of the fp16 row exactly as the MMA sees it (zero-point term)
         const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));
         const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&packed.y));
         float z = (f0.x + f0.y) + (f1.x + f1.y);
+        if (a.c.q_bits == 32) {  // plus the low parts
+          const uint2 lw = *reinterpret_cast<const uint2*>(
+              qlo + (((lane & 7) >> 1) * 32 + 4 * q + (lane >> 3)) * 4 + 2 * (lane & 1));
+          const float2 l0 = __half22float2(*reinterpret_cast<const __half2*>(&lw.x));
+          const float2 l1 = __half22float2(*reinterpret_cast<const __half2*>(&lw.y));
+          z += (l0.x + l0.y) + (l1.x + l1.y);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
         if (lane == 0) qs[kMaxGroup + q] = z;
@@ -640,6 +677,18 @@ __device__ __forceinline__ bool convert_query(const DecodeArgs& a, int buf, cons
     }
     *reinterpret_cast<uint2*>(qh + q * kHeadDim + 4 * lane) = packed;
   }
+}
+
+// Once the copies of prefetch buffer `buf` have landed (every consumer thread
+// has waited on its cp.async groups), turn the raw rows into B-operand rows
+// and load this thread's fragments.
+template <bool kBf16Q, bool ASYM>
+__device__ __forceinline__ bool convert_query(const DecodeArgs& a, int buf, const uint16_t* qraw, const float* fraw,
+                                              uint16_t* qh, uint32_t* qlo, float* qs, const Scratch& sc,
+                                              uint32_t& cphase, int warp, int lane, uint32_t (&qf)[16], float& qs0,
+                                              float& qs1, float& qz0, float& qz1) {
+  if (!consumer_sync(sc.cbar, cphase)) return false;  // the factor row was copied by warp 0
+  write_query_rows<kBf16Q, ASYM>(a, buf, qraw, fraw, qh, qlo, qs, warp, lane);
   if (!consumer_sync(sc.cbar, cphase)) return false;
   load_query(qh, qs, qf, qs0, qs1, lane);
   if constexpr (ASYM) {
@@ -876,7 +925,8 @@ __device__ __forceinline__ void scan_geometry(const DecodeArgs& a, int B, int W,
   __syncthreads();
 }
 
-template <int KB, int VB, bool ASYM>
+// LOQ: the two-part fp16 query (q_bits 32) of code blocks.
+template <int KB, int VB, bool ASYM, bool LOQ>
 __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   using F = Fmt<KB, VB, ASYM>;
   constexpr int S = F::kStages;
@@ -885,12 +935,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   const int P = prm.P, Uw = prm.Uw;
   const int H = a.c.H, G = a.G, B = a.B;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const SmemMap mp = smem_map(S * F::kStageBytes, S, B);
+  const SmemMap mp = smem_map(S * F::kStageBytes, S, B, LOQ);
   Scratch sc;
   sc.merge_o = reinterpret_cast<float*>(smem + mp.merge_o);
   sc.merge_m = reinterpret_cast<float*>(smem + mp.merge_ml);
   sc.merge_l = sc.merge_m + kConsumerWarps * kMaxGroup;
   uint16_t* qh = reinterpret_cast<uint16_t*>(smem + mp.qh);
+  uint32_t* qlo_s = reinterpret_cast<uint32_t*>(smem + mp.qlo);
   float* qs = reinterpret_cast<float*>(smem + mp.qs);
   uint16_t* qraw = reinterpret_cast<uint16_t*>(smem + mp.qraw);
   float* fraw = reinterpret_cast<float*>(smem + mp.fraw);
@@ -913,6 +964,15 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     mbar_init(sc.cbar, kConsumers);
     sc.misc[0] = 0;
     fence_mbar_init();
+  }
+  if constexpr (!F::kBf16) {
+    // keys with per-channel scales only have no per-token key scale: the
+    // producer never copies into the key-scale slots of the ring, which keep 1.0
+    if (a.c.k_chan)
+      for (int i = tid; i < S * F::kBlocksPerStage * kBlock; i += kThreads) {
+        const int st = i / (F::kBlocksPerStage * kBlock), r = i % (F::kBlocksPerStage * kBlock);
+        reinterpret_cast<float*>(smem + st * F::kStageBytes + F::kOffKS)[r] = 1.f;
+      }
   }
   // Programmatic dependent launch: this grid may start while the previous
   // kernel on the stream is still finishing.  Let the next kernel launch
@@ -955,7 +1015,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       const uint8_t* const vbs[1] = {vb};
       const float* const nos[1] = {nullptr};
       const int val[1] = {min(kBlock, nw - j * kBlock)};
-      process_blocks<16, 16, 1, false>(kbs, vbs, nos, nos, nos, nos, val, qf, qs0, qs1, 0.f, 0.f, st, lane, a.err);
+      process_blocks<16, 16, 1, false, false>(kbs, vbs, nos, nos, nos, nos, val, qf, nullptr, qs0, qs1, 0.f, 0.f, st, lane,
+                                       a.err);
     }
     const size_t slot = size_t(P) + U + u;
     if (!finish_segment<false>(a, st, u, slot, len_s, geo, T, Pe, P, sc, cphase, warp, lane, tid))
@@ -1051,7 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       }
       if (lane == 0) {
         hdr[s] = make_int4(b * H + h, local, n, 0);
-        mbar_arrive_expect_tx(&full[s], uint32_t(n * F::kPerBlock));
+        mbar_arrive_expect_tx(&full[s], uint32_t(n * (a.c.k_chan ? F::kPerBlock - F::kSCB : F::kPerBlock)));
       }
       __syncwarp();
       if (start) {
@@ -1060,7 +1121,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         bulk_g2s(st + F::kOffK + lane * F::kKBB, a.c.k_codes + hb * F::kKBB, run * F::kKBB, &full[s], pol);
         bulk_g2s(st + F::kOffV + lane * F::kVBB, a.c.v_codes + hb * F::kVBB, run * F::kVBB, &full[s], pol);
         if constexpr (!F::kBf16) {
-          bulk_g2s(st + F::kOffKS + lane * F::kSCB, a.c.k_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
+          if (!a.c.k_chan)
+            bulk_g2s(st + F::kOffKS + lane * F::kSCB, a.c.k_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
           bulk_g2s(st + F::kOffVS + lane * F::kSCB, a.c.v_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
         }
         if constexpr (ASYM) {
@@ -1111,11 +1173,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     } else {
       cp_async_wait<0>();
     }
-    if (!convert_query<F::kBf16, ASYM>(a, 0, qraw, fraw, qh, qs, sc, cphase, warp, lane, qf, qs0, qs1, qz0, qz1)) {
+    if (!convert_query<F::kBf16, ASYM>(a, 0, qraw, fraw, qh, qlo_s, qs, sc, cphase, warp, lane, qf, qs0, qs1, qz0, qz1)) {
       flag(a.err, KVQ_DEVERR_TIMEOUT);
       return;
     }
   }
+  // low query parts of code blocks (only for the two-part fp16 query, q_bits = 32)
+  const uint4* qlo = LOQ ? reinterpret_cast<const uint4*>(qlo_s) + lane : nullptr;
   int s = 0;
   uint32_t ph = 0;  // stage index and the parity of its current use
   for (;;) {
@@ -1140,7 +1204,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       const int cb = cur / H;
       cur_lq = W > 0 ? max(len_s[cb] - W, 0) : len_s[cb];
       cp_async_wait<0>();
-      if (!convert_query<F::kBf16, ASYM>(a, qbuf, qraw, fraw, qh, qs, sc, cphase, warp, lane, qf, qs0, qs1, qz0, qz1)) {
+      if (!convert_query<F::kBf16, ASYM>(a, qbuf, qraw, fraw, qh, qlo_s, qs, sc, cphase, warp, lane, qf, qs0, qs1, qz0,
+                                      qz1)) {
         flag(a.err, KVQ_DEVERR_TIMEOUT);
         return;
       }
@@ -1170,7 +1235,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const float* const kos[2] = {kop(j0), kop(j1)};
         const float* const vos[2] = {vop(j0), vop(j1)};
         const int vals[2] = {val(j0), val(j1)};
-        process_blocks<KB, VB, 2, ASYM>(kbs, vbs, kss, vss, kos, vos, vals, qf, qs0, qs1, qz0, qz1, st, lane, a.err);
+        process_blocks<KB, VB, 2, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qs0, qs1, qz0, qz1, st, lane,
+                                        a.err);
       } else {
         const uint8_t* const kbs[1] = {kp(j0)};
         const uint8_t* const vbs[1] = {vp(j0)};
@@ -1179,7 +1245,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const float* const kos[1] = {kop(j0)};
         const float* const vos[1] = {vop(j0)};
         const int vals[1] = {val(j0)};
-        process_blocks<KB, VB, 1, ASYM>(kbs, vbs, kss, vss, kos, vos, vals, qf, qs0, qs1, qz0, qz1, st, lane, a.err);
+        process_blocks<KB, VB, 1, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qs0, qs1, qz0, qz1, st, lane,
+                                        a.err);
       }
     }
     __syncwarp();
@@ -1192,10 +1259,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
 }
 
 // ------------------------------------------------------------------ host side
-template <int KB, int VB, bool ASYM>
+template <int KB, int VB, bool ASYM, bool LOQ>
 struct Kernel {
   using F = Fmt<KB, VB, ASYM>;
-  static int smem_bytes(int B) { return smem_map(F::kStages * F::kStageBytes, F::kStages, B).total; }
+  static int smem_bytes(int B) { return smem_map(F::kStages * F::kStageBytes, F::kStages, B, LOQ).total; }
   // Allow the largest opt-in dynamic shared memory once per device; the
   // per-launch size (which depends on the batch) then always fits.
   static void ensure_attribute(int dev) {
@@ -1205,11 +1272,11 @@ struct Kernel {
     if (done.count(dev)) return;
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    cudaFuncSetAttribute(decode_kernel<KB, VB, ASYM>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    cudaFuncSetAttribute(decode_kernel<KB, VB, ASYM, LOQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     // Ask for the largest shared-memory carveout: the occupancy used to size
     // the single wave assumes it, and a smaller split (chosen by default)
     // would fit one CTA fewer per SM and turn the wave into 1.5 waves.
-    cudaFuncSetAttribute(decode_kernel<KB, VB, ASYM>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    cudaFuncSetAttribute(decode_kernel<KB, VB, ASYM, LOQ>, cudaFuncAttributePreferredSharedMemoryCarveout,
                          cudaSharedmemCarveoutMaxShared);
     done[dev] = true;
   }
@@ -1225,7 +1292,7 @@ struct Kernel {
     auto itc = cache.find(key);
     if (itc != cache.end()) return itc->second;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KB, VB, ASYM>, kThreads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<KB, VB, ASYM, LOQ>, kThreads, smem) != cudaSuccess)
       n = 1;
     n = n < 1 ? 1 : n;
     cache[key] = n;
@@ -1248,7 +1315,7 @@ struct Kernel {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<KB, VB, ASYM>, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<KB, VB, ASYM, LOQ>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }

@@ -20,7 +20,8 @@ struct CacheView {
   float* v_offsets;
   const float* factor;  // [H][128] or null
   int window, window_batch;
-  int q_bits;      // 8: int8-quantized query rows (integer dot), else the bf16 query
+  int q_bits;      // query format: 8 int8 rows (integer dot), 16 fp16, 32 fp16 hi + lo
+  int k_chan;      // 1: keys carry per-channel scales (factor) only, no per-token key scale
   uint8_t* k_win;  // bf16 ring: [window_batch][H][W/16] fragment-native bf16 blocks
   uint8_t* v_win;
 };
@@ -78,10 +79,13 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 // Resident decode CTAs per SM for this cache format and batch (occupancy
 // query on the current device, cached); 0 for an unsupported format.
-int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int batch);
+int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int q_bits, int batch);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 // The asymmetric instantiations (kvq_decode_asym.cu).
 int decode_ctas_per_sm_asym(int k_bits, int v_bits, int batch);
 cudaError_t launch_decode_asym(const DecodeArgs& a, cudaStream_t s);
+// The two-part fp16 query instantiations (kvq_decode_q32.cu).
+int decode_ctas_per_sm_q32(int k_bits, int v_bits, bool asym, int batch);
+cudaError_t launch_decode_q32(const DecodeArgs& a, cudaStream_t s);
 
 }  // namespace kvq

@@ -57,6 +57,7 @@ class Workload:
     outlier_mult: float = 10.0
     asym: bool = False               # asymmetric format: per-token scale and zero point
     q_bits: int = 16                 # 8: int8-quantized query rows (integer dot)
+    k_per_channel: bool = False      # keys carry per-channel scales only (needs channel_factor)
     head_dim: int = HEAD_DIM
     block_size: int = BLOCK_SIZE
     seed: int = 0
@@ -181,9 +182,18 @@ def make_inputs(w: Workload, seed: int | None = None) -> Inputs:
     if w.append_one:
         k_new = _bf16_tokens(rng, B, w.kv_heads, D, w.k_dist, outliers, w.outlier_mult)
         v_new = _bf16_tokens(rng, B, w.kv_heads, D, "normal")
-    # per-channel key factor: the per-channel absmax of the seeded keys (0 -> 1)
+    # per-channel key factor: the per-channel absmax of the seeded keys (0 -> 1).
+    # With per-channel key scales only, the caller's calibration is the
+    # per-channel absmax of the first half of the cached tokens divided by the
+    # code range (127 or 7): later tokens can fall outside it.
     factor = None
-    if w.channel_factor:
+    if w.channel_factor and w.k_per_channel:
+        kf = bf16_bits_to_f32(k[: max(n_tok // 2, 1)]) if n_tok else np.ones((1, w.kv_heads, D), np.float32)
+        qmax = np.float32(127.0 if w.k_bits == 8 else 7.0)
+        factor = (np.abs(kf).max(axis=0) / qmax).astype(np.float32)
+        factor[factor == 0] = 1.0
+        del kf
+    elif w.channel_factor:
         kf = bf16_bits_to_f32(k)
         factor = np.abs(kf).max(axis=0).astype(np.float32) if n_tok else np.ones((w.kv_heads, D), np.float32)
         if k_new is not None:

@@ -31,7 +31,8 @@ def oracle_state(inp, b):
     w = inp.workload
     k, v = seq_kv(inp, b)
     c = None if inp.channel_factor is None else inp.channel_factor.astype(np.float64)
-    return O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c, asym=w.asym)
+    return O.quantize_sequence(k, v, w.k_bits, w.v_bits, window=w.window, c=c, asym=w.asym,
+                               k_per_channel=w.k_per_channel)
 
 
 def oracle_decode(inp, units=None):

@@ -86,8 +86,12 @@ def _fake_desc(lib, **kw):
     (dict(k_offsets=0xA000), 1), (dict(v_offsets=0xA000), 1), (dict(k_offsets=0xA000, v_offsets=0xB008), 3),
     (dict(k_bits=16, v_bits=16, k_scales=None, v_scales=None, k_offsets=0xA000, v_offsets=0xB000), 2),
     # quantized query: 8 (or 0/16 for bf16), quantized blocks only, not factor + window together
-    (dict(q_bits=4), 2), (dict(k_bits=16, v_bits=16, k_scales=None, v_scales=None, q_bits=8), 2),
+    (dict(q_bits=4), 2), (dict(q_bits=24), 2), (dict(k_bits=16, v_bits=16, k_scales=None, v_scales=None, q_bits=8), 2),
     (dict(q_bits=8, k_channel_factor=0xC000, window=16, window_batch=1, k_window=0xD000, v_window=0xE000), 2),
+    # per-channel key scales only: needs the factor, symmetric quantized keys; k_scales may be NULL
+    (dict(k_per_channel=1), 1), (dict(k_per_channel=2, k_channel_factor=0xC000), 1),
+    (dict(k_per_channel=1, k_channel_factor=0xC000, k_offsets=0xA000, v_offsets=0xB000), 2),
+    (dict(k_per_channel=1, k_channel_factor=0xC000, k_scales=None, v_scales=None), 1),
 ])
 def test_host_validation_without_a_gpu(lib, kw, status):
     desc = _fake_desc(lib, **kw)

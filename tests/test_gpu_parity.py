@@ -51,6 +51,19 @@ SMALL = {
                                              v_bits=8, len_range=(1, 500), window=32, k_dist="t3", q_bits=8),
     "qint8_asym_k8v4_g1": small_workload("qint8_asym_k8v4_g1", batch=3, q_heads=4, kv_heads=4, k_bits=8, v_bits=4,
                                          len_range=(1, 300), asym=True, q_bits=8),
+    # keys under per-channel scales only (calibrated on the first half of the tokens: the clamp binds)
+    "kchan_int8_g4": small_workload("kchan_int8_g4", channel_factor=True, k_per_channel=True, outlier_channels=4),
+    # heavy-tailed keys under per-channel scales give scores near 10: the fp16
+    # query's 11 bits are not enough for 2e-3, the two-part query is (q_bits 32)
+    "kchan_k4v8_window32_g8": small_workload("kchan_k4v8_window32_g8", batch=3, q_heads=16, kv_heads=2, k_bits=4,
+                                             v_bits=8, len_range=(1, 500), window=32, channel_factor=True,
+                                             k_per_channel=True, k_dist="t3", q_bits=32),
+    "kchan_qint8_int4_g8": small_workload("kchan_qint8_int4_g8", batch=4, q_heads=16, kv_heads=2, k_bits=4,
+                                          v_bits=4, channel_factor=True, k_per_channel=True, q_bits=8),
+    # two-part fp16 query (q_bits 32)
+    "q32_int8_g4": small_workload("q32_int8_g4", q_bits=32, outlier_channels=4, window=32, len_range=(1, 200)),
+    "q32_asym_int4_factor_g8": small_workload("q32_asym_int4_factor_g8", batch=4, q_heads=16, kv_heads=2, k_bits=4,
+                                              v_bits=4, channel_factor=True, asym=True, q_bits=32),
 }
 
 
@@ -90,9 +103,11 @@ def check_stored_cache(inp, run, units=None, max_positions=None):
         else:
             np.testing.assert_array_equal(kc[phys, :, tok], st["k_codes"][pos])
             np.testing.assert_array_equal(vc[phys, :, tok], st["v_codes"][pos])
-            ks = scales_by_block(pools["k_scales"], w.kv_heads)[phys, :, tok]
             vs = scales_by_block(pools["v_scales"], w.kv_heads)[phys, :, tok]
-            np.testing.assert_array_equal(ks.view(np.uint32), st["k_scale"][pos].astype(np.float32).view(np.uint32))
+            if not w.k_per_channel:
+                ks = scales_by_block(pools["k_scales"], w.kv_heads)[phys, :, tok]
+                np.testing.assert_array_equal(ks.view(np.uint32),
+                                              st["k_scale"][pos].astype(np.float32).view(np.uint32))
             np.testing.assert_array_equal(vs.view(np.uint32), st["v_scale"][pos].astype(np.float32).view(np.uint32))
             if w.asym:
                 ko = scales_by_block(pools["k_offsets"], w.kv_heads)[phys, :, tok]
@@ -153,6 +168,25 @@ def test_dequant_asym_returns_rn32_of_code_times_scale_plus_offset(runs, name):
         np.testing.assert_array_equal(got.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("name", ["kchan_int8_g4", "kchan_k4v8_window32_g8"])
+def test_dequant_per_channel_keys_return_rn32_of_code_times_channel_scale(runs, name):
+    inp, run = runs(name)
+    w = inp.workload
+    st = oracle_state(inp, 0)
+    pos = np.arange(st["Lq"])
+    if pos.size == 0:
+        pytest.skip("sequence 0 lies entirely in the window")
+    slots = inp.block_table[0, pos // 16].astype(np.int64) * 16 + pos % 16
+    ko = torch.empty((len(pos), w.kv_heads, 128), dtype=torch.float32, device="cuda")
+    vo = torch.empty_like(ko)
+    run.lib.kvq_dequant(run.cache.desc, torch.from_numpy(slots.astype(np.int32)).cuda(), ko, vo)
+    torch.cuda.synchronize()
+    ref_k = (st["k_codes"][pos].astype(np.float64) * inp.channel_factor.astype(np.float64)).astype(np.float32)
+    np.testing.assert_array_equal(ko.cpu().numpy().view(np.uint32), ref_k.view(np.uint32))
+    if w.k_bits == 8:  # calibrated on the first half of the tokens: later ones hit the clamp
+        assert np.abs(st["k_codes"]).max() == 127
+
+
 @pytest.mark.parametrize("name", ["int8_g4", "int4_factor_g8", "k4v8_g8_t3", "bf16"])
 def test_dequant_returns_rn32_of_code_times_scale(runs, name):
     inp, run = runs(name)
@@ -201,6 +235,26 @@ def test_decode_split_count_does_not_change_result(runs, name):
         out, lse = run.decode(out_fp32=True, stream_ctas=p)
         np.testing.assert_allclose(out, base, rtol=0, atol=atol)
         np.testing.assert_allclose(lse, base_lse, rtol=0, atol=2e-5)
+
+
+def test_two_part_query_removes_the_query_rounding_error():
+    """On heavy-tailed keys under per-channel scales (scores near 10) the fp16
+    query (q_bits 16) leaves a score error that the log-sum-exp shows directly;
+    the fp16 hi + lo query (q_bits 32) cuts it at least fourfold and brings the
+    whole comparison inside the tolerance."""
+    base = SMALL["kchan_k4v8_window32_g8"]
+    lse_err, ratio = {}, {}
+    for qb in (16, 32):
+        inp = make_inputs(base.with_(name=f"kchan_q{qb}", q_bits=qb))
+        run = GpuRun(inp)
+        out, lse = run.decode(out_fp32=True)
+        ref = oracle_decode(inp)
+        G = inp.workload.group
+        lse_err[qb] = max(float(np.abs(lse[b, h * G:(h + 1) * G] - l).max()) for (b, h), (_, l) in ref.items())
+        ratio[qb] = compare_outputs(inp, out, lse, ref, out_is_bf16=False)
+        assert run.err_bits() == 0
+    assert lse_err[32] * 4 <= lse_err[16], lse_err
+    assert ratio[32] <= 1.0, ratio
 
 
 @pytest.mark.parametrize("window", [0, 32])
@@ -331,6 +385,9 @@ FULL["asym_long_k4v8_b4_t131072"] = WORKLOADS["long_k4v8_b4_t131072"].with_(name
 # the quantized-query mode on the int4 / per-channel factor shape
 FULL["qint8_int4_factor_b32_len1k_8k"] = WORKLOADS["int4_factor_b32_len1k_8k"].with_(
     name="qint8_int4_factor_b32_len1k_8k", q_bits=8)
+# per-channel key scales only on the int4 / factor shape
+FULL["kchan_int4_factor_b32_len1k_8k"] = WORKLOADS["int4_factor_b32_len1k_8k"].with_(
+    name="kchan_int4_factor_b32_len1k_8k", k_per_channel=True)
 
 
 @pytest.mark.parametrize("name", list(FULL))
