@@ -274,8 +274,7 @@ def main():
         replicas = [base]
         for _ in range(reps - 1):
             c = cache_for_inputs(inp_, dev)
-            for name in ("k_codes", "v_codes", "k_scales", "v_scales", "k_offsets", "v_offsets", "k_window",
-                         "v_window"):
+            for name in ("k_codes", "v_codes", "meta", "k_window", "v_window"):
                 src, dst = getattr(base, name), getattr(c, name)
                 if src is not None:
                     dst.copy_(src)

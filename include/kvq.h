@@ -49,10 +49,13 @@
  *     code c in [-8,7] (-8 never produced) is the nibble c + 8.  In the
  *     asymmetric format the unsigned code u (int8: 0..255, int4: 0..15) is
  *     stored as the byte or nibble u itself.
- *   Scale pool  : float [num_kv_heads][num_blocks][16], natural token order
- *                 (absent for a bf16 cache).
- *   Offset pool : asymmetric format only: the per-token zero point m, same
- *                 layout as the scale pool.
+ *   Metadata pool: float [num_kv_heads][num_blocks][M], one record of M floats
+ *                 per block (absent for a bf16 cache), tokens in natural order:
+ *                 symmetric M = 32: the block's 16 key scales, then its 16
+ *                 value scales; asymmetric M = 64: key scales, key zero points,
+ *                 value scales, value zero points.  A block's record is one
+ *                 128-byte (256-byte) read.  Keys under per-channel scales only
+ *                 leave the key-scale entries unused.
  *   Window ring : bf16 [window_batch][num_kv_heads][window / 16][4096 bytes]:
  *                 window / 16 blocks per (sequence, head) for keys and for
  *                 values, each in the bf16 key / value block order above;
@@ -105,24 +108,22 @@ typedef struct {
   int32_t v_bits;         /* 8 or 4, or 16                                          */
   void* k_codes;          /* codes pool for keys (see layout above)                 */
   void* v_codes;          /* codes pool for values                                  */
-  float* k_scales;        /* per-token key scales; NULL for a bf16 cache            */
-  float* v_scales;        /* per-token value scales; NULL for a bf16 cache          */
+  float* meta;            /* metadata pool (layout above); NULL for a bf16 cache    */
+  /* Asymmetric format ([P1] "Quantization granularity defines which values
+   * share a scale": a scale and, depending on the scheme, a zero point; [P3]
+   * "Per-token scales and where they can live": a scale and zero point cost
+   * twice the metadata).  0: symmetric codes.  1 (8- or 4-bit blocks only): per
+   * token per head m = min(x), s = RN32((max(x) - min(x)) / (2^bits - 1))
+   * (difference and quotient in double; a constant vector stores s = 1), u =
+   * clamp(round_half_even((x - m) / s), 0, 2^bits - 1) with the difference and
+   * quotient in double, x_hat = u * s + m; K and V both. */
+  int32_t asym;
   const float* k_channel_factor; /* [num_kv_heads][128] positive, or NULL           */
   int32_t window;         /* recent-token bf16 window W: 0 = none, or 16..128 in    */
                           /* steps of 16                                            */
   int32_t window_batch;   /* first dimension of the ring buffers (sequences)        */
   void* k_window;         /* bf16 ring (layout above), or NULL if W == 0            */
   void* v_window;
-  /* Asymmetric format ([P1] "Quantization granularity defines which values
-   * share a scale": a scale and, depending on the scheme, a zero point; [P3]
-   * "Per-token scales and where they can live": a scale and zero point cost
-   * twice the metadata).  Both NULL: symmetric codes.  Both set (8- or 4-bit
-   * blocks only): per token per head m = min(x), s = RN32((max(x) - min(x)) /
-   * (2^bits - 1)) (difference and quotient in double; a constant vector stores
-   * s = 1), u = clamp(round_half_even((x - m) / s), 0, 2^bits - 1) with the
-   * difference and quotient in double, x_hat = u * s + m. */
-  float* k_offsets;       /* per-token key zero points (offset pool), or NULL      */
-  float* v_offsets;       /* per-token value zero points, or NULL                  */
   /* Query format of kvq_decode against this cache ([P3] "Precision floors and
    * mixed cache formats": an 8-bit query meets the integer key codes, the dot
    * product accumulates in integers and is converted to float before the
@@ -143,8 +144,9 @@ typedef struct {
    * factor (if any) divides the keys before the per-token quantizer.  1: the
    * keys carry no per-token scale: code_j = clamp(round_half_even(k_j / c_j))
    * with c = k_channel_factor as the per-channel scale (required; the clamp
-   * binds for values beyond qmax * c_j), k_hat_j = c_j * code_j; k_scales is
-   * not read or written and may be NULL.  Symmetric 8- or 4-bit keys only. */
+   * binds for values beyond qmax * c_j), k_hat_j = c_j * code_j; the key-scale
+   * entries of the metadata pool are not read or written.  Symmetric 8- or
+   * 4-bit keys only. */
   int32_t k_per_channel;
 } kvq_cache_desc;
 
@@ -164,9 +166,9 @@ kvq_status kvq_block_bytes(int32_t bits, size_t* bytes);
  * vector -> codes 0 and s = 1.  qmax = 127 (int8) or 7 (int4).  With a
  * per-channel key factor c, keys are first divided by c (float32, RN) and then
  * quantized per token ([P3] "The axis choice is a kernel decision").  Codes are
- * the correctly rounded quotient of the exact x / s.  With k_offsets/v_offsets
- * set, the asymmetric quantizer of kvq_cache_desc is used instead and the zero
- * point is stored beside the scale.
+ * the correctly rounded quotient of the exact x / s.  With asym = 1 the
+ * asymmetric quantizer of kvq_cache_desc is used instead and the zero point is
+ * stored beside the scale.
  *   k_new, v_new : device bf16 [n][num_kv_heads][128]
  *   n            : number of new tokens (0 is a no-op)
  *   seq_idx, pos : device int32 [n]; token r belongs to sequence seq_idx[r] at

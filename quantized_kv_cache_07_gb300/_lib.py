@@ -43,11 +43,10 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [
         ("num_kv_heads", c_int32), ("head_dim", c_int32), ("block_size", c_int32), ("num_blocks", c_int32),
         ("k_bits", c_int32), ("v_bits", c_int32),
-        ("k_codes", c_void_p), ("v_codes", c_void_p), ("k_scales", c_void_p), ("v_scales", c_void_p),
+        ("k_codes", c_void_p), ("v_codes", c_void_p), ("meta", c_void_p), ("asym", c_int32),
         ("k_channel_factor", c_void_p),
         ("window", c_int32), ("window_batch", c_int32),
         ("k_window", c_void_p), ("v_window", c_void_p),
-        ("k_offsets", c_void_p), ("v_offsets", c_void_p),
         ("q_bits", c_int32), ("k_per_channel", c_int32),
     ]
 

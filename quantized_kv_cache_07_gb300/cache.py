@@ -24,7 +24,7 @@ class KVCache:
     """Block pools (+ optional bf16 window ring) of one attention layer.
 
     ``asym=True`` selects the asymmetric format: a per-token zero point is
-    stored beside each scale (offset pools of the same shape).  ``q_bits=8``
+    stored beside each scale in the metadata pool.  ``q_bits=8``
     makes kvq_decode quantize each query row to int8 (integer dot product).
     """
 
@@ -41,15 +41,13 @@ class KVCache:
         self.v_codes = torch.zeros(self.num_blocks * kv_heads * vbb, dtype=torch.uint8, device=device)
         quant = k_bits != 16
         self.k_per_channel = bool(k_per_channel)
-        n_sc = self.num_blocks * kv_heads * BLOCK_SIZE
-        self.k_scales = (torch.zeros(n_sc, dtype=torch.float32, device=device)
-                         if quant and not self.k_per_channel else None)
-        self.v_scales = torch.zeros(n_sc, dtype=torch.float32, device=device) if quant else None
         self.asym = bool(asym)
         if self.asym and not quant:
             raise ValueError("the asymmetric format needs 8- or 4-bit blocks")
-        self.k_offsets = torch.zeros(n_sc, dtype=torch.float32, device=device) if self.asym else None
-        self.v_offsets = torch.zeros(n_sc, dtype=torch.float32, device=device) if self.asym else None
+        # metadata pool: per block K scales, (K zero points,) V scales, (V zero points)
+        self.meta_floats = (4 if self.asym else 2) * BLOCK_SIZE
+        self.meta = (torch.zeros(self.num_blocks * kv_heads * self.meta_floats, dtype=torch.float32, device=device)
+                     if quant else None)
         self.channel_factor = None
         if channel_factor is not None:
             self.channel_factor = torch.as_tensor(np.ascontiguousarray(channel_factor, dtype=np.float32)
@@ -63,14 +61,11 @@ class KVCache:
             num_kv_heads=kv_heads, head_dim=HEAD_DIM, block_size=BLOCK_SIZE, num_blocks=self.num_blocks,
             k_bits=k_bits, v_bits=v_bits,
             k_codes=self.k_codes.data_ptr(), v_codes=self.v_codes.data_ptr(),
-            k_scales=self.k_scales.data_ptr() if self.k_scales is not None else None,
-            v_scales=self.v_scales.data_ptr() if quant else None,
+            meta=self.meta.data_ptr() if quant else None, asym=int(self.asym),
             k_channel_factor=self.channel_factor.data_ptr() if self.channel_factor is not None else None,
             window=self.window, window_batch=max(window_batch, 1) if window > 0 else 0,
             k_window=self.k_window.data_ptr() if self.k_window is not None else None,
             v_window=self.v_window.data_ptr() if self.v_window is not None else None,
-            k_offsets=self.k_offsets.data_ptr() if self.asym else None,
-            v_offsets=self.v_offsets.data_ptr() if self.asym else None,
             q_bits=int(q_bits), k_per_channel=int(self.k_per_channel))
 
     # bytes the decode reads per cached token per KV head (codes + scales + zero points)
@@ -81,8 +76,7 @@ class KVCache:
         return kb + vb
 
     def allocated_bytes(self) -> int:
-        ts = [self.k_codes, self.v_codes, self.k_scales, self.v_scales, self.k_offsets, self.v_offsets,
-              self.k_window, self.v_window]
+        ts = [self.k_codes, self.v_codes, self.meta, self.k_window, self.v_window]
         return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
 

@@ -30,18 +30,14 @@ kvq_status check_cache(const kvq_cache_desc* c) {
   if (!c->k_codes || !c->v_codes) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(c->k_codes) || !aligned16(c->v_codes)) return KVQ_ERR_ALIGNMENT;
   const bool quant = c->k_bits != 16;
+  if (c->asym != 0 && c->asym != 1) return KVQ_ERR_INVALID_ARG;
   if (c->k_per_channel != 0 && c->k_per_channel != 1) return KVQ_ERR_INVALID_ARG;
-  if (c->k_per_channel && (!quant || c->k_offsets || c->v_offsets)) return KVQ_ERR_UNSUPPORTED;
+  if (c->asym && !quant) return KVQ_ERR_UNSUPPORTED;  // zero points only on quantized blocks
+  if (c->k_per_channel && (!quant || c->asym)) return KVQ_ERR_UNSUPPORTED;
   if (c->k_per_channel && !c->k_channel_factor) return KVQ_ERR_INVALID_ARG;
   if (quant) {
-    if ((!c->k_scales && !c->k_per_channel) || !c->v_scales) return KVQ_ERR_INVALID_ARG;
-    if ((c->k_scales && !aligned16(c->k_scales)) || !aligned16(c->v_scales)) return KVQ_ERR_ALIGNMENT;
-  }
-  // zero points: both tensors or neither, and only on quantized blocks
-  if ((c->k_offsets != nullptr) != (c->v_offsets != nullptr)) return KVQ_ERR_INVALID_ARG;
-  if (c->k_offsets) {
-    if (!quant) return KVQ_ERR_UNSUPPORTED;
-    if (!aligned16(c->k_offsets) || !aligned16(c->v_offsets)) return KVQ_ERR_ALIGNMENT;
+    if (!c->meta) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(c->meta)) return KVQ_ERR_ALIGNMENT;
   }
   if (c->k_channel_factor) {
     if (!quant) return KVQ_ERR_UNSUPPORTED;
@@ -66,10 +62,9 @@ kvq::CacheView view(const kvq_cache_desc* c) {
   v.v_bits = c->v_bits;
   v.k_codes = static_cast<uint8_t*>(c->k_codes);
   v.v_codes = static_cast<uint8_t*>(c->v_codes);
-  v.k_scales = c->k_scales;
-  v.v_scales = c->v_scales;
-  v.k_offsets = c->k_offsets;
-  v.v_offsets = c->v_offsets;
+  v.meta = c->meta;
+  v.asym = c->asym;
+  v.meta_floats = c->asym ? 64 : 32;
   v.factor = c->k_channel_factor;
   v.window = c->window;
   v.window_batch = c->window_batch;
@@ -99,7 +94,7 @@ int auto_stream_ctas(const kvq_cache_desc* c, int batch) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, c->k_offsets != nullptr, c->q_bits, batch);
+  const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, c->asym != 0, c->q_bits, batch);
   return stream_ctas_for(sms * per, c->window > 0 ? batch * c->num_kv_heads : 0, batch * c->num_kv_heads);
 }
 

@@ -159,7 +159,7 @@ __device__ void write_block_store(const AppendArgs& a, bool is_key, int b, int p
   }
   int code[4];
   float s, m = 0.f;
-  const bool asym = c.k_offsets != nullptr;
+  const bool asym = c.asym != 0;
   if (asym) {
     quantize_asym_warp(x, bits, code, s, m);
   } else {
@@ -170,9 +170,11 @@ __device__ void write_block_store(const AppendArgs& a, bool is_key, int b, int p
   }
   store_codes(is_key, bits, blk, tok, code, lane);
   if (lane == 0) {
-    const size_t e = (size_t(h) * c.num_blocks + phys) * kBlock + tok;
-    (is_key ? c.k_scales : c.v_scales)[e] = s;
-    if (asym) (is_key ? c.k_offsets : c.v_offsets)[e] = m;
+    // metadata record: K scales, (K zero points,) V scales, (V zero points)
+    float* rec = c.meta + (size_t(h) * c.num_blocks + phys) * c.meta_floats;
+    const int off = is_key ? 0 : c.meta_floats / 2;
+    rec[off + tok] = s;
+    if (asym) rec[off + kBlock + tok] = m;
   }
 }
 
@@ -249,12 +251,13 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
   const int bits = is_key ? a.c.k_bits : a.c.v_bits;
   const uint8_t* blk = (is_key ? a.c.k_codes : a.c.v_codes) + (size_t(h) * a.c.num_blocks + phys) * block_bytes(bits);
   float s = 1.0f, m = 0.0f;
-  const bool asym = a.c.k_offsets != nullptr;
+  const bool asym = a.c.asym != 0;
   const bool chan = is_key && a.c.k_chan;  // per-channel key scale c_j instead of a per-token one
   if (bits != 16 && !chan) {
-    const size_t e = (size_t(h) * a.c.num_blocks + phys) * kBlock + tok;
-    s = (is_key ? a.c.k_scales : a.c.v_scales)[e];
-    if (asym) m = (is_key ? a.c.k_offsets : a.c.v_offsets)[e];
+    const float* rec = a.c.meta + (size_t(h) * a.c.num_blocks + phys) * a.c.meta_floats;
+    const int off = is_key ? 0 : a.c.meta_floats / 2;
+    s = rec[off + tok];
+    if (asym) m = rec[off + kBlock + tok];
   }
   const int bias = asym ? 0 : (bits == 8 ? 128 : 8);
 #pragma unroll

@@ -21,7 +21,7 @@ int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int q_bits, int B)
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   const int kb = a.c.k_bits, vb = a.c.v_bits;
   if (a.c.q_bits == 32 && kb != 16) return launch_decode_q32(a, s);
-  if (a.c.k_offsets) return launch_decode_asym(a, s);
+  if (a.c.asym) return launch_decode_asym(a, s);
   if (kb == 8 && vb == 8) return Kernel<8, 8, false, false>::launch(a, s);
   if (kb == 4 && vb == 4) return Kernel<4, 4, false, false>::launch(a, s);
   if (kb == 4 && vb == 8) return Kernel<4, 8, false, false>::launch(a, s);

@@ -72,9 +72,10 @@ struct Fmt {
   static_assert(!(kBf16 && ASYM), "bf16 blocks carry no zero point");
   static constexpr int kKBB = block_bytes(KB);
   static constexpr int kVBB = block_bytes(VB);
-  static constexpr int kSCB = kBf16 ? 0 : kBlock * 4;  // scale bytes per block per tensor
-  static constexpr int kOFB = ASYM ? kBlock * 4 : 0;   // zero-point bytes per block per tensor
-  static constexpr int kPerBlock = kKBB + kVBB + 2 * kSCB + 2 * kOFB;
+  // metadata record per block: K scales, (K zero points,) V scales, (V zero points)
+  static constexpr int kMF = kBf16 ? 0 : (ASYM ? 4 : 2) * kBlock;  // floats
+  static constexpr int kMB = kMF * 4;                               // bytes
+  static constexpr int kPerBlock = kKBB + kVBB + kMB;
   // 4-bit keys: each consumer warp takes two blocks per stage (two independent
   // dependency chains, one softmax reduction per 32 tokens)
   static constexpr int kBPW = (KB == 4) ? 2 : 1;
@@ -86,10 +87,9 @@ struct Fmt {
   // stage sub-buffers
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kBlocksPerStage * kKBB;
-  static constexpr int kOffKS = kOffV + kBlocksPerStage * kVBB;
-  static constexpr int kOffVS = kOffKS + kBlocksPerStage * kSCB;
-  static constexpr int kOffKO = kOffVS + kBlocksPerStage * kSCB;
-  static constexpr int kOffVO = kOffKO + kBlocksPerStage * kOFB;
+  static constexpr int kOffMeta = kOffV + kBlocksPerStage * kVBB;
+  // float offsets inside a block's record
+  static constexpr int kKS = 0, kKO = kBlock, kVS = kMF / 2, kVO = kMF / 2 + kBlock;
 };
 
 // Shared-memory map after the stage ring (all offsets 16-byte aligned).
@@ -971,7 +971,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     if (a.c.k_chan)
       for (int i = tid; i < S * F::kBlocksPerStage * kBlock; i += kThreads) {
         const int st = i / (F::kBlocksPerStage * kBlock), r = i % (F::kBlocksPerStage * kBlock);
-        reinterpret_cast<float*>(smem + st * F::kStageBytes + F::kOffKS)[r] = 1.f;
+        reinterpret_cast<float*>(smem + st * F::kStageBytes + F::kOffMeta)[(r / kBlock) * F::kMF + F::kKS +
+                                                                           r % kBlock] = 1.f;
       }
   }
   // Programmatic dependent launch: this grid may start while the previous
@@ -1112,7 +1113,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       }
       if (lane == 0) {
         hdr[s] = make_int4(b * H + h, local, n, 0);
-        mbar_arrive_expect_tx(&full[s], uint32_t(n * (a.c.k_chan ? F::kPerBlock - F::kSCB : F::kPerBlock)));
+        // per-channel key scales only: the value half of each record, not the key scales
+        mbar_arrive_expect_tx(&full[s], uint32_t(n * (a.c.k_chan ? F::kPerBlock - F::kMB / 2 : F::kPerBlock)));
       }
       __syncwarp();
       if (start) {
@@ -1121,13 +1123,16 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         bulk_g2s(st + F::kOffK + lane * F::kKBB, a.c.k_codes + hb * F::kKBB, run * F::kKBB, &full[s], pol);
         bulk_g2s(st + F::kOffV + lane * F::kVBB, a.c.v_codes + hb * F::kVBB, run * F::kVBB, &full[s], pol);
         if constexpr (!F::kBf16) {
-          if (!a.c.k_chan)
-            bulk_g2s(st + F::kOffKS + lane * F::kSCB, a.c.k_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
-          bulk_g2s(st + F::kOffVS + lane * F::kSCB, a.c.v_scales + hb * kBlock, run * F::kSCB, &full[s], pol);
+          if (!a.c.k_chan)  // the run's metadata records: one contiguous copy
+            bulk_g2s(st + F::kOffMeta + lane * F::kMB, a.c.meta + hb * F::kMF, run * F::kMB, &full[s], pol);
         }
-        if constexpr (ASYM) {
-          bulk_g2s(st + F::kOffKO + lane * F::kOFB, a.c.k_offsets + hb * kBlock, run * F::kOFB, &full[s], pol);
-          bulk_g2s(st + F::kOffVO + lane * F::kOFB, a.c.v_offsets + hb * kBlock, run * F::kOFB, &full[s], pol);
+      }
+      if constexpr (!F::kBf16) {
+        if (a.c.k_chan && lane < n) {  // per-channel keys: each block's value half alone
+          uint8_t* st = smem + s * F::kStageBytes;
+          const size_t hb = size_t(h) * a.c.num_blocks + phys;
+          bulk_g2s(st + F::kOffMeta + lane * F::kMB + F::kVS * 4, a.c.meta + hb * F::kMF + F::kVS, F::kMB / 2,
+                   &full[s], pol);
         }
       }
       x += n;
@@ -1217,14 +1222,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       const uint8_t* stg = smem + s * F::kStageBytes;
       auto kp = [&](int j) { return stg + F::kOffK + j * F::kKBB; };
       auto vp = [&](int j) { return stg + F::kOffV + j * F::kVBB; };
-      auto ksp = [&](int j) {
-        return F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffKS + j * F::kSCB);
-      };
+      auto meta = [&](int j) { return reinterpret_cast<const float*>(stg + F::kOffMeta + j * F::kMB); };
+      auto ksp = [&](int j) { return F::kBf16 ? nullptr : meta(j) + F::kKS; };
       auto vsp = [&](int j) {
-        return F::kBf16 ? nullptr : reinterpret_cast<const float*>(stg + F::kOffVS + j * F::kSCB);
+        return F::kBf16 ? nullptr : meta(j) + F::kVS;
       };
-      auto kop = [&](int j) { return ASYM ? reinterpret_cast<const float*>(stg + F::kOffKO + j * F::kOFB) : nullptr; };
-      auto vop = [&](int j) { return ASYM ? reinterpret_cast<const float*>(stg + F::kOffVO + j * F::kOFB) : nullptr; };
+      auto kop = [&](int j) { return ASYM ? meta(j) + F::kKO : nullptr; };
+      auto vop = [&](int j) { return ASYM ? meta(j) + F::kVO : nullptr; };
       auto val = [&](int j) { return min(kBlock, cur_lq - (hd.y + j) * kBlock); };
       const int j0 = warp, j1 = warp + kConsumerWarps;
       if (F::kBPW == 2 && j1 < hd.z) {

@@ -23,7 +23,7 @@ int decode_ctas_per_sm_q32(int k_bits, int v_bits, bool asym, int B) {
 
 cudaError_t launch_decode_q32(const DecodeArgs& a, cudaStream_t s) {
   const int kb = a.c.k_bits, vb = a.c.v_bits;
-  if (a.c.k_offsets) {
+  if (a.c.asym) {
     if (kb == 8 && vb == 8) return Kernel<8, 8, true, true>::launch(a, s);
     if (kb == 4 && vb == 4) return Kernel<4, 4, true, true>::launch(a, s);
     if (kb == 4 && vb == 8) return Kernel<4, 8, true, true>::launch(a, s);

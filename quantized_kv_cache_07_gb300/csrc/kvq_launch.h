@@ -14,10 +14,9 @@ struct CacheView {
   int k_bits, v_bits;
   uint8_t* k_codes;
   uint8_t* v_codes;
-  float* k_scales;
-  float* v_scales;
-  float* k_offsets;  // zero points, same layout as the scales; null: symmetric format
-  float* v_offsets;
+  float* meta;      // [H][num_blocks][meta_floats]: K scales, (K zero points,) V scales, (V zero points)
+  int asym;         // 1: scale and zero point per token (meta_floats 64), else 32
+  int meta_floats;
   const float* factor;  // [H][128] or null
   int window, window_batch;
   int q_bits;      // query format: 8 int8 rows (integer dot), 16 fp16, 32 fp16 hi + lo

@@ -130,7 +130,6 @@ class GpuRun:
     def pools(self):
         c = self.cache
         get = lambda t: None if t is None else t.cpu().numpy()
-        return dict(k_codes=get(c.k_codes), v_codes=get(c.v_codes), k_scales=get(c.k_scales),
-                    v_scales=get(c.v_scales), k_offsets=get(c.k_offsets), v_offsets=get(c.v_offsets),
+        return dict(k_codes=get(c.k_codes), v_codes=get(c.v_codes), meta=get(c.meta),
                     k_window=None if c.k_window is None else c.k_window.view(self.torch.uint8).cpu().numpy(),
                     v_window=None if c.v_window is None else c.v_window.view(self.torch.uint8).cpu().numpy())

@@ -67,6 +67,11 @@ def offsets_are_a_permutation(bits: int, is_key: bool) -> bool:
     return np.array_equal(np.sort(cells), np.arange(n))
 
 
-def scales_by_block(pool: np.ndarray, heads: int) -> np.ndarray:
-    """float [heads * num_blocks * 16] (head-major) -> [num_blocks, heads, 16]."""
-    return pool.reshape(heads, -1, BLOCK).transpose(1, 0, 2)
+def meta_by_block(pool: np.ndarray, heads: int, asym: bool = False) -> dict:
+    """Metadata pool float [heads * num_blocks * M] (head-major, M = 32, or 64
+    asymmetric) -> {"k_scale", "v_scale"(, "k_offset", "v_offset")} each
+    [num_blocks, heads, 16]: per block K scales, (K zero points,) V scales,
+    (V zero points)."""
+    parts = ("k_scale", "k_offset", "v_scale", "v_offset") if asym else ("k_scale", "v_scale")
+    rec = pool.reshape(heads, -1, len(parts), BLOCK).transpose(1, 0, 2, 3)
+    return {name: rec[:, :, i] for i, name in enumerate(parts)}

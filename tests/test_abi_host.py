@@ -73,25 +73,25 @@ def test_decode_plan_one_wave_of_ctas(lib):
 
 def _fake_desc(lib, **kw):
     d = dict(num_kv_heads=8, head_dim=128, block_size=16, num_blocks=4, k_bits=8, v_bits=8,
-             k_codes=0x1000, v_codes=0x2000, k_scales=0x3000, v_scales=0x4000)
+             k_codes=0x1000, v_codes=0x2000, meta=0x3000)
     d.update(kw)
     return lib.CacheDesc(**d)
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=64), 2), (dict(block_size=32), 2), (dict(k_bits=2), 2), (dict(k_bits=16, v_bits=8), 2),
-    (dict(k_codes=0x1004), 3), (dict(k_scales=None), 1), (dict(num_kv_heads=0), 1), (dict(window=256), 2),
+    (dict(k_codes=0x1004), 3), (dict(meta=None), 1), (dict(meta=0x3008), 3), (dict(num_kv_heads=0), 1),
+    (dict(window=256), 2),
     (dict(window=16), 1), (dict(window=24), 2),
     # zero points: both or neither, 16-byte aligned, only on quantized blocks
-    (dict(k_offsets=0xA000), 1), (dict(v_offsets=0xA000), 1), (dict(k_offsets=0xA000, v_offsets=0xB008), 3),
-    (dict(k_bits=16, v_bits=16, k_scales=None, v_scales=None, k_offsets=0xA000, v_offsets=0xB000), 2),
+    (dict(asym=2), 1), (dict(k_bits=16, v_bits=16, meta=None, asym=1), 2),
     # quantized query: 8 (or 0/16 for bf16), quantized blocks only, not factor + window together
-    (dict(q_bits=4), 2), (dict(q_bits=24), 2), (dict(k_bits=16, v_bits=16, k_scales=None, v_scales=None, q_bits=8), 2),
+    (dict(q_bits=4), 2), (dict(q_bits=24), 2), (dict(k_bits=16, v_bits=16, meta=None, q_bits=8), 2),
     (dict(q_bits=8, k_channel_factor=0xC000, window=16, window_batch=1, k_window=0xD000, v_window=0xE000), 2),
-    # per-channel key scales only: needs the factor, symmetric quantized keys; k_scales may be NULL
+    # per-channel key scales only: needs the factor and symmetric quantized keys
     (dict(k_per_channel=1), 1), (dict(k_per_channel=2, k_channel_factor=0xC000), 1),
-    (dict(k_per_channel=1, k_channel_factor=0xC000, k_offsets=0xA000, v_offsets=0xB000), 2),
-    (dict(k_per_channel=1, k_channel_factor=0xC000, k_scales=None, v_scales=None), 1),
+    (dict(k_per_channel=1, k_channel_factor=0xC000, asym=1), 2),
+    (dict(k_per_channel=1, k_channel_factor=0xC000, meta=None), 1),
 ])
 def test_host_validation_without_a_gpu(lib, kw, status):
     desc = _fake_desc(lib, **kw)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from harness import GpuRun, compare_outputs, oracle_decode, oracle_state, small_workload
-from layout_ref import scales_by_block, unpack_blocks
+from layout_ref import meta_by_block, unpack_blocks
 from oracle import kvq_oracle as O
 from synth import WORKLOADS, make_inputs
 
@@ -103,15 +103,16 @@ def check_stored_cache(inp, run, units=None, max_positions=None):
         else:
             np.testing.assert_array_equal(kc[phys, :, tok], st["k_codes"][pos])
             np.testing.assert_array_equal(vc[phys, :, tok], st["v_codes"][pos])
-            vs = scales_by_block(pools["v_scales"], w.kv_heads)[phys, :, tok]
+            md = meta_by_block(pools["meta"], w.kv_heads, w.asym)
+            vs = md["v_scale"][phys, :, tok]
             if not w.k_per_channel:
-                ks = scales_by_block(pools["k_scales"], w.kv_heads)[phys, :, tok]
+                ks = md["k_scale"][phys, :, tok]
                 np.testing.assert_array_equal(ks.view(np.uint32),
                                               st["k_scale"][pos].astype(np.float32).view(np.uint32))
             np.testing.assert_array_equal(vs.view(np.uint32), st["v_scale"][pos].astype(np.float32).view(np.uint32))
             if w.asym:
-                ko = scales_by_block(pools["k_offsets"], w.kv_heads)[phys, :, tok]
-                vo = scales_by_block(pools["v_offsets"], w.kv_heads)[phys, :, tok]
+                ko = md["k_offset"][phys, :, tok]
+                vo = md["v_offset"][phys, :, tok]
                 np.testing.assert_array_equal(ko.view(np.uint32),
                                               st["k_offset"][pos].astype(np.float32).view(np.uint32))
                 np.testing.assert_array_equal(vo.view(np.uint32),
@@ -316,8 +317,8 @@ def test_step_append_equals_bulk_fill():
     kc_b = unpack_blocks(a["k_codes"], 4, True, w.kv_heads)
     vc_s = unpack_blocks(step_cache.v_codes.cpu().numpy(), 4, False, w.kv_heads)
     vc_b = unpack_blocks(a["v_codes"], 4, False, w.kv_heads)
-    ks_s = scales_by_block(step_cache.k_scales.cpu().numpy(), w.kv_heads)
-    ks_b = scales_by_block(a["k_scales"], w.kv_heads)
+    ks_s = meta_by_block(step_cache.meta.cpu().numpy(), w.kv_heads)["k_scale"]
+    ks_b = meta_by_block(a["meta"], w.kv_heads)["k_scale"]
     for b in range(w.batch):
         for p in range(max(int(inp.lengths[b]) - w.window, 0)):
             ph, t = inp.block_table[b, p // 16], p % 16
