@@ -258,12 +258,21 @@ def test_two_part_query_removes_the_query_rounding_error():
     assert ratio[32] <= 1.0, ratio
 
 
+EDGE_FORMATS = {
+    "int8": {},
+    "asym_k4v8": dict(k_bits=4, v_bits=8, asym=True),
+    "qint8": dict(q_bits=8),
+    "kchan_int4_q32": dict(k_bits=4, v_bits=4, channel_factor=True, k_per_channel=True, q_bits=32),
+}
+
+
+@pytest.mark.parametrize("fmt", list(EDGE_FORMATS))
 @pytest.mark.parametrize("window", [0, 32])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
-def test_decode_edge_lengths(window, group):
+def test_decode_edge_lengths(window, group, fmt):
     lengths = np.array([0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 129], dtype=np.int32)
-    w = small_workload(f"edge_{window}_{group}", batch=len(lengths), q_heads=2 * group, kv_heads=2,
-                       seq_len=1, len_range=None, window=window)
+    w = small_workload(f"edge_{window}_{group}_{fmt}", batch=len(lengths), q_heads=2 * group, kv_heads=2,
+                       seq_len=1, len_range=None, window=window, **EDGE_FORMATS[fmt])
     inp = make_inputs(w)
     # replace the lengths (and the matching packed K/V rows) by the edge set
     rng = np.random.default_rng(3)
@@ -290,12 +299,19 @@ def test_decode_edge_lengths(window, group):
     assert run.err_bits() == 0
 
 
-def test_step_append_equals_bulk_fill():
+STEP_FORMATS = {
+    "int4_factor": dict(k_bits=4, v_bits=4, channel_factor=True),
+    "asym_int8": dict(k_bits=8, v_bits=8, asym=True),
+    "kchan_k4v8": dict(k_bits=4, v_bits=8, channel_factor=True, k_per_channel=True),
+}
+
+
+@pytest.mark.parametrize("fmt", list(STEP_FORMATS))
+def test_step_append_equals_bulk_fill(fmt):
     """Token-by-token window steps leave the same bytes as the bulk fill."""
     from quantized_kv_cache_07_gb300 import _lib
     from quantized_kv_cache_07_gb300.cache import cache_for_inputs
-    w = small_workload("step_vs_bulk", batch=3, len_range=(1, 90), window=32, k_bits=4, v_bits=4,
-                       channel_factor=True)
+    w = small_workload(f"step_vs_bulk_{fmt}", batch=3, len_range=(1, 90), window=32, **STEP_FORMATS[fmt])
     inp = make_inputs(w)
     bulk = GpuRun(inp)
     step_cache = cache_for_inputs(inp)
@@ -313,18 +329,21 @@ def test_step_append_equals_bulk_fill():
     for key in ("k_window", "v_window"):
         np.testing.assert_array_equal(getattr(step_cache, key).view(torch.uint8).cpu().numpy(), a[key])
     # block store: compare every position older than the window
-    kc_s = unpack_blocks(step_cache.k_codes.cpu().numpy(), 4, True, w.kv_heads)
-    kc_b = unpack_blocks(a["k_codes"], 4, True, w.kv_heads)
-    vc_s = unpack_blocks(step_cache.v_codes.cpu().numpy(), 4, False, w.kv_heads)
-    vc_b = unpack_blocks(a["v_codes"], 4, False, w.kv_heads)
-    ks_s = meta_by_block(step_cache.meta.cpu().numpy(), w.kv_heads)["k_scale"]
-    ks_b = meta_by_block(a["meta"], w.kv_heads)["k_scale"]
+    kc_s = unpack_blocks(step_cache.k_codes.cpu().numpy(), w.k_bits, True, w.kv_heads, w.asym)
+    kc_b = unpack_blocks(a["k_codes"], w.k_bits, True, w.kv_heads, w.asym)
+    vc_s = unpack_blocks(step_cache.v_codes.cpu().numpy(), w.v_bits, False, w.kv_heads, w.asym)
+    vc_b = unpack_blocks(a["v_codes"], w.v_bits, False, w.kv_heads, w.asym)
+    md_s = meta_by_block(step_cache.meta.cpu().numpy(), w.kv_heads, w.asym)
+    md_b = meta_by_block(a["meta"], w.kv_heads, w.asym)
     for b in range(w.batch):
         for p in range(max(int(inp.lengths[b]) - w.window, 0)):
             ph, t = inp.block_table[b, p // 16], p % 16
             np.testing.assert_array_equal(kc_s[ph, :, t], kc_b[ph, :, t])
             np.testing.assert_array_equal(vc_s[ph, :, t], vc_b[ph, :, t])
-            np.testing.assert_array_equal(ks_s[ph, :, t], ks_b[ph, :, t])
+            for key in md_b:
+                if key == "k_scale" and w.k_per_channel:
+                    continue  # not written under per-channel key scales
+                np.testing.assert_array_equal(md_s[key][ph, :, t], md_b[key][ph, :, t])
 
 
 def test_device_errors_are_flagged_not_trapped():
@@ -389,6 +408,9 @@ FULL["qint8_int4_factor_b32_len1k_8k"] = WORKLOADS["int4_factor_b32_len1k_8k"].w
 # per-channel key scales only on the int4 / factor shape
 FULL["kchan_int4_factor_b32_len1k_8k"] = WORKLOADS["int4_factor_b32_len1k_8k"].with_(
     name="kchan_int4_factor_b32_len1k_8k", k_per_channel=True)
+# the asymmetric format on the paged append-then-decode shape
+FULL["asym_paged_int8_b64_len2k_32k"] = WORKLOADS["paged_int8_b64_len2k_32k"].with_(
+    name="asym_paged_int8_b64_len2k_32k", asym=True)
 
 
 @pytest.mark.parametrize("name", list(FULL))

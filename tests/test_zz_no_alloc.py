@@ -24,7 +24,8 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
 
-@pytest.mark.parametrize("fmt", [dict(k_bits=8, v_bits=8, window=32), dict(k_bits=4, v_bits=8, q_heads=32)])
+@pytest.mark.parametrize("fmt", [dict(k_bits=8, v_bits=8, window=32), dict(k_bits=4, v_bits=8, q_heads=32),
+                                 dict(k_bits=4, v_bits=4, asym=True, q_bits=8)])
 def test_static_scratch_matches_workspace_decode_on_two_calls(fmt):
     kw = dict(batch=5, q_heads=16, kv_heads=4, len_range=(1, 400))
     kw.update(fmt)
