@@ -179,6 +179,10 @@ __device__ void write_block_store(const AppendArgs& a, bool is_key, int b, int p
 }
 
 __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  // Programmatic dependent launch: wait for the previous kernel on the stream
+  // (its writes visible) before touching memory; let the next one launch early.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long vec = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int H = a.c.H;
@@ -187,6 +191,9 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   const int kv = int((vec / H) % 2);
   const int h = int(vec % H);
   const bool is_key = kv == 0;
+  // the new vector does not depend on the destination: load it with the indices
+  const uint16_t* src = (is_key ? a.k_new : a.v_new) + (size_t(r) * H + h) * kHeadDim + 4 * lane;
+  const uint2 v_new = *reinterpret_cast<const uint2*>(src);
   const int b = a.seq_idx[r];
   const int p = a.pos[r];
   if (b < 0 || b >= a.batch || p < 0 ||
@@ -194,10 +201,9 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
     if (lane == 0) flag(a.err, KVQ_DEVERR_POSITION);
     return;
   }
-  const uint16_t* src = (is_key ? a.k_new : a.v_new) + (size_t(r) * H + h) * kHeadDim + 4 * lane;
   uint16_t xb[4];
   {
-    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    const uint2 v = v_new;
     xb[0] = uint16_t(v.x & 0xFFFF);
     xb[1] = uint16_t(v.x >> 16);
     xb[2] = uint16_t(v.y & 0xFFFF);
@@ -283,7 +289,20 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   if (vecs == 0) return cudaSuccess;
   const int warps = 8;
   const long long grid = (vecs + warps - 1) / warps;
-  append_kernel<<<unsigned(grid), warps * 32, 0, s>>>(a);
+  // launched with programmatic stream serialisation, so the launch overlaps the
+  // tail of the previous kernel (the kernel waits for it before reading memory)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(warps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, append_kernel, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
