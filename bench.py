@@ -45,9 +45,16 @@ def measured_peaks():
 
 
 def decode_kernel_hash() -> str:
+    """sha256[:12] of the default-path decode sources with comments and blank
+    lines removed (editing a comment does not invalidate a recorded capture)."""
+    import re
     h = hashlib.sha256()
     for f in ("kvq_decode_impl.cuh", "kvq_decode.cu", "kvq_device.cuh"):  # the default-path kernels
-        h.update(open(os.path.join(ROOT, "quantized_kv_cache_07_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "quantized_kv_cache_07_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+        h.update(src.encode())
     return h.hexdigest()[:12]
 
 

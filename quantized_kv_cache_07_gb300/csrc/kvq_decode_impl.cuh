@@ -34,22 +34,30 @@
 //     unit (atomic ticket, no spinning) merges its partials with a log-sum-exp
 //     reduce.  A unit held by a single CTA is normalised in place.
 //   * One producer warp streams whole 16-token blocks (codes of K and V plus
-//     their scales) with cp.async.bulk into a ring of shared-memory stages
-//     guarded by mbarriers; four consumer warps each take one block per stage.
+//     the block's metadata record of scales and zero points) with cp.async.bulk
+//     into a ring of shared-memory stages guarded by mbarriers, one copy per run
+//     of consecutive physical blocks; four consumer warps each take one block per
+//     stage (two for 4-bit keys).
+//   * Programmatic dependent launch: each CTA lets the next kernel on the stream
+//     launch at once and waits for the previous one before reading memory.
 //   * The GQA group (G <= 8 query heads sharing the KV head) makes the two small
 //     contractions dense: S^T = Kcodes . Q^T and O^T += V^T . (p*s_v)^T run on
 //     mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens/dims on M, the query
 //     group on N.  Codes are converted exactly to fp16 in registers; the cache
 //     is stored in the fragment order so every lane reads 16 contiguous bytes.
 //   * The query is scaled by an exact power of two into fp16's range; the score
-//     scale s_k * 2^-e * log2(e) / sqrt(D) is applied per score in fp32.
+//     scale s_k * 2^-e * log2(e) / sqrt(D) is applied per score in fp32.  Query
+//     formats: fp16 (default), fp16 high + low parts (LOQ instantiations, one
+//     more MMA per k-slice), or int8 codes with s_q in the score scale (the MMA
+//     then forms the integer dot product exactly: "KV Cache Quantization and
+//     Per-Token Scale Placement", section "Precision floors and mixed cache
+//     formats").
 #pragma once
 
 #include <cuda_runtime.h>
 
-#include <mutex>
 #include <map>
-#include <tuple>
+#include <mutex>
 
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
