@@ -165,8 +165,10 @@ kvq_status kvq_block_bytes(int32_t bits, size_t* bytes);
  * (stored as float32, RN), code = clamp(round_half_even(x / s)), all-zero
  * vector -> codes 0 and s = 1.  qmax = 127 (int8) or 7 (int4).  With a
  * per-channel key factor c, keys are first divided by c (float32, RN) and then
- * quantized per token ([P3] "The axis choice is a kernel decision").  Codes are
- * the correctly rounded quotient of the exact x / s.  With asym = 1 the
+ * quantized per token ([P3] "The axis choice is a kernel decision"); with
+ * k_per_channel = 1 a key's codes are clamp(round_half_even(k_j / c_j)) and no
+ * key scale is stored.  Codes are the correctly rounded quotient of the exact
+ * x / s.  With asym = 1 the
  * asymmetric quantizer of kvq_cache_desc is used instead and the zero point is
  * stored beside the scale.
  *   k_new, v_new : device bf16 [n][num_kv_heads][128]
