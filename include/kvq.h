@@ -130,7 +130,7 @@ typedef struct {
    * exponential).  0 or 16: the bf16 query, carried into the code contraction
    * as fp16 scaled by a power of two (11 significant bits; default).  32: the
    * same fp16 value plus an fp16 low part (about 22 significant bits, one more
-   * MMA per k-slice: 2-13 % more time), for scores large enough that 11 bits
+   * MMA per k-slice: 3-6 % more time measured), for scores large enough that 11 bits
    * of query cost more than the output tolerance.  8: each query row, after
    * the per-channel key factor is multiplied onto it in float32, is quantized
    * per row with the symmetric int8 rule of kvq_append (s_q = RN32(max|x| /
