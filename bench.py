@@ -8,7 +8,7 @@ identical cache replicas that the bytes cycled exceed 4x the L2 size (or the
 cache alone exceeds L2), so every step reads its cache from HBM.
 
 Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle
-(the reference arm of this build) on a bounded sample of the same workload.
+(the reference arm) on a bounded sample of the same workload.
 """
 from __future__ import annotations
 

@@ -79,7 +79,7 @@ def compare_outputs(inp, out, lse, ref, out_is_bf16: bool):
     return worst
 
 
-class GpuRun:
+class DeviceRun:
     """Build the cache of ``inp`` on the GPU with kvq_append and run kvq_decode."""
 
     def __init__(self, inp, device="cuda"):

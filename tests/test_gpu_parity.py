@@ -8,7 +8,7 @@ named workloads run at full size on sampled (sequence, kv head) units.
 import numpy as np
 import pytest
 
-from harness import GpuRun, compare_outputs, oracle_decode, oracle_state, small_workload
+from harness import DeviceRun, compare_outputs, oracle_decode, oracle_state, small_workload
 from layout_ref import meta_by_block, unpack_blocks
 from oracle import kvq_oracle as O
 from synth import WORKLOADS, make_inputs
@@ -74,7 +74,7 @@ def runs():
     def get(name):
         if name not in cache:
             inp = make_inputs(SMALL[name])
-            cache[name] = (inp, GpuRun(inp))
+            cache[name] = (inp, DeviceRun(inp))
         return cache[name]
     return get
 
@@ -247,7 +247,7 @@ def test_two_part_query_removes_the_query_rounding_error():
     lse_err, ratio = {}, {}
     for qb in (16, 32):
         inp = make_inputs(base.with_(name=f"kchan_q{qb}", q_bits=qb))
-        run = GpuRun(inp)
+        run = DeviceRun(inp)
         out, lse = run.decode(out_fp32=True)
         ref = oracle_decode(inp)
         G = inp.workload.group
@@ -290,7 +290,7 @@ def test_decode_edge_lengths(window, group, fmt):
         off += nb
     inp.block_table = table
     inp.num_blocks = off
-    run = GpuRun(inp)
+    run = DeviceRun(inp)
     for out_fp32 in (True, False):
         out, lse = run.decode(out_fp32=out_fp32)
         ref = oracle_decode(inp)
@@ -313,7 +313,7 @@ def test_step_append_equals_bulk_fill(fmt):
     from quantized_kv_cache_07_gb300.cache import cache_for_inputs
     w = small_workload(f"step_vs_bulk_{fmt}", batch=3, len_range=(1, 90), window=32, **STEP_FORMATS[fmt])
     inp = make_inputs(w)
-    bulk = GpuRun(inp)
+    bulk = DeviceRun(inp)
     step_cache = cache_for_inputs(inp)
     table = bulk.table
     for p in range(int(inp.lengths.max())):
@@ -348,7 +348,7 @@ def test_step_append_equals_bulk_fill(fmt):
 
 def test_device_errors_are_flagged_not_trapped():
     inp = make_inputs(small_workload("errs", batch=2, len_range=(40, 80)))
-    run = GpuRun(inp)
+    run = DeviceRun(inp)
     bad = run.table.clone()
     bad[1, 1] = inp.num_blocks + 5                 # block id out of range
     from quantized_kv_cache_07_gb300.cache import DecodeWorkspace
@@ -375,7 +375,7 @@ def test_device_errors_are_flagged_not_trapped():
 
 def test_host_validation_errors():
     inp = make_inputs(small_workload("val", batch=1, len_range=(10, 10)))
-    run = GpuRun(inp)
+    run = DeviceRun(inp)
     lib = run.lib
     w = inp.workload
     out = torch.zeros((1, w.q_heads, 128), dtype=torch.float32, device="cuda")
@@ -417,7 +417,7 @@ FULL["asym_paged_int8_b64_len2k_32k"] = WORKLOADS["paged_int8_b64_len2k_32k"].wi
 def test_full_size_workload(name):
     w = FULL[name]
     inp = make_inputs(w)
-    run = GpuRun(inp)
+    run = DeviceRun(inp)
     units = _sample_units(w, 6 if w.batch * w.kv_heads > 8 else 4)
     assert check_stored_cache(inp, run, units=units, max_positions=2048) > 0
     out, lse = run.decode(out_fp32=False)

@@ -14,7 +14,7 @@ first failure has already run every other test.
 import numpy as np
 import pytest
 
-from harness import TOL, GpuRun, small_workload
+from harness import TOL, DeviceRun, small_workload
 from synth import make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -30,7 +30,7 @@ def test_static_scratch_matches_workspace_decode_on_two_calls(fmt):
     kw = dict(batch=5, q_heads=16, kv_heads=4, len_range=(1, 400))
     kw.update(fmt)
     inp = make_inputs(small_workload("no_alloc", **kw))
-    run = GpuRun(inp)
+    run = DeviceRun(inp)
     lib = run.lib
     w = inp.workload
     ref, ref_lse = run.decode(out_fp32=True)
@@ -49,7 +49,7 @@ def test_static_scratch_matches_workspace_decode_on_two_calls(fmt):
 
 def test_static_scratch_refuses_plans_beyond_its_size():
     inp = make_inputs(small_workload("no_alloc_big", batch=2, len_range=(20, 40)))
-    run = GpuRun(inp)
+    run = DeviceRun(inp)
     lib = run.lib
     big_batch, q_heads = 4096, 8               # 8192 units: far more scratch than the fixed array holds
     plan = lib.kvq_decode_device_plan(run.cache.desc, big_batch, q_heads)
