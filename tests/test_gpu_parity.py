@@ -346,6 +346,23 @@ def test_step_append_equals_bulk_fill(fmt):
                 np.testing.assert_array_equal(md_s[key][ph, :, t], md_b[key][ph, :, t])
 
 
+def test_unit_channel_factor_gives_the_plain_result_bit_for_bit():
+    """A per-channel key factor of all ones divides and multiplies by one: the
+    stored codes and the decode output equal the run without a factor exactly."""
+    w = small_workload("unit_factor", batch=3, q_heads=16, kv_heads=2, k_bits=4, v_bits=8, len_range=(1, 300))
+    inp = make_inputs(w)
+    plain = DeviceRun(inp)
+    inp1 = make_inputs(w.with_(channel_factor=True))
+    inp1.channel_factor = np.ones_like(inp1.channel_factor)
+    unit = DeviceRun(inp1)
+    torch.cuda.synchronize()
+    assert np.array_equal(plain.pools()["k_codes"], unit.pools()["k_codes"])
+    o0, l0 = plain.decode(out_fp32=True)
+    o1, l1 = unit.decode(out_fp32=True)
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+
+
 def test_device_errors_are_flagged_not_trapped():
     inp = make_inputs(small_workload("errs", batch=2, len_range=(40, 80)))
     run = DeviceRun(inp)

@@ -640,3 +640,21 @@ def test_per_channel_sequence_reconstruction_and_bytes():
     assert O.cache_bytes_per_token_head(128, 8, 8, k_per_channel=True) == 128 + 128 + 4
     with pytest.raises(ValueError):
         O.quantize_sequence(k, v, 8, 8, c=None, k_per_channel=True)
+
+
+def test_unit_channel_factor_reduces_to_the_plain_path():
+    """c == 1 divides and multiplies by one: codes, scales, reconstruction and the
+    decode output equal the path without a factor exactly."""
+    rng = np.random.default_rng(13)
+    L, H, D = 33, 2, 128
+    k = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    v = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    qb = f32_to_bf16_bits(rng.standard_normal((2 * H, D)).astype(np.float32))
+    ones = np.ones((H, D))
+    for bits in (8, 4):
+        a = O.quantize_sequence(k, v, bits, 8, c=ones)
+        b = O.quantize_sequence(k, v, bits, 8)
+        assert np.array_equal(a["k_codes"], b["k_codes"]) and np.array_equal(a["k_scale"], b["k_scale"])
+        oa, la = O.decode_sequence(qb, a, H)
+        ob, lb = O.decode_sequence(qb, b, H)
+        assert np.array_equal(oa, ob) and np.array_equal(la, lb)
