@@ -1,0 +1,39 @@
+"""The bench's algorithmic bytes per step agree with the oracle's byte
+accounting (which is pinned to the metadata fractions and the cache-size
+formula the pages print), for every named workload and format variant."""
+import numpy as np
+import pytest
+
+import bench
+from oracle import kvq_oracle as O
+from synth import WORKLOADS, make_inputs
+
+VARIANTS = [dict(), dict(asym=True), dict(k_bits=16, v_bits=16, window=0, channel_factor=False)]
+
+
+def expected_bytes(inp) -> int:
+    w = inp.workload
+    per_q = O.cache_bytes_per_token_head(w.head_dim, w.k_bits, w.v_bits, asym=w.asym,
+                                         k_per_channel=w.k_per_channel)
+    total = 0
+    for L in inp.decode_lengths.astype(int):
+        lq = O.window_split(int(L), w.window)
+        total += per_q * lq + 2 * w.head_dim * 2 * (int(L) - lq)      # bf16 window tokens: K and V
+    return w.kv_heads * total
+
+
+@pytest.mark.parametrize("name", ["int8_b1_h4_t256", "gqa_int8_window128_b8_t4096"])
+@pytest.mark.parametrize("variant", range(len(VARIANTS)))
+def test_bench_bytes_match_oracle_accounting(name, variant):
+    w = WORKLOADS[name].with_(**VARIANTS[variant])
+    inp = make_inputs(w)
+    assert bench.cache_bytes_per_step(inp) == expected_bytes(inp)
+
+
+def test_bench_bytes_per_channel_keys_drop_the_key_scales():
+    w = WORKLOADS["int4_factor_b32_len1k_8k"].with_(k_per_channel=True)
+    inp = make_inputs(w)
+    base = make_inputs(WORKLOADS["int4_factor_b32_len1k_8k"])
+    tokens = int(np.sum(inp.decode_lengths)) * w.kv_heads
+    assert bench.cache_bytes_per_step(base) - bench.cache_bytes_per_step(inp) == 4 * tokens
+    assert bench.cache_bytes_per_step(inp) == expected_bytes(inp)
