@@ -390,6 +390,44 @@ def test_device_errors_are_flagged_not_trapped():
     assert compare_outputs(inp, o2, l2, oracle_decode(inp), out_is_bf16=False) <= 1.0
 
 
+def test_value_scale_beyond_fp16_weight_range_is_flagged():
+    """Value scales above 1023 would overflow the fp16 weights p * s_v: the
+    decode flags KVQ_DEVERR_RANGE instead of returning silently."""
+    from synth import f32_to_bf16_bits
+    inp = make_inputs(small_workload("range", batch=2, len_range=(40, 80)))
+    big = (O.bf16_to_f64(inp.v) * 2.0 ** 18).astype(np.float32)     # exact: a power of two
+    inp.v = f32_to_bf16_bits(big)
+    run = DeviceRun(inp)
+    assert run.err_bits() == 0                                       # appending is fine
+    run.decode(out_fp32=True)
+    assert run.err_bits() & run.lib.KVQ_DEVERR_RANGE
+
+
+def test_append_out_of_range_positions_are_flagged_and_skipped():
+    """A sequence index outside the batch or a position beyond the block
+    table's capacity sets KVQ_DEVERR_POSITION and writes nothing."""
+    inp = make_inputs(small_workload("pos", batch=2, len_range=(20, 40)))
+    run = DeviceRun(inp)
+    w = inp.workload
+    before = {k: v.copy() for k, v in run.pools().items() if v is not None}
+    kt = torch.from_numpy(inp.k[:2].view(np.int16)).cuda().view(torch.bfloat16)
+    vt = torch.from_numpy(inp.v[:2].view(np.int16)).cuda().view(torch.bfloat16)
+    for si, po in (([w.batch, 0], [5, 5]), ([0, 1], [inp.max_blocks * 16, inp.max_blocks * 16 + 3])):
+        run.err.zero_()
+        run.lib.kvq_append(run.cache.desc, kt, vt, torch.tensor(si, dtype=torch.int32, device="cuda"),
+                           torch.tensor(po, dtype=torch.int32, device="cuda"), run.lib.APPEND_QUANT, run.table,
+                           w.batch, inp.max_blocks, err_word=run.err)
+        assert run.err_bits() & run.lib.KVQ_DEVERR_POSITION
+    after = run.pools()
+    # the second call wrote nothing; the first wrote only sequence 0 (row 1): check sequence 1's blocks
+    for key in ("k_codes", "v_codes"):
+        assert after[key].shape == before[key].shape
+    kc_b = unpack_blocks(before["k_codes"], w.k_bits, True, w.kv_heads)
+    kc_a = unpack_blocks(after["k_codes"], w.k_bits, True, w.kv_heads)
+    ph1 = inp.block_table[1, : (int(inp.lengths[1]) + 15) // 16]
+    np.testing.assert_array_equal(kc_a[ph1], kc_b[ph1])
+
+
 def test_host_validation_errors():
     inp = make_inputs(small_workload("val", batch=1, len_range=(10, 10)))
     run = DeviceRun(inp)
