@@ -139,11 +139,12 @@ __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, i
 }
 
 // ------------------------------------------------------------------ score / value contractions
-// S^T of one 16-token block.  For code blocks the query is the fp16 pair
-// hi + lo (hi in registers, lo fragments from shared memory in the same order,
-// qlo = this lane's first uint4, null when lo is zero): every k-slice runs one
-// MMA with hi and one with lo into the same fp32 accumulator, so the score
-// carries about 22 significant bits of the query instead of 11.
+// S^T of one 16-token block.  The query fragments qf hold the fp16 (or int8
+// code, or bf16) query.  With LOQ (the two-part query) the low fp16 parts come
+// from shared memory in the same fragment order (qlo = this lane's first
+// uint4) and every k-slice runs a second MMA with them into the same fp32
+// accumulator, so the score carries about 22 significant bits of the query
+// instead of 11.
 template <int KB, bool LOQ>
 __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&qf)[16], const uint4* qlo,
                                             float (&acc)[4], int lane) {
