@@ -134,13 +134,15 @@ def test_quantizer_golden_worked_examples(golden_dir):
         assert list(map(int, c)) == [int(v) for v in codes.split(",")]
 
 
-def _page_listing_restated(vec, qmax):
-    """The page listing's semantics restated: float64 scale, Python round."""
-    amax = max(abs(float(v)) for v in vec)
-    if amax == 0.0:
-        return [0] * len(vec), 1.0
-    scale = amax / qmax
-    return [max(-qmax, min(qmax, round(float(v) / scale))) for v in vec], scale
+def _float64_scale_quantizer(vec, qmax):
+    """The rule of [P3] "The axis choice is a kernel decision" with the scale
+    kept in float64 (the page keeps it as a Python float) instead of the stored
+    float32: vectorised, half-to-even rounding of x / scale, clamp to +-qmax."""
+    x = np.asarray(vec, dtype=np.float64)
+    scale = float(np.abs(x).max()) / qmax
+    if scale == 0.0:
+        return np.zeros(x.shape, dtype=np.int64), 1.0
+    return np.clip(np.rint(x / scale), -qmax, qmax).astype(np.int64), scale
 
 
 def test_quantizer_agrees_with_page_listing_except_near_ties():
@@ -150,7 +152,7 @@ def test_quantizer_agrees_with_page_listing_except_near_ties():
     for _ in range(200):
         x = bf16_vec(128)
         codes, s = O.quantize(x, 8)
-        ref, scale64 = _page_listing_restated(x, 127)
+        ref, scale64 = _float64_scale_quantizer(x, 127)
         assert abs(float(s) - scale64) <= scale64 * 2.0 ** -24
         for xi, c, r in zip(x, codes, ref):
             frac = abs(xi / scale64) % 1.0
@@ -497,6 +499,72 @@ def test_asym_score_fold_is_exact_in_rationals():
     rhs = Fraction(float(s)) * sum(a * int(c) for a, c in zip(qf, u)) + Fraction(float(m)) * sum(qf)
     assert lhs == rhs
     assert abs(float(q @ O.dequantize_asym(u, s, m)) - float(lhs)) <= 1e-12 * max(1.0, abs(float(lhs)))
+
+
+def rn32_signed(r: Fraction) -> Fraction:
+    """Round a rational to binary32 (ties to even), either sign."""
+    if r == 0:
+        return Fraction(0)
+    return rn_float32(r) if r > 0 else -rn_float32(-r)
+
+
+def _check_asym_keys_under_channel_factor(bits):
+    """Asymmetric keys with a per-channel factor c ([P3] "The axis choice is a
+    kernel decision": the factor comes out of the keys and onto the query;
+    [P1] "Quantization granularity defines which values share a scale": scale
+    and zero point per token).  Exact reference: k'_j = RN32(k_j / c_j), the
+    asymmetric quantizer on k' in rationals, and k_hat_j = c_j * (u_j * s + m):
+    the factor multiplies the zero point as well as the scaled code.  The
+    oracle's float64 reconstruction must lie within a few roundings of it, and
+    the plausible slip of scaling only the code term (c_j * u_j * s + m) must
+    fall far outside that bound."""
+    rng = np.random.default_rng(21 + bits)
+    L, H, D = 7, 2, 128
+    k = O.bf16_to_f64(f32_to_bf16_bits((rng.standard_t(3, (L, H, D)) + 0.7).astype(np.float32)))
+    v = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    c = (np.abs(k).max(axis=0) * rng.uniform(0.5, 2.0, (H, D))).astype(np.float32).astype(np.float64)
+    st = O.quantize_sequence(k, v, bits, 8, c=c, asym=True)
+    slip_caught = 0
+    for h in range(H):
+        k_hat, _ = O.reconstruct_sequence(st, h)
+        for t in range(L):
+            kp = [rn32_signed(Fraction(float(k[t, h, j])) / Fraction(float(c[h, j]))) for j in range(D)]
+            u, s, m = exact_quantize_asym([float(x) for x in kp], bits)
+            assert list(map(int, st["k_codes"][t, h])) == u
+            assert Fraction(float(st["k_scale"][t, h])) == s and Fraction(float(st["k_offset"][t, h])) == m
+            for j in range(D):
+                cj = Fraction(float(c[h, j]))
+                ref = cj * (u[j] * s + m)
+                bound = 2.0 ** -50 * float(cj * (abs(u[j] * s) + abs(m)))
+                assert abs(k_hat[t, j] - float(ref)) <= bound
+                slip = float(cj * u[j] * s + m)
+                slip_caught += abs(slip - float(ref)) > 1e6 * bound
+    assert slip_caught > 0.9 * H * L * D
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_asym_keys_under_channel_factor_match_exact_rationals(bits):
+    _check_asym_keys_under_channel_factor(bits)
+
+
+def test_asym_factor_pin_catches_a_zero_point_left_unscaled(monkeypatch):
+    """Plant the slip in the oracle (the factor multiplies u * s but not m):
+    the exact-rational pin above must fail."""
+    real = O.reconstruct_sequence
+
+    def planted(st, head):
+        k_hat, v_hat = real(st, head)
+        if st.get("asym") and st["c"] is not None:
+            Lq = st["Lq"]
+            c = np.asarray(st["c"][head], np.float64)
+            m = np.asarray(st["k_offset"][:, head], np.float64)[:, None]
+            k_hat = k_hat.copy()
+            k_hat[:Lq] = k_hat[:Lq] - c * m + m
+        return k_hat, v_hat
+
+    monkeypatch.setattr(O, "reconstruct_sequence", planted)
+    with pytest.raises(AssertionError):
+        _check_asym_keys_under_channel_factor(8)
 
 
 def test_asym_metadata_fraction_is_the_printed_six_percent(golden_dir):
