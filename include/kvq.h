@@ -263,9 +263,11 @@ kvq_status kvq_decode(const kvq_cache_desc* cache, const void* q, int32_t batch,
  * all inputs and outputs.
  *   - A call whose plan (kvq_decode_device_plan) needs more than
  *     KVQ_STATIC_SCRATCH_BYTES returns KVQ_ERR_WORKSPACE and launches nothing.
- *   - The first call on each device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *   - The first call on each device does the set-up: it looks up the array's
+ *     device address (with that device current) and caches it with the CUDA
+ *     context it belongs to; make that first call before any stream capture.
+ *     A call under a different context (after cudaDeviceReset, for example)
+ *     repeats the set-up, which then also must not fall inside a capture.
  *   - Every call clears the merge counters with cudaMemsetAsync on `stream`
  *     (no allocation) and then runs kvq_decode on the shared array.
  *   - All calls on a device share the one array, which keeps the last call's

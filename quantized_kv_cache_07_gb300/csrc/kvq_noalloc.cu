@@ -3,6 +3,7 @@
 // merge counters) lives in one fixed file-scope device array instead of a
 // caller-provided workspace; nothing here calls cudaMalloc, cudaFree or any
 // allocating routine.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -18,23 +19,58 @@ static_assert(kStaticScratchBytes % 256 == 0, "scratch size must keep 256-byte a
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 // In host code g_decode_scratch names a host-side stand-in, not device memory:
-// the device address is looked up once per device (with that device current)
-// and cached here.
+// the device address is looked up at set-up, once per device, with that
+// device current, and cached here together with the CUDA context it belongs
+// to.  A later call under another context (after cudaDeviceReset, or once the
+// primary context has been torn down and recreated) repeats the set-up, so a
+// cached address never outlives the module instance it points into.
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+  CUcontext ctx;
+  void* addr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// cuCtxGetCurrent through the runtime's driver entry-point query (no link
+// against the driver library is needed); null if it cannot be resolved.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static const CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return CtxGetCurrentFn(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+kvq_status current_context(CUcontext* ctx) {
+  *ctx = nullptr;
+  const CtxGetCurrentFn fn = ctx_get_current();
+  if (fn && fn(ctx) != CUDA_SUCCESS) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
 
 kvq_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_UNSUPPORTED;
+  CUcontext ctx = nullptr;
+  if (current_context(&ctx) != KVQ_OK) return KVQ_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchEntry& e = g_scratch[dev];
+  if (!e.addr || !ctx || e.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    // the lookup binds the device's primary context if none was current
+    if (current_context(&ctx) != KVQ_OK) return KVQ_ERR_CUDA;
+    e.ctx = ctx;
+    e.addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = e.addr;
   return KVQ_OK;
 }
 

@@ -41,6 +41,27 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(declared_functions()) <= set(lib.SIGNATURES)
 
 
+def header_constants():
+    """Integer #define constants of include/kvq.h (u suffixes and shifts evaluated)."""
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    out = {}
+    for name, expr in re.findall(r"^#define\s+(KVQ_\w+)\s+(.+?)\s*(?:/\*.*)?$", src, flags=re.M):
+        expr = re.sub(r"(\d+)u\b", r"\1", expr)
+        if re.fullmatch(r"[\d\s()<>+*]+", expr):
+            out[name] = int(eval(expr))
+    return out
+
+
+def test_binding_constants_match_the_header(lib):
+    """The Python binding repeats a few numbers of include/kvq.h; they must not drift."""
+    h = header_constants()
+    assert lib.STATIC_SCRATCH_BYTES == h["KVQ_STATIC_SCRATCH_BYTES"]
+    for name in ("BLOCK_ID", "SEQ_LEN", "TIMEOUT", "RANGE", "POSITION"):
+        assert getattr(lib, "KVQ_DEVERR_" + name) == h["KVQ_DEVERR_" + name]
+    for name in ("QUANT", "RING", "STEP"):
+        assert getattr(lib, "APPEND_" + name) == h["KVQ_APPEND_" + name]
+
+
 def test_status_strings_and_block_bytes(lib):
     assert lib.status_string(0) == "KVQ_OK"
     assert "WORKSPACE" in lib.status_string(lib.KVQ_ERR_WORKSPACE)
