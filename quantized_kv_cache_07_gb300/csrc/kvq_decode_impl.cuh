@@ -144,10 +144,10 @@ __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, i
 // from shared memory in the same fragment order (qlo = this lane's first
 // uint4) and every k-slice runs a second MMA with them into the same fp32
 // accumulator, so the score carries about 22 significant bits of the query
-// instead of 11.
+// instead of 11.  km holds kMagicF16x2 for the 4-bit conversion (magic_f16x2).
 template <int KB, bool LOQ>
 __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&qf)[16], const uint4* qlo,
-                                            float (&acc)[4], int lane) {
+                                            float (&acc)[4], int lane, uint32_t km) {
   // two accumulators halve the dependent MMA chain; summed at the end
   float acc2[4] = {0.f, 0.f, 0.f, 0.f};
   const uint4* p = reinterpret_cast<const uint4*>(kb) + lane;
@@ -177,8 +177,8 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
       uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-      s4x8_to_f16(g0[wi], x0, x1, x2, x3);
-      s4x8_to_f16(g8[wi], y0, y1, y2, y3);
+      s4x8_to_f16(g0[wi], km, x0, x1, x2, x3);
+      s4x8_to_f16(g8[wi], km, y0, y1, y2, y3);
       mma_f16(acc, x0, y0, x1, y1, qf[4 * wi], qf[4 * wi + 1]);
       mma_f16(acc2, x2, y2, x3, y3, qf[4 * wi + 2], qf[4 * wi + 3]);
       if constexpr (LOQ) {
@@ -206,7 +206,7 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
 
 template <int VB>
 __device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint32_t b1, uint32_t b0lo,
-                                            uint32_t b1lo, float (&O)[8][4], int lane) {
+                                            uint32_t b1lo, float (&O)[8][4], int lane, uint32_t km) {
   const uint4* p = reinterpret_cast<const uint4*>(vb) + lane;
   if constexpr (VB == 8) {
 #pragma unroll
@@ -228,7 +228,7 @@ __device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t x0, x1, x2, x3;
-        s4x8_to_f16(w[k], x0, x1, x2, x3);
+        s4x8_to_f16(w[k], km, x0, x1, x2, x3);
         mma_f16(O[4 * h + k], x0, x2, x1, x3, b0, b1);
       }
     }
@@ -363,7 +363,7 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
                                                const float* const (&ko)[NB], const float* const (&vo)[NB],
                                                const int (&valid)[NB], const uint32_t (&qf)[16],
                                                const uint4* qlo, float qs0, float qs1, float qz0, float qz1,
-                                               WarpState& st, int lane, uint32_t* err) {
+                                               WarpState& st, int lane, uint32_t* err, uint32_t km) {
   constexpr bool kBf16 = (KB == 16);
   // offset-binary centre of the code conversion: c' = u - kKC
   constexpr float kKC = (KB == 8) ? 128.f : 8.f, kVC = (VB == 8) ? 128.f : 8.f;
@@ -374,7 +374,7 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
 #pragma unroll
   for (int j = 0; j < NB; ++j) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    score_block<KB, LOQ>(kb[j], qf, qlo, acc, lane);
+    score_block<KB, LOQ>(kb[j], qf, qlo, acc, lane, km);
     float sk0 = 1.f, sk1 = 1.f;
     sv[j][0] = sv[j][1] = 1.f;
     if constexpr (!kBf16) {
@@ -490,7 +490,7 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
       b0lo = (g & 1) ? q01 : q00;
       b1lo = (g & 1) ? q11 : q10;
     }
-    value_block<VB>(vb[j], b0, b1, b0lo, b1lo, st.O, lane);
+    value_block<VB>(vb[j], b0, b1, b0lo, b1lo, st.O, lane, km);
   }
 }
 
@@ -1026,7 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       const float* const nos[1] = {nullptr};
       const int val[1] = {min(kBlock, nw - j * kBlock)};
       process_blocks<16, 16, 1, false, false>(kbs, vbs, nos, nos, nos, nos, val, qf, nullptr, qs0, qs1, 0.f, 0.f, st, lane,
-                                       a.err);
+                                       a.err, 0u);
     }
     const size_t slot = size_t(P) + U + u;
     if (!finish_segment<false>(a, st, u, slot, len_s, geo, T, Pe, P, sc, cphase, warp, lane, tid))
@@ -1168,6 +1168,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   }
 
   // -------------------------------------------------------------- consumer warps
+  const uint32_t km = magic_f16x2(a.B);  // the int4 conversion's fp16 magic, in a register
   WarpState st;
   st.reset();
   uint32_t qf[16];
@@ -1249,7 +1250,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const float* const vos[2] = {vop(j0), vop(j1)};
         const int vals[2] = {val(j0), val(j1)};
         process_blocks<KB, VB, 2, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qs0, qs1, qz0, qz1, st, lane,
-                                        a.err);
+                                        a.err, km);
       } else {
         const uint8_t* const kbs[1] = {kp(j0)};
         const uint8_t* const vbs[1] = {vp(j0)};
@@ -1259,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const float* const vos[1] = {vop(j0)};
         const int vals[1] = {val(j0)};
         process_blocks<KB, VB, 1, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qs0, qs1, qz0, qz1, st, lane,
-                                        a.err);
+                                        a.err, km);
       }
     }
     __syncwarp();

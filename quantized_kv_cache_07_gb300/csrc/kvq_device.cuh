@@ -104,15 +104,28 @@ __device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
   asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
 }
 
+// The fp16 bit pattern of 1024.0 in both halves, the "magic" the int4 codes
+// are placed under.  Callers pass it in a register whose value the compiler
+// cannot see (magic_f16x2), so each nibble mask below is one three-input
+// logic instruction (w & mask) | magic instead of two: an instruction takes
+// one immediate operand, and the mask is it.
+constexpr uint32_t kMagicF16x2 = 0x64006400u;
+
+// kMagicF16x2 as a run-time value: the batch size is at most 4096 (checked on
+// the host), so b >> 16 is zero, but the compiler cannot fold it.
+__device__ __forceinline__ uint32_t magic_f16x2(int b) { return kMagicF16x2 | (uint32_t(b) >> 16); }
+
 // Eight int4 codes (biased nibbles n0..n7 of w) -> fp16 pairs (c0,c4) (c1,c5) (c2,c6) (c3,c7).
 // Odd nibbles land at 16 * u in the mantissa; a fused (x / 16 - 72) recovers c.
-__device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
+// km must hold kMagicF16x2 (see magic_f16x2).
+__device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t km, uint32_t& p0, uint32_t& p1, uint32_t& p2,
                                             uint32_t& p3) {
   const uint32_t s = w >> 8;
-  const uint32_t a = (w & 0x000F000Fu) | 0x64006400u;  // 1024 + u0, 1024 + u4
-  const uint32_t b = (w & 0x00F000F0u) | 0x64006400u;  // 1024 + 16 u1, 1024 + 16 u5
-  const uint32_t c = (s & 0x000F000Fu) | 0x64006400u;
-  const uint32_t d = (s & 0x00F000F0u) | 0x64006400u;
+  uint32_t a, b, c, d;  // lop3 table 0xEA: (x & mask) | km
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a) : "r"(w), "n"(0x000F000F), "r"(km));  // 1024 + u0, 1024 + u4
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(b) : "r"(w), "n"(0x00F000F0), "r"(km));  // 1024 + 16 u1, 1024 + 16 u5
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(c) : "r"(s), "n"(0x000F000F), "r"(km));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(s), "n"(0x00F000F0), "r"(km));
   const uint32_t bias = 0x64086408u;       // 1032 = 1024 + 8
   const uint32_t sixteenth = 0x2C002C00u;  // 1/16
   const uint32_t m72 = 0xD480D480u;        // -72 = -(1024/16 + 8)
