@@ -53,14 +53,24 @@ Readings taken where the pages leave a step open:
     kernel's precision, because it decides integer codes.  The score is
     s_q * s_k * (q_int . k_int) / sqrt(D); against bf16 window keys the query
     is q_int * s_q / c (q_int * s_q without a factor).
+  * 2-bit codes with token-group scales ([P3] "Per-token scales and where they
+    can live": at 2 bits a 4-byte per-token scale is 12 percent of the entry,
+    which is why 2-bit schemes group several tokens under one scale): the
+    symmetric rule with qmax = 2^(2-1) - 1 = 1 (codes in [-2, 1], -2 never
+    produced), applied to a group of up to 16 consecutive positions of one
+    head -- one 16-token cache block -- as if the group were one vector: one
+    scale from the absolute maximum over all its values.  The asymmetric rule
+    (u in [0, 3]) applies to the same groups when the cache is asymmetric.  The
+    last group of a sequence may be partial: it is quantized over the
+    positions it holds.
 Every function below is pinned by tests/test_oracle_pins.py.
 """
 from __future__ import annotations
 
 import numpy as np
 
-QMAX = {8: 127, 4: 7}
-CLAMP = {8: (-127, 127), 4: (-8, 7)}
+QMAX = {8: 127, 4: 7, 2: 1}
+CLAMP = {8: (-127, 127), 4: (-8, 7), 2: (-2, 1)}
 
 
 # ---------------------------------------------------------------- inputs
@@ -95,7 +105,7 @@ def quantize(x: np.ndarray, bits: int):
     return codes, s
 
 
-QMAXU = {8: 255, 4: 15}
+QMAXU = {8: 255, 4: 15, 2: 3}
 
 
 def quantize_asym(x: np.ndarray, bits: int):
@@ -121,6 +131,36 @@ def dequantize_asym(codes: np.ndarray, scale: np.ndarray, offset: np.ndarray) ->
     """x_hat = u * s + m, exact in float64."""
     return (np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[..., None]
             + np.asarray(offset, np.float64)[..., None])
+
+
+GROUP_TOKENS = 16
+
+
+def quantize_token_groups(x: np.ndarray, bits: int, asym: bool = False, group: int = GROUP_TOKENS):
+    """Quantize x [L, H, D] with one scale (and, asymmetric, one zero point) per
+    group of ``group`` consecutive positions of each head (see the module notes
+    on 2-bit codes).  Each group's values are quantized by the per-vector rule
+    (quantize / quantize_asym) applied to the group flattened into one vector.
+
+    Returns codes [L, H, D] and per-position scale [L, H] (and offset [L, H]),
+    the group's scale repeated for each of its positions.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    L, H, D = x.shape
+    codes = np.zeros((L, H, D), dtype=np.uint16 if asym else np.int16)
+    scale = np.zeros((L, H), dtype=np.float32)
+    offset = np.zeros((L, H), dtype=np.float32)
+    for g0 in range(0, L, group):
+        g1 = min(L, g0 + group)
+        flat = x[g0:g1].transpose(1, 0, 2).reshape(H, (g1 - g0) * D)      # one vector per head
+        if asym:
+            c, s, m = quantize_asym(flat, bits)
+            offset[g0:g1] = m[None, :]
+        else:
+            c, s = quantize(flat, bits)
+        codes[g0:g1] = c.reshape(H, g1 - g0, D).transpose(1, 0, 2)
+        scale[g0:g1] = s[None, :]
+    return (codes, scale, offset) if asym else (codes, scale)
 
 
 def dequantize(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
@@ -245,6 +285,19 @@ def quantize_sequence(k, v, k_bits: int, v_bits: int, window: int = 0, c=None, a
     st = {"Lq": Lq, "k_bits": k_bits, "v_bits": v_bits, "c": c, "asym": asym, "k_per_channel": k_per_channel}
     if k_per_channel and (c is None or asym or k_bits == 16):
         raise ValueError("per-channel-only key scales need c, symmetric codes and 8- or 4-bit keys")
+    if (k_bits == 2) != (v_bits == 2) or (k_bits == 2 and k_per_channel):
+        raise ValueError("2-bit codes come as K and V together, with token-group scales")
+    if k_bits == 2:
+        kx = k[:Lq] if c is None else divide_by_channel_factor(k[:Lq], c)
+        if asym:
+            st["k_codes"], st["k_scale"], st["k_offset"] = quantize_token_groups(kx, 2, asym=True)
+            st["v_codes"], st["v_scale"], st["v_offset"] = quantize_token_groups(v[:Lq], 2, asym=True)
+        else:
+            st["k_codes"], st["k_scale"] = quantize_token_groups(kx, 2)
+            st["v_codes"], st["v_scale"] = quantize_token_groups(v[:Lq], 2)
+        st["k_window"] = k[Lq:]
+        st["v_window"] = v[Lq:]
+        return st
     if k_bits == 16:
         st["k_plain"] = k[:Lq]
     elif k_per_channel:
@@ -325,10 +378,14 @@ def metadata_fraction(head_dim: int, bits: int, metadata_bytes: int) -> float:
 
 
 def cache_bytes_per_token_head(head_dim: int, k_bits: int, v_bits: int, scale_bytes: int = 4,
-                               asym: bool = False, k_per_channel: bool = False) -> int:
+                               asym: bool = False, k_per_channel: bool = False) -> float:
     """Bytes read per cached token per KV head: codes plus one scale (and, for
     the asymmetric format, one offset) for each of K and V (no metadata for a
-    16-bit cache, none for keys under per-channel scales only)."""
+    16-bit cache, none for keys under per-channel scales only).  2-bit codes
+    share their scales over a 16-token group, stored as one 16-byte record
+    (K scale, K offset, V scale, V offset) per group: one byte per token."""
+    if k_bits == 2:
+        return 2 * head_dim * 2 / 8 + 16 / GROUP_TOKENS
     meta = scale_bytes * (2 if asym else 1)
     kb = head_dim * k_bits // 8 + (0 if (k_bits == 16 or k_per_channel) else meta)
     vb = head_dim * v_bits // 8 + (0 if v_bits == 16 else meta)

@@ -47,8 +47,8 @@ def rn_float32(r: Fraction) -> Fraction:
 
 def exact_quantize(xs, bits):
     """Exact rational restatement of the page definition (float32 stored scale)."""
-    qmax = {8: 127, 4: 7}[bits]
-    lo, hi = {8: (-127, 127), 4: (-8, 7)}[bits]
+    qmax = {8: 127, 4: 7, 2: 1}[bits]
+    lo, hi = {8: (-127, 127), 4: (-8, 7), 2: (-2, 1)}[bits]
     fr = [Fraction(float(x)) for x in xs]
     amax = max(abs(f) for f in fr)
     if amax == 0:
@@ -443,7 +443,7 @@ def test_pins_catch_a_planted_missing_sqrt_d(monkeypatch):
 def exact_quantize_asym(xs, bits):
     """Exact rational restatement: offset = min, s = RN32((max - min)/qmaxu),
     u = clamp(RNE((x - min)/s), 0, qmaxu)."""
-    qmaxu = {8: 255, 4: 15}[bits]
+    qmaxu = {8: 255, 4: 15, 2: 3}[bits]
     fr = [Fraction(float(x)) for x in xs]
     lo, hi = min(fr), max(fr)
     if hi == lo:
@@ -726,3 +726,84 @@ def test_unit_channel_factor_reduces_to_the_plain_path():
         oa, la = O.decode_sequence(qb, a, H)
         ob, lb = O.decode_sequence(qb, b, H)
         assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+# ---------------------------------------------------------------- 2-bit codes with token-group scales
+def test_token_group_quantizer_matches_exact_rationals_per_group():
+    """Each 16-position group of each head is one vector for the rule: codes
+    and the one scale equal the exact rational quantizer applied to the
+    group's values (the last, partial group over the positions it holds)."""
+    rng = np.random.default_rng(31)
+    for trial in range(12):
+        L, H, D = int(rng.integers(1, 40)), 2, 24
+        x = O.bf16_to_f64(f32_to_bf16_bits((rng.standard_t(3, (L, H, D)) * 2.0 ** rng.integers(-6, 6))
+                                           .astype(np.float32)))
+        asym = trial % 2 == 1
+        res = O.quantize_token_groups(x, 2, asym=asym)
+        for g0 in range(0, L, 16):
+            g1 = min(L, g0 + 16)
+            for h in range(H):
+                flat = x[g0:g1, h].reshape(-1)
+                if asym:
+                    ref_c, ref_s, ref_m = exact_quantize_asym(flat, 2)
+                    assert np.all(res[2][g0:g1, h] == np.float32(float(ref_m)))
+                else:
+                    ref_c, ref_s = exact_quantize(flat, 2)
+                assert list(map(int, res[0][g0:g1, h].reshape(-1))) == ref_c
+                assert np.all(res[1][g0:g1, h] == np.float32(float(ref_s)))
+
+
+def test_token_group_quantizer_invariants_and_ternary_codes():
+    """Symmetric 2-bit: qmax = 1, so s = max|x| over the group, codes are in
+    {-1, 0, 1} (the clamp's -2 is unreachable), every non-zero group has a code
+    of magnitude 1, and |x - code * s| <= s / 2."""
+    rng = np.random.default_rng(32)
+    x = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((100, 3, 128)).astype(np.float32)))
+    codes, s = O.quantize_token_groups(x, 2)
+    assert set(np.unique(codes)) <= {-1, 0, 1}
+    xh = codes * s.astype(np.float64)[..., None]
+    assert np.all(np.abs(x - xh) <= s.astype(np.float64)[..., None] / 2)
+    for g0 in range(0, 100, 16):
+        for h in range(3):
+            grp = x[g0:g0 + 16, h]
+            assert float(s[g0, h]) == np.float32(np.abs(grp).max())
+            assert np.abs(codes[g0:g0 + 16, h]).max() == 1
+
+
+def test_token_groups_are_cache_blocks_and_a_single_token_group_is_the_per_token_rule():
+    """Groups are positions [16j, 16j + 16): a change inside group 1 leaves
+    group 0 untouched; a group of one position is the per-token quantizer."""
+    rng = np.random.default_rng(33)
+    x = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((40, 2, 128)).astype(np.float32)))
+    c0, s0 = O.quantize_token_groups(x, 2)
+    y = x.copy()
+    y[20, 1, 5] = 1000.0
+    c1, s1 = O.quantize_token_groups(y, 2)
+    assert np.array_equal(c0[:16], c1[:16]) and np.array_equal(s0[:16], s1[:16])
+    assert np.array_equal(c0[32:], c1[32:]) and float(s1[16, 1]) == 1000.0
+    one_c, one_s = O.quantize_token_groups(x[:1], 2)
+    ref_c, ref_s = O.quantize(x[0], 2)
+    assert np.array_equal(one_c[0], ref_c) and np.array_equal(one_s[0], ref_s)
+
+
+def test_two_bit_sequence_reconstruction_and_bytes():
+    """A 2-bit sequence: keys (after the per-channel factor) and values in
+    token groups, window positions kept in bf16; one 16-byte metadata record
+    per group makes the read 64 + 1 bytes per token per head, against the
+    4-byte per-token scale that would add the printed 12 percent."""
+    rng = np.random.default_rng(34)
+    L, H, D = 45, 2, 128
+    k = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    v = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    c = (np.abs(k).max(axis=0)).astype(np.float32).astype(np.float64)
+    st = O.quantize_sequence(k, v, 2, 2, window=16, c=c)
+    assert st["Lq"] == 29
+    kc, ks = O.quantize_token_groups(O.divide_by_channel_factor(k[:29], c), 2)
+    assert np.array_equal(st["k_codes"], kc) and np.array_equal(st["k_scale"], ks)
+    k_hat, v_hat = O.reconstruct_sequence(st, 1)
+    assert np.array_equal(k_hat[:29], kc[:, 1] * ks[:, 1, None].astype(np.float64) * c[1])
+    assert np.array_equal(k_hat[29:], k[29:, 1]) and np.array_equal(v_hat[29:], v[29:, 1])
+    assert O.cache_bytes_per_token_head(128, 2, 2) == 65
+    assert O.metadata_fraction(128, 2, 4) == 0.125               # the per-token cost it avoids
+    with pytest.raises(ValueError):
+        O.quantize_sequence(k, v, 2, 8)
