@@ -36,26 +36,35 @@
  *         int8 : chunk = 2*hi + (e >> 4), byte = e & 15
  *         int4 : chunk = hi, word = e >> 3, nibble = ((e & 7) >> 1) + 4*(e & 1)
  *         bf16 : chunk = 4*hi + (e >> 3), element = e & 7 (2 bytes each)
+ *         int2 : chunk = 0, word = e >> 3, field bit = 16*(e & 1) + 8*((e >> 2) & 1)
+ *                + 2*(hi + 2*((e & 3) >> 1))
  *     Values, element (token i, dim d):
  *         mt = d >> 4, r = d & 15, g = r & 7, hi = r >> 3,
  *         t = (i & 7) >> 1, j = 2*(i & 1) + (i >> 3)
  *         int8 : chunk = mt >> 1, word = 2*(mt & 1) + hi, byte j of the word
  *         int4 : chunk = mt >> 2, word = mt & 3, nibble = 2*hi + (j >> 1) + 4*(j & 1)
  *         bf16 : chunk = mt, word = 2*hi + (j >> 1), element j & 1 of the word
- *     Byte offset = chunk*512 + lane*16 + word*4 + (byte or nibble/2 or 2*element);
- *     for int8 keys "byte" is the offset inside the lane's 16 bytes.  Nibble n
- *     of a little-endian 32-bit word occupies bits 4n..4n+3.  Codes are stored
- *     offset-binary: an int8 code c in [-127,127] is the byte c + 128, an int4
- *     code c in [-8,7] (-8 never produced) is the nibble c + 8.  In the
- *     asymmetric format the unsigned code u (int8: 0..255, int4: 0..15) is
- *     stored as the byte or nibble u itself.
+ *         int2 : chunk = 0, word = mt >> 1, field bit = 16*(j & 1) + 8*(mt & 1)
+ *                + 2*(hi + 2*(j >> 1))
+ *     Byte offset = chunk*512 + lane*16 + word*4 + (byte or nibble/2 or 2*element
+ *     or field bit/8); for int8 keys "byte" is the offset inside the lane's 16
+ *     bytes.  Nibble n of a little-endian 32-bit word occupies bits 4n..4n+3; a
+ *     2-bit field at "field bit" b occupies bits b..b+1 of the word.  Codes are
+ *     stored offset-binary: an int8 code c in [-127,127] is the byte c + 128, an
+ *     int4 code c in [-8,7] (-8 never produced) is the nibble c + 8, an int2
+ *     code c in [-2,1] (-2 never produced) is the field c + 2.  In the
+ *     asymmetric format the unsigned code u (int8: 0..255, int4: 0..15, int2:
+ *     0..3) is stored as the byte, nibble or field u itself.
  *   Metadata pool: float [num_kv_heads][num_blocks][M], one record of M floats
  *                 per block (absent for a bf16 cache), tokens in natural order:
  *                 symmetric M = 32: the block's 16 key scales, then its 16
  *                 value scales; asymmetric M = 64: key scales, key zero points,
  *                 value scales, value zero points.  A block's record is one
  *                 128-byte (256-byte) read.  Keys under per-channel scales only
- *                 leave the key-scale entries unused.
+ *                 leave the key-scale entries unused.  2-bit blocks (token-group
+ *                 scales) M = 4: the block's key scale, key zero point, value
+ *                 scale, value zero point (zero points 0 when symmetric), one
+ *                 16-byte read.
  *   Window ring : bf16 [window_batch][num_kv_heads][window / 16][4096 bytes]:
  *                 window / 16 blocks per (sequence, head) for keys and for
  *                 values, each in the bf16 key / value block order above;
@@ -88,7 +97,8 @@ typedef enum {
 #define KVQ_DEVERR_BLOCK_ID 1u  /* block-table entry outside [0, num_blocks)        */
 #define KVQ_DEVERR_SEQ_LEN 2u   /* length < 0 or beyond the block table's capacity  */
 #define KVQ_DEVERR_TIMEOUT 4u   /* a pipeline wait gave up (the CTA skipped work)   */
-#define KVQ_DEVERR_RANGE 8u     /* a value scale above 1023 (fp16 weight range)     */
+#define KVQ_DEVERR_RANGE 8u     /* reserved: no longer raised (any value scale is   */
+                                /* decoded; the weights are kept in fp16 range)     */
 #define KVQ_DEVERR_POSITION 16u /* append: sequence index or position out of range  */
 
 /* kvq_append modes */
@@ -128,10 +138,13 @@ typedef struct {
    * mixed cache formats": an 8-bit query meets the integer key codes, the dot
    * product accumulates in integers and is converted to float before the
    * exponential).  0 or 16: the bf16 query, carried into the code contraction
-   * as fp16 scaled by a power of two (11 significant bits; default).  32: the
-   * same fp16 value plus an fp16 low part (about 22 significant bits, one more
-   * MMA per k-slice: 3-6 % more time measured), for scores large enough that 11 bits
-   * of query cost more than the output tolerance.  8: each query row, after
+   * as fp16 scaled by a power of two (11 significant bits), and the value
+   * weights p * s_v as fp16 (default).  32 (two-part mode): the query and the
+   * value weights each carried as an fp16 high part plus an fp16 low part
+   * (about 22 significant bits; one more MMA per k-slice of each contraction:
+   * 4-8 % more time measured), for scores large enough that 11 bits of query
+   * cost more than the output tolerance, and so that results do not depend on
+   * how the token range is split beyond fp32 rounding.  8: each query row, after
    * the per-channel key factor is multiplied onto it in float32, is quantized
    * per row with the symmetric int8 rule of kvq_append (s_q = RN32(max|x| /
    * 127), q_int = clamp(round_half_even(x / s_q))) and the score is
@@ -211,8 +224,14 @@ kvq_status kvq_decode_device_plan(const kvq_cache_desc* cache, int32_t batch, in
 kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t batch, int32_t q_heads,
                                      int32_t stream_ctas, size_t* bytes);
 
-/* Zero a decode workspace (its merge counters must start at zero; every
- * kvq_decode leaves them at zero again).  Call once after allocating it. */
+/* Zero a decode workspace.  Its merge counters (the first 4 * batch *
+ * num_kv_heads bytes) must start at zero; a kvq_decode that completes leaves
+ * them at zero again, including one that flagged KVQ_DEVERR_BLOCK_ID,
+ * KVQ_DEVERR_SEQ_LEN or KVQ_DEVERR_RANGE.  A call that flagged
+ * KVQ_DEVERR_TIMEOUT may leave counters of the units it gave up on non-zero:
+ * after that bit, call kvq_workspace_init again before the workspace's next
+ * kvq_decode (otherwise later merges would combine the wrong records).  Call it
+ * once after allocating the workspace. */
 kvq_status kvq_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /*
@@ -236,7 +255,8 @@ kvq_status kvq_workspace_init(void* workspace, size_t bytes, void* stream);
  *   lse        : device float [batch][q_heads] natural-log log-sum-exp of the
  *                scores, or NULL
  *   workspace  : device, >= kvq_decode_workspace_size bytes, zeroed once by
- *                kvq_workspace_init; one workspace per concurrently running call
+ *                kvq_workspace_init (again after a KVQ_DEVERR_TIMEOUT); one
+ *                workspace per concurrently running call
  *   stream_ctas: 0 = one wave on all SMs, > 0 = explicit count (tests)
  * Requirements: q_heads % num_kv_heads == 0, q_heads / num_kv_heads <= 8.
  */

@@ -43,9 +43,10 @@ class KVCache:
         self.k_per_channel = bool(k_per_channel)
         self.asym = bool(asym)
         if self.asym and not quant:
-            raise ValueError("the asymmetric format needs 8- or 4-bit blocks")
-        # metadata pool: per block K scales, (K zero points,) V scales, (V zero points)
-        self.meta_floats = (4 if self.asym else 2) * BLOCK_SIZE
+            raise ValueError("the asymmetric format needs 8-, 4- or 2-bit blocks")
+        # metadata pool: per block K scales, (K zero points,) V scales, (V zero
+        # points); 2-bit blocks: one K scale, K zero point, V scale, V zero point
+        self.meta_floats = 4 if k_bits == 2 else (4 if self.asym else 2) * BLOCK_SIZE
         self.meta = (torch.zeros(self.num_blocks * kv_heads * self.meta_floats, dtype=torch.float32, device=device)
                      if quant else None)
         self.channel_factor = None
@@ -68,8 +69,11 @@ class KVCache:
             v_window=self.v_window.data_ptr() if self.v_window is not None else None,
             q_bits=int(q_bits), k_per_channel=int(self.k_per_channel))
 
-    # bytes the decode reads per cached token per KV head (codes + scales + zero points)
-    def bytes_per_token_head(self) -> int:
+    # bytes the decode reads per cached token per KV head (codes + scales + zero
+    # points); 2-bit blocks share one 16-byte record per 16 tokens
+    def bytes_per_token_head(self) -> float:
+        if self.k_bits == 2:
+            return 2 * HEAD_DIM * 2 / 8 + 16 / BLOCK_SIZE
         meta = 8 if self.asym else 4
         kb = HEAD_DIM * self.k_bits // 8 + (0 if self.k_bits == 16 or self.k_per_channel else meta)
         vb = HEAD_DIM * self.v_bits // 8 + (0 if self.v_bits == 16 else meta)
@@ -99,7 +103,9 @@ def fill_from_inputs(cache: KVCache, inp, device="cuda", chunk_tokens: int = 1 <
 
     Positions older than the window are quantized into the block store
     (kvq_append QUANT); the last ``window`` positions go to the bf16 ring
-    (kvq_append RING).  Runs on the current stream; returns the device block
+    (kvq_append RING).  Calls are cut into chunks of about ``chunk_tokens``
+    rows (at 16-token block boundaries for 2-bit caches, whose blocks are
+    quantized whole).  Runs on the current stream; returns the device block
     table and cached lengths.
     """
     w = inp.workload
@@ -115,8 +121,13 @@ def fill_from_inputs(cache: KVCache, inp, device="cuda", chunk_tokens: int = 1 <
     else:
         row_ring = np.zeros(n_tok, dtype=bool)
     H = w.kv_heads
-    for r0 in range(0, n_tok, chunk_tokens):
+    r0 = 0
+    while r0 < n_tok:
         r1 = min(n_tok, r0 + chunk_tokens)
+        if w.k_bits == 2:
+            # 2-bit blocks are quantized whole: end the chunk at a block boundary
+            while r1 < n_tok and row_pos[r1] % BLOCK_SIZE != 0:
+                r1 += 1
         for mode, sel in ((_lib.APPEND_QUANT, ~row_ring[r0:r1]), (_lib.APPEND_RING, row_ring[r0:r1])):
             idx = np.nonzero(sel)[0] + r0
             if idx.size == 0:
@@ -130,6 +141,7 @@ def fill_from_inputs(cache: KVCache, inp, device="cuda", chunk_tokens: int = 1 <
             si = torch.from_numpy(row_seq[idx]).to(device)
             po = torch.from_numpy(row_pos[idx]).to(device)
             _lib.kvq_append(cache.desc, kt, vt, si, po, mode, table, w.batch, inp.max_blocks, err_word=err_word)
+        r0 = r1
     return table, torch.from_numpy(inp.lengths.astype(np.int32)).to(device)
 
 

@@ -19,7 +19,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool format_supported(int kb, int vb) {
   return (kb == 8 && vb == 8) || (kb == 4 && vb == 4) || (kb == 4 && vb == 8) || (kb == 8 && vb == 4) ||
-         (kb == 16 && vb == 16);
+         (kb == 2 && vb == 2) || (kb == 16 && vb == 16);
 }
 
 kvq_status check_cache(const kvq_cache_desc* c) {
@@ -33,7 +33,7 @@ kvq_status check_cache(const kvq_cache_desc* c) {
   if (c->asym != 0 && c->asym != 1) return KVQ_ERR_INVALID_ARG;
   if (c->k_per_channel != 0 && c->k_per_channel != 1) return KVQ_ERR_INVALID_ARG;
   if (c->asym && !quant) return KVQ_ERR_UNSUPPORTED;  // zero points only on quantized blocks
-  if (c->k_per_channel && (!quant || c->asym)) return KVQ_ERR_UNSUPPORTED;
+  if (c->k_per_channel && (!quant || c->asym || c->k_bits == 2)) return KVQ_ERR_UNSUPPORTED;
   if (c->k_per_channel && !c->k_channel_factor) return KVQ_ERR_INVALID_ARG;
   if (quant) {
     if (!c->meta) return KVQ_ERR_INVALID_ARG;
@@ -64,7 +64,7 @@ kvq::CacheView view(const kvq_cache_desc* c) {
   v.v_codes = static_cast<uint8_t*>(c->v_codes);
   v.meta = c->meta;
   v.asym = c->asym;
-  v.meta_floats = c->asym ? 64 : 32;
+  v.meta_floats = c->k_bits == 2 ? 4 : (c->asym ? 64 : 32);
   v.factor = c->k_channel_factor;
   v.window = c->window;
   v.window_batch = c->window_batch;
@@ -112,7 +112,7 @@ kvq_status check_decode_shape(const kvq_cache_desc* c, int batch, int q_heads) {
 namespace kvq {
 
 DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas) {
-  (void)Hq;
+  const int G = H > 0 ? Hq / H : 0;
   DecodeLayout L;
   L.stream_ctas = stream_ctas;
   L.units = B * H;
@@ -128,11 +128,11 @@ DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas) {
   L.off_counter = o;
   o = round_up(o + size_t(L.units) * 4, 256);
   L.off_m = o;
-  o = round_up(o + size_t(L.slots) * kMaxGroup * 4, 256);
+  o = round_up(o + size_t(L.slots) * G * 4, 256);
   L.off_l = o;
-  o = round_up(o + size_t(L.slots) * kMaxGroup * 4, 256);
+  o = round_up(o + size_t(L.slots) * G * 4, 256);
   L.off_o = o;
-  o = round_up(o + size_t(L.slots) * kMaxGroup * kHeadDim * 4, 256);
+  o = round_up(o + size_t(L.slots) * G * kHeadDim * 4, 256);
   L.total = o;
   return L;
 }
@@ -155,7 +155,7 @@ const char* kvq_status_string(kvq_status s) {
 
 kvq_status kvq_block_bytes(int32_t bits, size_t* bytes) {
   if (!bytes) return KVQ_ERR_INVALID_ARG;
-  if (bits != 4 && bits != 8 && bits != 16) return KVQ_ERR_UNSUPPORTED;
+  if (bits != 2 && bits != 4 && bits != 8 && bits != 16) return KVQ_ERR_UNSUPPORTED;
   *bytes = size_t(kvq::block_bytes(bits));
   return KVQ_OK;
 }
@@ -173,6 +173,9 @@ kvq_status kvq_append(const kvq_cache_desc* cache, const void* k_new, const void
     return KVQ_ERR_ALIGNMENT;
   if (batch < 1) return KVQ_ERR_INVALID_ARG;
   if (mode != KVQ_APPEND_QUANT && cache->window == 0) return KVQ_ERR_INVALID_ARG;
+  // 2-bit blocks are quantized whole (one scale per 16-token block): a decode
+  // step cannot evict a single token into one
+  if (mode == KVQ_APPEND_STEP && cache->k_bits == 2) return KVQ_ERR_UNSUPPORTED;
   if (mode != KVQ_APPEND_RING && (!block_table || max_blocks_per_seq < 1)) return KVQ_ERR_INVALID_ARG;
   if ((long long)n * 2 * cache->num_kv_heads > (1ll << 36)) return KVQ_ERR_UNSUPPORTED;
   kvq::AppendArgs a;

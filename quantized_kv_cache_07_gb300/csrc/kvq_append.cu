@@ -11,7 +11,13 @@
 // section "Quantization granularity defines which values share a scale" (a
 // scale and a zero point per group; here per token per head).
 //
-// One warp quantizes one 128-element vector; lane l owns dims 4l..4l+3.
+// 2-bit codes share one scale (and zero point) per 16-token block: "KV Cache
+// Quantization and Per-Token Scale Placement", section "Per-token scales and
+// where they can live" (at 2 bits, schemes group several tokens under one
+// scale).  A block is quantized as one vector of up to 16 x 128 values.
+//
+// One warp quantizes one 128-element vector (or one 2-bit token group); lane l
+// owns dims 4l..4l+3.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -238,6 +244,126 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   for (int j = 0; j < 4; ++j) *reinterpret_cast<uint16_t*>(ring + off[j]) = xb[j];
 }
 
+// 2-bit blocks: one warp per (group, head, K or V).  A group is the run of rows
+// of one call that fills positions 16j, 16j + 1, ... (up to 16) of one
+// sequence; the row at position 16j leads it.  A row whose position is not at
+// a block start and is not part of such a run is flagged and skipped: 2-bit
+// blocks are written whole, in one call.
+constexpr int kGroupWarps = 8;
+
+__global__ void __launch_bounds__(kGroupWarps * 32) append_group_kernel(AppendArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ uint32_t img[kGroupWarps][kBlock * kHeadDim * 2 / 32];  // one 512-byte block per warp
+  const int lane = threadIdx.x & 31, wslot = threadIdx.x >> 5;
+  const long long vec = (long long)blockIdx.x * kGroupWarps + wslot;
+  const int H = a.c.H;
+  if (vec >= (long long)a.n * 2 * H) return;
+  const int r = int(vec / (2 * H));
+  const bool is_key = ((vec / H) % 2) == 0;
+  const int h = int(vec % H);
+  const int b = a.seq_idx[r];
+  const int p = a.pos[r];
+  if (b < 0 || b >= a.batch || p < 0) {
+    if (lane == 0) flag(a.err, KVQ_DEVERR_POSITION);
+    return;
+  }
+  const int j = p % kBlock;
+  if (j != 0) {
+    // covered by the run led by row r - j?
+    bool covered = r - j >= 0;
+    for (int k = 0; covered && k < j; ++k) covered = a.seq_idx[r - j + k] == b && a.pos[r - j + k] == p - j + k;
+    if (!covered && lane == 0) flag(a.err, KVQ_DEVERR_POSITION);
+    return;
+  }
+  int m = 1;
+  while (m < kBlock && r + m < a.n && a.seq_idx[r + m] == b && a.pos[r + m] == p + m) ++m;
+  if (p + m > a.mbps * kBlock) {
+    if (lane == 0) flag(a.err, KVQ_DEVERR_POSITION);
+    return;
+  }
+  const int phys = a.table[size_t(b) * a.mbps + p / kBlock];
+  if (phys < 0 || phys >= a.c.num_blocks) {
+    if (lane == 0) flag(a.err, KVQ_DEVERR_BLOCK_ID);
+    return;
+  }
+  // the group's values, lane l holding dims 4l..4l+3 of each row
+  float x[kBlock][4];
+  const uint16_t* src = is_key ? a.k_new : a.v_new;
+#pragma unroll
+  for (int k = 0; k < kBlock; ++k) {
+    if (k < m) {
+      const uint2 v = *reinterpret_cast<const uint2*>(src + (size_t(r + k) * H + h) * kHeadDim + 4 * lane);
+      x[k][0] = __uint_as_float(v.x << 16);
+      x[k][1] = __uint_as_float(v.x & 0xFFFF0000u);
+      x[k][2] = __uint_as_float(v.y << 16);
+      x[k][3] = __uint_as_float(v.y & 0xFFFF0000u);
+      if (is_key && a.c.factor) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[k][e] = __fdiv_rn(x[k][e], a.c.factor[h * kHeadDim + 4 * lane + e]);
+      }
+    } else {
+      x[k][0] = x[k][1] = x[k][2] = x[k][3] = 0.f;
+    }
+  }
+  const bool asym = a.c.asym != 0;
+  float s = 1.f, zp = 0.f;
+  float lo = x[0][0], hi = x[0][0], am = 0.f;
+#pragma unroll
+  for (int k = 0; k < kBlock; ++k)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (k < m) {
+        lo = fminf(lo, x[k][e]);
+        hi = fmaxf(hi, x[k][e]);
+        am = fmaxf(am, fabsf(x[k][e]));
+      }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(kFull, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(kFull, hi, o));
+    am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
+  }
+  if (asym) {
+    // asymmetric rule over the group: m = min, s = RN32((max - min) / 3) (1 for
+    // a constant group), u = clamp(rint((x - m) / s), 0, 3), in double
+    const double rng = __dsub_rn(double(hi), double(lo));
+    s = rng == 0.0 ? 1.0f : __double2float_rn(__ddiv_rn(rng, 3.0));
+    zp = lo;
+  } else if (am > 0.f) {
+    s = am;  // RN32(amax / qmax) with qmax = 1
+  }
+  uint32_t* im = img[wslot];
+#pragma unroll
+  for (int i = lane; i < kBlock * kHeadDim * 2 / 32; i += 32) im[i] = 0u;
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < kBlock; ++k) {
+    if (k >= m) break;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int u;
+      if (asym) {
+        const double q = rint(__ddiv_rn(__dsub_rn(double(x[k][e]), double(lo)), double(s)));
+        u = q >= 3.0 ? 3 : (q > 0.0 ? int(q) : 0);
+      } else {
+        const float q = am > 0.f ? round_quotient(x[k][e], s) : 0.f;
+        u = int(fminf(1.f, fmaxf(-2.f, q))) + 2;  // offset binary
+      }
+      const Loc L = is_key ? key_loc(2, k, 4 * lane + e) : value_loc(2, k, 4 * lane + e);
+      atomicOr(&im[L.byte >> 2], uint32_t(u) << (8 * (L.byte & 3) + L.shift));
+    }
+  }
+  __syncwarp();
+  uint8_t* blk = (is_key ? a.c.k_codes : a.c.v_codes) + (size_t(h) * a.c.num_blocks + phys) * block_bytes(2);
+  reinterpret_cast<uint4*>(blk)[lane] = reinterpret_cast<const uint4*>(im)[lane];
+  if (lane == 0) {
+    float* rec = a.c.meta + (size_t(h) * a.c.num_blocks + phys) * a.c.meta_floats;
+    rec[is_key ? 0 : 2] = s;
+    rec[is_key ? 1 : 3] = zp;
+  }
+}
+
 __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
   const int lane = threadIdx.x & 31;
   const long long vec = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -259,13 +385,17 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
   float s = 1.0f, m = 0.0f;
   const bool asym = a.c.asym != 0;
   const bool chan = is_key && a.c.k_chan;  // per-channel key scale c_j instead of a per-token one
-  if (bits != 16 && !chan) {
+  if (bits == 2) {
+    const float* rec = a.c.meta + (size_t(h) * a.c.num_blocks + phys) * a.c.meta_floats;
+    s = rec[is_key ? 0 : 2];
+    m = rec[is_key ? 1 : 3];
+  } else if (bits != 16 && !chan) {
     const float* rec = a.c.meta + (size_t(h) * a.c.num_blocks + phys) * a.c.meta_floats;
     const int off = is_key ? 0 : a.c.meta_floats / 2;
     s = rec[off + tok];
     if (asym) m = rec[off + kBlock + tok];
   }
-  const int bias = asym ? 0 : (bits == 8 ? 128 : 8);
+  const int bias = asym ? 0 : (bits == 8 ? 128 : (bits == 4 ? 8 : 2));
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int d = 4 * lane + j;
@@ -274,7 +404,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
     if (bits == 16) {
       v = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(blk + L.byte));
     } else {
-      const int raw = bits == 8 ? int(blk[L.byte]) : int((blk[L.byte] >> L.shift) & 0xF);
+      const int raw = bits == 8 ? int(blk[L.byte]) : int((blk[L.byte] >> L.shift) & (bits == 4 ? 0xF : 0x3));
       const float sd = chan ? a.c.factor[h * kHeadDim + d] : s;
       v = asym ? __fmaf_rn(float(raw), s, m) : __fmul_rn(float(raw - bias), sd);
     }
@@ -287,7 +417,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantArgs a) {
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   const long long vecs = (long long)a.n * 2 * a.c.H;
   if (vecs == 0) return cudaSuccess;
-  const int warps = 8;
+  const bool group = a.c.k_bits == 2 && a.mode == KVQ_APPEND_QUANT;
+  const int warps = group ? kGroupWarps : 8;
   const long long grid = (vecs + warps - 1) / warps;
   // launched with programmatic stream serialisation, so the launch overlaps the
   // tail of the previous kernel (the kernel waits for it before reading memory)
@@ -301,7 +432,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, append_kernel, a);
+  const cudaError_t e = group ? cudaLaunchKernelEx(&cfg, append_group_kernel, a) : cudaLaunchKernelEx(&cfg, append_kernel, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -14,6 +14,7 @@ int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int q_bits, int B)
   if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, false, false>::ctas_per_sm(B);
   if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, false, false>::ctas_per_sm(B);
   if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, false, false>::ctas_per_sm(B);
+  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, false, false>::ctas_per_sm(B);
   if (k_bits == 16 && v_bits == 16) return Kernel<16, 16, false, false>::ctas_per_sm(B);
   return 0;
 }
@@ -26,6 +27,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (kb == 4 && vb == 4) return Kernel<4, 4, false, false>::launch(a, s);
   if (kb == 4 && vb == 8) return Kernel<4, 8, false, false>::launch(a, s);
   if (kb == 8 && vb == 4) return Kernel<8, 4, false, false>::launch(a, s);
+  if (kb == 2 && vb == 2) return Kernel<2, 2, false, false>::launch(a, s);
   if (kb == 16 && vb == 16) return Kernel<16, 16, false, false>::launch(a, s);
   return cudaErrorInvalidValue;
 }

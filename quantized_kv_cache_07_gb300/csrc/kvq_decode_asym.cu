@@ -10,6 +10,7 @@ int decode_ctas_per_sm_asym(int k_bits, int v_bits, int B) {
   if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, true, false>::ctas_per_sm(B);
   if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, true, false>::ctas_per_sm(B);
   if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, true, false>::ctas_per_sm(B);
+  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, true, false>::ctas_per_sm(B);
   return 0;
 }
 
@@ -19,6 +20,7 @@ cudaError_t launch_decode_asym(const DecodeArgs& a, cudaStream_t s) {
   if (kb == 4 && vb == 4) return Kernel<4, 4, true, false>::launch(a, s);
   if (kb == 4 && vb == 8) return Kernel<4, 8, true, false>::launch(a, s);
   if (kb == 8 && vb == 4) return Kernel<8, 4, true, false>::launch(a, s);
+  if (kb == 2 && vb == 2) return Kernel<2, 2, true, false>::launch(a, s);
   return cudaErrorInvalidValue;
 }
 

@@ -47,8 +47,9 @@
 //     is stored in the fragment order so every lane reads 16 contiguous bytes.
 //   * The query is scaled by an exact power of two into fp16's range; the score
 //     scale s_k * 2^-e * log2(e) / sqrt(D) is applied per score in fp32.  Query
-//     formats: fp16 (default), fp16 high + low parts (LOQ instantiations, one
-//     more MMA per k-slice), or int8 codes with s_q in the score scale (the MMA
+//     formats: fp16 (default), fp16 high + low parts for both the query and the
+//     value weights (LOQ instantiations, one more MMA per k-slice of either
+//     contraction), or int8 codes with s_q in the score scale (the MMA
 //     then forms the integer dot product exactly: "KV Cache Quantization and
 //     Per-Token Scale Placement", section "Precision floors and mixed cache
 //     formats").
@@ -78,15 +79,19 @@ template <int KB, int VB, bool ASYM>
 struct Fmt {
   static constexpr bool kBf16 = (KB == 16);
   static_assert(!(kBf16 && ASYM), "bf16 blocks carry no zero point");
+  // 2-bit blocks carry one scale (and zero point) per 16-token block for K and V
+  static constexpr bool kGroup = (KB == 2);
+  static_assert((KB == 2) == (VB == 2), "2-bit keys and values come together");
   static constexpr int kKBB = block_bytes(KB);
   static constexpr int kVBB = block_bytes(VB);
-  // metadata record per block: K scales, (K zero points,) V scales, (V zero points)
-  static constexpr int kMF = kBf16 ? 0 : (ASYM ? 4 : 2) * kBlock;  // floats
-  static constexpr int kMB = kMF * 4;                               // bytes
+  // metadata record per block: K scales, (K zero points,) V scales, (V zero
+  // points); 2-bit blocks: K scale, K zero point, V scale, V zero point
+  static constexpr int kMF = kBf16 ? 0 : (kGroup ? 4 : (ASYM ? 4 : 2) * kBlock);  // floats
+  static constexpr int kMB = kMF * 4;                                             // bytes
   static constexpr int kPerBlock = kKBB + kVBB + kMB;
-  // 4-bit keys: each consumer warp takes two blocks per stage (two independent
-  // dependency chains, one softmax reduction per 32 tokens)
-  static constexpr int kBPW = (KB == 4) ? 2 : 1;
+  // 4- and 2-bit keys: each consumer warp takes two blocks per stage (two
+  // independent dependency chains, one softmax reduction per 32 tokens)
+  static constexpr int kBPW = (KB == 4 || KB == 2) ? 2 : 1;
   static constexpr int kBlocksPerStage = kConsumerWarps * kBPW;
   static constexpr int kStageBytes = kBlocksPerStage * kPerBlock;
   // ~52 KB ring (56 KB with zero points, which keeps three 4-bit stages): 3 CTAs per SM
@@ -97,7 +102,8 @@ struct Fmt {
   static constexpr int kOffV = kBlocksPerStage * kKBB;
   static constexpr int kOffMeta = kOffV + kBlocksPerStage * kVBB;
   // float offsets inside a block's record
-  static constexpr int kKS = 0, kKO = kBlock, kVS = kMF / 2, kVO = kMF / 2 + kBlock;
+  static constexpr int kKS = 0, kKO = kGroup ? 1 : kBlock, kVS = kGroup ? 2 : kMF / 2;
+  static constexpr int kVO = kGroup ? 3 : kMF / 2 + kBlock;
 };
 
 // Shared-memory map after the stage ring (all offsets 16-byte aligned).
@@ -170,6 +176,22 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
         if constexpr (LOQ) mma_f16(ac, a0, a1, a2, a3, h ? lo.z : lo.x, h ? lo.w : lo.y);
       }
     }
+  } else if constexpr (KB == 2) {
+    // one 16-byte load: word w holds k-slices 2w (outputs 0-3) and 2w+1 (4-7)
+    const uint4 r = p[0];
+    const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t o[8];
+      s2x16_to_f16(wd[wi], km, o);
+      mma_f16(acc, o[0], o[1], o[2], o[3], qf[4 * wi], qf[4 * wi + 1]);
+      mma_f16(acc2, o[4], o[5], o[6], o[7], qf[4 * wi + 2], qf[4 * wi + 3]);
+      if constexpr (LOQ) {
+        const uint4 lo = qlo[wi * 32];
+        mma_f16(acc, o[0], o[1], o[2], o[3], lo.x, lo.y);
+        mma_f16(acc2, o[4], o[5], o[6], o[7], lo.z, lo.w);
+      }
+    }
   } else if constexpr (KB == 4) {
     const uint4 r0 = p[0], r1 = p[32];
     const uint32_t g0[4] = {r0.x, r0.y, r0.z, r0.w};
@@ -204,7 +226,11 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
   for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
 }
 
-template <int VB>
+// O^T += V^T . W^T for one 16-token block.  b0, b1 hold the fp16 (bf16 for
+// bf16 blocks) weights p * s_v; with LOW (the two-part mode of code blocks, and
+// always for bf16 blocks) b0lo, b1lo hold their low parts and a second MMA per
+// slice adds them, so the weights carry about 22 significant bits instead of 11.
+template <int VB, bool LOW>
 __device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint32_t b1, uint32_t b0lo,
                                             uint32_t b1lo, float (&O)[8][4], int lane, uint32_t km) {
   const uint4* p = reinterpret_cast<const uint4*>(vb) + lane;
@@ -216,9 +242,25 @@ __device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint
       s8x4_to_f16(c.x, a0, a2);
       s8x4_to_f16(c.y, a1, a3);
       mma_f16(O[2 * h], a0, a1, a2, a3, b0, b1);
+      if constexpr (LOW) mma_f16(O[2 * h], a0, a1, a2, a3, b0lo, b1lo);
       s8x4_to_f16(c.z, a0, a2);
       s8x4_to_f16(c.w, a1, a3);
       mma_f16(O[2 * h + 1], a0, a1, a2, a3, b0, b1);
+      if constexpr (LOW) mma_f16(O[2 * h + 1], a0, a1, a2, a3, b0lo, b1lo);
+    }
+  } else if constexpr (VB == 2) {
+    // one 16-byte load: word w holds m-tiles 2w (outputs 0-3) and 2w+1 (4-7)
+    const uint4 c = p[0];
+    const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t o[8];
+      s2x16_to_f16(wd[wi], km, o);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mma_f16(O[2 * wi + h], o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3], b0, b1);
+        if constexpr (LOW) mma_f16(O[2 * wi + h], o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3], b0lo, b1lo);
+      }
     }
   } else if constexpr (VB == 4) {
 #pragma unroll
@@ -230,6 +272,7 @@ __device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint
         uint32_t x0, x1, x2, x3;
         s4x8_to_f16(w[k], km, x0, x1, x2, x3);
         mma_f16(O[4 * h + k], x0, x2, x1, x3, b0, b1);
+        if constexpr (LOW) mma_f16(O[4 * h + k], x0, x2, x1, x3, b0lo, b1lo);
       }
     }
   } else {
@@ -279,18 +322,30 @@ __device__ __forceinline__ void locate_unit(const Geo& g, long long x, int& b, i
   h = int((x - (long long)g.H * g.vpre[b]) / geo_vlen(g, b));
 }
 
-// Base-2 exponential: the PTX ex2.approx.f32 instruction (max relative error
-// about 2^-22 per the PTX ISA; ex2(-inf) = +0, subnormal results kept).
+// Base-2 exponential: the PTX ex2.approx.ftz.f32 instruction (max relative
+// error about 2^-22 per the PTX ISA; ex2(-inf) = +0).  Results below 2^-126
+// flush to zero: a weight that small is below fp32 resolution of the sum l,
+// which holds at least one weight of 2^sigma >= 1.
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// Slack of the lazy running maximum (log2 units) and the largest value scale
-// whose fp16 weight p * s_v (p <= 2^kMaxSlack) stays below 65504.
+// Slack of the lazy running maximum (log2 units).  The softmax weights are
+// p = 2^(x - m + sigma) with a warp-uniform power-of-two offset sigma (the same
+// factor scales l and O, so it cancels in o = O / l), chosen so that the fp16
+// value weights p * s_v <= 2^(kMaxSlack + sigma) * s_v stay at or below
+// 2^kWeightExp: in fp16's normal range with room to spare, so they carry their
+// full 11 (two-part: 22) significant bits instead of falling into subnormals.
+// sigma starts at kSigma0, which allows value scales up to 2^-11, and steps
+// down, with an exact power-of-two rescale of l and O, whenever a block brings
+// a larger value scale: the first block of a segment sets it from its own
+// scales, so small and large values alike keep their weights in range.  l
+// stays below 2^(kSigma0 + kMaxSlack) per token, far inside fp32.
 constexpr float kMaxSlack = 6.f;
-constexpr float kMaxValueScale = 1023.f;
+constexpr int kWeightExp = 15;
+constexpr int kSigma0 = 20;
 
 // A stream CTA owns at least this many blocks (fewer, deeper splits for tiny problems).
 constexpr int kMinBlocksPerCta = 16;
@@ -337,14 +392,20 @@ __device__ __forceinline__ void unit_segments(const DecodeArgs& a, const int* le
 }
 
 // Online-softmax state of one consumer warp; each thread holds queries 2t, 2t+1.
+// l and O are in units of 2^(m - sg): the exponent base of the weights is
+// m - sg (sg = sigma, warp-uniform), which finish_segment records.
 struct WarpState {
   float O[8][4];
   float m0, m1, l0, l1;
   float z0, z1;  // asymmetric values: sum of p * m'_v of this thread's tokens
+  float sg;      // sigma (an integer)
+  float svlim;   // 2^(kWeightExp - kMaxSlack - sigma): the largest value scale sigma allows
   __device__ __forceinline__ void reset() {
     m0 = m1 = kNegInf;
     l0 = l1 = 0.f;
     z0 = z1 = 0.f;
+    sg = float(kSigma0);
+    svlim = ldexpf(1.f, kWeightExp - int(kMaxSlack) - kSigma0);  // 2^-11
 #pragma unroll
     for (int i = 0; i < 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
   }
@@ -363,10 +424,12 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
                                                const float* const (&ko)[NB], const float* const (&vo)[NB],
                                                const int (&valid)[NB], const uint32_t (&qf)[16],
                                                const uint4* qlo, float qs0, float qs1, float qz0, float qz1,
-                                               WarpState& st, int lane, uint32_t* err, uint32_t km) {
+                                               WarpState& st, int lane, uint32_t km) {
   constexpr bool kBf16 = (KB == 16);
   // offset-binary centre of the code conversion: c' = u - kKC
-  constexpr float kKC = (KB == 8) ? 128.f : 8.f, kVC = (VB == 8) ? 128.f : 8.f;
+  constexpr float kKC = (KB == 8) ? 128.f : (KB == 4 ? 8.f : 2.f), kVC = (VB == 8) ? 128.f : (VB == 4 ? 8.f : 2.f);
+  // token g's (and g + 8's) entry of a per-token record; 2-bit blocks hold one per block
+  constexpr bool kGroup = (KB == 2);
   const int g = lane >> 2, t = lane & 3;
   float x[NB][4];
   float sv[NB][2];
@@ -377,16 +440,17 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
     score_block<KB, LOQ>(kb[j], qf, qlo, acc, lane, km);
     float sk0 = 1.f, sk1 = 1.f;
     sv[j][0] = sv[j][1] = 1.f;
+    const int i0 = kGroup ? 0 : g, i1 = kGroup ? 0 : g + 8;
     if constexpr (!kBf16) {
-      sk0 = ks[j][g];  // per-channel key scales only: the ring holds 1.0 here (never copied over)
-      sk1 = ks[j][g + 8];
-      sv[j][0] = vs[j][g];
-      sv[j][1] = vs[j][g + 8];
+      sk0 = ks[j][i0];  // per-channel key scales only: the ring holds 1.0 here (never copied over)
+      sk1 = ks[j][i1];
+      sv[j][0] = vs[j][i0];
+      sv[j][1] = vs[j][i1];
     }
     if constexpr (ASYM) {
-      const float mk0 = fmaf(kKC, sk0, ko[j][g]), mk1 = fmaf(kKC, sk1, ko[j][g + 8]);
-      mv[j][0] = fmaf(kVC, sv[j][0], vo[j][g]);
-      mv[j][1] = fmaf(kVC, sv[j][1], vo[j][g + 8]);
+      const float mk0 = fmaf(kKC, sk0, ko[j][i0]), mk1 = fmaf(kKC, sk1, ko[j][i1]);
+      mv[j][0] = fmaf(kVC, sv[j][0], vo[j][i0]);
+      mv[j][1] = fmaf(kVC, sv[j][1], vo[j][i1]);
       x[j][0] = fmaf(acc[0], sk0, mk0 * qz0) * qs0;  // token g, query 2t
       x[j][1] = fmaf(acc[1], sk0, mk0 * qz1) * qs1;  // token g, query 2t+1
       x[j][2] = fmaf(acc[2], sk1, mk1 * qz0) * qs0;  // token g+8, query 2t
@@ -439,7 +503,41 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
     st.m0 = mn0;
     st.m1 = mn1;
   }
-  const float base0 = (st.m0 == kNegInf) ? 0.f : st.m0, base1 = (st.m1 == kNegInf) ? 0.f : st.m1;
+  if constexpr (!kBf16) {
+    // the largest value scale of this call's tokens (empty slots of a partial
+    // block are not data); a larger one than sigma allows lowers sigma
+    float svm = 0.f;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const bool v0 = valid[j] >= kBlock || g < valid[j], v1 = valid[j] >= kBlock || g + 8 < valid[j];
+      svm = fmaxf(svm, fmaxf(v0 ? sv[j][0] : 0.f, v1 ? sv[j][1] : 0.f));
+    }
+    if (__any_sync(kFull, svm > st.svlim)) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) svm = fmaxf(svm, __shfl_xor_sync(kFull, svm, o));
+      int e;
+      frexpf(svm, &e);  // svm < 2^e
+      const int sg_new = min(int(st.sg), kWeightExp - int(kMaxSlack) - e);
+      const float f = ldexpf(1.f, sg_new - int(st.sg));  // exact power of two
+      st.l0 *= f;
+      st.l1 *= f;
+      if constexpr (ASYM) {
+        st.z0 *= f;
+        st.z1 *= f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        st.O[i][0] *= f;
+        st.O[i][1] *= f;
+        st.O[i][2] *= f;
+        st.O[i][3] *= f;
+      }
+      st.sg = float(sg_new);
+      st.svlim = ldexpf(1.f, kWeightExp - int(kMaxSlack) - sg_new);
+    }
+  }
+  const float base0 = (st.m0 == kNegInf) ? 0.f : st.m0 - st.sg;
+  const float base1 = (st.m1 == kNegInf) ? 0.f : st.m1 - st.sg;
   const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
 #pragma unroll
   for (int j = 0; j < NB; ++j) {
@@ -455,16 +553,14 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
       pk0lo = pack_bf162(p00 - __low2float(h0), p10 - __high2float(h0));
       pk1lo = pack_bf162(p01 - __low2float(h1), p11 - __high2float(h1));
     } else {
-      // weights are at most 2^kMaxSlack, so p * s_v stays finite in fp16 while s_v <= kMaxValueScale
+      // weights are at most 2^(kMaxSlack + sigma) and s_v <= svlim: p * s_v <= 2^kWeightExp
       float w00 = p00 * sv[j][0], w10 = p10 * sv[j][1], w01 = p01 * sv[j][0], w11 = p11 * sv[j][1];
-      float svmax = fmaxf(sv[j][0], sv[j][1]);
       if (valid[j] < kBlock) {  // scales of empty slots of a partial block are not data
         const bool v0 = g < valid[j], v1 = g + 8 < valid[j];
         w00 = v0 ? w00 : 0.f;
         w01 = v0 ? w01 : 0.f;
         w10 = v1 ? w10 : 0.f;
         w11 = v1 ? w11 : 0.f;
-        svmax = fmaxf(v0 ? sv[j][0] : 0.f, v1 ? sv[j][1] : 0.f);
         if constexpr (ASYM) {
           mv[j][0] = v0 ? mv[j][0] : 0.f;
           mv[j][1] = v1 ? mv[j][1] : 0.f;
@@ -474,9 +570,14 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
         st.z0 = fmaf(p00, mv[j][0], fmaf(p10, mv[j][1], st.z0));
         st.z1 = fmaf(p01, mv[j][0], fmaf(p11, mv[j][1], st.z1));
       }
-      if (svmax > kMaxValueScale) flag(err, KVQ_DEVERR_RANGE);
       pk0 = pack_half2(w00, w10);
       pk1 = pack_half2(w01, w11);
+      if constexpr (LOQ) {  // two-part mode: the fp16 low parts w - hi (exact in fp32)
+        const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&pk0));
+        const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&pk1));
+        pk0lo = pack_half2(w00 - h0.x, w10 - h0.y);
+        pk1lo = pack_half2(w01 - h1.x, w11 - h1.y);
+      }
     }
     // transpose the weights from the score accumulator layout (token rows,
     // query columns) into the B-operand layout of the value contraction
@@ -484,13 +585,13 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
     const uint32_t r10 = __shfl_sync(kFull, pk0, src1), r11 = __shfl_sync(kFull, pk1, src1);
     const uint32_t b0 = (g & 1) ? r01 : r00, b1 = (g & 1) ? r11 : r10;
     uint32_t b0lo = 0, b1lo = 0;
-    if constexpr (kBf16) {
+    if constexpr (kBf16 || LOQ) {
       const uint32_t q00 = __shfl_sync(kFull, pk0lo, src0), q01 = __shfl_sync(kFull, pk1lo, src0);
       const uint32_t q10 = __shfl_sync(kFull, pk0lo, src1), q11 = __shfl_sync(kFull, pk1lo, src1);
       b0lo = (g & 1) ? q01 : q00;
       b1lo = (g & 1) ? q11 : q10;
     }
-    value_block<VB>(vb[j], b0, b1, b0lo, b1lo, st.O, lane, km);
+    value_block<VB, kBf16 || LOQ>(vb[j], b0, b1, b0lo, b1lo, st.O, lane, km);
   }
 }
 
@@ -738,9 +839,9 @@ __device__ __noinline__ void merge_unit(const DecodeArgs& a, int u, long long c0
         if (j < cnt) {
           const int r = base + j;
           const size_t slot = r < ns ? size_t(c0 + r + u) : wslot;
-          mr[j] = __ldcg(pm + slot * kMaxGroup + q);
-          lr[j] = __ldcg(pl + slot * kMaxGroup + q);
-          orr[j] = __ldcg(reinterpret_cast<const float4*>(po + (slot * kMaxGroup + q) * kHeadDim) + d4);
+          mr[j] = __ldcg(pm + slot * G + q);
+          lr[j] = __ldcg(pl + slot * G + q);
+          orr[j] = __ldcg(reinterpret_cast<const float4*>(po + (slot * G + q) * kHeadDim) + d4);
         } else {
           mr[j] = kNegInf;
           lr[j] = 0.f;
@@ -812,8 +913,9 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
     }
   }
   if (g == 0) {
-    sc.merge_m[warp * kMaxGroup + 2 * t] = st.m0;
-    sc.merge_m[warp * kMaxGroup + 2 * t + 1] = st.m1;
+    // the exponent base of l and O (m - sigma; -inf stays -inf)
+    sc.merge_m[warp * kMaxGroup + 2 * t] = st.m0 - st.sg;
+    sc.merge_m[warp * kMaxGroup + 2 * t + 1] = st.m1 - st.sg;
     sc.merge_l[warp * kMaxGroup + 2 * t] = st.l0;
     sc.merge_l[warp * kMaxGroup + 2 * t + 1] = st.l1;
   }
@@ -856,10 +958,10 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
       if (nseg == 1) {
         write_out(a, b, h * G + q, d, o, l, M);
       } else {
-        po[(slot * kMaxGroup + q) * kHeadDim + d] = o;
+        po[(slot * G + q) * kHeadDim + d] = o;
         if (d == 0) {
-          pm[slot * kMaxGroup + q] = M;
-          pl[slot * kMaxGroup + q] = l;
+          pm[slot * G + q] = M;
+          pl[slot * G + q] = l;
         }
       }
     }
@@ -934,7 +1036,8 @@ __device__ __forceinline__ void scan_geometry(const DecodeArgs& a, int B, int W,
   __syncthreads();
 }
 
-// LOQ: the two-part fp16 query (q_bits 32) of code blocks.
+// LOQ: the two-part mode (q_bits 32) of code blocks: the query and the value
+// weights p * s_v each carried as fp16 high + low parts.
 template <int KB, int VB, bool ASYM, bool LOQ>
 __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   using F = Fmt<KB, VB, ASYM>;
@@ -1026,7 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       const float* const nos[1] = {nullptr};
       const int val[1] = {min(kBlock, nw - j * kBlock)};
       process_blocks<16, 16, 1, false, false>(kbs, vbs, nos, nos, nos, nos, val, qf, nullptr, qs0, qs1, 0.f, 0.f, st, lane,
-                                       a.err, 0u);
+                                       0u);
     }
     const size_t slot = size_t(P) + U + u;
     if (!finish_segment<false>(a, st, u, slot, len_s, geo, T, Pe, P, sc, cphase, warp, lane, tid))
@@ -1250,7 +1353,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const float* const vos[2] = {vop(j0), vop(j1)};
         const int vals[2] = {val(j0), val(j1)};
         process_blocks<KB, VB, 2, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qs0, qs1, qz0, qz1, st, lane,
-                                        a.err, km);
+                                        km);
       } else {
         const uint8_t* const kbs[1] = {kp(j0)};
         const uint8_t* const vbs[1] = {vp(j0)};
@@ -1260,7 +1363,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const float* const vos[1] = {vop(j0)};
         const int vals[1] = {val(j0)};
         process_blocks<KB, VB, 1, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qs0, qs1, qz0, qz1, st, lane,
-                                        a.err, km);
+                                        km);
       }
     }
     __syncwarp();

@@ -12,12 +12,14 @@ int decode_ctas_per_sm_q32(int k_bits, int v_bits, bool asym, int B) {
     if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, true, true>::ctas_per_sm(B);
     if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, true, true>::ctas_per_sm(B);
     if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, true, true>::ctas_per_sm(B);
+    if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, true, true>::ctas_per_sm(B);
     return 0;
   }
   if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, false, true>::ctas_per_sm(B);
   if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, false, true>::ctas_per_sm(B);
   if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, false, true>::ctas_per_sm(B);
   if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, false, true>::ctas_per_sm(B);
+  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, false, true>::ctas_per_sm(B);
   return 0;
 }
 
@@ -28,12 +30,14 @@ cudaError_t launch_decode_q32(const DecodeArgs& a, cudaStream_t s) {
     if (kb == 4 && vb == 4) return Kernel<4, 4, true, true>::launch(a, s);
     if (kb == 4 && vb == 8) return Kernel<4, 8, true, true>::launch(a, s);
     if (kb == 8 && vb == 4) return Kernel<8, 4, true, true>::launch(a, s);
+    if (kb == 2 && vb == 2) return Kernel<2, 2, true, true>::launch(a, s);
     return cudaErrorInvalidValue;
   }
   if (kb == 8 && vb == 8) return Kernel<8, 8, false, true>::launch(a, s);
   if (kb == 4 && vb == 4) return Kernel<4, 4, false, true>::launch(a, s);
   if (kb == 4 && vb == 8) return Kernel<4, 8, false, true>::launch(a, s);
   if (kb == 8 && vb == 4) return Kernel<8, 4, false, true>::launch(a, s);
+  if (kb == 2 && vb == 2) return Kernel<2, 2, false, true>::launch(a, s);
   return cudaErrorInvalidValue;
 }
 

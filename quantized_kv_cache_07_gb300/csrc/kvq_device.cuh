@@ -32,6 +32,12 @@ struct Loc {
 __host__ __device__ inline Loc key_loc(int bits, int i, int d) {
   const int g = i & 7, hi = i >> 3, t = d >> 5, e = d & 31, lane = 4 * g + t;
   if (bits == 8) return {(2 * hi + (e >> 4)) * 512 + lane * 16 + (e & 15), 0};
+  if (bits == 2) {
+    // word e >> 3 holds k-slices 2w, 2w+1 (h); field r = token half + 2 * dim pair
+    const int h = (e >> 2) & 1, w = e & 3, r = hi + 2 * (w >> 1);
+    const int bit = 16 * (w & 1) + 8 * h + 2 * r;
+    return {lane * 16 + (e >> 3) * 4 + (bit >> 3), bit & 7};
+  }
   if (bits == 4) {
     const int nib = ((e & 7) >> 1) + 4 * (e & 1);
     return {hi * 512 + lane * 16 + (e >> 3) * 4 + (nib >> 1), (nib & 1) * 4};
@@ -43,6 +49,12 @@ __host__ __device__ inline Loc value_loc(int bits, int i, int d) {
   const int mt = d >> 4, r = d & 15, g = r & 7, hi = r >> 3;
   const int t = (i & 7) >> 1, j = 2 * (i & 1) + (i >> 3), lane = 4 * g + t;
   if (bits == 8) return {(mt >> 1) * 512 + lane * 16 + (2 * (mt & 1) + hi) * 4 + j, 0};
+  if (bits == 2) {
+    // word mt >> 1 holds m-tiles 2w, 2w+1 (h); field r = dim half + 2 * token pair
+    const int h = mt & 1, r = hi + 2 * (j >> 1);
+    const int bit = 16 * (j & 1) + 8 * h + 2 * r;
+    return {lane * 16 + (mt >> 1) * 4 + (bit >> 3), bit & 7};
+  }
   if (bits == 4) {
     const int nib = 2 * hi + (j >> 1) + 4 * (j & 1);
     return {(mt >> 2) * 512 + lane * 16 + (mt & 3) * 4 + (nib >> 1), (nib & 1) * 4};
@@ -133,6 +145,35 @@ __device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t km, uint32_t& p
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p1) : "r"(b), "r"(sixteenth), "r"(m72));
   asm("sub.f16x2 %0, %1, %2;" : "=r"(p2) : "r"(c), "r"(bias));
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p3) : "r"(d), "r"(sixteenth), "r"(m72));
+}
+
+// Sixteen 2-bit codes (biased fields u = c + 2, or the asymmetric u itself) of
+// w -> eight fp16 pairs.  Output 4h + r holds the fields at bits 8h + 2r (low
+// half) and 16 + 8h + 2r (high half): the field sits at 4^r * u under the
+// magic, and (x / 4^r) - (1024 / 4^r + 2) recovers u - 2 exactly.  km must
+// hold kMagicF16x2 (see magic_f16x2).
+__device__ __forceinline__ void s2x16_to_f16(uint32_t w, uint32_t km, uint32_t (&o)[8]) {
+  const uint32_t s = w >> 8;
+  uint32_t a[8];
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[0]) : "r"(w), "n"(0x00030003), "r"(km));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[1]) : "r"(w), "n"(0x000C000C), "r"(km));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[2]) : "r"(w), "n"(0x00300030), "r"(km));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[3]) : "r"(w), "n"(0x00C000C0), "r"(km));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[4]) : "r"(s), "n"(0x00030003), "r"(km));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[5]) : "r"(s), "n"(0x000C000C), "r"(km));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[6]) : "r"(s), "n"(0x00300030), "r"(km));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(a[7]) : "r"(s), "n"(0x00C000C0), "r"(km));
+  const uint32_t bias = 0x64026402u;                     // 1026 = 1024 + 2
+  const uint32_t q4 = 0x34003400u, m258 = 0xDC08DC08u;   // 1/4, -258
+  const uint32_t q16 = 0x2C002C00u, m66 = 0xD420D420u;   // 1/16, -66
+  const uint32_t q64 = 0x24002400u, m18 = 0xCC80CC80u;   // 1/64, -18
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(o[4 * h]) : "r"(a[4 * h]), "r"(bias));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[4 * h + 1]) : "r"(a[4 * h + 1]), "r"(q4), "r"(m258));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[4 * h + 2]) : "r"(a[4 * h + 2]), "r"(q16), "r"(m66));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[4 * h + 3]) : "r"(a[4 * h + 3]), "r"(q64), "r"(m18));
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {

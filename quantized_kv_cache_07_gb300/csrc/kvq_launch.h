@@ -51,7 +51,8 @@ struct DequantArgs {
 struct DecodeLayout {
   int stream_ctas, window_ctas, units, slots;
   int switch_blocks;  // virtual blocks charged for starting a unit (0: unit-aligned split)
-  size_t off_counter, off_m, off_l, off_o, total;
+  size_t off_counter;  // int [units]: merge arrival counters
+  size_t off_m, off_l, off_o, total;  // partial records: m, l [slots][G], o [slots][G][128]
 };
 
 struct DecodeArgs {

@@ -35,14 +35,15 @@ def oracle_state(inp, b):
                                k_per_channel=w.k_per_channel)
 
 
-def oracle_decode(inp, units=None):
-    """Oracle outputs {(b, h): (o [G, D], lse [G])} for the requested units."""
+def oracle_decode(inp, units=None, states=None):
+    """Oracle outputs {(b, h): (o [G, D], lse [G])} for the requested units
+    (``states``: optional {b: oracle_state(inp, b)} computed beforehand)."""
     w = inp.workload
     G = w.group
     res = {}
     bs = sorted({b for b, _ in units}) if units is not None else range(w.batch)
     for b in bs:
-        st = oracle_state(inp, b)
+        st = states[b] if states is not None else oracle_state(inp, b)
         q = O.bf16_to_f64(inp.q[b])
         for h in range(w.kv_heads):
             if units is not None and (b, h) not in units:

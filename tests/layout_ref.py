@@ -18,6 +18,9 @@ def key_offsets(bits: int):
     lane = 4 * g + t
     if bits == 8:
         return (2 * hi + (e >> 4)) * 512 + lane * 16 + (e & 15), np.zeros((BLOCK, D), int)
+    if bits == 2:
+        bit = 16 * (e & 1) + 8 * ((e >> 2) & 1) + 2 * (hi + 2 * ((e & 3) >> 1))
+        return lane * 16 + (e >> 3) * 4 + bit // 8, bit % 8
     if bits == 4:
         nib = ((e & 7) >> 1) + 4 * (e & 1)
         return hi * 512 + lane * 16 + (e >> 3) * 4 + nib // 2, (nib & 1) * 4
@@ -33,6 +36,9 @@ def value_offsets(bits: int):
     lane = 4 * g + t
     if bits == 8:
         return (mt >> 1) * 512 + lane * 16 + (2 * (mt & 1) + hi) * 4 + j, np.zeros((BLOCK, D), int)
+    if bits == 2:
+        bit = 16 * (j & 1) + 8 * (mt & 1) + 2 * (hi + 2 * (j >> 1))
+        return lane * 16 + (mt >> 1) * 4 + bit // 8, bit % 8
     if bits == 4:
         nib = 2 * hi + (j >> 1) + 4 * (j & 1)
         return (mt >> 2) * 512 + lane * 16 + (mt & 3) * 4 + nib // 2, (nib & 1) * 4
@@ -54,6 +60,8 @@ def unpack_blocks(pool: np.ndarray, bits: int, is_key: bool, heads: int, asym: b
     raw = blocks[..., off].astype(np.int32)
     if bits == 8:
         return raw if asym else raw - 128
+    if bits == 2:
+        return ((raw >> sh) & 0x3) - (0 if asym else 2)
     return ((raw >> sh) & 0xF) - (0 if asym else 8)
 
 
@@ -62,16 +70,23 @@ def offsets_are_a_permutation(bits: int, is_key: bool) -> bool:
     if bits == 16:
         cells = np.concatenate([off.ravel(), off.ravel() + 1])
         return np.array_equal(np.sort(cells), np.arange(block_bytes(16)))
-    cells = (off * 2 + sh // 4).ravel() if bits == 4 else off.ravel()
-    n = block_bytes(bits) * (2 if bits == 4 else 1)
+    per_byte = {2: 4, 4: 2}.get(bits, 1)
+    cells = (off * per_byte + sh // (8 // per_byte)).ravel()
+    n = block_bytes(bits) * per_byte
     return np.array_equal(np.sort(cells), np.arange(n))
 
 
-def meta_by_block(pool: np.ndarray, heads: int, asym: bool = False) -> dict:
+def meta_by_block(pool: np.ndarray, heads: int, asym: bool = False, group: bool = False) -> dict:
     """Metadata pool float [heads * num_blocks * M] (head-major, M = 32, or 64
     asymmetric) -> {"k_scale", "v_scale"(, "k_offset", "v_offset")} each
     [num_blocks, heads, 16]: per block K scales, (K zero points,) V scales,
-    (V zero points)."""
+    (V zero points).  group (2-bit blocks, M = 4): one record (K scale, K zero
+    point, V scale, V zero point) per block, repeated for its 16 tokens."""
+    if group:
+        rec = pool.reshape(heads, -1, 4).transpose(1, 0, 2)
+        out = {name: np.repeat(rec[:, :, i:i + 1], BLOCK, axis=2)
+               for i, name in enumerate(("k_scale", "k_offset", "v_scale", "v_offset"))}
+        return out if asym else {"k_scale": out["k_scale"], "v_scale": out["v_scale"]}
     parts = ("k_scale", "k_offset", "v_scale", "v_offset") if asym else ("k_scale", "v_scale")
     rec = pool.reshape(heads, -1, len(parts), BLOCK).transpose(1, 0, 2, 3)
     return {name: rec[:, :, i] for i, name in enumerate(parts)}

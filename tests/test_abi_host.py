@@ -66,6 +66,7 @@ def test_status_strings_and_block_bytes(lib):
     assert lib.status_string(0) == "KVQ_OK"
     assert "WORKSPACE" in lib.status_string(lib.KVQ_ERR_WORKSPACE)
     assert lib.block_bytes(8) == 2048 and lib.block_bytes(4) == 1024 and lib.block_bytes(16) == 4096
+    assert lib.block_bytes(2) == 512
     with pytest.raises(lib.KvqError):
         lib.block_bytes(3)
 
@@ -77,9 +78,11 @@ def test_decode_plan_one_wave_of_ctas(lib):
     assert p5.stream_ctas == 448                                               # 14 CTAs per unit
     p3 = lib.kvq_make_decode_plan(32, 32, 8, 0, num_sms=152, ctas_per_sm=3)
     assert p3.stream_ctas == 456                                               # 456 % 256 too large to drop
+    # one record slot per (CTA, unit) pair a CTA's range can touch (slot c + u)
     assert p.partial_slots == 456 + 512
     slots = p.partial_slots
-    assert p.workspace_bytes >= slots * 8 * (128 + 2) * 4 + 512 * 4
+    G = 32 // 8                                   # records hold the GQA group's rows
+    assert p.workspace_bytes >= slots * G * (128 + 2) * 4 + 512 * 4 + 8
     pw = lib.kvq_make_decode_plan(8, 32, 8, 128, num_sms=152, ctas_per_sm=3)
     # window CTAs (one per unit) run first and take their slots out of the wave
     assert pw.window_ctas == 64 and pw.stream_ctas == 384        # 456 - 64 = 392, rounded to 6 x 64 units
@@ -101,6 +104,9 @@ def _fake_desc(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=64), 2), (dict(block_size=32), 2), (dict(k_bits=2), 2), (dict(k_bits=16, v_bits=8), 2),
+    (dict(k_bits=8, v_bits=2), 2), (dict(k_bits=3, v_bits=3), 2),
+    # 2-bit blocks (token-group scales): both K and V, no per-channel-only keys
+    (dict(k_bits=2, v_bits=2, k_per_channel=1, k_channel_factor=0xC000), 2),
     (dict(k_codes=0x1004), 3), (dict(meta=None), 1), (dict(meta=0x3008), 3), (dict(num_kv_heads=0), 1),
     (dict(window=256), 2),
     (dict(window=16), 1), (dict(window=24), 2),
@@ -133,6 +139,10 @@ def test_append_and_decode_reject_bad_shapes_before_any_launch(lib):
     # ring mode needs a window
     assert so.kvq_append(ctypes.byref(desc), 0x5000, 0x5100, 1, 0x6000, 0x6100, lib.APPEND_RING, 0x7000, 1, 1,
                          None, None) == lib.KVQ_ERR_INVALID_ARG
+    # a decode-step eviction cannot write into a 2-bit block (blocks are quantized whole)
+    d2 = _fake_desc(lib, k_bits=2, v_bits=2, window=16, window_batch=1, k_window=0xD000, v_window=0xE000)
+    assert so.kvq_append(ctypes.byref(d2), 0x5000, 0x5100, 1, 0x6000, 0x6100, lib.APPEND_STEP, 0x7000, 1, 1,
+                         None, None) == lib.KVQ_ERR_UNSUPPORTED
     # zero tokens is a no-op
     assert so.kvq_append(ctypes.byref(desc), None, None, 0, None, None, 0, None, 1, 1, None, None) == 0
     # too-small workspace
@@ -140,7 +150,7 @@ def test_append_and_decode_reject_bad_shapes_before_any_launch(lib):
                          None, None) == lib.KVQ_ERR_WORKSPACE
 
 
-@pytest.mark.parametrize("bits", [4, 8, 16])
+@pytest.mark.parametrize("bits", [2, 4, 8, 16])
 @pytest.mark.parametrize("is_key", [True, False])
 def test_layout_reader_is_a_bijection(bits, is_key):
     assert offsets_are_a_permutation(bits, is_key)
