@@ -7,8 +7,12 @@ bracketed by a barrier and a device synchronize; steps rotate over enough
 identical cache replicas that the bytes cycled exceed 4x the L2 size (or the
 cache alone exceeds L2), so every step reads its cache from HBM.
 
-Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle
-(the reference arm) on a bounded sample of the same workload.
+Prints one JSON line (rank 0): the headline workload (the paged int8 serving
+step, the largest single-GPU one) and, at one GPU, a per_config object with the
+same measurements for each of the five named workloads (decode roofline,
+same-design bf16-cache kernel, and the float64 oracle timed on a bounded sample
+on the host cores).  --impl reference times the float64 CPU oracle (the
+reference arm) on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -26,7 +30,11 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "gqa_int8_window128_b8_t4096"
+# The headline: the largest single-GPU workload (paged int8 serving step,
+# 2.39 GB of cache per step).  Every named workload is measured too (per_config).
+DEFAULT_WORKLOAD = "paged_int8_b64_len2k_32k"
+ALL_WORKLOADS = ["int8_b1_h4_t256", "gqa_int8_window128_b8_t4096", "int4_factor_b32_len1k_8k",
+                 "paged_int8_b64_len2k_32k", "long_k4v8_b4_t131072"]
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -133,6 +141,11 @@ def cache_bytes_per_step(inp) -> int:
     w = inp.workload
     L = inp.decode_lengths.astype(int)
     D = w.head_dim
+    if w.k_bits == 2:
+        # 2-bit codes of K and V plus one 16-byte metadata record per 16-token block
+        lq = [max(int(l) - w.window, 0) if w.window else int(l) for l in L]
+        return w.kv_heads * sum(2 * D * 2 // 8 * x + 16 * ((x + 15) // 16) + 4 * D * (int(l) - x)
+                                for l, x in zip(L, lq))
     per_q = (D * w.k_bits // 8 + D * w.v_bits // 8
              + (0 if w.k_bits == 16 else (16 if w.asym else 8)) - (4 if w.k_per_channel else 0))
     if w.window:
@@ -144,7 +157,7 @@ def cache_bytes_per_step(inp) -> int:
 
 # ------------------------------------------------------------------ reference arm / CPU baseline
 CPU_SAMPLE_SNIPPET = r"""
-import json, sys, time
+import json, os, sys, time
 sys.path.insert(0, {root!r})
 import numpy as np
 from synth import WORKLOADS, make_inputs
@@ -160,7 +173,7 @@ G = w.group
 budget = {budget}
 rng = np.random.default_rng(5)
 units = [(int(b), int(h)) for b in rng.permutation(w.batch) for h in range(w.kv_heads)]
-per_tok = (128 * w.k_bits // 8 + 128 * w.v_bits // 8 + (0 if w.k_bits == 16 else (16 if w.asym else 8))
+per_tok = (128 * w.k_bits // 8 + 128 * w.v_bits // 8 + (0 if w.k_bits in (16, 2) else (16 if w.asym else 8))
            - (4 if w.k_per_channel else 0))
 tot_t, tot_b, n, i = 0.0, 0, 0, 0
 while tot_t < budget or n == 0:
@@ -181,23 +194,47 @@ while tot_t < budget or n == 0:
     O.attention(qv, kh, vh)
     tot_t += time.perf_counter() - t1
     L = k.shape[0]; Lq = st["Lq"]
-    tot_b += per_tok * Lq + 512 * (L - Lq); n += 1
-print(json.dumps({{"seconds": tot_t, "bytes": tot_b, "units": n}}))
+    tot_b += per_tok * Lq + 512 * (L - Lq) + (16 * ((Lq + 15) // 16) if w.k_bits == 2 else 0); n += 1
+print(json.dumps({{"seconds": tot_t, "bytes": tot_b, "units": n, "distinct_units": min(n, len(units))}}))
 """
 
+# The oracle runs single-threaded: these variables pin numpy's BLAS to one thread.
+CPU_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
 
-def run_cpu_sample(name: str, budget_s: float, steps: int = 1, bf16: bool = False, asym: bool = False,
-                   qbits: int = 16):
-    """Time the oracle's decode (dequantize + attention, float64) on a bounded
-    sample of the workload's units, in a fresh single-threaded process."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def start_cpu_sample(name: str, budget_s: float, bf16: bool = False, asym: bool = False, qbits: int = 16):
+    """Start the oracle's decode (dequantize + attention, float64) on a bounded
+    sample of the workload's units in a fresh single-threaded process."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", **CPU_THREAD_ENV)
     code = CPU_SAMPLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, bf16=bf16, asym=asym, qbits=qbits)
-    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
-    if res.returncode != 0:
-        raise RuntimeError("oracle sample failed: " + res.stderr[-2000:])
-    d = json.loads(res.stdout.strip().splitlines()[-1])
-    return d
+    return subprocess.Popen([sys.executable, "-c", code], stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
+                            env=env)
+
+
+def finish_cpu_sample(proc, timeout: float = 1800) -> dict:
+    out, err = proc.communicate(timeout=timeout)
+    if proc.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + err[-2000:])
+    return json.loads(out.strip().splitlines()[-1])
+
+
+def run_cpu_sample(name: str, budget_s: float, **kw) -> dict:
+    return finish_cpu_sample(start_cpu_sample(name, budget_s, **kw))
+
+
+def cpu_baseline_entry(d: dict, wname: str) -> dict:
+    return {"value": round(d["bytes"] / d["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "host_cores": host_cores(), "blas_threads": 1, "kind": "oracle",
+            "sample": f"{d['units']} (sequence, kv_head) unit decodes ({d['distinct_units']} distinct) of {wname}, "
+                      f"float64 dequantize + attention, one thread (BLAS pinned to 1 thread), "
+                      f"{d['seconds']:.1f} s of CPU work on a host with {host_cores()} cores"}
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -212,86 +249,42 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 
 
 # ------------------------------------------------------------------ GPU arm
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-bf16", action="store_true", help="skip the same-design bf16-cache comparison run")
-    ap.add_argument("--no-asym", action="store_true",
-                    help="skip the same-shape run in the asymmetric (scale + zero point) format")
-    ap.add_argument("--asym", action="store_true",
-                    help="time the workload in the asymmetric (scale + zero point) format")
-    ap.add_argument("--q-bits", type=int, default=16, choices=[8, 16, 32],
-                    help="query format: 8 int8 rows (integer dot), 16 fp16 (default), 32 fp16 hi + lo")
-    ap.add_argument("--no-qint8", action="store_true",
-                    help="skip the same-shape run with int8-quantized query rows")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--stream-ctas", type=int, default=0)
-    ap.add_argument("--soak", type=float, default=1.0,
-                    help="seconds of untimed steps before the timed region (clock sampling, steady state)")
-    args = ap.parse_args()
+class GpuArm:
+    """Builds a workload's cache replicas on the device and times its steps."""
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    def __init__(self, args, dev, world, local):
+        import torch
+        from quantized_kv_cache_07_gb300 import _lib
+        self.torch, self.lib = torch, _lib
+        self.args, self.dev, self.world, self.local = args, dev, world, local
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20
 
-    if args.impl == "reference":
-        return reference_arm(args, rank, world)
-
-    import numpy as np
-    import torch
-    import torch.distributed as dist
-
-    from quantized_kv_cache_07_gb300 import _lib
-    from quantized_kv_cache_07_gb300.build import build
-    from quantized_kv_cache_07_gb300.cache import DecodeWorkspace, cache_for_inputs, fill_from_inputs
-    from synth import WORKLOADS, make_inputs
-
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    if rank == 0:
-        build()
-    if world > 1:
-        dist.barrier()
-    _lib.load()
-
-    w = WORKLOADS[args.workload]
-    if args.asym:
-        w = w.with_(asym=True)
-    if args.q_bits != 16:
-        w = w.with_(q_bits=args.q_bits)
-    inp = make_inputs(w)
-    dev = torch.device("cuda", local)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20
-
-    def build_replicas(inp_, k_bits=None):
-        base = cache_for_inputs(inp_, dev)
-        table, lens = fill_from_inputs(base, inp_, dev)
+    def build_replicas(self, inp_):
+        from quantized_kv_cache_07_gb300.cache import cache_for_inputs, fill_from_inputs
+        base = cache_for_inputs(inp_, self.dev)
+        table, lens = fill_from_inputs(base, inp_, self.dev)
         nbytes = base.allocated_bytes()
-        reps = max(1, math.ceil(4 * l2 / max(cache_bytes_per_step(inp_), 1)))
+        reps = max(1, math.ceil(4 * self.l2 / max(cache_bytes_per_step(inp_), 1)))
         reps = min(reps, 64)
         replicas = [base]
         for _ in range(reps - 1):
-            c = cache_for_inputs(inp_, dev)
+            c = cache_for_inputs(inp_, self.dev)
             for name in ("k_codes", "v_codes", "meta", "k_window", "v_window"):
                 src, dst = getattr(base, name), getattr(c, name)
                 if src is not None:
                     dst.copy_(src)
             replicas.append(c)
-        torch.cuda.synchronize()
+        self.torch.cuda.synchronize()
         return replicas, table, lens, nbytes
 
-    def run_arm(inp_, label):
+    def run(self, inp_):
+        import numpy as np
+        torch, _lib, args, dev, world = self.torch, self.lib, self.args, self.dev, self.world
+        import torch.distributed as dist
+        from quantized_kv_cache_07_gb300.cache import DecodeWorkspace
         wl = inp_.workload
-        replicas, table, lens, alloc = build_replicas(inp_)
+        replicas, table, lens, alloc = self.build_replicas(inp_)
         B, Hq = wl.batch, wl.q_heads
         q = torch.from_numpy(inp_.q.view(np.int16)).to(dev).view(torch.bfloat16)
         out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=dev)
@@ -334,21 +327,49 @@ def main():
             per = max((time.perf_counter() - t_est) / 20, 1e-6)
             soak = int(min(max(args.soak / per, 0), 200000))
         K = args.steps
+        # The K timed steps are captured once in a CUDA graph and replayed: the
+        # host's per-call launch cost (ctypes marshalling, launch API) stays out
+        # of the device timing of kernels that run for 10-400 us.  The same K
+        # steps launched one by one from Python are timed beside it (eager).
+        graph = None
+        if not args.eager:
+            try:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    for k in range(K):
+                        step(k)
+                graph.replay()
+                torch.cuda.synchronize()
+            except Exception as e:  # reported, then timed eagerly
+                graph = None
+                self.graph_error = f"{type(e).__name__}: {e}"[:300]
         e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with ClockSampler(local) as clk:
+        with ClockSampler(self.local) as clk:
             for k in range(soak):
                 step(k)
             if world > 1:
                 dist.barrier()
             torch.cuda.synchronize()
             e_start.record(stream)
-            for k in range(K):      # exactly K back-to-back steps, nothing else in the timed region
-                step(k)
+            if graph is not None:   # exactly K back-to-back steps, nothing else in the timed region
+                graph.replay()
+            else:
+                for k in range(K):
+                    step(k)
             e_end.record(stream)
             torch.cuda.synchronize()
             if world > 1:
                 dist.barrier()
         ms_total = e_start.elapsed_time(e_end)
+        ms_eager = ms_total / K
+        if graph is not None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in range(K):
+                step(k)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms_eager = e0.elapsed_time(e1) / K
         # The timed steps run back to back (one decode launch each, plus the
         # append launch for append workloads).  Without an append the decode
         # kernel's average duration is the step time; with one, K decode
@@ -374,17 +395,30 @@ def main():
         if wl.append_one:
             # the decode kernel's own rate: K decode launches back to back (no append
             # in between), timed the same way as the steps
+            def decodes():
+                for k in range(K):
+                    c = replicas[k % len(replicas)]
+                    _lib.kvq_decode(c.desc, q, B, Hq, dec_lens, table, inp_.max_blocks, out, lse=lse,
+                                    workspace=ws.buf, workspace_bytes=ws.nbytes, stream_ctas=args.stream_ctas,
+                                    err_word=err)
+            dgraph = None
+            if graph is not None:
+                dgraph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(dgraph):
+                    decodes()
+                dgraph.replay()
+                torch.cuda.synchronize()
             ed0, ed1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ed0.record(stream)
-            for k in range(K):
-                c = replicas[k % len(replicas)]
-                _lib.kvq_decode(c.desc, q, B, Hq, dec_lens, table, inp_.max_blocks, out, lse=lse, workspace=ws.buf,
-                                workspace_bytes=ws.nbytes, stream_ctas=args.stream_ctas, err_word=err)
+            if dgraph is not None:
+                dgraph.replay()
+            else:
+                decodes()
             ed1.record(stream)
             torch.cuda.synchronize()
-            dec_ms = [ed0.elapsed_time(ed1) / K]
+            dec_ms = ed0.elapsed_time(ed1) / K
         else:
-            dec_ms = [ms_total / K]
+            dec_ms = ms_total / K
         # e2e through the public API: pinned host q (and new tokens) in, output out, every step
         q_host = torch.from_numpy(inp_.q.view(np.int16)).view(torch.bfloat16).pin_memory()
         out_host = torch.empty((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
@@ -414,19 +448,139 @@ def main():
             stream.synchronize()
         e2e_s = (time.perf_counter() - t0) / K
         errbits = int(err.item())
-        return dict(ms_step=ms_total / K, dec_ms=statistics.mean(dec_ms), dec_ms_iso=statistics.mean(dec_iso),
-                    app_ms=app_ms,
-                    e2e_s=e2e_s, h2d=h2d, d2h=d2h, bytes=cache_bytes_per_step(inp_), replicas=len(replicas),
-                    alloc=alloc, clocks=clk.summary(), launches=launches_per_step * K, err=errbits,
-                    plan={"stream_ctas": plan.stream_ctas, "window_ctas": plan.window_ctas,
-                          "workspace_bytes": plan.workspace_bytes})
+        res = dict(ms_step=ms_total / K, ms_eager=ms_eager, timing="cuda graph of the K steps" if graph is not None
+                   else "eager launches (graph capture unavailable: %s)" % getattr(self, "graph_error", "disabled"),
+                   dec_ms=dec_ms, dec_ms_iso=statistics.mean(dec_iso), app_ms=app_ms,
+                   e2e_s=e2e_s, h2d=h2d, d2h=d2h, bytes=cache_bytes_per_step(inp_), replicas=len(replicas),
+                   alloc=alloc, clocks=clk.summary(), launches=launches_per_step * K, err=errbits,
+                   plan={"stream_ctas": plan.stream_ctas, "window_ctas": plan.window_ctas,
+                         "workspace_bytes": plan.workspace_bytes})
+        del replicas, ws, q, out, lse, graph
+        torch.cuda.empty_cache()
+        return res
 
-    res = run_arm(inp, "quant")
+
+def bf16_inputs(inp):
+    """The same seeded bits as a plain bf16 cache (same shapes, no window, no
+    factor): the same-design bf16-cache comparison."""
+    import dataclasses
+    wb = inp.workload.with_(k_bits=16, v_bits=16, window=0, channel_factor=False, asym=False, q_bits=16,
+                            k_per_channel=False, name=inp.workload.name + "_bf16")
+    return dataclasses.replace(inp, workload=wb, channel_factor=None)
+
+
+def summarize(w, res, peak, peak_kind, world=1):
+    """Decode-kernel roofline and step figures of one measured workload."""
+    achieved = res["bytes"] / (res["dec_ms"] / 1e3) / 1e9
+    kernel = "decode_asym" if w.asym else "decode"
+    return {
+        "workload": w.name,
+        "ms_per_step": round(res["ms_step"], 6),
+        "ms_per_step_eager": round(res["ms_eager"], 6),
+        "timing": res["timing"],
+        "steps_per_s": round(world * 1e3 / res["ms_step"], 2),
+        "cache_bytes_per_step": res["bytes"],
+        "effective_gbs": round(world * res["bytes"] / (res["ms_step"] / 1e3) / 1e9, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(w.name, kernel), "kernel": "kvq decode_kernel",
+                     "decode_ms_back_to_back": round(res["dec_ms"], 6),
+                     "append_ms_per_step": round(res["app_ms"], 6),
+                     "decode_ms_isolated_launch": round(res["dec_ms_iso"], 6)},
+        "e2e": {"value": round(world * res["bytes"] / res["e2e_s"] / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "ms_per_step": round(res["e2e_s"] * 1e3, 6)},
+        "clocks": res["clocks"],
+        "decode_grid": res["plan"],
+        "l2": f"steps rotate over {res['replicas']} cache replicas "
+              f"({res['replicas'] * res['bytes'] / 2**20:.0f} MiB >= 4x L2 or cache > L2)",
+        "device_err_word": res["err"],
+    }
+
+
+def bf16_entry(rb, res, peak):
+    g = rb["bytes"] / (rb["dec_ms"] / 1e3) / 1e9
+    return {"ms_per_step": round(rb["ms_step"], 6), "decode_ms": round(rb["dec_ms"], 6),
+            "decode_ms_isolated_launch": round(rb["dec_ms_iso"], 6), "bytes_per_step": rb["bytes"],
+            "effective_gbs": round(g, 1), "frac_of_peak": round(g / peak, 4),
+            "speedup_quant_vs_bf16": round(rb["dec_ms"] / res["dec_ms"], 4), "err_word": rb["err"]}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the same-design bf16-cache comparison runs")
+    ap.add_argument("--no-asym", action="store_true",
+                    help="skip the same-shape run in the asymmetric (scale + zero point) format")
+    ap.add_argument("--asym", action="store_true",
+                    help="time the workload in the asymmetric (scale + zero point) format")
+    ap.add_argument("--q-bits", type=int, default=16, choices=[8, 16, 32],
+                    help="query format: 8 int8 rows (integer dot), 16 fp16 (default), 32 two-part fp16")
+    ap.add_argument("--no-qint8", action="store_true",
+                    help="skip the same-shape run with int8-quantized query rows")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only the headline workload (no per_config object)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the headline cpu_baseline (per_config entries: a third)")
+    ap.add_argument("--stream-ctas", type=int, default=0)
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph of the steps")
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of untimed steps before each timed region (clock sampling, steady state)")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    from quantized_kv_cache_07_gb300 import _lib
+    from quantized_kv_cache_07_gb300.build import build
+    from synth import WORKLOADS, make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    _lib.load()
+
+    w = WORKLOADS[args.workload]
+    if args.asym:
+        w = w.with_(asym=True)
+    if args.q_bits != 16:
+        w = w.with_(q_bits=args.q_bits)
+    per_config_names = [] if (args.no_per_config or world > 1) else list(ALL_WORKLOADS)
+    # the oracle samples run on the host cores while the GPU is measured
+    cpu_jobs = {}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_jobs[w.name] = start_cpu_sample(args.workload, args.cpu_budget, asym=w.asym, qbits=w.q_bits)
+        for n in per_config_names:
+            if n != args.workload or w.asym or w.q_bits != 16:
+                cpu_jobs[n + "/per_config"] = start_cpu_sample(n, args.cpu_budget / 3)
+
+    dev = torch.device("cuda", local)
+    arm = GpuArm(args, dev, world, local)
     peak, peak_kind = measured_peaks()
 
     def allmax(x):
         return max_over_ranks(x, world, dev)
 
+    inp = make_inputs(w)
+    res = arm.run(inp)
     ms_step = allmax(res["ms_step"])
     e2e_s = allmax(res["e2e_s"])
     bytes_step = res["bytes"]
@@ -435,38 +589,45 @@ def main():
 
     bf16 = None
     if not args.no_bf16 and w.k_bits != 16:
-        wb = w.with_(k_bits=16, v_bits=16, window=0, channel_factor=False, name=w.name + "_bf16")
-        inb = make_inputs(wb)
-        rb = run_arm(inb, "bf16")
-        bf16 = {"workload": wb.name, "ms_per_step": rb["ms_step"], "decode_ms": rb["dec_ms"],
-                "decode_ms_isolated_launch": rb["dec_ms_iso"],
-                "bytes_per_step": rb["bytes"], "effective_gbs": rb["bytes"] / (rb["dec_ms"] / 1e3) / 1e9,
-                "frac_of_peak": rb["bytes"] / (rb["dec_ms"] / 1e3) / 1e9 / peak,
-                "speedup_quant_vs_bf16": rb["dec_ms"] / res["dec_ms"], "err_word": rb["err"]}
-        del inb
+        bf16 = dict(workload=w.name + "_bf16", **bf16_entry(arm.run(bf16_inputs(inp)), res, peak))
 
     asym = None
     if not args.no_asym and w.k_bits != 16 and not w.asym:
+        import dataclasses
         wa = w.with_(asym=True, name=w.name + "_asym")
-        ina = make_inputs(wa)
-        ra = run_arm(ina, "asym")
+        ra = arm.run(dataclasses.replace(inp, workload=wa))     # same bits, scale + zero point
         asym = {"workload": wa.name, "ms_per_step": ra["ms_step"], "decode_ms": ra["dec_ms"],
                 "decode_ms_isolated_launch": ra["dec_ms_iso"], "bytes_per_step": ra["bytes"],
                 "effective_gbs": ra["bytes"] / (ra["dec_ms"] / 1e3) / 1e9,
                 "frac_of_peak": ra["bytes"] / (ra["dec_ms"] / 1e3) / 1e9 / peak,
                 "time_vs_symmetric": ra["dec_ms"] / res["dec_ms"], "err_word": ra["err"]}
-        del ina
 
     qint8 = None
     if not args.no_qint8 and w.k_bits != 16 and w.q_bits != 8 and not (w.channel_factor and w.window):
+        import dataclasses
         wq = w.with_(q_bits=8, name=w.name + "_qint8")
-        inq = make_inputs(wq)
-        rq = run_arm(inq, "qint8")
+        rq = arm.run(dataclasses.replace(inp, workload=wq))     # same bits, int8 query rows
         qint8 = {"workload": wq.name, "ms_per_step": rq["ms_step"], "decode_ms": rq["dec_ms"],
                  "bytes_per_step": rq["bytes"], "effective_gbs": rq["bytes"] / (rq["dec_ms"] / 1e3) / 1e9,
                  "frac_of_peak": rq["bytes"] / (rq["dec_ms"] / 1e3) / 1e9 / peak,
                  "time_vs_bf16_query": rq["dec_ms"] / res["dec_ms"], "err_word": rq["err"]}
-        del inq
+
+    # every named workload, one after another (rank 0 at one GPU)
+    per_config = {}
+    for n in per_config_names:
+        if n == args.workload and not w.asym and w.q_bits == 16:
+            entry = summarize(w, res, peak, peak_kind)
+            entry["bf16_same_design"] = bf16
+        else:
+            wn = WORKLOADS[n]
+            inn = make_inputs(wn)
+            rn = arm.run(inn)
+            entry = summarize(wn, rn, peak, peak_kind)
+            entry["bf16_same_design"] = (None if args.no_bf16 else
+                                         dict(workload=n + "_bf16", **bf16_entry(arm.run(bf16_inputs(inn)), rn,
+                                                                                 peak)))
+            del inn
+        per_config[n] = entry
 
     line = {
         "metric": "quantized-KV decode attention: effective HBM GB/s (% of peak), steps/s",
@@ -486,14 +647,16 @@ def main():
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits,
                    "window": w.window, "paged": w.paged, "append_one": w.append_one,
                    "format": "asymmetric (scale + zero point)" if w.asym else "symmetric (scale)",
-                   "query": {8: "int8 rows, integer dot", 16: "fp16", 32: "fp16 hi + lo"}[w.q_bits],
+                   "query": {8: "int8 rows, integer dot", 16: "fp16", 32: "two-part fp16 (hi + lo)"}[w.q_bits],
                    "cache_bytes_per_step": bytes_step, "allocated_cache_bytes": res["alloc"],
                    "l2": f"steps rotate over {res['replicas']} cache replicas "
                          f"({res['replicas'] * bytes_step / 2**20:.0f} MiB >= 4x L2 or cache > L2)",
-                   "parallelism": f"replicas x{world}", "decode_grid": res["plan"]},
+                   "parallelism": f"replicas x{world}", "decode_grid": res["plan"], "timing": res["timing"],
+                   "ms_per_step_eager": round(res["ms_eager"], 6)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": recorded_traffic(w.name, "decode_asym" if w.asym else "decode"), "kernel": "kvq decode_kernel",
+                     "traffic": recorded_traffic(w.name, "decode_asym" if w.asym else "decode"),
+                     "kernel": "kvq decode_kernel",
                      "decode_ms_back_to_back": round(res["dec_ms"], 6),
                      "append_ms_per_step": round(res["app_ms"], 6),
                      "decode_ms_isolated_launch": round(res["dec_ms_iso"], 6)},
@@ -507,17 +670,21 @@ def main():
         "qint8_same_shape": qint8,
         "device_err_word": res["err"],
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if per_config:
+        line["per_config"] = per_config
+    for key, proc in cpu_jobs.items():
+        name = key.split("/")[0]
         try:
-            d = run_cpu_sample(args.workload, args.cpu_budget, asym=w.asym, qbits=w.q_bits)
-            line["cpu_baseline"] = {"value": round(d["bytes"] / d["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
-                                    "kind": "oracle",
-                                    "sample": f"{d['units']} (sequence, kv_head) units of {w.name}, float64 "
-                                              f"dequantize + attention, single thread, "
-                                              f"{d['seconds']:.1f} s of CPU work"}
+            entry = cpu_baseline_entry(finish_cpu_sample(proc), name)
         except Exception as e:  # reported, not fatal
-            line["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                    "sample": f"failed: {e}"}
+            entry = {"value": None, "unit": "GB/s", "cores": 1, "host_cores": host_cores(), "kind": "oracle",
+                     "sample": f"failed: {e}"}
+        if key.endswith("/per_config"):
+            per_config[name]["cpu_baseline"] = entry
+        else:
+            line["cpu_baseline"] = entry
+            if name in per_config:
+                per_config[name]["cpu_baseline"] = entry
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -534,7 +701,7 @@ def reference_arm(args, rank, world):
     K = args.steps
     # bounded: about 60 s of oracle work for the whole timed run, split over K steps
     per_step_budget = min(60.0 / max(K, 1), 5.0)
-    d = run_cpu_sample(w.name, per_step_budget * K, steps=K)
+    d = run_cpu_sample(w.name, per_step_budget * K)
     gbs = d["bytes"] / d["seconds"] / 1e9
     ms = d["seconds"] / K * 1e3
     line = {
@@ -545,8 +712,7 @@ def reference_arm(args, rank, world):
         "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": w.name, "description": w.description,
                    "sample": "each step: a bounded sample of (sequence, kv_head) units"},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{d['units']} units of {w.name} over {K} steps, {d['seconds']:.1f} s"},
+        "cpu_baseline": cpu_baseline_entry(d, w.name),
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -8,7 +8,8 @@ import bench
 from oracle import kvq_oracle as O
 from synth import WORKLOADS, make_inputs
 
-VARIANTS = [dict(), dict(asym=True), dict(k_bits=16, v_bits=16, window=0, channel_factor=False)]
+VARIANTS = [dict(), dict(asym=True), dict(k_bits=16, v_bits=16, window=0, channel_factor=False),
+            dict(k_bits=2, v_bits=2), dict(k_bits=2, v_bits=2, asym=True)]
 
 
 def expected_bytes(inp) -> int:
@@ -18,6 +19,11 @@ def expected_bytes(inp) -> int:
     total = 0
     for L in inp.decode_lengths.astype(int):
         lq = O.window_split(int(L), w.window)
+        if w.k_bits == 2:
+            # codes per token, plus the 16-byte record of each started 16-token group
+            per_code = per_q - 16 / O.GROUP_TOKENS
+            total += int(per_code * lq) + 16 * -(-lq // O.GROUP_TOKENS) + 2 * w.head_dim * 2 * (int(L) - lq)
+            continue
         total += per_q * lq + 2 * w.head_dim * 2 * (int(L) - lq)      # bf16 window tokens: K and V
     return w.kv_heads * total
 
