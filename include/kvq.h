@@ -300,6 +300,44 @@ kvq_status kvq_decode_static_scratch(const kvq_cache_desc* cache, const void* q,
                                      int32_t stream_ctas, uint32_t* err_word, void* stream);
 
 /*
+ * kvq_prefill -- chunked-prefill attention over the quantized cache, with the
+ * chunk's own quantize-on-write.  The cache is written incrementally and read
+ * repeatedly ("KV Cache Quantization and Per-Token Scale Placement", opening
+ * section): a chunk of n new positions is first quantized into the block
+ * store (exactly kvq_append in KVQ_APPEND_QUANT mode, when k_new and v_new
+ * are given), and then every new position attends causally to the stored
+ * cache of its sequence, itself included:
+ *   for row r, query head hq:  o = sum_{i <= pos[r]} softmax(score)_i v_hat_i,
+ *   score_i = q[r][hq] . k_hat_i / sqrt(D), over positions 0..pos[r] of
+ *   sequence seq_idx[r], read from the quantized blocks as kvq_decode reads them.
+ * The write and the attention are two launches in stream order (the second
+ * starts under programmatic dependent launch and waits for the first).  Every
+ * row is one query group of the decode kernel's split, so rows of one
+ * sequence read overlapping prefixes (mostly from L2 when they run together).
+ *   q          : device bf16 [n][q_heads][128]
+ *   seq_idx,pos: device int32 [n] (as kvq_append); a row with a sequence outside
+ *                [0, batch) sets KVQ_DEVERR_POSITION and gets out = 0, lse = -inf
+ *   k_new,v_new: device bf16 [n][num_kv_heads][128] to write first, or both NULL
+ *                when the chunk is already in the cache; for 2-bit caches the
+ *                chunk's positions must start at a block boundary (blocks are
+ *                written whole)
+ *   block_table: device int32 [batch][max_blocks_per_seq]
+ *   out, lse   : device [n][q_heads][128] (bf16 or float32), float [n][q_heads] or NULL
+ *   workspace  : >= kvq_prefill_workspace_size bytes, zeroed once by kvq_workspace_init
+ * Requirements: window == 0 (KVQ_ERR_UNSUPPORTED otherwise), n <= 4096, the
+ * kvq_decode requirements on q_heads.
+ */
+kvq_status kvq_prefill(const kvq_cache_desc* cache, const void* q, int32_t n, int32_t q_heads,
+                       const int32_t* seq_idx, const int32_t* pos, const void* k_new, const void* v_new,
+                       const int32_t* block_table, int32_t batch, int32_t max_blocks_per_seq, void* out,
+                       int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes, int32_t stream_ctas,
+                       uint32_t* err_word, void* stream);
+
+/* Workspace bytes kvq_prefill needs for n rows on the current device. */
+kvq_status kvq_prefill_workspace_size(const kvq_cache_desc* cache, int32_t n, int32_t q_heads, int32_t stream_ctas,
+                                      size_t* bytes);
+
+/*
  * kvq_dequant -- read the block store back: x_hat = RN32(code * s)
  * ([P2] "Quantization needs a scale convention"), without the per-channel key
  * factor; in the asymmetric format x_hat = RN32(u * s + m) (one fused

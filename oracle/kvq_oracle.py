@@ -364,6 +364,21 @@ def decode_sequence(q_bits, st, kv_heads: int, query_bits: int = 16):
     return o, lse
 
 
+def prefill_attention(q_rows: np.ndarray, st, head: int, pos: np.ndarray):
+    """Chunked prefill over one stored sequence: row r (query [G, D] of KV head
+    ``head``) is the new position pos[r] and attends causally to the stored
+    positions 0..pos[r], itself included ([P3] opening section: the cache is
+    written incrementally and read repeatedly; each query reads the entries
+    written before it and its own).  Returns (o [R, G, D], lse [R, G])."""
+    k_hat, v_hat = reconstruct_sequence(st, head)
+    outs, lses = [], []
+    for r, p in enumerate(np.asarray(pos, dtype=np.int64)):
+        o, lse = attention(q_rows[r], k_hat[: p + 1], v_hat[: p + 1])
+        outs.append(o)
+        lses.append(lse)
+    return np.stack(outs), np.stack(lses)
+
+
 # ---------------------------------------------------------------- byte accounting
 def kv_payload_bytes(layers: int, kv_heads: int, head_dim: int, tokens: int, bytes_per_elem: float) -> float:
     """KV_bytes = 2 * L * H_kv * D * T * b ([P2] "Cache precision is separate from

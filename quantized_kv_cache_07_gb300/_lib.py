@@ -73,6 +73,10 @@ SIGNATURES = {
     "kvq_decode": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32,
                              c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_int32, c_void_p, c_void_p]),
     "kvq_dequant": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
+    "kvq_prefill": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                              c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_int32,
+                              c_void_p, c_void_p]),
+    "kvq_prefill_workspace_size": (c_int32, [POINTER(CacheDesc), c_int32, c_int32, c_int32, POINTER(c_size_t)]),
     "kvq_decode_static_scratch": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p,
                                             c_int32, c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_void_p]),
 }
@@ -170,6 +174,26 @@ def kvq_decode(desc: CacheDesc, q, batch: int, q_heads: int, seq_lens, block_tab
     _check(load().kvq_decode(ctypes.byref(desc), _ptr(q), batch, q_heads, _ptr(seq_lens), _ptr(block_table),
                              max_blocks_per_seq, _ptr(out), int(bool(out_fp32)), _ptr(lse), _ptr(workspace),
                              workspace_bytes, stream_ctas, _ptr(err_word), _stream(stream)), "kvq_decode")
+
+
+def kvq_prefill_workspace_size(desc: CacheDesc, n: int, q_heads: int, stream_ctas: int = 0) -> int:
+    out = c_size_t(0)
+    _check(load().kvq_prefill_workspace_size(ctypes.byref(desc), n, q_heads, stream_ctas, ctypes.byref(out)),
+           "kvq_prefill_workspace_size")
+    return out.value
+
+
+def kvq_prefill(desc: CacheDesc, q, q_heads: int, seq_idx, pos, block_table, batch: int, max_blocks_per_seq: int,
+                out, k_new=None, v_new=None, lse=None, workspace=None, workspace_bytes: int = 0, stream_ctas: int = 0,
+                err_word=None, stream=None, out_fp32: bool | None = None, n: int | None = None):
+    n = int(seq_idx.shape[0]) if n is None else n
+    if out_fp32 is None:
+        import torch
+        out_fp32 = out.dtype == torch.float32
+    _check(load().kvq_prefill(ctypes.byref(desc), _ptr(q), n, q_heads, _ptr(seq_idx), _ptr(pos), _ptr(k_new),
+                              _ptr(v_new), _ptr(block_table), batch, max_blocks_per_seq, _ptr(out),
+                              int(bool(out_fp32)), _ptr(lse), _ptr(workspace), workspace_bytes, stream_ctas,
+                              _ptr(err_word), _stream(stream)), "kvq_prefill")
 
 
 def kvq_dequant(desc: CacheDesc, slots, k_out, v_out, stream=None, n: int | None = None):

@@ -89,12 +89,12 @@ int stream_ctas_for(int slots, int window_ctas, int units) {
   return left;
 }
 
-// Stream CTAs for the current device (0 on failure).
-int auto_stream_ctas(const kvq_cache_desc* c, int batch) {
+// Stream CTAs for the current device (0 on failure); rows: a prefill call.
+int auto_stream_ctas(const kvq_cache_desc* c, int batch, bool rows = false) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, c->asym != 0, c->q_bits, batch);
+  const int per = kvq::decode_ctas_per_sm_for(c->k_bits, c->v_bits, c->asym != 0, c->q_bits, batch, rows);
   return stream_ctas_for(sms * per, c->window > 0 ? batch * c->num_kv_heads : 0, batch * c->num_kv_heads);
 }
 
@@ -275,6 +275,9 @@ kvq_status kvq_decode(const kvq_cache_desc* cache, const void* q, int32_t batch,
   a.Hq = q_heads;
   a.G = q_heads / cache->num_kv_heads;
   a.seq_lens = seq_lens;
+  a.pos = nullptr;
+  a.seq_of = nullptr;
+  a.nseq = batch;
   a.table = block_table;
   a.mbps = max_blocks_per_seq;
   a.out = out;
@@ -284,6 +287,68 @@ kvq_status kvq_decode(const kvq_cache_desc* cache, const void* q, int32_t batch,
   a.lay = L;
   a.err = err_word;
   if (kvq::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_prefill(const kvq_cache_desc* cache, const void* q, int32_t n, int32_t q_heads,
+                       const int32_t* seq_idx, const int32_t* pos, const void* k_new, const void* v_new,
+                       const int32_t* block_table, int32_t batch, int32_t max_blocks_per_seq, void* out,
+                       int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes, int32_t stream_ctas,
+                       uint32_t* err_word, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (cache->window != 0) return KVQ_ERR_UNSUPPORTED;  // positions live in the block store only
+  st = check_decode_shape(cache, n, q_heads);
+  if (st != KVQ_OK) return st;
+  if (n == 0) return KVQ_OK;
+  if (!q || !seq_idx || !pos || !block_table || !out || max_blocks_per_seq < 1 || batch < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGNMENT;
+  if (stream_ctas < 0) return KVQ_ERR_INVALID_ARG;
+  const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, n, true);
+  if (P <= 0) return KVQ_ERR_CUDA;
+  const kvq::DecodeLayout L = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P);
+  if (!workspace || workspace_bytes < L.total) return KVQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVQ_ERR_ALIGNMENT;
+  if (k_new) {  // the chunk's own keys and values first: quantize-on-write
+    st = kvq_append(cache, k_new, v_new, n, seq_idx, pos, KVQ_APPEND_QUANT, block_table, batch, max_blocks_per_seq,
+                    err_word, stream);
+    if (st != KVQ_OK) return st;
+  }
+  kvq::DecodeArgs a;
+  a.c = view(cache);
+  a.q = static_cast<const uint16_t*>(q);
+  a.B = n;
+  a.Hq = q_heads;
+  a.G = q_heads / cache->num_kv_heads;
+  a.seq_lens = nullptr;
+  a.pos = pos;
+  a.seq_of = seq_idx;
+  a.nseq = batch;
+  a.table = block_table;
+  a.mbps = max_blocks_per_seq;
+  a.out = out;
+  a.out_fp32 = out_fp32 ? 1 : 0;
+  a.lse = lse;
+  a.ws = static_cast<uint8_t*>(workspace);
+  a.lay = L;
+  a.err = err_word;
+  if (kvq::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_prefill_workspace_size(const kvq_cache_desc* cache, int32_t n, int32_t q_heads, int32_t stream_ctas,
+                                      size_t* bytes) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!bytes) return KVQ_ERR_INVALID_ARG;
+  if (cache->window != 0) return KVQ_ERR_UNSUPPORTED;
+  st = check_decode_shape(cache, n, q_heads);
+  if (st != KVQ_OK) return st;
+  const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, n, true);
+  if (P <= 0) return KVQ_ERR_CUDA;
+  *bytes = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P).total;
   return KVQ_OK;
 }
 

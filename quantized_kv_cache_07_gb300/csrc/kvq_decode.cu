@@ -7,15 +7,15 @@
 
 namespace kvq {
 
-int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int q_bits, int B) {
-  if (q_bits == 32 && k_bits != 16) return decode_ctas_per_sm_q32(k_bits, v_bits, asym, B);
-  if (asym) return decode_ctas_per_sm_asym(k_bits, v_bits, B);
-  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, false, false>::ctas_per_sm(B);
-  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, false, false>::ctas_per_sm(B);
-  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, false, false>::ctas_per_sm(B);
-  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, false, false>::ctas_per_sm(B);
-  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, false, false>::ctas_per_sm(B);
-  if (k_bits == 16 && v_bits == 16) return Kernel<16, 16, false, false>::ctas_per_sm(B);
+int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int q_bits, int B, bool rows) {
+  if (q_bits == 32 && k_bits != 16) return decode_ctas_per_sm_q32(k_bits, v_bits, asym, B, rows);
+  if (asym) return decode_ctas_per_sm_asym(k_bits, v_bits, B, rows);
+  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, false, false>::ctas_per_sm(B, rows);
+  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, false, false>::ctas_per_sm(B, rows);
+  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, false, false>::ctas_per_sm(B, rows);
+  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, false, false>::ctas_per_sm(B, rows);
+  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, false, false>::ctas_per_sm(B, rows);
+  if (k_bits == 16 && v_bits == 16) return Kernel<16, 16, false, false>::ctas_per_sm(B, rows);
   return 0;
 }
 

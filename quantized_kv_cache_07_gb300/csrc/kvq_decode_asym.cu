@@ -5,12 +5,12 @@
 
 namespace kvq {
 
-int decode_ctas_per_sm_asym(int k_bits, int v_bits, int B) {
-  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, true, false>::ctas_per_sm(B);
-  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, true, false>::ctas_per_sm(B);
-  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, true, false>::ctas_per_sm(B);
-  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, true, false>::ctas_per_sm(B);
-  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, true, false>::ctas_per_sm(B);
+int decode_ctas_per_sm_asym(int k_bits, int v_bits, int B, bool rows) {
+  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, true, false>::ctas_per_sm(B, rows);
+  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, true, false>::ctas_per_sm(B, rows);
+  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, true, false>::ctas_per_sm(B, rows);
+  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, true, false>::ctas_per_sm(B, rows);
+  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, true, false>::ctas_per_sm(B, rows);
   return 0;
 }
 

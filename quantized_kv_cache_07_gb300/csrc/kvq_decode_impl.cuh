@@ -121,10 +121,11 @@ struct SmemMap {
   int len;       // int [B]
   int pre;       // int [B+1]
   int vpre;      // int [B+1]
+  int rows;      // int [B]: sequence of each row (prefill only)
   int total;
 };
 
-__host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, int B, bool loq) {
+__host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, int B, bool loq, bool rows) {
   SmemMap m;
   int o = stage_bytes_total;
   m.merge_o = o;  o += kConsumerWarps * 4 * kHeadDim * 4;
@@ -140,6 +141,7 @@ __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, i
   m.len = o;      o += ((B * 4 + 15) / 16) * 16;
   m.pre = o;      o += (((B + 1) * 4 + 15) / 16) * 16;
   m.vpre = o;     o += (((B + 1) * 4 + 15) / 16) * 16;
+  m.rows = o;     o += rows ? ((B * 4 + 15) / 16) * 16 : 0;
   m.total = o;
   return m;
 }
@@ -1047,7 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   const int P = prm.P, Uw = prm.Uw;
   const int H = a.c.H, G = a.G, B = a.B;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const SmemMap mp = smem_map(S * F::kStageBytes, S, B, LOQ);
+  const SmemMap mp = smem_map(S * F::kStageBytes, S, B, LOQ, a.pos != nullptr);
   Scratch sc;
   sc.merge_o = reinterpret_cast<float*>(smem + mp.merge_o);
   sc.merge_m = reinterpret_cast<float*>(smem + mp.merge_ml);
@@ -1065,6 +1067,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   int* len_s = reinterpret_cast<int*>(smem + mp.len);
   int* pre_s = reinterpret_cast<int*>(smem + mp.pre);
   int* vpre_s = reinterpret_cast<int*>(smem + mp.vpre);
+  int* rows_s = reinterpret_cast<int*>(smem + mp.rows);  // prefill: each row's sequence
   const int X = a.lay.switch_blocks;
 
   const int W = a.c.window;
@@ -1095,7 +1098,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- sequence geometry: clamped lengths and block prefix sums
-  scan_geometry(a, B, W, X, len_s, pre_s, vpre_s, [&](int b) { return a.seq_lens[b]; }, tid, warp, lane);
+  scan_geometry(a, B, W, X, len_s, pre_s, vpre_s, [&](int b) {
+    if (!a.pos) return a.seq_lens[b];
+    // prefill: row b is position pos[b] of sequence seq_of[b] and attends to 0..pos[b]
+    const int sb = a.seq_of[b];
+    if (sb < 0 || sb >= a.nseq) {
+      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_POSITION);
+      rows_s[b] = 0;
+      return 0;
+    }
+    rows_s[b] = sb;
+    return a.pos[b] + 1;
+  }, tid, warp, lane);
   const Geo geo{pre_s, vpre_s, B, H, X};
   const long long T = (long long)H * vpre_s[B];  // virtual blocks in total
   const int U = B * H;
@@ -1193,7 +1207,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const int idx = local + lane;
         int v = 0;
         if (idx < nblk) {
-          v = a.table[size_t(b) * a.mbps + idx];
+          v = a.table[size_t(a.pos ? rows_s[b] : b) * a.mbps + idx];
           if (v < 0 || v >= a.c.num_blocks) {
             flag(a.err, KVQ_DEVERR_BLOCK_ID);
             v = 0;
@@ -1379,7 +1393,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
 template <int KB, int VB, bool ASYM, bool LOQ>
 struct Kernel {
   using F = Fmt<KB, VB, ASYM>;
-  static int smem_bytes(int B) { return smem_map(F::kStages * F::kStageBytes, F::kStages, B, LOQ).total; }
+  static int smem_bytes(int B, bool rows) {
+    return smem_map(F::kStages * F::kStageBytes, F::kStages, B, LOQ, rows).total;
+  }
   // Allow the largest opt-in dynamic shared memory once per device; the
   // per-launch size (which depends on the batch) then always fits.
   static void ensure_attribute(int dev) {
@@ -1397,13 +1413,13 @@ struct Kernel {
                          cudaSharedmemCarveoutMaxShared);
     done[dev] = true;
   }
-  static int ctas_per_sm(int B) {
+  static int ctas_per_sm(int B, bool rows) {
     static std::mutex mu;
     static std::map<std::pair<int, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
     ensure_attribute(dev);
-    const int smem = smem_bytes(B);
+    const int smem = smem_bytes(B, rows);
     std::lock_guard<std::mutex> lk(mu);
     auto key = std::make_pair(dev, smem);
     auto itc = cache.find(key);
@@ -1416,7 +1432,7 @@ struct Kernel {
     return n;
   }
   static cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
-    const int smem = smem_bytes(a.B);
+    const int smem = smem_bytes(a.B, a.pos != nullptr);
     int dev = 0;
     cudaGetDevice(&dev);
     ensure_attribute(dev);

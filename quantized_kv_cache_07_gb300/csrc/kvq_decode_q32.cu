@@ -6,20 +6,20 @@
 
 namespace kvq {
 
-int decode_ctas_per_sm_q32(int k_bits, int v_bits, bool asym, int B) {
+int decode_ctas_per_sm_q32(int k_bits, int v_bits, bool asym, int B, bool rows) {
   if (asym) {
-    if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, true, true>::ctas_per_sm(B);
-    if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, true, true>::ctas_per_sm(B);
-    if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, true, true>::ctas_per_sm(B);
-    if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, true, true>::ctas_per_sm(B);
-    if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, true, true>::ctas_per_sm(B);
+    if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, true, true>::ctas_per_sm(B, rows);
+    if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, true, true>::ctas_per_sm(B, rows);
+    if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, true, true>::ctas_per_sm(B, rows);
+    if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, true, true>::ctas_per_sm(B, rows);
+    if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, true, true>::ctas_per_sm(B, rows);
     return 0;
   }
-  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, false, true>::ctas_per_sm(B);
-  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, false, true>::ctas_per_sm(B);
-  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, false, true>::ctas_per_sm(B);
-  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, false, true>::ctas_per_sm(B);
-  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, false, true>::ctas_per_sm(B);
+  if (k_bits == 8 && v_bits == 8) return Kernel<8, 8, false, true>::ctas_per_sm(B, rows);
+  if (k_bits == 4 && v_bits == 4) return Kernel<4, 4, false, true>::ctas_per_sm(B, rows);
+  if (k_bits == 4 && v_bits == 8) return Kernel<4, 8, false, true>::ctas_per_sm(B, rows);
+  if (k_bits == 8 && v_bits == 4) return Kernel<8, 4, false, true>::ctas_per_sm(B, rows);
+  if (k_bits == 2 && v_bits == 2) return Kernel<2, 2, false, true>::ctas_per_sm(B, rows);
   return 0;
 }
 

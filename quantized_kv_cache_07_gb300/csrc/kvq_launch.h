@@ -60,6 +60,11 @@ struct DecodeArgs {
   const uint16_t* q;  // bf16 [B][Hq][128]
   int B, Hq, G;
   const int* seq_lens;
+  // Prefill (pos != null): row b of the call is position pos[b] of sequence
+  // seq_of[b] (< nseq); it attends to positions 0..pos[b] of that sequence.
+  const int* pos;
+  const int* seq_of;
+  int nseq;
   const int* table;
   int mbps;
   void* out;
@@ -79,13 +84,13 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 // Resident decode CTAs per SM for this cache format and batch (occupancy
 // query on the current device, cached); 0 for an unsupported format.
-int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int q_bits, int batch);
+int decode_ctas_per_sm_for(int k_bits, int v_bits, bool asym, int q_bits, int batch, bool rows = false);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 // The asymmetric instantiations (kvq_decode_asym.cu).
-int decode_ctas_per_sm_asym(int k_bits, int v_bits, int batch);
+int decode_ctas_per_sm_asym(int k_bits, int v_bits, int batch, bool rows);
 cudaError_t launch_decode_asym(const DecodeArgs& a, cudaStream_t s);
 // The two-part fp16 query instantiations (kvq_decode_q32.cu).
-int decode_ctas_per_sm_q32(int k_bits, int v_bits, bool asym, int batch);
+int decode_ctas_per_sm_q32(int k_bits, int v_bits, bool asym, int batch, bool rows);
 cudaError_t launch_decode_q32(const DecodeArgs& a, cudaStream_t s);
 
 }  // namespace kvq

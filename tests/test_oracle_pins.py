@@ -807,3 +807,45 @@ def test_two_bit_sequence_reconstruction_and_bytes():
     assert O.metadata_fraction(128, 2, 4) == 0.125               # the per-token cost it avoids
     with pytest.raises(ValueError):
         O.quantize_sequence(k, v, 2, 8)
+
+
+# ---------------------------------------------------------------- chunked prefill (causal rows)
+def test_prefill_rows_match_torch_sdpa_with_a_causal_offset_mask():
+    """Rows of a chunk at positions p0..p0+C-1 attend to keys 0..p (plain bf16
+    values, no quantization): equal to the library routine with a boolean mask
+    key <= position, in float64."""
+    rng = np.random.default_rng(41)
+    L, H, D, G, C = 37, 2, 128, 4, 9
+    k = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    v = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    st = O.quantize_sequence(k, v, 16, 16)
+    pos = np.arange(L - C, L)
+    q = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((C, G, D)).astype(np.float32)))
+    for h in range(H):
+        o, lse = O.prefill_attention(q, st, h, pos)
+        mask = torch.from_numpy(np.arange(L)[None, :] <= pos[:, None])            # [C, L]
+        qt = torch.from_numpy(q.transpose(1, 0, 2))                                 # [G, C, D]
+        kt = torch.from_numpy(k[:, h])[None].expand(G, L, D)
+        vt = torch.from_numpy(v[:, h])[None].expand(G, L, D)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask[None])
+        np.testing.assert_allclose(o.transpose(1, 0, 2), ref.numpy(), rtol=0, atol=1e-12)
+        assert lse.shape == (C, G) and np.all(np.isfinite(lse))
+
+
+def test_prefill_last_row_is_the_decode_of_the_whole_sequence():
+    """The chunk's last row sees every stored position: it is the decode step
+    over the whole (quantized) sequence; a row at position 0 sees one key."""
+    rng = np.random.default_rng(42)
+    L, H, D = 50, 2, 128
+    k = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    v = O.bf16_to_f64(f32_to_bf16_bits(rng.standard_normal((L, H, D)).astype(np.float32)))
+    st = O.quantize_sequence(k, v, 4, 8)
+    qb = f32_to_bf16_bits(rng.standard_normal((2 * H, D)).astype(np.float32))
+    o_dec, l_dec = O.decode_sequence(qb, st, H)
+    q = O.bf16_to_f64(qb)
+    for h in range(H):
+        o, lse = O.prefill_attention(q[None, 2 * h:2 * h + 2], st, h, np.array([L - 1]))
+        assert np.array_equal(o[0], o_dec[2 * h:2 * h + 2]) and np.array_equal(lse[0], l_dec[2 * h:2 * h + 2])
+        o0, _ = O.prefill_attention(q[None, 2 * h:2 * h + 2], st, h, np.array([0]))
+        _, v_hat = O.reconstruct_sequence(st, h)
+        assert np.array_equal(o0[0], np.broadcast_to(v_hat[0], (2, D)))
