@@ -142,7 +142,7 @@ typedef struct {
    * weights p * s_v as fp16 (default).  32 (two-part mode): the query and the
    * value weights each carried as an fp16 high part plus an fp16 low part
    * (about 22 significant bits; one more MMA per k-slice of each contraction:
-   * 4-8 % more time measured), for scores large enough that 11 bits of query
+   * 6-15 % more time measured), for scores large enough that 11 bits of query
    * cost more than the output tolerance, and so that results do not depend on
    * how the token range is split beyond fp32 rounding.  8: each query row, after
    * the per-channel key factor is multiplied onto it in float32, is quantized
