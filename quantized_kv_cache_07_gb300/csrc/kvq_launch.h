@@ -75,7 +75,8 @@ struct DecodeArgs {
   uint32_t* err;
 };
 
-// Partial-result records hold this many query rows (G <= 8).
+// The largest GQA group (query heads per KV head) the decode kernel takes: one
+// 8-wide MMA tile of query columns.
 constexpr int kMaxGroup = 8;
 
 DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas);
