@@ -660,3 +660,41 @@ def test_full_size_workload(name):
         # properties that hold for every unit: finite outputs and lse
         assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
     assert run.err_bits() == 0
+
+
+# ---------------------------------------------------------------- seeded random configurations
+def _random_workload(i):
+    """A valid small workload drawn from the whole option space (seeded)."""
+    rng = np.random.default_rng(1000 + i)
+    kb, vb = [(8, 8), (4, 4), (4, 8), (8, 4), (2, 2), (16, 16)][int(rng.integers(6))]
+    quant = kb != 16
+    G = int(rng.choice([1, 2, 4, 8]))
+    H = int(rng.integers(1, 4))
+    kw = dict(batch=int(rng.integers(1, 5)), q_heads=G * H, kv_heads=H, k_bits=kb, v_bits=vb,
+              len_range=(1, int(rng.integers(20, 400))), paged=bool(rng.integers(2)),
+              k_dist=str(rng.choice(["normal", "t3"])), outlier_channels=int(rng.choice([0, 4])))
+    if quant:
+        kw["asym"] = bool(rng.integers(2))
+        kw["channel_factor"] = bool(rng.integers(2))
+        if kw["channel_factor"] and not kw["asym"] and kb != 2 and rng.integers(3) == 0:
+            kw["k_per_channel"] = True
+        kw["q_bits"] = int(rng.choice([16, 32, 8]))
+    kw["window"] = int(rng.choice([0, 16, 48]))
+    if kw.get("q_bits") == 8 and kw.get("channel_factor") and kw["window"]:
+        kw["q_bits"] = 16                    # int8 query rows, a factor and a window: refused by the library
+    if kw.get("k_per_channel") and kw.get("q_bits") == 16 and kw["k_dist"] == "t3":
+        kw["q_bits"] = 32                    # heavy tails under per-channel scales need the two-part query
+    kw["append_one"] = kb != 2 and not kw["window"] and bool(rng.integers(2))
+    return small_workload(f"random_{i}", **kw)
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_configuration_matches_the_oracle(i):
+    w = _random_workload(i)
+    inp = make_inputs(w)
+    run = DeviceRun(inp)
+    check_stored_cache(inp, run)                 # codes, scales, zero points and ring: bit for bit
+    out, lse = run.decode(out_fp32=True)
+    worst = compare_outputs(inp, out, lse, oracle_decode(inp), out_is_bf16=False)
+    assert worst <= 1.0, f"{w}: max error ratio {worst:.3f}"
+    assert run.err_bits() == 0
