@@ -27,7 +27,8 @@
  * Cache layout (device memory, all pools 16-byte aligned)
  *   Codes pool  : [num_kv_heads][num_blocks][block_bytes] (head-major, so the
  *                 consecutive blocks of one head are adjacent in memory), with
- *                 block_bytes = 16 * 128 * bits / 8 (int4 1024, int8 2048, bf16 4096).
+ *                 block_bytes = 16 * 128 * bits / 8 (int2 512, int4 1024, int8 2048,
+ *                 bf16 4096).
  *                 Inside a block the bytes are ordered so that each lane of a
  *                 warp reads its tensor-core operand with one 16-byte load per
  *                 512-byte chunk ("fragment-native" order).  Let lane = 4*g + t.
@@ -114,16 +115,19 @@ typedef struct {
   int32_t head_dim;       /* must be 128                                            */
   int32_t block_size;     /* must be 16                                             */
   int32_t num_blocks;     /* physical blocks in each pool                           */
-  int32_t k_bits;         /* 8 or 4 (quantized), or 16 together with v_bits = 16    */
-  int32_t v_bits;         /* 8 or 4, or 16                                          */
+  int32_t k_bits;         /* 8 or 4 (quantized), 2 together with v_bits = 2 (token- */
+                          /* group scales, see kvq_append), or 16 together with     */
+                          /* v_bits = 16 (plain bf16 cache)                         */
+  int32_t v_bits;         /* 8 or 4, 2 with k_bits = 2, or 16 with k_bits = 16      */
   void* k_codes;          /* codes pool for keys (see layout above)                 */
   void* v_codes;          /* codes pool for values                                  */
   float* meta;            /* metadata pool (layout above); NULL for a bf16 cache    */
   /* Asymmetric format ([P1] "Quantization granularity defines which values
    * share a scale": a scale and, depending on the scheme, a zero point; [P3]
    * "Per-token scales and where they can live": a scale and zero point cost
-   * twice the metadata).  0: symmetric codes.  1 (8- or 4-bit blocks only): per
-   * token per head m = min(x), s = RN32((max(x) - min(x)) / (2^bits - 1))
+   * twice the metadata).  0: symmetric codes.  1 (8-, 4- or 2-bit blocks): per
+   * token per head (2-bit blocks: per 16-token group per head, over all the
+   * group's values) m = min(x), s = RN32((max(x) - min(x)) / (2^bits - 1))
    * (difference and quotient in double; a constant vector stores s = 1), u =
    * clamp(round_half_even((x - m) / s), 0, 2^bits - 1) with the difference and
    * quotient in double, x_hat = u * s + m; K and V both. */
@@ -149,7 +153,7 @@ typedef struct {
    * per row with the symmetric int8 rule of kvq_append (s_q = RN32(max|x| /
    * 127), q_int = clamp(round_half_even(x / s_q))) and the score is
    * s_q * s_k * (q_int . k_int) / sqrt(D), the integer dot exact; bf16 window
-   * keys see q_int * s_q.  Needs 8- or 4-bit blocks; not combined with both a
+   * keys see q_int * s_q.  Needs 8-, 4- or 2-bit blocks; not combined with both a
    * per-channel key factor and a window (KVQ_ERR_UNSUPPORTED). */
   int32_t q_bits;
   /* Per-channel key scales only ([P3] "The axis choice is a kernel decision":
@@ -166,7 +170,7 @@ typedef struct {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* kvq_status_string(kvq_status status);
 
-/* Bytes of one 16-token block of one KV head for a code width (4, 8 or 16). */
+/* Bytes of one 16-token block of one KV head for a code width (2, 4, 8 or 16). */
 kvq_status kvq_block_bytes(int32_t bits, size_t* bytes);
 
 /*
@@ -184,6 +188,17 @@ kvq_status kvq_block_bytes(int32_t bits, size_t* bytes);
  * x / s.  With asym = 1 the
  * asymmetric quantizer of kvq_cache_desc is used instead and the zero point is
  * stored beside the scale.
+ * 2-bit caches ([P3] "Per-token scales and where they can live": several
+ * tokens under one scale): the unit of quantization is the 16-token block of
+ * one head.  The same rule (qmax = 1, codes in [-1, 1]; asymmetric u in
+ * [0, 3]) is applied to all of a block's present values as one vector, after
+ * the per-channel key factor division; absent tokens of a block (the tail of a
+ * sequence) store code 0 and are never read.  KVQ_APPEND_QUANT writes a block
+ * whole: the rows of one call at positions 16j, 16j+1, ... of one sequence
+ * must follow each other in the call, led by the row at 16j (up to 16 rows); a
+ * row that is not part of such a run sets KVQ_DEVERR_POSITION and is skipped.
+ * KVQ_APPEND_STEP is refused (KVQ_ERR_UNSUPPORTED): a growing 2-bit cache keeps
+ * its recent tokens in the bf16 window (RING) and quantizes whole blocks.
  *   k_new, v_new : device bf16 [n][num_kv_heads][128]
  *   n            : number of new tokens (0 is a no-op)
  *   seq_idx, pos : device int32 [n]; token r belongs to sequence seq_idx[r] at
