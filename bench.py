@@ -155,6 +155,27 @@ def cache_bytes_per_step(inp) -> int:
     return w.kv_heads * per_q * int(sum(L))
 
 
+# Chunked prefill (kvq_prefill): each of `batch` sequences holds a quantized
+# prefix and takes a chunk of new positions in one call, which quantizes them
+# into the cache and lets each attend causally to its sequence up to itself.
+PREFILL = dict(name="prefill_int8_b8_prefix1920_chunk128", batch=8, q_heads=32, kv_heads=8, k_bits=8, v_bits=8,
+               prefix=1920, chunk=128)
+# The 2-bit token-group format is timed on the shape of this workload.
+INT2_SHAPE = "int4_factor_b32_len1k_8k"
+
+
+def token_head_bytes(k_bits: int, v_bits: int) -> int:
+    """Stored bytes of one token of one KV head in the symmetric 8-/4-bit
+    formats: K and V codes plus one fp32 scale each."""
+    return 128 * k_bits // 8 + 128 * v_bits // 8 + 8
+
+
+def prefill_row_bytes(prefix: int, chunk: int, batch: int, kv_heads: int, per_token: int) -> int:
+    """Cache bytes the rows of one prefill call read: the row at position p
+    attends to positions 0..p of its sequence, for every KV head."""
+    return batch * kv_heads * per_token * sum(p + 1 for p in range(prefix, prefix + chunk))
+
+
 # ------------------------------------------------------------------ reference arm / CPU baseline
 CPU_SAMPLE_SNIPPET = r"""
 import json, os, sys, time
@@ -462,6 +483,79 @@ class GpuArm:
         torch.cuda.empty_cache()
         return res
 
+    def prefill(self, K: int):
+        """kvq_prefill on the PREFILL recipe: K calls back to back, with the
+        chunk's quantizing write fused into the call and without it."""
+        import numpy as np
+        from quantized_kv_cache_07_gb300.cache import cache_for_inputs
+        from synth import Workload, make_inputs, query_rows
+        torch, _lib, dev = self.torch, self.lib, self.dev
+        r = PREFILL
+        L = r["prefix"] + r["chunk"]
+        w = Workload(r["name"], batch=r["batch"], q_heads=r["q_heads"], kv_heads=r["kv_heads"],
+                     k_bits=r["k_bits"], v_bits=r["v_bits"], seq_len=L, paged=True)
+        inp = make_inputs(w)
+        B, Hq = w.batch, w.q_heads
+        cache = cache_for_inputs(inp, dev)
+        table = torch.from_numpy(inp.block_table).to(dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def bits(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        def rows(p0, p1):
+            idx = np.concatenate([inp.seq_offsets[b] + np.arange(p0, p1) for b in range(B)])
+            seq = np.repeat(np.arange(B, dtype=np.int32), p1 - p0)
+            pos = np.tile(np.arange(p0, p1, dtype=np.int32), B)
+            return idx, torch.from_numpy(seq).to(dev), torch.from_numpy(pos).to(dev)
+
+        pi, ps, pp = rows(0, r["prefix"])
+        _lib.kvq_append(cache.desc, bits(inp.k[pi]), bits(inp.v[pi]), ps, pp, _lib.APPEND_QUANT, table, B,
+                        inp.max_blocks, err_word=err)
+        ci, cs, cp = rows(r["prefix"], L)
+        n = len(ci)
+        kn, vn = bits(inp.k[ci]), bits(inp.v[ci])
+        q = bits(query_rows(n, Hq, w.seed + 1))
+        out = torch.empty((n, Hq, 128), dtype=torch.bfloat16, device=dev)
+        nb = _lib.kvq_prefill_workspace_size(cache.desc, n, Hq)
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=dev)
+        times = {}
+        for fused in (True, False):
+            def call():
+                _lib.kvq_prefill(cache.desc, q, Hq, cs, cp, table, B, inp.max_blocks, out,
+                                 k_new=kn if fused else None, v_new=vn if fused else None, workspace=ws,
+                                 workspace_bytes=nb, err_word=err)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_device(torch)
+            e0.record()
+            for _ in range(K):
+                call()
+            e1.record()
+            torch.cuda.synchronize()
+            times[fused] = e0.elapsed_time(e1) / K
+        per_token = token_head_bytes(w.k_bits, w.v_bits)
+        req = prefill_row_bytes(r["prefix"], r["chunk"], B, w.kv_heads, per_token)
+        uniq = B * w.kv_heads * per_token * L
+        res = {"workload": w.name,
+               "description": f"chunked prefill: {B} sequences x ({r['prefix']} cached + {r['chunk']} new "
+                              f"positions), {Hq}/{w.kv_heads} heads, int{w.k_bits} K/V, paged; the new "
+                              "positions are quantized into the cache and attend causally in the same call",
+               "rows_per_call": n, "ms_per_call": round(times[True], 6),
+               "ms_per_call_attention_only": round(times[False], 6),
+               "rows_per_s": round(n / (times[True] / 1e3), 1),
+               "row_read_bytes_per_call": req,
+               "row_read_gbs": round(req / (times[False] / 1e3) / 1e9, 1),
+               "cache_bytes": uniq,
+               "note": "each row is one query group of the decode kernel's split and reads its whole prefix "
+                       "(mostly from L2): the bound is the per-block work of the rows, not HBM",
+               "err_word": int(err.item())}
+        del cache, ws, out, q, kn, vn
+        torch.cuda.empty_cache()
+        return res
+
 
 def hold_device(torch, cycles: int = 1_000_000):
     """Queue a short device-side wait (about 0.5 ms) ahead of a timed region,
@@ -533,6 +627,8 @@ def main():
                     help="time the workload in the asymmetric (scale + zero point) format")
     ap.add_argument("--q-bits", type=int, default=16, choices=[8, 16, 32],
                     help="query format: 8 int8 rows (integer dot), 16 fp16 (default), 32 two-part fp16")
+    ap.add_argument("--no-int2", action="store_true", help="skip the 2-bit run on the int4 workload's shape")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the kvq_prefill measurement")
     ap.add_argument("--no-qint8", action="store_true",
                     help="skip the same-shape run with int8-quantized query rows")
     ap.add_argument("--no-per-config", action="store_true",
@@ -638,8 +734,18 @@ def main():
             entry["bf16_same_design"] = (None if args.no_bf16 else
                                          dict(workload=n + "_bf16", **bf16_entry(arm.run(bf16_inputs(inn)), rn,
                                                                                  peak)))
+            if n == INT2_SHAPE and not args.no_int2:
+                import dataclasses
+                w2 = wn.with_(k_bits=2, v_bits=2, name=n.replace("int4", "int2"))
+                r2 = arm.run(dataclasses.replace(inn, workload=w2))     # same bits, 2-bit token groups
+                entry["int2_same_shape"] = {
+                    "workload": w2.name, "ms_per_step": round(r2["ms_step"], 6), "bytes_per_step": r2["bytes"],
+                    "effective_gbs": round(r2["bytes"] / (r2["dec_ms"] / 1e3) / 1e9, 1),
+                    "frac_of_peak": round(r2["bytes"] / (r2["dec_ms"] / 1e3) / 1e9 / peak, 4),
+                    "time_vs_int4": round(r2["dec_ms"] / rn["dec_ms"], 4), "err_word": r2["err"]}
             del inn
         per_config[n] = entry
+    prefill = None if (args.no_prefill or world > 1) else arm.prefill(args.steps)
 
     line = {
         "metric": "quantized-KV decode attention: effective HBM GB/s (% of peak), steps/s",
@@ -680,6 +786,7 @@ def main():
         "bf16_same_design": bf16,
         "asym_same_shape": asym,
         "qint8_same_shape": qint8,
+        "prefill": prefill,
         "device_err_word": res["err"],
     }
     if per_config:

@@ -205,6 +205,13 @@ def make_inputs(w: Workload, seed: int | None = None) -> Inputs:
                   channel_factor=factor, outlier_ids=outliers)
 
 
+def query_rows(n: int, q_heads: int, seed: int) -> np.ndarray:
+    """Seeded query rows for a prefill chunk: N(0, 1) in float32 rounded to
+    bf16, uint16 bits [n, q_heads, 128]."""
+    rng = np.random.default_rng(seed)
+    return f32_to_bf16_bits(rng.standard_normal((n, q_heads, HEAD_DIM), dtype=np.float32))
+
+
 def shard_units(num_units: int, rank: int, world: int) -> range:
     """Contiguous share of ``num_units`` independent work units for one rank."""
     per, rem = divmod(num_units, world)

@@ -43,3 +43,17 @@ def test_bench_bytes_per_channel_keys_drop_the_key_scales():
     tokens = int(np.sum(inp.decode_lengths)) * w.kv_heads
     assert bench.cache_bytes_per_step(base) - bench.cache_bytes_per_step(inp) == 4 * tokens
     assert bench.cache_bytes_per_step(inp) == expected_bytes(inp)
+
+
+@pytest.mark.parametrize("bits", [(8, 8), (4, 4), (4, 8)])
+def test_token_head_bytes_match_oracle_accounting(bits):
+    assert bench.token_head_bytes(*bits) == O.cache_bytes_per_token_head(128, *bits)
+
+
+def test_prefill_row_bytes_count_every_row_prefix():
+    """Each row at position p reads positions 0..p of its sequence: brute force
+    over the rows of a small chunked-prefill call."""
+    prefix, chunk, batch, heads, per = 37, 5, 3, 2, 264
+    rows = [(b, p) for b in range(batch) for p in range(prefix, prefix + chunk)]
+    total = sum(len(range(0, p + 1)) * per * heads for _, p in rows)
+    assert bench.prefill_row_bytes(prefix, chunk, batch, heads, per) == total

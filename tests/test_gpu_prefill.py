@@ -61,9 +61,8 @@ def _run(fmt, chunk=24, fused=True, stream_ctas=0, seed=5):
     pos = np.concatenate([list(chunk_pos[b]) for b in range(w.batch)]).astype(np.int32)
     rows = np.concatenate([inp.seq_offsets[b] + np.asarray(chunk_pos[b], dtype=np.int64) for b in range(w.batch)])
     n = len(seq)
-    rng = np.random.default_rng(seed)
-    from synth import f32_to_bf16_bits
-    qbits = f32_to_bf16_bits(rng.standard_normal((n, w.q_heads, 128)).astype(np.float32))
+    from synth import query_rows
+    qbits = query_rows(n, w.q_heads, seed)
     out = torch.zeros((n, w.q_heads, 128), dtype=torch.float32, device="cuda")
     lse = torch.zeros((n, w.q_heads), dtype=torch.float32, device="cuda")
     nb = _lib.kvq_prefill_workspace_size(cache.desc, n, w.q_heads, stream_ctas)
