@@ -517,14 +517,18 @@ class GpuArm:
         kn, vn = bits(inp.k[ci]), bits(inp.v[ci])
         q = bits(query_rows(n, Hq, w.seed + 1))
         out = torch.empty((n, Hq, 128), dtype=torch.bfloat16, device=dev)
-        nb = _lib.kvq_prefill_workspace_size(cache.desc, n, Hq)
+        split = 3 * torch.cuda.get_device_properties(dev).multi_processor_count
+        nb = _lib.kvq_prefill_workspace_size(cache.desc, n, Hq, split)
         ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=dev)
+        _lib.kvq_workspace_init(ws, nb)
         times = {}
-        for fused in (True, False):
+        # (fused write, path): the query-tile path with and without the write,
+        # and the split-rows path (every row a query group of the decode split)
+        for fused, path in ((True, _lib.PREFILL_TILES), (False, _lib.PREFILL_TILES), (False, split)):
             def call():
                 _lib.kvq_prefill(cache.desc, q, Hq, cs, cp, table, B, inp.max_blocks, out,
                                  k_new=kn if fused else None, v_new=vn if fused else None, workspace=ws,
-                                 workspace_bytes=nb, err_word=err)
+                                 workspace_bytes=nb, stream_ctas=path, err_word=err)
             for _ in range(3):
                 call()
             torch.cuda.synchronize()
@@ -535,7 +539,7 @@ class GpuArm:
                 call()
             e1.record()
             torch.cuda.synchronize()
-            times[fused] = e0.elapsed_time(e1) / K
+            times[(fused, path)] = e0.elapsed_time(e1) / K
         per_token = token_head_bytes(w.k_bits, w.v_bits)
         req = prefill_row_bytes(r["prefix"], r["chunk"], B, w.kv_heads, per_token)
         uniq = B * w.kv_heads * per_token * L
@@ -543,14 +547,17 @@ class GpuArm:
                "description": f"chunked prefill: {B} sequences x ({r['prefix']} cached + {r['chunk']} new "
                               f"positions), {Hq}/{w.kv_heads} heads, int{w.k_bits} K/V, paged; the new "
                               "positions are quantized into the cache and attend causally in the same call",
-               "rows_per_call": n, "ms_per_call": round(times[True], 6),
-               "ms_per_call_attention_only": round(times[False], 6),
-               "rows_per_s": round(n / (times[True] / 1e3), 1),
+               "rows_per_call": n, "path": "query tiles (16 query vectors per CTA)",
+               "ms_per_call": round(times[(True, _lib.PREFILL_TILES)], 6),
+               "ms_per_call_attention_only": round(times[(False, _lib.PREFILL_TILES)], 6),
+               "rows_per_s": round(n / (times[(True, _lib.PREFILL_TILES)] / 1e3), 1),
+               "ms_per_call_split_rows_attention_only": round(times[(False, split)], 6),
+               "tiles_speedup_vs_split_rows": round(times[(False, split)] / times[(False, _lib.PREFILL_TILES)], 3),
                "row_read_bytes_per_call": req,
-               "row_read_gbs": round(req / (times[False] / 1e3) / 1e9, 1),
                "cache_bytes": uniq,
-               "note": "each row is one query group of the decode kernel's split and reads its whole prefix "
-                       "(mostly from L2): the bound is the per-block work of the rows, not HBM",
+               "note": "causal attention of every row over its whole prefix: the tile path reads each "
+                       "(sequence, KV head) prefix once per 16 query vectors, the split-rows path once per row "
+                       "(mostly from L2); neither is bound by HBM",
                "err_word": int(err.item())}
         del cache, ws, out, q, kn, vn
         torch.cuda.empty_cache()

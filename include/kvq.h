@@ -109,6 +109,9 @@ typedef enum {
                            /* pos >= window) leaves the ring and is quantized into the  */
                            /* block store, then the new token enters the ring           */
 
+/* kvq_prefill: stream_ctas value that selects the query-tile path */
+#define KVQ_PREFILL_TILES (-1)
+
 /* Description of one layer's cache.  Every pointer is caller-owned device memory. */
 typedef struct {
   int32_t num_kv_heads;   /* H_kv >= 1                                              */
@@ -326,9 +329,22 @@ kvq_status kvq_decode_static_scratch(const kvq_cache_desc* cache, const void* q,
  *   score_i = q[r][hq] . k_hat_i / sqrt(D), over positions 0..pos[r] of
  *   sequence seq_idx[r], read from the quantized blocks as kvq_decode reads them.
  * The write and the attention are two launches in stream order (the second
- * starts under programmatic dependent launch and waits for the first).  Every
- * row is one query group of the decode kernel's split, so rows of one
- * sequence read overlapping prefixes (mostly from L2 when they run together).
+ * starts under programmatic dependent launch and waits for the first).  Two
+ * attention paths, chosen by stream_ctas:
+ *   KVQ_PREFILL_TILES (-1): query tiles.  A CTA takes 16 / G consecutive rows
+ *     x the G query heads of one KV head (16 query vectors, one tensor-core
+ *     row tile) and streams the blocks of their sequence once for all of
+ *     them; rows of one tile that belong to different sequences are taken in
+ *     turn.  Symmetric 8-/4-bit caches with q_bits 0/16 only
+ *     (KVQ_ERR_UNSUPPORTED otherwise); needs no workspace (NULL accepted).
+ *   > 0: split rows.  Every row is one query group of the decode kernel's
+ *     split over that many stream CTAs, so rows of one sequence read
+ *     overlapping prefixes (mostly from L2 when they run together).  Every
+ *     cache format.
+ *   0: the tile path when the cache format allows it and there are at least
+ *     as many (tile, KV head) pairs as SMs; split rows otherwise.
+ * Both paths compute the same attention within the output tolerance (they
+ * differ in rounding order only).
  *   q          : device bf16 [n][q_heads][128]
  *   seq_idx,pos: device int32 [n] (as kvq_append); a row with a sequence outside
  *                [0, batch) sets KVQ_DEVERR_POSITION and gets out = 0, lse = -inf
@@ -339,6 +355,7 @@ kvq_status kvq_decode_static_scratch(const kvq_cache_desc* cache, const void* q,
  *   block_table: device int32 [batch][max_blocks_per_seq]
  *   out, lse   : device [n][q_heads][128] (bf16 or float32), float [n][q_heads] or NULL
  *   workspace  : >= kvq_prefill_workspace_size bytes, zeroed once by kvq_workspace_init
+ *                (the split-rows path; unused by the tile path)
  * Requirements: window == 0 (KVQ_ERR_UNSUPPORTED otherwise), n <= 4096, the
  * kvq_decode requirements on q_heads.
  */
@@ -348,7 +365,9 @@ kvq_status kvq_prefill(const kvq_cache_desc* cache, const void* q, int32_t n, in
                        int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes, int32_t stream_ctas,
                        uint32_t* err_word, void* stream);
 
-/* Workspace bytes kvq_prefill needs for n rows on the current device. */
+/* Workspace bytes kvq_prefill needs for n rows on the current device with
+ * this stream_ctas (0 for KVQ_PREFILL_TILES; with 0 the split-rows size, since
+ * the automatic choice may take that path). */
 kvq_status kvq_prefill_workspace_size(const kvq_cache_desc* cache, int32_t n, int32_t q_heads, int32_t stream_ctas,
                                       size_t* bytes);
 

@@ -30,6 +30,7 @@ KVQ_DEVERR_POSITION = 16
 APPEND_QUANT = 0
 APPEND_RING = 1
 APPEND_STEP = 2
+PREFILL_TILES = -1  # kvq_prefill stream_ctas: the query-tile path
 
 
 class KvqError(RuntimeError):

@@ -107,6 +107,14 @@ kvq_status check_decode_shape(const kvq_cache_desc* c, int batch, int q_heads) {
   return KVQ_OK;
 }
 
+// CTAs of the prefill tile path: 16 / G consecutive rows x G heads per tile,
+// one CTA per (tile, KV head).
+long long prefill_tiles(int n, int q_heads, int kv_heads) {
+  const int G = q_heads / kv_heads;
+  const int TR = 16 / G;
+  return (long long)((n + TR - 1) / TR) * kv_heads;
+}
+
 }  // namespace
 
 namespace kvq {
@@ -305,12 +313,26 @@ kvq_status kvq_prefill(const kvq_cache_desc* cache, const void* q, int32_t n, in
     return KVQ_ERR_INVALID_ARG;
   if ((k_new == nullptr) != (v_new == nullptr)) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGNMENT;
-  if (stream_ctas < 0) return KVQ_ERR_INVALID_ARG;
-  const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, n, true);
-  if (P <= 0) return KVQ_ERR_CUDA;
-  const kvq::DecodeLayout L = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P);
-  if (!workspace || workspace_bytes < L.total) return KVQ_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return KVQ_ERR_ALIGNMENT;
+  if (stream_ctas < 0 && stream_ctas != KVQ_PREFILL_TILES) return KVQ_ERR_INVALID_ARG;
+  const bool tiles_ok = kvq::prefill_tiles_supported(view(cache));
+  if (stream_ctas == KVQ_PREFILL_TILES && !tiles_ok) return KVQ_ERR_UNSUPPORTED;
+  bool tiles = stream_ctas == KVQ_PREFILL_TILES;
+  if (stream_ctas == 0 && tiles_ok) {
+    // enough 16-vector tiles to fill the GPU: the tile path; else split rows
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      return KVQ_ERR_CUDA;
+    tiles = prefill_tiles(n, q_heads, cache->num_kv_heads) >= (long long)sms;
+  }
+  kvq::DecodeLayout L{};
+  if (!tiles) {
+    const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, n, true);
+    if (P <= 0) return KVQ_ERR_CUDA;
+    L = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P);
+    if (!workspace || workspace_bytes < L.total) return KVQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KVQ_ERR_ALIGNMENT;
+  }
   if (k_new) {  // the chunk's own keys and values first: quantize-on-write
     st = kvq_append(cache, k_new, v_new, n, seq_idx, pos, KVQ_APPEND_QUANT, block_table, batch, max_blocks_per_seq,
                     err_word, stream);
@@ -334,7 +356,9 @@ kvq_status kvq_prefill(const kvq_cache_desc* cache, const void* q, int32_t n, in
   a.ws = static_cast<uint8_t*>(workspace);
   a.lay = L;
   a.err = err_word;
-  if (kvq::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  const cudaError_t e = tiles ? kvq::launch_prefill_tiles(a, static_cast<cudaStream_t>(stream))
+                              : kvq::launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }
 
@@ -346,6 +370,12 @@ kvq_status kvq_prefill_workspace_size(const kvq_cache_desc* cache, int32_t n, in
   if (cache->window != 0) return KVQ_ERR_UNSUPPORTED;
   st = check_decode_shape(cache, n, q_heads);
   if (st != KVQ_OK) return st;
+  if (stream_ctas < 0 && stream_ctas != KVQ_PREFILL_TILES) return KVQ_ERR_INVALID_ARG;
+  if (stream_ctas == KVQ_PREFILL_TILES) {  // the tile path needs no workspace
+    if (!kvq::prefill_tiles_supported(view(cache))) return KVQ_ERR_UNSUPPORTED;
+    *bytes = 0;
+    return KVQ_OK;
+  }
   const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, n, true);
   if (P <= 0) return KVQ_ERR_CUDA;
   *bytes = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P).total;

@@ -47,7 +47,7 @@ def header_constants():
     out = {}
     for name, expr in re.findall(r"^#define\s+(KVQ_\w+)\s+(.+?)\s*(?:/\*.*)?$", src, flags=re.M):
         expr = re.sub(r"(\d+)u\b", r"\1", expr)
-        if re.fullmatch(r"[\d\s()<>+*]+", expr):
+        if re.fullmatch(r"[\d\s()<>+*-]+", expr):
             out[name] = int(eval(expr))
     return out
 
@@ -60,6 +60,7 @@ def test_binding_constants_match_the_header(lib):
         assert getattr(lib, "KVQ_DEVERR_" + name) == h["KVQ_DEVERR_" + name]
     for name in ("QUANT", "RING", "STEP"):
         assert getattr(lib, "APPEND_" + name) == h["KVQ_APPEND_" + name]
+    assert lib.PREFILL_TILES == h["KVQ_PREFILL_TILES"]
 
 
 def test_status_strings_and_block_bytes(lib):

@@ -41,11 +41,15 @@ def _write(lib, cache, inp, rows_by_seq, table, err):
                    err_word=err)
 
 
-def _run(fmt, chunk=24, fused=True, stream_ctas=0, seed=5):
+def _run(fmt, chunk=24, fused=True, stream_ctas=0, seed=5, order="seq", heads=(8, 2)):
+    """Prefix written first, then one kvq_prefill call over the last `chunk`
+    positions of every sequence; rows grouped by sequence ("seq") or
+    alternating between sequences ("interleaved")."""
     from quantized_kv_cache_07_gb300 import _lib
     from quantized_kv_cache_07_gb300.cache import cache_for_inputs
-    w = small_workload(f"prefill_{fmt}", batch=3, q_heads=8, kv_heads=2, len_range=(40, 300), paged=True,
-                       **PREFILL_FORMATS[fmt])
+    spec = PREFILL_FORMATS.get(fmt) or TILE_FORMATS[fmt]
+    w = small_workload(f"prefill_{fmt}", batch=3, q_heads=heads[0], kv_heads=heads[1], len_range=(40, 300),
+                       paged=True, **spec)
     inp = make_inputs(w)
     L = inp.lengths.astype(int)
     # chunk = the last `chunk` positions of each sequence (a block boundary for 2-bit caches)
@@ -57,16 +61,21 @@ def _run(fmt, chunk=24, fused=True, stream_ctas=0, seed=5):
     prefix = {b: range(0, start[b]) for b in range(w.batch)}
     chunk_pos = {b: range(start[b], L[b]) for b in range(w.batch)}
     _write(_lib, cache, inp, prefix if fused else {b: range(0, L[b]) for b in range(w.batch)}, table, err)
-    seq = np.concatenate([[b] * len(chunk_pos[b]) for b in range(w.batch)]).astype(np.int32)
-    pos = np.concatenate([list(chunk_pos[b]) for b in range(w.batch)]).astype(np.int32)
-    rows = np.concatenate([inp.seq_offsets[b] + np.asarray(chunk_pos[b], dtype=np.int64) for b in range(w.batch)])
+    if order == "seq":
+        pairs = [(b, p) for b in range(w.batch) for p in chunk_pos[b]]
+    else:
+        longest = max(len(chunk_pos[b]) for b in range(w.batch))
+        pairs = [(b, chunk_pos[b][c]) for c in range(longest) for b in range(w.batch) if c < len(chunk_pos[b])]
+    seq = np.asarray([b for b, _ in pairs], dtype=np.int32)
+    pos = np.asarray([p for _, p in pairs], dtype=np.int32)
+    rows = np.asarray([inp.seq_offsets[b] + p for b, p in pairs], dtype=np.int64)
     n = len(seq)
     from synth import query_rows
     qbits = query_rows(n, w.q_heads, seed)
     out = torch.zeros((n, w.q_heads, 128), dtype=torch.float32, device="cuda")
     lse = torch.zeros((n, w.q_heads), dtype=torch.float32, device="cuda")
     nb = _lib.kvq_prefill_workspace_size(cache.desc, n, w.q_heads, stream_ctas)
-    ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
     _lib.kvq_prefill(cache.desc, _bits(qbits), w.q_heads, torch.from_numpy(seq).cuda(), torch.from_numpy(pos).cuda(),
                      table, w.batch, inp.max_blocks, out, k_new=_bits(inp.k[rows]) if fused else None,
                      v_new=_bits(inp.v[rows]) if fused else None, lse=lse, workspace=ws, workspace_bytes=nb,
@@ -102,6 +111,14 @@ PREFILL_FORMATS = {
     "q32_k8v4": dict(k_bits=8, v_bits=4, q_bits=32),
     "qint8_int8": dict(k_bits=8, v_bits=8, q_bits=8),
 }
+
+
+# formats the query-tile path takes (symmetric 8-/4-bit blocks, fp16 query)
+TILE_FORMATS = {
+    "k4v8_t3": dict(k_bits=4, v_bits=8, k_dist="t3"),
+    "k8v4_chan": dict(k_bits=8, v_bits=4, channel_factor=True, k_per_channel=True),
+}
+TILE_PATH_FORMATS = ["int8", "int4_factor", "k4v8_t3", "k8v4_chan"]
 
 
 @pytest.mark.parametrize("fmt", list(PREFILL_FORMATS))
@@ -156,3 +173,82 @@ def test_prefill_rejects_a_window_and_flags_bad_sequences():
     torch.cuda.synchronize()
     assert int(err.item()) & _lib.KVQ_DEVERR_POSITION
     assert np.all(out.cpu().numpy() == 0) and np.all(np.isneginf(lse.cpu().numpy()))
+
+
+def _check_against_oracle(res):
+    inp, cache, qbits, seq, pos, out, lse, err = res
+    assert err == 0
+    o_ref, l_ref = _oracle(inp, qbits, seq, pos)
+    assert np.max(np.abs(out - o_ref)) <= TOL
+    assert np.max(np.abs(lse - l_ref)) <= TOL
+
+
+@pytest.mark.parametrize("fmt", TILE_PATH_FORMATS)
+@pytest.mark.parametrize("order", ["seq", "interleaved"])
+def test_prefill_tiles_match_the_oracle(fmt, order):
+    """The query-tile path (16 query vectors per CTA): rows grouped by sequence,
+    and rows alternating between sequences so that every tile holds rows of
+    several sequences (taken in turn)."""
+    from quantized_kv_cache_07_gb300 import _lib
+    _check_against_oracle(_run(fmt, stream_ctas=_lib.PREFILL_TILES, order=order))
+
+
+@pytest.mark.parametrize("heads", [(4, 4), (6, 2), (16, 2)], ids=["g1", "g3", "g8"])
+def test_prefill_tiles_group_sizes(heads):
+    """16 / G rows per tile for G = 1 (16 rows), 3 (5 rows, 15 vectors) and 8 (2 rows)."""
+    from quantized_kv_cache_07_gb300 import _lib
+    _check_against_oracle(_run("int8", stream_ctas=_lib.PREFILL_TILES, order="interleaved", heads=heads))
+
+
+def test_prefill_tiles_and_split_rows_agree_without_the_write():
+    from quantized_kv_cache_07_gb300 import _lib
+    a = _run("int4_factor", fused=False, stream_ctas=_lib.PREFILL_TILES)
+    b = _run("int4_factor", fused=False, stream_ctas=5)
+    assert a[7] == 0 and b[7] == 0
+    np.testing.assert_allclose(a[5], b[5], rtol=0, atol=TOL)
+    np.testing.assert_allclose(a[6], b[6], rtol=0, atol=TOL)
+
+
+@pytest.mark.parametrize("fmt", ["asym_k4v8", "int2", "q32_k8v4", "qint8_int8"])
+def test_prefill_tiles_refuse_other_formats(fmt):
+    from quantized_kv_cache_07_gb300 import _lib
+    with pytest.raises(_lib.KvqError) as e:
+        _run(fmt, stream_ctas=_lib.PREFILL_TILES)
+    assert e.value.status == _lib.KVQ_ERR_UNSUPPORTED
+
+
+def test_prefill_tiles_flag_bad_sequences_and_clamp_positions():
+    """Rows with a sequence outside [0, batch): out = 0, lse = -inf and the
+    POSITION bit; a position beyond the block table's capacity: the SEQ_LEN bit
+    and attention over the capacity, as the split-rows path."""
+    from quantized_kv_cache_07_gb300 import _lib
+    from quantized_kv_cache_07_gb300.cache import KVCache
+    c0 = KVCache(8, 2, 8, 8)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    kv = torch.randn((8 * 16, 2, 128), generator=g, device="cuda").bfloat16()
+    seq0 = torch.zeros(8 * 16, dtype=torch.int32, device="cuda")
+    pos0 = torch.arange(8 * 16, dtype=torch.int32, device="cuda")
+    table = torch.arange(8, dtype=torch.int32, device="cuda").view(2, 4)
+    _lib.kvq_append(c0.desc, kv[:64], kv[64:], seq0[:64], pos0[:64], _lib.APPEND_QUANT, table, 2, 4)
+    q = torch.randn((3, 8, 128), generator=g, device="cuda").bfloat16()
+    seq = torch.tensor([5, 0, 0], dtype=torch.int32, device="cuda")       # sequence 5 of a batch of 2
+    pos = torch.tensor([3, 10, 200], dtype=torch.int32, device="cuda")    # 200 is beyond 4 blocks
+    outs = []
+    for sc in (_lib.PREFILL_TILES, 3):
+        nb = _lib.kvq_prefill_workspace_size(c0.desc, 3, 8, sc)
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.full((3, 8, 128), 7.0, dtype=torch.float32, device="cuda")
+        lse = torch.zeros((3, 8), dtype=torch.float32, device="cuda")
+        _lib.kvq_prefill(c0.desc, q, 8, seq, pos, table, 2, 4, out, lse=lse, workspace=ws, workspace_bytes=nb,
+                         stream_ctas=sc, err_word=err)
+        torch.cuda.synchronize()
+        e = int(err.item())
+        assert e & _lib.KVQ_DEVERR_POSITION and e & _lib.KVQ_DEVERR_SEQ_LEN
+        o, l = out.cpu().numpy(), lse.cpu().numpy()
+        assert np.all(o[0] == 0) and np.all(np.isneginf(l[0]))
+        assert np.all(np.isfinite(o[1:])) and np.all(np.isfinite(l[1:]))
+        outs.append((o, l))
+    np.testing.assert_allclose(outs[0][0], outs[1][0], rtol=0, atol=TOL)
+    np.testing.assert_allclose(outs[0][1], outs[1][1], rtol=0, atol=TOL)
