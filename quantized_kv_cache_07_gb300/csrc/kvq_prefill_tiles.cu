@@ -32,8 +32,8 @@ namespace kvq {
 namespace {
 
 constexpr int kTileQ = 16;       // query vectors per tile: one m16 row tile
-constexpr int kQStride = 136;    // fp16 row stride of the staged query tile (bank spread)
 constexpr int kOStride = 132;    // float row stride of the combine buffer (bank spread)
+constexpr int kCombineBytes = kConsumerWarps * kTileQ * kOStride * 4;
 
 template <int KB, int VB>
 struct TileFmt {
@@ -45,10 +45,12 @@ struct TileFmt {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kBlocksPerStage * F::kKBB;
   static constexpr int kOffMeta = kOffV + kBlocksPerStage * F::kVBB;
+  // the four warps' states merge in the ring once a sub-pass has drained it
+  static_assert(kStages * kStageBytes >= kCombineBytes, "combine buffer must fit in the ring");
 };
 
 struct TileSmem {
-  int qh, qs, qlen, cm, cl, co, rowseq, rowlen, bars, total;
+  int qf, qs, qlen, cm, cl, rowseq, rowlen, bars, total;
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
@@ -56,8 +58,8 @@ __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 __host__ __device__ inline TileSmem tile_smem(int ring_bytes, int stages) {
   TileSmem m{};
   int o = align16(ring_bytes);
-  m.qh = o;
-  o = align16(o + kTileQ * kQStride * 2);
+  m.qf = o;  // query tile in fragment order: [slice kk][vector][t] x 4 fp16
+  o = align16(o + 8 * kTileQ * 4 * 8);
   m.qs = o;
   o = align16(o + kTileQ * 4);
   m.qlen = o;
@@ -66,14 +68,12 @@ __host__ __device__ inline TileSmem tile_smem(int ring_bytes, int stages) {
   o = align16(o + kConsumerWarps * kTileQ * 4);
   m.cl = o;
   o = align16(o + kConsumerWarps * kTileQ * 4);
-  m.co = o;
-  o = align16(o + kConsumerWarps * kTileQ * kOStride * 4);
   m.rowseq = o;
   o = align16(o + kTileQ * 4);
   m.rowlen = o;
   o = align16(o + kTileQ * 4);
   m.bars = o;
-  o = align16(o + (2 * stages + 1) * 8);
+  o = align16(o + (2 * stages + 2) * 8);
   m.total = o;
   return m;
 }
@@ -101,6 +101,17 @@ __device__ __forceinline__ SubPass sub_pass_at(const int* rowseq, const int* row
   return sp;
 }
 
+// Four int8 codes -> fp16 pairs as s8x4_to_f16, with the byte constant 0x64
+// of the permutes in a register (c64 = 0x64646464 from the caller) instead of
+// being rebuilt before every permute.
+__device__ __forceinline__ void s8x4_to_f16_r(uint32_t w, uint32_t c64, uint32_t& lo, uint32_t& hi) {
+  const uint32_t a = __byte_perm(w, c64, 0x4140);
+  const uint32_t b = __byte_perm(w, c64, 0x4342);
+  const uint32_t bias = 0x64806480u;  // (1152, 1152) = 1024 + 128
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
 __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
@@ -125,10 +136,19 @@ struct TileState {
 
 // Scores of one block: s[n][c] for n-tile n (tokens 8n..8n+7), row g (c < 2)
 // or g + 8, token 8n + 2t + (c & 1).  Key slice kk covers dims 32t + 4kk + 0..3
-// of every lane (the fragment-native key order), matching qa[kk].
+// of every lane (the fragment-native key order); qf holds the query tile in
+// the same order, so the A operand of slice kk is two 8-byte loads.
 template <int KB>
-__device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint32_t (&qa)[8][4], float (&s)[2][4], int lane,
-                                            uint32_t km) {
+__device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint2* qf, float (&s)[2][4], int lane,
+                                            uint32_t km, uint32_t c64) {
+  const int g = lane >> 2, t = lane & 3;
+  auto qa = [&](int kk, uint32_t (&r)[4]) {
+    const uint2 u = qf[(kk * kTileQ + g) * 4 + t], v = qf[(kk * kTileQ + g + 8) * 4 + t];
+    r[0] = u.x;
+    r[1] = v.x;
+    r[2] = u.y;
+    r[3] = v.y;
+  };
   float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // odd slices: a second chain
 #pragma unroll
   for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
@@ -139,12 +159,13 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint32_t (&
     const uint32_t g8[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      s8x4_to_f16(g0[kk], a0, a2);  // tokens 0-7
-      s8x4_to_f16(g8[kk], a1, a3);  // tokens 8-15
+      uint32_t a0, a1, a2, a3, q[4];
+      qa(kk, q);
+      s8x4_to_f16_r(g0[kk], c64, a0, a2);  // tokens 0-7
+      s8x4_to_f16_r(g8[kk], c64, a1, a3);  // tokens 8-15
       float(&d)[2][4] = (kk & 1) ? e : s;
-      mma_f16(d[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], a0, a2);
-      mma_f16(d[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], a1, a3);
+      mma_f16(d[0], q[0], q[1], q[2], q[3], a0, a2);
+      mma_f16(d[1], q[0], q[1], q[2], q[3], a1, a3);
     }
   } else {
     const uint4 r0 = p[0], r1 = p[32];
@@ -155,11 +176,13 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint32_t (&
       uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
       s4x8_to_f16(g0[wi], km, x0, x1, x2, x3);
       s4x8_to_f16(g8[wi], km, y0, y1, y2, y3);
-      const int k0 = 2 * wi, k1 = 2 * wi + 1;
-      mma_f16(s[0], qa[k0][0], qa[k0][1], qa[k0][2], qa[k0][3], x0, x1);
-      mma_f16(s[1], qa[k0][0], qa[k0][1], qa[k0][2], qa[k0][3], y0, y1);
-      mma_f16(e[0], qa[k1][0], qa[k1][1], qa[k1][2], qa[k1][3], x2, x3);
-      mma_f16(e[1], qa[k1][0], qa[k1][1], qa[k1][2], qa[k1][3], y2, y3);
+      uint32_t q0[4], q1[4];
+      qa(2 * wi, q0);
+      qa(2 * wi + 1, q1);
+      mma_f16(s[0], q0[0], q0[1], q0[2], q0[3], x0, x1);
+      mma_f16(s[1], q0[0], q0[1], q0[2], q0[3], y0, y1);
+      mma_f16(e[0], q1[0], q1[1], q1[2], q1[3], x2, x3);
+      mma_f16(e[1], q1[0], q1[1], q1[2], q1[3], y2, y3);
     }
   }
 #pragma unroll
@@ -173,7 +196,7 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint32_t (&
 // of dims 16 mt + g (O[2 mt]) and 16 mt + 8 + g (O[2 mt + 1]).
 template <int VB>
 __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3,
-                                            float (&O)[16][4], int lane, uint32_t km) {
+                                            float (&O)[16][4], int lane, uint32_t km, uint32_t c64) {
   const uint4* p = reinterpret_cast<const uint4*>(vb) + lane;
   if constexpr (VB == 8) {
 #pragma unroll
@@ -183,7 +206,7 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t b0, b1;
-        s8x4_to_f16(w[k], b0, b1);
+        s8x4_to_f16_r(w[k], c64, b0, b1);
         mma_f16(O[4 * h + k], p0, p1, p2, p3, b0, b1);
       }
     }
@@ -208,10 +231,10 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
 template <int KB, int VB>
 __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb, const float* ks, const float* vs,
                                            int tok0, int maxlen, int len0, int len1, float qs0, float qs1,
-                                           const uint32_t (&qa)[8][4], TileState& st, int lane, uint32_t km) {
+                                           const uint2* qf, TileState& st, int lane, uint32_t km, uint32_t c64) {
   const int t = lane & 3;
   float x[2][4];
-  tile_scores<KB>(kb, qa, x, lane, km);
+  tile_scores<KB>(kb, qf, x, lane, km, c64);
   // this thread's tokens: 8n + 2t + j (n = 0, 1; j = 0, 1)
   const float2 k0 = *reinterpret_cast<const float2*>(ks + 2 * t);
   const float2 k1 = *reinterpret_cast<const float2*>(ks + 8 + 2 * t);
@@ -293,27 +316,28 @@ __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb,
   const uint32_t p1 = pack_half2(w[0][2], w[1][2]);  // row g + 8
   const uint32_t p2 = pack_half2(w[0][1], w[1][1]);
   const uint32_t p3 = pack_half2(w[0][3], w[1][3]);
-  tile_values<VB>(vb, p0, p1, p2, p3, st.O, lane, km);
+  tile_values<VB>(vb, p0, p1, p2, p3, st.O, lane, km, c64);
 }
 
 template <int KB, int VB>
-__global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeArgs a, int n_tiles, int TR) {
+__global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeArgs a, int n_tiles, int TR) {
   using F = Fmt<KB, VB, false>;
   using T = TileFmt<KB, VB>;
   constexpr int S = T::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   const TileSmem mp = tile_smem(S * T::kStageBytes, S);
-  uint16_t* qh = reinterpret_cast<uint16_t*>(smem + mp.qh);
+  uint2* qf = reinterpret_cast<uint2*>(smem + mp.qf);
   float* qs_s = reinterpret_cast<float*>(smem + mp.qs);
   int* qlen_s = reinterpret_cast<int*>(smem + mp.qlen);
   float* cm = reinterpret_cast<float*>(smem + mp.cm);
   float* cl = reinterpret_cast<float*>(smem + mp.cl);
-  float* co = reinterpret_cast<float*>(smem + mp.co);
+  float* co = reinterpret_cast<float*>(smem);  // over the ring (see cdone)
   int* rowseq = reinterpret_cast<int*>(smem + mp.rowseq);
   int* rowlen = reinterpret_cast<int*>(smem + mp.rowlen);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + mp.bars);
   uint64_t* empty = full + S;
   uint64_t* cbar = empty + S;
+  uint64_t* cdone = cbar + 1;  // consumers have merged a sub-pass: the ring may be refilled
 
   const int G = a.G;
   const int tile = blockIdx.x % n_tiles, h = blockIdx.x / n_tiles;
@@ -327,14 +351,19 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeA
       mbar_init(&empty[i], kConsumerWarps);
     }
     mbar_init(cbar, kConsumers);
+    mbar_init(cdone, 1);
     fence_mbar_init();
   }
-  if (a.c.k_chan)  // keys under per-channel scales only: the key-scale slots keep 1.0 (never copied over)
-    for (int i = tid; i < S * T::kBlocksPerStage * kBlock; i += kThreads) {
+  // keys under per-channel scales only: the key-scale slots of the ring hold
+  // 1.0 (the producer never copies over them; refilled after each merge)
+  auto unit_key_scales = [&](int first, int stride) {
+    for (int i = first; i < S * T::kBlocksPerStage * kBlock; i += stride) {
       const int st = i / (T::kBlocksPerStage * kBlock), r = i % (T::kBlocksPerStage * kBlock);
       reinterpret_cast<float*>(smem + st * T::kStageBytes + T::kOffMeta)[(r / kBlock) * F::kMF + F::kKS + r % kBlock] =
           1.f;
     }
+  };
+  if (a.c.k_chan) unit_key_scales(tid, kThreads);
   // programmatic dependent launch: wait for the previous kernel (the chunk's
   // quantizing write) before reading memory
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -382,9 +411,19 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeA
     uint32_t ph = 0;
     bool ok = true;
     const uint32_t meta_bytes = a.c.k_chan ? F::kMB / 2 : F::kMB;
+    int spi = 0;  // sub-passes issued
     for (int ri = 0; ri < nrows && ok; ++ri) {
       const SubPass sp = sub_pass_at(rowseq, rowlen, nrows, ri);
       if (sp.seq < 0) continue;
+      if (spi > 0) {  // the previous sub-pass's merge uses the ring
+        bool w_ok = true;
+        if (lane == 0) w_ok = mbar_wait(cdone, uint32_t(spi - 1) & 1u);
+        if (!__shfl_sync(kFull, w_ok ? 1 : 0, 0)) {
+          if (lane == 0) flag(a.err, KVQ_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+      ++spi;
       for (int b0 = 0; b0 < sp.nblk; b0 += T::kBlocksPerStage) {
         const int nb = min(T::kBlocksPerStage, sp.nblk - b0);
         if (it >= S) {
@@ -433,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeA
 
   // ------------------------------------------------------------------ consumers
   const uint32_t km = magic_f16x2(a.B);
+  const uint32_t c64 = 0x64646464u | (uint32_t(a.B) >> 16);  // a.B <= 4096: the constant itself
   const int g = lane >> 2, t = lane & 3;
   const int nq = TR * G;  // query vectors of a full tile (<= 16)
   int s = 0;
@@ -473,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeA
       uint2 packed;
       packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
       packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
-      *reinterpret_cast<uint2*>(qh + v * kQStride + 4 * lane) = packed;
+      qf[((lane & 7) * kTileQ + v) * 4 + (lane >> 3)] = packed;  // dims 4 lane = 32t + 4kk
       if (lane == 0) {
         qs_s[v] = act ? ldexpf(kLog2e * kInvSqrtD, -e) : 0.f;
         qlen_s[v] = act ? rowlen[rr] : 0;
@@ -482,24 +522,6 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeA
     if (!consumer_sync(cbar, cphase)) {
       flag(a.err, KVQ_DEVERR_TIMEOUT);
       return;
-    }
-    // A-operand fragments: slice kk of rows g / g + 8 = dims 32t + 4kk + 0..3
-    uint32_t qa[8][4];
-    {
-      const uint4* qg = reinterpret_cast<const uint4*>(qh + g * kQStride + 32 * t);
-      const uint4* q8 = reinterpret_cast<const uint4*>(qh + (g + 8) * kQStride + 32 * t);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 u = qg[i], w = q8[i];
-        qa[2 * i][0] = u.x;
-        qa[2 * i][2] = u.y;
-        qa[2 * i + 1][0] = u.z;
-        qa[2 * i + 1][2] = u.w;
-        qa[2 * i][1] = w.x;
-        qa[2 * i][3] = w.y;
-        qa[2 * i + 1][1] = w.z;
-        qa[2 * i + 1][3] = w.w;
-      }
     }
     const float qs0 = qs_s[g], qs1 = qs_s[g + 8];
     const int len0 = qlen_s[g], len1 = qlen_s[g + 8];
@@ -515,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeA
         const uint8_t* stg = smem + s * T::kStageBytes;
         const float* meta = reinterpret_cast<const float*>(stg + T::kOffMeta + warp * F::kMB);
         tile_block<KB, VB>(stg + T::kOffK + warp * F::kKBB, stg + T::kOffV + warp * F::kVBB, meta + F::kKS,
-                           meta + F::kVS, blk * kBlock, sp.maxlen, len0, len1, qs0, qs1, qa, st, lane, km);
+                           meta + F::kVS, blk * kBlock, sp.maxlen, len0, len1, qs0, qs1, qf, st, lane, km, c64);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -529,6 +551,11 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeA
     for (int o = 1; o < 4; o <<= 1) {
       st.l0 += __shfl_xor_sync(kFull, st.l0, o);
       st.l1 += __shfl_xor_sync(kFull, st.l1, o);
+    }
+    // every warp has read its last block: the ring is free for the merge
+    if (!consumer_sync(cbar, cphase)) {
+      flag(a.err, KVQ_DEVERR_TIMEOUT);
+      return;
     }
     if (t == 0) {
       cm[warp * kTileQ + g] = st.m0 == kNegInf ? kNegInf : st.m0 - st.sg;
@@ -589,11 +616,14 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tile_kernel(const DecodeA
         if ((tid & 7) == 0 && a.lse) a.lse[row] = (M + log2f(L)) * kLn2;
       }
     }
-    // the next sub-pass rewrites the query tile and the combine buffers
+    // the next sub-pass rewrites the query tile and the combine buffers; the
+    // producer may refill the ring
     if (!consumer_sync(cbar, cphase)) {
       flag(a.err, KVQ_DEVERR_TIMEOUT);
       return;
     }
+    if (a.c.k_chan) unit_key_scales(tid, kConsumers);  // the merge wrote over them
+    if (tid == 0) mbar_arrive(cdone);
   }
 }
 
