@@ -58,8 +58,8 @@ __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
 __host__ __device__ inline TileSmem tile_smem(int ring_bytes, int stages) {
   TileSmem m{};
   int o = align16(ring_bytes);
-  m.qf = o;  // query tile in fragment order: [slice kk][vector][t] x 4 fp16
-  o = align16(o + 8 * kTileQ * 4 * 8);
+  m.qf = o;  // query tile in A-operand order: [slice kk][g][t] x (rows g, g + 8) x 4 fp16
+  o = align16(o + 8 * 8 * 4 * 16);
   m.qs = o;
   o = align16(o + kTileQ * 4);
   m.qlen = o;
@@ -137,17 +137,17 @@ struct TileState {
 // Scores of one block: s[n][c] for n-tile n (tokens 8n..8n+7), row g (c < 2)
 // or g + 8, token 8n + 2t + (c & 1).  Key slice kk covers dims 32t + 4kk + 0..3
 // of every lane (the fragment-native key order); qf holds the query tile in
-// the same order, so the A operand of slice kk is two 8-byte loads.
+// the same order with rows g and g + 8 interleaved, so the A operand of slice
+// kk is one 16-byte load, its four registers in operand order.
 template <int KB>
-__device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint2* qf, float (&s)[2][4], int lane,
+__device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, float (&s)[2][4], int lane,
                                             uint32_t km, uint32_t c64) {
-  const int g = lane >> 2, t = lane & 3;
   auto qa = [&](int kk, uint32_t (&r)[4]) {
-    const uint2 u = qf[(kk * kTileQ + g) * 4 + t], v = qf[(kk * kTileQ + g + 8) * 4 + t];
+    const uint4 u = qf[kk * 32 + lane];
     r[0] = u.x;
-    r[1] = v.x;
-    r[2] = u.y;
-    r[3] = v.y;
+    r[1] = u.y;
+    r[2] = u.z;
+    r[3] = u.w;
   };
   float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // odd slices: a second chain
 #pragma unroll
@@ -231,7 +231,7 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
 template <int KB, int VB>
 __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb, const float* ks, const float* vs,
                                            int tok0, int maxlen, int len0, int len1, float qs0, float qs1,
-                                           const uint2* qf, TileState& st, int lane, uint32_t km, uint32_t c64) {
+                                           const uint4* qf, TileState& st, int lane, uint32_t km, uint32_t c64) {
   const int t = lane & 3;
   float x[2][4];
   tile_scores<KB>(kb, qf, x, lane, km, c64);
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
   constexpr int S = T::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   const TileSmem mp = tile_smem(S * T::kStageBytes, S);
-  uint2* qf = reinterpret_cast<uint2*>(smem + mp.qf);
+  uint32_t* qf = reinterpret_cast<uint32_t*>(smem + mp.qf);
   float* qs_s = reinterpret_cast<float*>(smem + mp.qs);
   int* qlen_s = reinterpret_cast<int*>(smem + mp.qlen);
   float* cm = reinterpret_cast<float*>(smem + mp.cm);
@@ -513,7 +513,11 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
       uint2 packed;
       packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
       packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
-      qf[((lane & 7) * kTileQ + v) * 4 + (lane >> 3)] = packed;  // dims 4 lane = 32t + 4kk
+      {  // dims 4 lane .. +3 = 32t + 4kk + 0..3 of vector v = row g (+ 8)
+        uint32_t* f = qf + (((lane & 7) * 8 + (v & 7)) * 4 + (lane >> 3)) * 4 + (v >> 3);
+        f[0] = packed.x;
+        f[2] = packed.y;
+      }
       if (lane == 0) {
         qs_s[v] = act ? ldexpf(kLog2e * kInvSqrtD, -e) : 0.f;
         qlen_s[v] = act ? rowlen[rr] : 0;
@@ -537,7 +541,8 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
         const uint8_t* stg = smem + s * T::kStageBytes;
         const float* meta = reinterpret_cast<const float*>(stg + T::kOffMeta + warp * F::kMB);
         tile_block<KB, VB>(stg + T::kOffK + warp * F::kKBB, stg + T::kOffV + warp * F::kVBB, meta + F::kKS,
-                           meta + F::kVS, blk * kBlock, sp.maxlen, len0, len1, qs0, qs1, qf, st, lane, km, c64);
+                           meta + F::kVS, blk * kBlock, sp.maxlen, len0, len1, qs0, qs1,
+                           reinterpret_cast<const uint4*>(qf), st, lane, km, c64);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
