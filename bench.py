@@ -160,6 +160,12 @@ def cache_bytes_per_step(inp) -> int:
 # into the cache and lets each attend causally to its sequence up to itself.
 PREFILL = dict(name="prefill_int8_b8_prefix1920_chunk128", batch=8, q_heads=32, kv_heads=8, k_bits=8, v_bits=8,
                prefix=1920, chunk=128)
+# Decode calls declare their lengths and block tables ready ahead of the
+# previous kernel (KVQ_DECODE_GEOMETRY_READY): every step's tables and lengths
+# are written before the timed steps, and the kernels just ahead of a decode
+# (the previous step's decode, kvq_append) write queries, outputs and cache
+# entries only.
+DECODE_FLAGS = 1
 # The 2-bit token-group format is timed on the shape of this workload.
 INT2_SHAPE = "int4_factor_b32_len1k_8k"
 
@@ -331,7 +337,8 @@ class GpuArm:
                 ev0.record(stream)
             _lib.kvq_decode(c.desc, q if q_ is None else q_, B, Hq, dec_lens, table, inp_.max_blocks, out,
                             lse=lse, workspace=ws.buf, workspace_bytes=ws.nbytes,
-                            stream_ctas=args.stream_ctas, err_word=err)
+                            stream_ctas=args.stream_ctas, err_word=err,
+                            flags=DECODE_FLAGS)
             if ev1 is not None:
                 ev1.record(stream)
 
@@ -423,7 +430,7 @@ class GpuArm:
                     c = replicas[k % len(replicas)]
                     _lib.kvq_decode(c.desc, q, B, Hq, dec_lens, table, inp_.max_blocks, out, lse=lse,
                                     workspace=ws.buf, workspace_bytes=ws.nbytes, stream_ctas=args.stream_ctas,
-                                    err_word=err)
+                                    err_word=err, flags=DECODE_FLAGS)
             dgraph = None
             if graph is not None:
                 dgraph = torch.cuda.CUDAGraph()
@@ -777,6 +784,7 @@ def main():
                    "l2": f"steps rotate over {res['replicas']} cache replicas "
                          f"({res['replicas'] * bytes_step / 2**20:.0f} MiB >= 4x L2 or cache > L2)",
                    "parallelism": f"replicas x{world}", "decode_grid": res["plan"], "timing": res["timing"],
+                   "decode_flags": "KVQ_DECODE_GEOMETRY_READY" if DECODE_FLAGS else "0",
                    "ms_per_step_eager": round(res["ms_eager"], 6)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,

@@ -283,6 +283,29 @@ kvq_status kvq_decode(const kvq_cache_desc* cache, const void* q, int32_t batch,
                       void* out, int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes,
                       int32_t stream_ctas, uint32_t* err_word, void* stream);
 
+/* kvq_decode_ex flag: seq_lens and block_table hold their final values before
+ * the kernel that precedes this call on the stream ends -- they are written by
+ * host copies or by kernels that completed before that kernel started, never
+ * by it (nor by a kernel it overlaps).  The usual decode step qualifies: the
+ * scheduler writes lengths and tables before the step; the kernels just ahead
+ * of attention (projections, kvq_append) write queries and cache entries.  The
+ * decode kernel then reads the lengths, and works out its split, while that
+ * kernel finishes, instead of after it (0.5-1 us per call on GB300). */
+#define KVQ_DECODE_GEOMETRY_READY 1u
+
+/*
+ * kvq_decode_ex -- kvq_decode with flags (0 or KVQ_DECODE_GEOMETRY_READY; any
+ * other bit: KVQ_ERR_INVALID_ARG).  Same arguments, results and errors
+ * otherwise; kvq_decode is kvq_decode_ex with flags 0.  With the flag the
+ * results are identical (the same arithmetic); only the order of the loads
+ * changes.  A device error found in the lengths or the table is reported the
+ * same way.
+ */
+kvq_status kvq_decode_ex(const kvq_cache_desc* cache, const void* q, int32_t batch, int32_t q_heads,
+                         const int32_t* seq_lens, const int32_t* block_table, int32_t max_blocks_per_seq,
+                         void* out, int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes,
+                         int32_t stream_ctas, uint32_t flags, uint32_t* err_word, void* stream);
+
 /* Size of the fixed device scratch behind kvq_decode_static_scratch (bytes). */
 #define KVQ_STATIC_SCRATCH_BYTES (8u << 20)
 

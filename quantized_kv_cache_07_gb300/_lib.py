@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_int32, c_size_t, c_void_p
+from ctypes import POINTER, c_char_p, c_int32, c_size_t, c_uint32, c_void_p
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkvq.so")
@@ -31,6 +31,7 @@ APPEND_QUANT = 0
 APPEND_RING = 1
 APPEND_STEP = 2
 PREFILL_TILES = -1  # kvq_prefill stream_ctas: the query-tile path
+DECODE_GEOMETRY_READY = 1  # kvq_decode_ex flag: lengths and block table final before the previous kernel ends
 
 
 class KvqError(RuntimeError):
@@ -73,6 +74,9 @@ SIGNATURES = {
     "kvq_workspace_init": (c_int32, [c_void_p, c_size_t, c_void_p]),
     "kvq_decode": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32,
                              c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_int32, c_void_p, c_void_p]),
+    "kvq_decode_ex": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32,
+                                c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_int32, c_uint32, c_void_p,
+                                c_void_p]),
     "kvq_dequant": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
     "kvq_prefill": (c_int32, [POINTER(CacheDesc), c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_int32,
@@ -168,10 +172,17 @@ def kvq_workspace_init(workspace, nbytes: int, stream=None):
 
 def kvq_decode(desc: CacheDesc, q, batch: int, q_heads: int, seq_lens, block_table, max_blocks_per_seq: int, out,
                lse=None, workspace=None, workspace_bytes: int = 0, stream_ctas: int = 0, err_word=None,
-               stream=None, out_fp32: bool | None = None):
+               stream=None, out_fp32: bool | None = None, flags: int = 0):
+    """kvq_decode (flags 0) or kvq_decode_ex with flags (DECODE_GEOMETRY_READY)."""
     if out_fp32 is None:
         import torch
         out_fp32 = out.dtype == torch.float32
+    if flags:
+        _check(load().kvq_decode_ex(ctypes.byref(desc), _ptr(q), batch, q_heads, _ptr(seq_lens), _ptr(block_table),
+                                    max_blocks_per_seq, _ptr(out), int(bool(out_fp32)), _ptr(lse), _ptr(workspace),
+                                    workspace_bytes, stream_ctas, flags, _ptr(err_word), _stream(stream)),
+               "kvq_decode_ex")
+        return
     _check(load().kvq_decode(ctypes.byref(desc), _ptr(q), batch, q_heads, _ptr(seq_lens), _ptr(block_table),
                              max_blocks_per_seq, _ptr(out), int(bool(out_fp32)), _ptr(lse), _ptr(workspace),
                              workspace_bytes, stream_ctas, _ptr(err_word), _stream(stream)), "kvq_decode")

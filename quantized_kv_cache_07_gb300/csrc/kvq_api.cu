@@ -263,6 +263,15 @@ kvq_status kvq_decode(const kvq_cache_desc* cache, const void* q, int32_t batch,
                       const int32_t* seq_lens, const int32_t* block_table, int32_t max_blocks_per_seq, void* out,
                       int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes, int32_t stream_ctas,
                       uint32_t* err_word, void* stream) {
+  return kvq_decode_ex(cache, q, batch, q_heads, seq_lens, block_table, max_blocks_per_seq, out, out_fp32, lse,
+                       workspace, workspace_bytes, stream_ctas, 0u, err_word, stream);
+}
+
+kvq_status kvq_decode_ex(const kvq_cache_desc* cache, const void* q, int32_t batch, int32_t q_heads,
+                         const int32_t* seq_lens, const int32_t* block_table, int32_t max_blocks_per_seq, void* out,
+                         int32_t out_fp32, float* lse, void* workspace, size_t workspace_bytes, int32_t stream_ctas,
+                         uint32_t flags, uint32_t* err_word, void* stream) {
+  if (flags & ~uint32_t(KVQ_DECODE_GEOMETRY_READY)) return KVQ_ERR_INVALID_ARG;
   kvq_status st = check_cache(cache);
   if (st != KVQ_OK) return st;
   st = check_decode_shape(cache, batch, q_heads);
@@ -294,6 +303,7 @@ kvq_status kvq_decode(const kvq_cache_desc* cache, const void* q, int32_t batch,
   a.ws = static_cast<uint8_t*>(workspace);
   a.lay = L;
   a.err = err_word;
+  a.ahead = (flags & KVQ_DECODE_GEOMETRY_READY) ? 1 : 0;
   if (kvq::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

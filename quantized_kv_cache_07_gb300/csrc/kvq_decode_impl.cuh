@@ -992,21 +992,23 @@ __device__ __forceinline__ bool finish_segment(const DecodeArgs& a, WarpState& s
 }
 
 // Clamped lengths and the two block prefix sums of every sequence, in shared
-// memory (all threads; ends with a block barrier).  `load` reads a length;
-// block 0 reports lengths that are negative or beyond the table's capacity.
+// memory (all threads; ends with a block barrier).  `load` reads a length.
+// Returns (in every thread) whether a length was negative or beyond the
+// table's capacity; the caller reports it.
 template <typename LoadLen>
-__device__ __forceinline__ void scan_geometry(const DecodeArgs& a, int B, int W, int X, int* len_s, int* pre_s,
+__device__ __forceinline__ bool scan_geometry(const DecodeArgs& a, int B, int W, int X, int* len_s, int* pre_s,
                                               int* vpre_s, LoadLen load, int tid, int warp, int lane) {
   const int cap = a.mbps * kBlock;
+  int bad = 0;
   for (int b = tid; b < B; b += kThreads) {
     int L = load(b);
     if (L < 0) {
-      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
+      bad = 1;
       L = 0;
     }
     int Lq = W > 0 ? max(L - W, 0) : L;
     if (Lq > cap) {
-      if (blockIdx.x == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
+      bad = 1;
       Lq = cap;
       L = W > 0 ? cap + W : cap;
     }
@@ -1035,7 +1037,7 @@ __device__ __forceinline__ void scan_geometry(const DecodeArgs& a, int B, int W,
       carry += __shfl_sync(kFull, v, 31);
     }
   }
-  __syncthreads();
+  return __syncthreads_or(bad) != 0;
 }
 
 // LOQ: the two-part mode (q_bits 32) of code blocks: the query and the value
@@ -1093,12 +1095,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
   // Programmatic dependent launch: this grid may start while the previous
   // kernel on the stream is still finishing.  Let the next kernel launch
   // early in turn, then wait until the previous kernel has completed (its
-  // writes visible) before reading any memory.
+  // writes visible) before reading memory it may write.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // ---- sequence geometry: clamped lengths and block prefix sums
-  scan_geometry(a, B, W, X, len_s, pre_s, vpre_s, [&](int b) {
+  auto load_len = [&](int b) {
     if (!a.pos) return a.seq_lens[b];
     // prefill: row b is position pos[b] of sequence seq_of[b] and attends to 0..pos[b]
     const int sb = a.seq_of[b];
@@ -1109,8 +1108,20 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
     }
     rows_s[b] = sb;
     return a.pos[b] + 1;
-  }, tid, warp, lane);
+  };
   const Geo geo{pre_s, vpre_s, B, H, X};
+  // Decode whose lengths and block table the caller declares final before the
+  // previous kernel ends: scan the geometry while that kernel finishes (an
+  // error found here is reported after the wait).  Reading the producer's
+  // first block-table entries ahead as well measured slower (register
+  // pressure in the block loop), so the table is read after the wait.
+  bool len_bad = false;
+  if (a.ahead) len_bad = scan_geometry(a, B, W, X, len_s, pre_s, vpre_s, load_len, tid, warp, lane);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- sequence geometry: clamped lengths and block prefix sums
+  if (!a.ahead) len_bad = scan_geometry(a, B, W, X, len_s, pre_s, vpre_s, load_len, tid, warp, lane);
+  if (len_bad && blockIdx.x == 0 && tid == 0) flag(a.err, KVQ_DEVERR_SEQ_LEN);
   const long long T = (long long)H * vpre_s[B];  // virtual blocks in total
   const int U = B * H;
   // Effective stream split: never more CTAs than blocks / kMinBlocksPerCta, so

@@ -73,6 +73,9 @@ struct DecodeArgs {
   uint8_t* ws;
   DecodeLayout lay;
   uint32_t* err;
+  // 1: seq_lens and the block table are final before the preceding kernel on
+  // the stream ends (KVQ_DECODE_GEOMETRY_READY): read them before the wait
+  int ahead = 0;
 };
 
 // The largest GQA group (query heads per KV head) the decode kernel takes: one

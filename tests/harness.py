@@ -110,7 +110,7 @@ class DeviceRun:
                             inp.max_blocks, err_word=self.err)
         self.lens = torch.from_numpy(inp.decode_lengths.astype(np.int32)).cuda()
 
-    def decode(self, out_fp32=True, stream_ctas=0, lens=None):
+    def decode(self, out_fp32=True, stream_ctas=0, lens=None, flags=0, table=None):
         from quantized_kv_cache_07_gb300.cache import DecodeWorkspace
         torch = self.torch
         w = self.inp.workload
@@ -119,8 +119,9 @@ class DeviceRun:
         lse = torch.zeros((w.batch, w.q_heads), dtype=torch.float32, device=self.device)
         ws = DecodeWorkspace(self.cache, w.batch, w.q_heads, stream_ctas)
         self.lib.kvq_decode(self.cache.desc, self.q, w.batch, w.q_heads, self.lens if lens is None else lens,
-                            self.table, self.inp.max_blocks, out, lse=lse, workspace=ws.buf,
-                            workspace_bytes=ws.nbytes, stream_ctas=stream_ctas, err_word=self.err)
+                            self.table if table is None else table, self.inp.max_blocks, out, lse=lse,
+                            workspace=ws.buf, workspace_bytes=ws.nbytes, stream_ctas=stream_ctas, err_word=self.err,
+                            flags=flags)
         torch.cuda.synchronize()
         return out.float().cpu().numpy(), lse.cpu().numpy()
 

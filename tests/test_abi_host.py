@@ -61,6 +61,7 @@ def test_binding_constants_match_the_header(lib):
     for name in ("QUANT", "RING", "STEP"):
         assert getattr(lib, "APPEND_" + name) == h["KVQ_APPEND_" + name]
     assert lib.PREFILL_TILES == h["KVQ_PREFILL_TILES"]
+    assert lib.DECODE_GEOMETRY_READY == h["KVQ_DECODE_GEOMETRY_READY"]
 
 
 def test_status_strings_and_block_bytes(lib):
@@ -149,6 +150,11 @@ def test_append_and_decode_reject_bad_shapes_before_any_launch(lib):
     # too-small workspace
     assert so.kvq_decode(ctypes.byref(desc), 0x5000, 4, 32, 0x6000, 0x7000, 1, 0x8000, 0, None, 0x9000, 64, 5,
                          None, None) == lib.KVQ_ERR_WORKSPACE
+    # kvq_decode_ex: the same validation; flag bits other than GEOMETRY_READY are refused
+    assert so.kvq_decode_ex(ctypes.byref(desc), 0x5000, 4, 32, 0x6000, 0x7000, 1, 0x8000, 0, None, 0x9000, 64, 5,
+                            lib.DECODE_GEOMETRY_READY, None, None) == lib.KVQ_ERR_WORKSPACE
+    assert so.kvq_decode_ex(ctypes.byref(desc), 0x5000, 4, 32, 0x6000, 0x7000, 1, 0x8000, 0, None, 0x9000, 1 << 20,
+                            5, 2, None, None) == lib.KVQ_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8, 16])

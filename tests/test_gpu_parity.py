@@ -509,6 +509,44 @@ def test_device_errors_are_flagged_not_trapped():
     assert compare_outputs(inp, o2, l2, oracle_decode(inp), out_is_bf16=False) <= 1.0
 
 
+@pytest.mark.parametrize("name", ["int8_g4", "window32_int8", "int4_factor_g8", "asym_int4_factor_g8", "int2_g4",
+                                  "bf16", "q32_int2_g1"])
+def test_geometry_ready_flag_gives_identical_results(runs, name):
+    """kvq_decode_ex with KVQ_DECODE_GEOMETRY_READY scans the lengths before
+    the dependency wait; the arithmetic is unchanged, so outputs and lse are
+    bit-identical to kvq_decode."""
+    inp, run = runs(name)
+    from quantized_kv_cache_07_gb300 import _lib
+    for p in (0, 5):
+        o0, l0 = run.decode(out_fp32=True, stream_ctas=p)
+        o1, l1 = run.decode(out_fp32=True, stream_ctas=p, flags=_lib.DECODE_GEOMETRY_READY)
+        np.testing.assert_array_equal(o0, o1)
+        np.testing.assert_array_equal(l0, l1)
+    assert run.err_bits() == 0
+
+
+def test_geometry_ready_flag_reports_device_errors():
+    """Lengths beyond the table's capacity (found before the dependency wait)
+    and out-of-range table entries are flagged as without the flag, with the
+    same outputs."""
+    from quantized_kv_cache_07_gb300 import _lib
+    inp = make_inputs(small_workload("ready_errs", batch=3, len_range=(40, 300)))
+    run = DeviceRun(inp)
+    bad = run.table.clone()
+    bad[0, 0] = inp.num_blocks + 3                 # the first entry a producer reads
+    bad[2, 1] = -1
+    long = run.lens.clone()
+    long[1] = inp.max_blocks * 16 + 50
+    res = []
+    for flags in (0, _lib.DECODE_GEOMETRY_READY):
+        run.err.zero_()
+        o, l = run.decode(out_fp32=True, lens=long, flags=flags, table=bad)
+        res.append((o, l, run.err_bits()))
+    assert res[0][2] == res[1][2] == (_lib.KVQ_DEVERR_BLOCK_ID | _lib.KVQ_DEVERR_SEQ_LEN)
+    np.testing.assert_array_equal(res[0][0], res[1][0])
+    np.testing.assert_array_equal(res[0][1], res[1][1])
+
+
 def test_workspace_counters_return_to_zero():
     """The merge counters at the head of the workspace are zero after every
     completed call: normal calls at several split counts, and a call whose
