@@ -119,7 +119,16 @@ long long prefill_tiles(int n, int q_heads, int kv_heads) {
 
 namespace kvq {
 
-DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas) {
+int switch_blocks_for(int k_bits) {
+  // Starting a unit (its query staging, the previous unit's record, ticket and
+  // possibly merge) costs about as much time as this many blocks of the
+  // format: more of the cheaper 4- and 2-bit blocks (measured optimum on
+  // 32 sequences of 1k-8k tokens: 40 for 4-/2-bit keys, 32 for int8 keys,
+  // 16 for a bf16 cache).
+  return k_bits == 16 ? 16 : (k_bits == 8 ? 32 : 40);
+}
+
+DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas, int switch_cost) {
   const int G = H > 0 ? Hq / H : 0;
   DecodeLayout L;
   L.stream_ctas = stream_ctas;
@@ -129,9 +138,8 @@ DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas) {
   // When the stream CTAs are a multiple of the units (equal lengths split
   // unit-aligned) every CTA starts exactly one unit: no start cost needed.
   // Otherwise starting a unit (query staging, record, ticket) is charged as
-  // kSwitchBlocks blocks of work so the split balances time, not blocks.
-  constexpr int kSwitchBlocks = 16;
-  L.switch_blocks = (L.units > 0 && L.units <= stream_ctas && stream_ctas % L.units == 0) ? 0 : kSwitchBlocks;
+  // switch_cost blocks of work so the split balances time, not blocks.
+  L.switch_blocks = (L.units > 0 && L.units <= stream_ctas && stream_ctas % L.units == 0) ? 0 : switch_cost;
   size_t o = 0;
   L.off_counter = o;
   o = round_up(o + size_t(L.units) * 4, 256);
@@ -212,7 +220,7 @@ kvq_status kvq_make_decode_plan(int32_t batch, int32_t q_heads, int32_t num_kv_h
     if (num_sms < 1 || ctas_per_sm < 1) return KVQ_ERR_INVALID_ARG;
     P = stream_ctas_for(num_sms * ctas_per_sm, window > 0 ? batch * num_kv_heads : 0, batch * num_kv_heads);
   }
-  const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, num_kv_heads, window, P);
+  const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, num_kv_heads, window, P, 16);
   plan->stream_ctas = L.stream_ctas;
   plan->window_ctas = L.window_ctas;
   plan->units = L.units;
@@ -230,7 +238,8 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t batch,
   if (st != KVQ_OK) return st;
   int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, batch);
   if (P <= 0) return KVQ_ERR_CUDA;
-  *bytes = kvq::decode_layout(batch, q_heads, cache->num_kv_heads, cache->window, P).total;
+  *bytes = kvq::decode_layout(batch, q_heads, cache->num_kv_heads, cache->window, P,
+                                                 kvq::switch_blocks_for(cache->k_bits)).total;
   return KVQ_OK;
 }
 
@@ -243,7 +252,8 @@ kvq_status kvq_decode_device_plan(const kvq_cache_desc* cache, int32_t batch, in
   if (st != KVQ_OK) return st;
   const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, batch);
   if (P <= 0) return KVQ_ERR_CUDA;
-  const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, cache->num_kv_heads, cache->window, P);
+  const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, cache->num_kv_heads, cache->window, P,
+                                                 kvq::switch_blocks_for(cache->k_bits));
   plan->stream_ctas = L.stream_ctas;
   plan->window_ctas = L.window_ctas;
   plan->units = L.units;
@@ -282,7 +292,8 @@ kvq_status kvq_decode_ex(const kvq_cache_desc* cache, const void* q, int32_t bat
   if (stream_ctas < 0) return KVQ_ERR_INVALID_ARG;
   const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, batch);
   if (P <= 0) return KVQ_ERR_CUDA;
-  const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, cache->num_kv_heads, cache->window, P);
+  const kvq::DecodeLayout L = kvq::decode_layout(batch, q_heads, cache->num_kv_heads, cache->window, P,
+                                                 kvq::switch_blocks_for(cache->k_bits));
   if (!workspace || workspace_bytes < L.total) return KVQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KVQ_ERR_ALIGNMENT;
   kvq::DecodeArgs a;
@@ -339,7 +350,7 @@ kvq_status kvq_prefill(const kvq_cache_desc* cache, const void* q, int32_t n, in
   if (!tiles) {
     const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, n, true);
     if (P <= 0) return KVQ_ERR_CUDA;
-    L = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P);
+    L = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P, kvq::switch_blocks_for(cache->k_bits));
     if (!workspace || workspace_bytes < L.total) return KVQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KVQ_ERR_ALIGNMENT;
   }
@@ -388,7 +399,7 @@ kvq_status kvq_prefill_workspace_size(const kvq_cache_desc* cache, int32_t n, in
   }
   const int P = stream_ctas > 0 ? stream_ctas : auto_stream_ctas(cache, n, true);
   if (P <= 0) return KVQ_ERR_CUDA;
-  *bytes = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P).total;
+  *bytes = kvq::decode_layout(n, q_heads, cache->num_kv_heads, 0, P, kvq::switch_blocks_for(cache->k_bits)).total;
   return KVQ_OK;
 }
 

@@ -82,7 +82,10 @@ struct DecodeArgs {
 // 8-wide MMA tile of query columns.
 constexpr int kMaxGroup = 8;
 
-DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas);
+// Unit-start charge of the split, in blocks of the cache's format.
+int switch_blocks_for(int k_bits);
+// switch_cost: the unit-start charge when the split is not unit-aligned.
+DecodeLayout decode_layout(int B, int Hq, int H, int window, int stream_ctas, int switch_cost);
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
