@@ -23,7 +23,9 @@
 // after the dot product ([P3] "The axis choice is a kernel decision").
 // Values: O (16 x 128) += (P * s_v) (16 x 16 tokens, fp16) . V (codes), the
 // value scale folded into the weight ([P2] "Keys and values need not have
-// identical error sensitivity").  The cache's fragment-native block order
+// identical error sensitivity").  Asymmetric blocks add the key zero-point
+// term m'_k * sum(q) to each score and sum(p * m'_v) to each output row, as
+// the decode kernel does.  The cache's fragment-native block order
 // (include/kvq.h) gives each lane exactly the B-operand pairs of these
 // products, the same registers the decode kernel uses as A operands.
 #include "kvq_decode_impl.cuh"
@@ -35,9 +37,9 @@ constexpr int kTileQ = 16;       // query vectors per tile: one m16 row tile
 constexpr int kOStride = 132;    // float row stride of the combine buffer (bank spread)
 constexpr int kCombineBytes = kConsumerWarps * kTileQ * kOStride * 4;
 
-template <int KB, int VB>
+template <int KB, int VB, bool ASYM>
 struct TileFmt {
-  using F = Fmt<KB, VB, false>;
+  using F = Fmt<KB, VB, ASYM>;
   static constexpr int kBlocksPerStage = kConsumerWarps;  // block w of a stage -> consumer warp w
   static constexpr int kStageBytes = kBlocksPerStage * F::kPerBlock;
   static constexpr int kStagesRaw = 65536 / kStageBytes;
@@ -50,7 +52,7 @@ struct TileFmt {
 };
 
 struct TileSmem {
-  int qf, qs, qlen, cm, cl, rowseq, rowlen, bars, total;
+  int qf, qs, qz, qlen, cm, cl, rowseq, rowlen, bars, total;
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
@@ -61,6 +63,8 @@ __host__ __device__ inline TileSmem tile_smem(int ring_bytes, int stages) {
   m.qf = o;  // query tile in A-operand order: [slice kk][g][t] x (rows g, g + 8) x 4 fp16
   o = align16(o + 8 * 8 * 4 * 16);
   m.qs = o;
+  o = align16(o + kTileQ * 4);
+  m.qz = o;  // asymmetric blocks: sum of each fp16 query vector as the MMA sees it
   o = align16(o + kTileQ * 4);
   m.qlen = o;
   o = align16(o + kTileQ * 4);
@@ -123,10 +127,12 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
 struct TileState {
   float O[16][4];
   float m0, m1, l0, l1;
+  float z0, z1;     // asymmetric values: sum of p * m'_v of this thread's tokens per row
   float sg, svlim;  // sigma and the largest value scale it allows (as in decode)
   __device__ __forceinline__ void reset() {
     m0 = m1 = kNegInf;
     l0 = l1 = 0.f;
+    z0 = z1 = 0.f;
     sg = float(kSigma0);
     svlim = ldexpf(1.f, kWeightExp - int(kMaxSlack) - kSigma0);
 #pragma unroll
@@ -228,10 +234,13 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
 
 // One block of one consumer warp: scores, causal mask, online softmax with the
 // lazy maximum and the sigma offset of the decode kernel, value product.
-template <int KB, int VB>
+template <int KB, int VB, bool ASYM>
 __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb, const float* ks, const float* vs,
-                                           int tok0, int maxlen, int len0, int len1, float qs0, float qs1,
-                                           const uint4* qf, TileState& st, int lane, uint32_t km, uint32_t c64) {
+                                           const float* ko, const float* vo, int tok0, int maxlen, int len0,
+                                           int len1, float qs0, float qs1, float qz0, float qz1, const uint4* qf,
+                                           TileState& st, int lane, uint32_t km, uint32_t c64) {
+  // offset-binary centre of the code conversion: c' = u - kKC (zero points: m' = m + kKC * s)
+  constexpr float kKC = KB == 8 ? 128.f : 8.f, kVC = VB == 8 ? 128.f : 8.f;
   const int t = lane & 3;
   float x[2][4];
   tile_scores<KB>(kb, qf, x, lane, km, c64);
@@ -242,14 +251,33 @@ __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb,
   const float2 v1 = *reinterpret_cast<const float2*>(vs + 8 + 2 * t);
   const float ksc[2][2] = {{k0.x, k0.y}, {k1.x, k1.y}};
   float vsc[2][2] = {{v0.x, v0.y}, {v1.x, v1.y}};
+  float mk[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, mv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  if constexpr (ASYM) {
+    const float2 a0 = *reinterpret_cast<const float2*>(ko + 2 * t), a1 = *reinterpret_cast<const float2*>(ko + 8 + 2 * t);
+    const float2 b0 = *reinterpret_cast<const float2*>(vo + 2 * t), b1 = *reinterpret_cast<const float2*>(vo + 8 + 2 * t);
+    mk[0][0] = fmaf(kKC, k0.x, a0.x);
+    mk[0][1] = fmaf(kKC, k0.y, a0.y);
+    mk[1][0] = fmaf(kKC, k1.x, a1.x);
+    mk[1][1] = fmaf(kKC, k1.y, a1.y);
+    mv[0][0] = fmaf(kVC, v0.x, b0.x);
+    mv[0][1] = fmaf(kVC, v0.y, b0.y);
+    mv[1][0] = fmaf(kVC, v1.x, b1.x);
+    mv[1][1] = fmaf(kVC, v1.y, b1.y);
+  }
   float svm = 0.f;
 #pragma unroll
   for (int n = 0; n < 2; ++n)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int pos = tok0 + 8 * n + 2 * t + j;
-      x[n][j] = pos < len0 ? x[n][j] * (ksc[n][j] * qs0) : kNegInf;
-      x[n][2 + j] = pos < len1 ? x[n][2 + j] * (ksc[n][j] * qs1) : kNegInf;
+      if constexpr (ASYM) {
+        x[n][j] = pos < len0 ? fmaf(x[n][j], ksc[n][j], mk[n][j] * qz0) * qs0 : kNegInf;
+        x[n][2 + j] = pos < len1 ? fmaf(x[n][2 + j], ksc[n][j], mk[n][j] * qz1) * qs1 : kNegInf;
+        mv[n][j] = pos < maxlen ? mv[n][j] : 0.f;
+      } else {
+        x[n][j] = pos < len0 ? x[n][j] * (ksc[n][j] * qs0) : kNegInf;
+        x[n][2 + j] = pos < len1 ? x[n][2 + j] * (ksc[n][j] * qs1) : kNegInf;
+      }
       // scales of slots past the sub-pass's longest row are not data
       vsc[n][j] = pos < maxlen ? vsc[n][j] : 0.f;
       svm = fmaxf(svm, vsc[n][j]);
@@ -267,6 +295,8 @@ __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb,
     const float al1 = (mn1 == kNegInf) ? 1.f : ex2(st.m1 - mn1);
     st.l0 *= al0;
     st.l1 *= al1;
+    st.z0 *= al0;
+    st.z1 *= al1;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       st.O[i][0] *= al0;
@@ -286,6 +316,8 @@ __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb,
     const float f = ldexpf(1.f, sg_new - int(st.sg));  // exact power of two
     st.l0 *= f;
     st.l1 *= f;
+    st.z0 *= f;
+    st.z1 *= f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       st.O[i][0] *= f;
@@ -306,6 +338,10 @@ __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb,
       const float pa = ex2(x[n][j] - base0), pb = ex2(x[n][2 + j] - base1);
       st.l0 += pa;
       st.l1 += pb;
+      if constexpr (ASYM) {
+        st.z0 = fmaf(pa, mv[n][j], st.z0);
+        st.z1 = fmaf(pb, mv[n][j], st.z1);
+      }
       w[n][j] = pa * vsc[n][j];
       w[n][2 + j] = pb * vsc[n][j];
     }
@@ -319,15 +355,16 @@ __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb,
   tile_values<VB>(vb, p0, p1, p2, p3, st.O, lane, km, c64);
 }
 
-template <int KB, int VB>
+template <int KB, int VB, bool ASYM>
 __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeArgs a, int n_tiles, int TR) {
-  using F = Fmt<KB, VB, false>;
-  using T = TileFmt<KB, VB>;
+  using F = Fmt<KB, VB, ASYM>;
+  using T = TileFmt<KB, VB, ASYM>;
   constexpr int S = T::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   const TileSmem mp = tile_smem(S * T::kStageBytes, S);
   uint32_t* qf = reinterpret_cast<uint32_t*>(smem + mp.qf);
   float* qs_s = reinterpret_cast<float*>(smem + mp.qs);
+  float* qz_s = reinterpret_cast<float*>(smem + mp.qz);
   int* qlen_s = reinterpret_cast<int*>(smem + mp.qlen);
   float* cm = reinterpret_cast<float*>(smem + mp.cm);
   float* cl = reinterpret_cast<float*>(smem + mp.cl);
@@ -513,6 +550,14 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
       uint2 packed;
       packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
       packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+      if constexpr (ASYM) {  // the vector's sum exactly as the MMA sees it
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&packed.y));
+        float z = (f0.x + f0.y) + (f1.x + f1.y);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
+        if (lane == 0) qz_s[v] = z;
+      }
       {  // dims 4 lane .. +3 = 32t + 4kk + 0..3 of vector v = row g (+ 8)
         uint32_t* f = qf + (((lane & 7) * 8 + (v & 7)) * 4 + (lane >> 3)) * 4 + (v >> 3);
         f[0] = packed.x;
@@ -528,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
       return;
     }
     const float qs0 = qs_s[g], qs1 = qs_s[g + 8];
+    const float qz0 = ASYM ? qz_s[g] : 0.f, qz1 = ASYM ? qz_s[g + 8] : 0.f;
     const int len0 = qlen_s[g], len1 = qlen_s[g + 8];
     TileState st;
     st.reset();
@@ -540,9 +586,10 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
       if (blk < sp.nblk) {
         const uint8_t* stg = smem + s * T::kStageBytes;
         const float* meta = reinterpret_cast<const float*>(stg + T::kOffMeta + warp * F::kMB);
-        tile_block<KB, VB>(stg + T::kOffK + warp * F::kKBB, stg + T::kOffV + warp * F::kVBB, meta + F::kKS,
-                           meta + F::kVS, blk * kBlock, sp.maxlen, len0, len1, qs0, qs1,
-                           reinterpret_cast<const uint4*>(qf), st, lane, km, c64);
+        tile_block<KB, VB, ASYM>(stg + T::kOffK + warp * F::kKBB, stg + T::kOffV + warp * F::kVBB, meta + F::kKS,
+                                 meta + F::kVS, ASYM ? meta + F::kKO : nullptr, ASYM ? meta + F::kVO : nullptr,
+                                 blk * kBlock, sp.maxlen, len0, len1, qs0, qs1, qz0, qz1,
+                                 reinterpret_cast<const uint4*>(qf), st, lane, km, c64);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -556,6 +603,20 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
     for (int o = 1; o < 4; o <<= 1) {
       st.l0 += __shfl_xor_sync(kFull, st.l0, o);
       st.l1 += __shfl_xor_sync(kFull, st.l1, o);
+    }
+    if constexpr (ASYM) {  // the value zero-point term is the same for every output dimension
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        st.z0 += __shfl_xor_sync(kFull, st.z0, o);
+        st.z1 += __shfl_xor_sync(kFull, st.z1, o);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        st.O[i][0] += st.z0;
+        st.O[i][1] += st.z0;
+        st.O[i][2] += st.z1;
+        st.O[i][3] += st.z1;
+      }
     }
     // every warp has read its last block: the ring is free for the merge
     if (!consumer_sync(cbar, cphase)) {
@@ -632,9 +693,9 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
   }
 }
 
-template <int KB, int VB>
+template <int KB, int VB, bool ASYM>
 struct TileKernel {
-  using T = TileFmt<KB, VB>;
+  using T = TileFmt<KB, VB, ASYM>;
   static int smem_bytes() { return tile_smem(T::kStages * T::kStageBytes, T::kStages).total; }
   static cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
     static std::mutex mu;
@@ -644,8 +705,8 @@ struct TileKernel {
     {
       std::lock_guard<std::mutex> lk(mu);
       if (!done.count(dev)) {
-        cudaFuncSetAttribute(prefill_tile_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
-        cudaFuncSetAttribute(prefill_tile_kernel<KB, VB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        cudaFuncSetAttribute(prefill_tile_kernel<KB, VB, ASYM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
+        cudaFuncSetAttribute(prefill_tile_kernel<KB, VB, ASYM>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
         done[dev] = true;
       }
@@ -662,7 +723,7 @@ struct TileKernel {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tile_kernel<KB, VB>, a, n_tiles, TR);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tile_kernel<KB, VB, ASYM>, a, n_tiles, TR);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
@@ -672,15 +733,20 @@ struct TileKernel {
 
 bool prefill_tiles_supported(const CacheView& c) {
   const bool bits = (c.k_bits == 8 || c.k_bits == 4) && (c.v_bits == 8 || c.v_bits == 4);
-  return bits && !c.asym && (c.q_bits == 0 || c.q_bits == 16) && c.window == 0;
+  return bits && (c.q_bits == 0 || c.q_bits == 16) && c.window == 0;
+}
+
+template <bool ASYM>
+cudaError_t launch_tiles(const DecodeArgs& a, cudaStream_t s) {
+  if (a.c.k_bits == 8 && a.c.v_bits == 8) return TileKernel<8, 8, ASYM>::launch(a, s);
+  if (a.c.k_bits == 4 && a.c.v_bits == 4) return TileKernel<4, 4, ASYM>::launch(a, s);
+  if (a.c.k_bits == 4 && a.c.v_bits == 8) return TileKernel<4, 8, ASYM>::launch(a, s);
+  if (a.c.k_bits == 8 && a.c.v_bits == 4) return TileKernel<8, 4, ASYM>::launch(a, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_prefill_tiles(const DecodeArgs& a, cudaStream_t s) {
-  if (a.c.k_bits == 8 && a.c.v_bits == 8) return TileKernel<8, 8>::launch(a, s);
-  if (a.c.k_bits == 4 && a.c.v_bits == 4) return TileKernel<4, 4>::launch(a, s);
-  if (a.c.k_bits == 4 && a.c.v_bits == 8) return TileKernel<4, 8>::launch(a, s);
-  if (a.c.k_bits == 8 && a.c.v_bits == 4) return TileKernel<8, 4>::launch(a, s);
-  return cudaErrorInvalidValue;
+  return a.c.asym ? launch_tiles<true>(a, s) : launch_tiles<false>(a, s);
 }
 
 }  // namespace kvq
