@@ -43,7 +43,7 @@ struct TileFmt {
   static constexpr int kBlocksPerStage = kConsumerWarps;  // block w of a stage -> consumer warp w
   static constexpr int kStageBytes = kBlocksPerStage * F::kPerBlock;
   static constexpr int kStagesRaw = 65536 / kStageBytes;
-  static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+  static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 16 ? 16 : kStagesRaw);
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kBlocksPerStage * F::kKBB;
   static constexpr int kOffMeta = kOffV + kBlocksPerStage * F::kVBB;
@@ -173,6 +173,22 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, 
       mma_f16(d[0], q[0], q[1], q[2], q[3], a0, a2);
       mma_f16(d[1], q[0], q[1], q[2], q[3], a1, a3);
     }
+  } else if constexpr (KB == 2) {
+    // one 16-byte load: word w holds slices 2w (outputs 0-3) and 2w+1 (4-7),
+    // outputs (token g, token g+8) x (dims +0,+1 and +2,+3) of the slice
+    const uint4 r = p[0];
+    const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t o[8], q0[4], q1[4];
+      s2x16_to_f16(wd[wi], km, o);
+      qa(2 * wi, q0);
+      qa(2 * wi + 1, q1);
+      mma_f16(s[0], q0[0], q0[1], q0[2], q0[3], o[0], o[2]);
+      mma_f16(s[1], q0[0], q0[1], q0[2], q0[3], o[1], o[3]);
+      mma_f16(e[0], q1[0], q1[1], q1[2], q1[3], o[4], o[6]);
+      mma_f16(e[1], q1[0], q1[1], q1[2], q1[3], o[5], o[7]);
+    }
   } else {
     const uint4 r0 = p[0], r1 = p[32];
     const uint32_t g0[4] = {r0.x, r0.y, r0.z, r0.w};
@@ -216,6 +232,20 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
         mma_f16(O[4 * h + k], p0, p1, p2, p3, b0, b1);
       }
     }
+  } else if constexpr (VB == 2) {
+    // one 16-byte load: word w holds m-tiles 2w (outputs 0-3) and 2w+1 (4-7)
+    const uint4 c = p[0];
+    const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t o[8];
+      s2x16_to_f16(wd[wi], km, o);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // m-tile 2 wi + h
+        mma_f16(O[2 * (2 * wi + h)], p0, p1, p2, p3, o[4 * h], o[4 * h + 2]);
+        mma_f16(O[2 * (2 * wi + h) + 1], p0, p1, p2, p3, o[4 * h + 1], o[4 * h + 3]);
+      }
+    }
   } else {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -240,21 +270,25 @@ __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb,
                                            int len1, float qs0, float qs1, float qz0, float qz1, const uint4* qf,
                                            TileState& st, int lane, uint32_t km, uint32_t c64) {
   // offset-binary centre of the code conversion: c' = u - kKC (zero points: m' = m + kKC * s)
-  constexpr float kKC = KB == 8 ? 128.f : 8.f, kVC = VB == 8 ? 128.f : 8.f;
+  constexpr float kKC = KB == 8 ? 128.f : (KB == 4 ? 8.f : 2.f), kVC = VB == 8 ? 128.f : (VB == 4 ? 8.f : 2.f);
+  // 2-bit blocks: one scale (and zero point) for the whole block
+  constexpr bool kGroup = KB == 2;
   const int t = lane & 3;
   float x[2][4];
   tile_scores<KB>(kb, qf, x, lane, km, c64);
   // this thread's tokens: 8n + 2t + j (n = 0, 1; j = 0, 1)
-  const float2 k0 = *reinterpret_cast<const float2*>(ks + 2 * t);
-  const float2 k1 = *reinterpret_cast<const float2*>(ks + 8 + 2 * t);
-  const float2 v0 = *reinterpret_cast<const float2*>(vs + 2 * t);
-  const float2 v1 = *reinterpret_cast<const float2*>(vs + 8 + 2 * t);
+  const float2 k0 = kGroup ? make_float2(ks[0], ks[0]) : *reinterpret_cast<const float2*>(ks + 2 * t);
+  const float2 k1 = kGroup ? make_float2(ks[0], ks[0]) : *reinterpret_cast<const float2*>(ks + 8 + 2 * t);
+  const float2 v0 = kGroup ? make_float2(vs[0], vs[0]) : *reinterpret_cast<const float2*>(vs + 2 * t);
+  const float2 v1 = kGroup ? make_float2(vs[0], vs[0]) : *reinterpret_cast<const float2*>(vs + 8 + 2 * t);
   const float ksc[2][2] = {{k0.x, k0.y}, {k1.x, k1.y}};
   float vsc[2][2] = {{v0.x, v0.y}, {v1.x, v1.y}};
   float mk[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, mv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
   if constexpr (ASYM) {
-    const float2 a0 = *reinterpret_cast<const float2*>(ko + 2 * t), a1 = *reinterpret_cast<const float2*>(ko + 8 + 2 * t);
-    const float2 b0 = *reinterpret_cast<const float2*>(vo + 2 * t), b1 = *reinterpret_cast<const float2*>(vo + 8 + 2 * t);
+    const float2 a0 = kGroup ? make_float2(ko[0], ko[0]) : *reinterpret_cast<const float2*>(ko + 2 * t);
+    const float2 a1 = kGroup ? make_float2(ko[0], ko[0]) : *reinterpret_cast<const float2*>(ko + 8 + 2 * t);
+    const float2 b0 = kGroup ? make_float2(vo[0], vo[0]) : *reinterpret_cast<const float2*>(vo + 2 * t);
+    const float2 b1 = kGroup ? make_float2(vo[0], vo[0]) : *reinterpret_cast<const float2*>(vo + 8 + 2 * t);
     mk[0][0] = fmaf(kKC, k0.x, a0.x);
     mk[0][1] = fmaf(kKC, k0.y, a0.y);
     mk[1][0] = fmaf(kKC, k1.x, a1.x);
@@ -732,7 +766,8 @@ struct TileKernel {
 }  // namespace
 
 bool prefill_tiles_supported(const CacheView& c) {
-  const bool bits = (c.k_bits == 8 || c.k_bits == 4) && (c.v_bits == 8 || c.v_bits == 4);
+  const bool bits = ((c.k_bits == 8 || c.k_bits == 4) && (c.v_bits == 8 || c.v_bits == 4)) ||
+                    (c.k_bits == 2 && c.v_bits == 2);
   return bits && (c.q_bits == 0 || c.q_bits == 16) && c.window == 0;
 }
 
@@ -742,6 +777,7 @@ cudaError_t launch_tiles(const DecodeArgs& a, cudaStream_t s) {
   if (a.c.k_bits == 4 && a.c.v_bits == 4) return TileKernel<4, 4, ASYM>::launch(a, s);
   if (a.c.k_bits == 4 && a.c.v_bits == 8) return TileKernel<4, 8, ASYM>::launch(a, s);
   if (a.c.k_bits == 8 && a.c.v_bits == 4) return TileKernel<8, 4, ASYM>::launch(a, s);
+  if (a.c.k_bits == 2 && a.c.v_bits == 2) return TileKernel<2, 2, ASYM>::launch(a, s);
   return cudaErrorInvalidValue;
 }
 
