@@ -200,10 +200,12 @@ def test_prefill_tiles_match_the_oracle(fmt, order):
 
 
 @pytest.mark.parametrize("heads", [(4, 4), (6, 2), (16, 2)], ids=["g1", "g3", "g8"])
-def test_prefill_tiles_group_sizes(heads):
+@pytest.mark.parametrize("fmt", ["int8", "asym_k4v8", "int2"])
+def test_prefill_tiles_group_sizes(heads, fmt):
     """16 / G rows per tile for G = 1 (16 rows), 3 (5 rows, 15 vectors) and 8 (2 rows)."""
     from quantized_kv_cache_07_gb300 import _lib
-    _check_against_oracle(_run("int8", stream_ctas=_lib.PREFILL_TILES, order="interleaved", heads=heads))
+    _check_against_oracle(_run(fmt, stream_ctas=_lib.PREFILL_TILES, order="interleaved", heads=heads,
+                               fused=fmt != "int2"))
 
 
 def test_prefill_tiles_and_split_rows_agree_without_the_write():
