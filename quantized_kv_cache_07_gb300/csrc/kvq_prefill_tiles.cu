@@ -575,15 +575,27 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
       float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
-      int e = 0;
-      if (am > 0.f) {
-        int ex;
-        frexpf(am, &ex);
-        e = 15 - ex;  // am * 2^e in [2^14, 2^15)
-      }
       uint2 packed;
-      packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
-      packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+      float qscale;  // score scale of the vector: log2(e) / sqrt(D) over its fp16 scaling
+      if (a.c.q_bits == 8) {
+        // int8 query rows: codes (exact in fp16) with the row scale s_q folded
+        // into the score scale; the MMA then forms the integer dot exactly
+        float cq[4];
+        const float sq = quantize_int8_row(x, am, cq);
+        packed.x = pack_half2(cq[0], cq[1]);
+        packed.y = pack_half2(cq[2], cq[3]);
+        qscale = sq * (kLog2e * kInvSqrtD);
+      } else {
+        int e = 0;
+        if (am > 0.f) {
+          int ex;
+          frexpf(am, &ex);
+          e = 15 - ex;  // am * 2^e in [2^14, 2^15)
+        }
+        packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
+        packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+        qscale = ldexpf(kLog2e * kInvSqrtD, -e);
+      }
       if constexpr (ASYM) {  // the vector's sum exactly as the MMA sees it
         const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));
         const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&packed.y));
@@ -598,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
         f[2] = packed.y;
       }
       if (lane == 0) {
-        qs_s[v] = act ? ldexpf(kLog2e * kInvSqrtD, -e) : 0.f;
+        qs_s[v] = act ? qscale : 0.f;
         qlen_s[v] = act ? rowlen[rr] : 0;
       }
     }
@@ -768,7 +780,7 @@ struct TileKernel {
 bool prefill_tiles_supported(const CacheView& c) {
   const bool bits = ((c.k_bits == 8 || c.k_bits == 4) && (c.v_bits == 8 || c.v_bits == 4)) ||
                     (c.k_bits == 2 && c.v_bits == 2);
-  return bits && (c.q_bits == 0 || c.q_bits == 16) && c.window == 0;
+  return bits && (c.q_bits == 0 || c.q_bits == 16 || c.q_bits == 8) && c.window == 0;
 }
 
 template <bool ASYM>
