@@ -358,8 +358,9 @@ kvq_status kvq_decode_static_scratch(const kvq_cache_desc* cache, const void* q,
  *     x the G query heads of one KV head (16 query vectors, one tensor-core
  *     row tile) and streams the blocks of their sequence once for all of
  *     them; rows of one tile that belong to different sequences are taken in
- *     turn.  8-/4-bit or 2-bit caches (symmetric or asymmetric) with q_bits 0, 16 or 8
- *     (KVQ_ERR_UNSUPPORTED otherwise); needs no workspace (NULL accepted).
+ *     turn.  Quantized caches (8-, 4- or 2-bit, symmetric or asymmetric, any
+ *     q_bits); a bf16 cache gives KVQ_ERR_UNSUPPORTED.  Needs no workspace
+ *     (NULL accepted).
  *   > 0: split rows.  Every row is one query group of the decode kernel's
  *     split over that many stream CTAs, so rows of one sequence read
  *     overlapping prefixes (mostly from L2 when they run together).  Every

@@ -99,8 +99,9 @@ cudaError_t launch_decode_asym(const DecodeArgs& a, cudaStream_t s);
 // The two-part fp16 query instantiations (kvq_decode_q32.cu).
 int decode_ctas_per_sm_q32(int k_bits, int v_bits, bool asym, int batch, bool rows);
 cudaError_t launch_decode_q32(const DecodeArgs& a, cudaStream_t s);
-// Prefill on 16-vector query tiles (kvq_prefill_tiles.cu): 8-/4-bit or 2-bit
-// blocks (symmetric or asymmetric), fp16 or int8 query, no window.  Needs no workspace.
+// Prefill on 16-vector query tiles (kvq_prefill_tiles.cu): quantized blocks
+// (8-, 4- or 2-bit, symmetric or asymmetric), any query format, no window.
+// Needs no workspace.
 bool prefill_tiles_supported(const CacheView& c);
 cudaError_t launch_prefill_tiles(const DecodeArgs& a, cudaStream_t s);
 

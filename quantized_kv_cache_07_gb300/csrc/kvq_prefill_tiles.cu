@@ -25,7 +25,9 @@
 // value scale folded into the weight ([P2] "Keys and values need not have
 // identical error sensitivity").  Asymmetric blocks add the key zero-point
 // term m'_k * sum(q) to each score and sum(p * m'_v) to each output row, as
-// the decode kernel does.  The cache's fragment-native block order
+// the decode kernel does.  In the two-part mode (q_bits 32) the query and the
+// weights p * s_v are each carried as fp16 high + low parts: a second product
+// per slice with the low parts, as in decode.  The cache's fragment-native block order
 // (include/kvq.h) gives each lane exactly the B-operand pairs of these
 // products, the same registers the decode kernel uses as A operands.
 #include "kvq_decode_impl.cuh"
@@ -52,7 +54,7 @@ struct TileFmt {
 };
 
 struct TileSmem {
-  int qf, qs, qz, qlen, cm, cl, rowseq, rowlen, bars, total;
+  int qf, qlo, qs, qz, qlen, cm, cl, rowseq, rowlen, bars, total;
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
@@ -61,6 +63,8 @@ __host__ __device__ inline TileSmem tile_smem(int ring_bytes, int stages) {
   TileSmem m{};
   int o = align16(ring_bytes);
   m.qf = o;  // query tile in A-operand order: [slice kk][g][t] x (rows g, g + 8) x 4 fp16
+  o = align16(o + 8 * 8 * 4 * 16);
+  m.qlo = o;  // two-part mode: the low fp16 parts in the same order
   o = align16(o + 8 * 8 * 4 * 16);
   m.qs = o;
   o = align16(o + kTileQ * 4);
@@ -145,15 +149,24 @@ struct TileState {
 // of every lane (the fragment-native key order); qf holds the query tile in
 // the same order with rows g and g + 8 interleaved, so the A operand of slice
 // kk is one 16-byte load, its four registers in operand order.
-template <int KB>
-__device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, float (&s)[2][4], int lane,
-                                            uint32_t km, uint32_t c64) {
+template <int KB, bool LOQ>
+__device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, const uint4* qlo, float (&s)[2][4],
+                                            int lane, uint32_t km, uint32_t c64) {
   auto qa = [&](int kk, uint32_t (&r)[4]) {
     const uint4 u = qf[kk * 32 + lane];
     r[0] = u.x;
     r[1] = u.y;
     r[2] = u.z;
     r[3] = u.w;
+  };
+  // one slice's product for n-tile d: the high query parts, then (two-part
+  // mode) the low parts into the same accumulator
+  auto mma2 = [&](float (&d)[4], int kk, const uint32_t (&q)[4], uint32_t b0, uint32_t b1) {
+    mma_f16(d, q[0], q[1], q[2], q[3], b0, b1);
+    if constexpr (LOQ) {
+      const uint4 l = qlo[kk * 32 + lane];
+      mma_f16(d, l.x, l.y, l.z, l.w, b0, b1);
+    }
   };
   float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // odd slices: a second chain
 #pragma unroll
@@ -170,8 +183,8 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, 
       s8x4_to_f16_r(g0[kk], c64, a0, a2);  // tokens 0-7
       s8x4_to_f16_r(g8[kk], c64, a1, a3);  // tokens 8-15
       float(&d)[2][4] = (kk & 1) ? e : s;
-      mma_f16(d[0], q[0], q[1], q[2], q[3], a0, a2);
-      mma_f16(d[1], q[0], q[1], q[2], q[3], a1, a3);
+      mma2(d[0], kk, q, a0, a2);
+      mma2(d[1], kk, q, a1, a3);
     }
   } else if constexpr (KB == 2) {
     // one 16-byte load: word w holds slices 2w (outputs 0-3) and 2w+1 (4-7),
@@ -184,10 +197,10 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, 
       s2x16_to_f16(wd[wi], km, o);
       qa(2 * wi, q0);
       qa(2 * wi + 1, q1);
-      mma_f16(s[0], q0[0], q0[1], q0[2], q0[3], o[0], o[2]);
-      mma_f16(s[1], q0[0], q0[1], q0[2], q0[3], o[1], o[3]);
-      mma_f16(e[0], q1[0], q1[1], q1[2], q1[3], o[4], o[6]);
-      mma_f16(e[1], q1[0], q1[1], q1[2], q1[3], o[5], o[7]);
+      mma2(s[0], 2 * wi, q0, o[0], o[2]);
+      mma2(s[1], 2 * wi, q0, o[1], o[3]);
+      mma2(e[0], 2 * wi + 1, q1, o[4], o[6]);
+      mma2(e[1], 2 * wi + 1, q1, o[5], o[7]);
     }
   } else {
     const uint4 r0 = p[0], r1 = p[32];
@@ -201,10 +214,10 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, 
       uint32_t q0[4], q1[4];
       qa(2 * wi, q0);
       qa(2 * wi + 1, q1);
-      mma_f16(s[0], q0[0], q0[1], q0[2], q0[3], x0, x1);
-      mma_f16(s[1], q0[0], q0[1], q0[2], q0[3], y0, y1);
-      mma_f16(e[0], q1[0], q1[1], q1[2], q1[3], x2, x3);
-      mma_f16(e[1], q1[0], q1[1], q1[2], q1[3], y2, y3);
+      mma2(s[0], 2 * wi, q0, x0, x1);
+      mma2(s[1], 2 * wi, q0, y0, y1);
+      mma2(e[0], 2 * wi + 1, q1, x2, x3);
+      mma2(e[1], 2 * wi + 1, q1, y2, y3);
     }
   }
 #pragma unroll
@@ -216,10 +229,15 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, 
 // O += P . V for one block: P in A-operand registers (rows g / g + 8, token
 // slots in the value block's order), V codes converted to the B-operand pairs
 // of dims 16 mt + g (O[2 mt]) and 16 mt + 8 + g (O[2 mt + 1]).
-template <int VB>
-__device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3,
+template <int VB, bool LOW>
+__device__ __forceinline__ void tile_values(const uint8_t* vb, const uint32_t (&ph)[4], const uint32_t (&pl)[4],
                                             float (&O)[16][4], int lane, uint32_t km, uint32_t c64) {
   const uint4* p = reinterpret_cast<const uint4*>(vb) + lane;
+  // the high weights, then (two-part mode) the low weights into the same accumulator
+  auto mma2 = [&](float (&d)[4], uint32_t b0, uint32_t b1) {
+    mma_f16(d, ph[0], ph[1], ph[2], ph[3], b0, b1);
+    if constexpr (LOW) mma_f16(d, pl[0], pl[1], pl[2], pl[3], b0, b1);
+  };
   if constexpr (VB == 8) {
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -229,7 +247,7 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
       for (int k = 0; k < 4; ++k) {
         uint32_t b0, b1;
         s8x4_to_f16_r(w[k], c64, b0, b1);
-        mma_f16(O[4 * h + k], p0, p1, p2, p3, b0, b1);
+        mma2(O[4 * h + k], b0, b1);
       }
     }
   } else if constexpr (VB == 2) {
@@ -242,8 +260,8 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
       s2x16_to_f16(wd[wi], km, o);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // m-tile 2 wi + h
-        mma_f16(O[2 * (2 * wi + h)], p0, p1, p2, p3, o[4 * h], o[4 * h + 2]);
-        mma_f16(O[2 * (2 * wi + h) + 1], p0, p1, p2, p3, o[4 * h + 1], o[4 * h + 3]);
+        mma2(O[2 * (2 * wi + h)], o[4 * h], o[4 * h + 2]);
+        mma2(O[2 * (2 * wi + h) + 1], o[4 * h + 1], o[4 * h + 3]);
       }
     }
   } else {
@@ -255,8 +273,8 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
       for (int k = 0; k < 4; ++k) {  // m-tile 4h + k
         uint32_t x0, x1, x2, x3;
         s4x8_to_f16(w[k], km, x0, x1, x2, x3);
-        mma_f16(O[2 * (4 * h + k)], p0, p1, p2, p3, x0, x1);
-        mma_f16(O[2 * (4 * h + k) + 1], p0, p1, p2, p3, x2, x3);
+        mma2(O[2 * (4 * h + k)], x0, x1);
+        mma2(O[2 * (4 * h + k) + 1], x2, x3);
       }
     }
   }
@@ -264,18 +282,18 @@ __device__ __forceinline__ void tile_values(const uint8_t* vb, uint32_t p0, uint
 
 // One block of one consumer warp: scores, causal mask, online softmax with the
 // lazy maximum and the sigma offset of the decode kernel, value product.
-template <int KB, int VB, bool ASYM>
+template <int KB, int VB, bool ASYM, bool LOQ>
 __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb, const float* ks, const float* vs,
                                            const float* ko, const float* vo, int tok0, int maxlen, int len0,
                                            int len1, float qs0, float qs1, float qz0, float qz1, const uint4* qf,
-                                           TileState& st, int lane, uint32_t km, uint32_t c64) {
+                                           const uint4* qlo, TileState& st, int lane, uint32_t km, uint32_t c64) {
   // offset-binary centre of the code conversion: c' = u - kKC (zero points: m' = m + kKC * s)
   constexpr float kKC = KB == 8 ? 128.f : (KB == 4 ? 8.f : 2.f), kVC = VB == 8 ? 128.f : (VB == 4 ? 8.f : 2.f);
   // 2-bit blocks: one scale (and zero point) for the whole block
   constexpr bool kGroup = KB == 2;
   const int t = lane & 3;
   float x[2][4];
-  tile_scores<KB>(kb, qf, x, lane, km, c64);
+  tile_scores<KB, LOQ>(kb, qf, qlo, x, lane, km, c64);
   // this thread's tokens: 8n + 2t + j (n = 0, 1; j = 0, 1)
   const float2 k0 = kGroup ? make_float2(ks[0], ks[0]) : *reinterpret_cast<const float2*>(ks + 2 * t);
   const float2 k1 = kGroup ? make_float2(ks[0], ks[0]) : *reinterpret_cast<const float2*>(ks + 8 + 2 * t);
@@ -382,14 +400,20 @@ __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb,
   // A operand of the value product: token slot k of the value block order
   // holds tokens (2t, 2t + 8) at k = (2t, 2t + 1) and (2t + 1, 2t + 9) at
   // k = (2t + 8, 2t + 9)
-  const uint32_t p0 = pack_half2(w[0][0], w[1][0]);  // row g
-  const uint32_t p1 = pack_half2(w[0][2], w[1][2]);  // row g + 8
-  const uint32_t p2 = pack_half2(w[0][1], w[1][1]);
-  const uint32_t p3 = pack_half2(w[0][3], w[1][3]);
-  tile_values<VB>(vb, p0, p1, p2, p3, st.O, lane, km, c64);
+  const float wr[4][2] = {{w[0][0], w[1][0]}, {w[0][2], w[1][2]}, {w[0][1], w[1][1]}, {w[0][3], w[1][3]}};
+  uint32_t ph[4], pl[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // registers: row g, row g + 8, row g, row g + 8
+    ph[i] = pack_half2(wr[i][0], wr[i][1]);
+    if constexpr (LOQ) {  // low parts w - hi (exact in fp32)
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&ph[i]));
+      pl[i] = pack_half2(wr[i][0] - hf.x, wr[i][1] - hf.y);
+    }
+  }
+  tile_values<VB, LOQ>(vb, ph, pl, st.O, lane, km, c64);
 }
 
-template <int KB, int VB, bool ASYM>
+template <int KB, int VB, bool ASYM, bool LOQ>
 __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeArgs a, int n_tiles, int TR) {
   using F = Fmt<KB, VB, ASYM>;
   using T = TileFmt<KB, VB, ASYM>;
@@ -397,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
   extern __shared__ __align__(128) uint8_t smem[];
   const TileSmem mp = tile_smem(S * T::kStageBytes, S);
   uint32_t* qf = reinterpret_cast<uint32_t*>(smem + mp.qf);
+  uint32_t* qlo = reinterpret_cast<uint32_t*>(smem + mp.qlo);
   float* qs_s = reinterpret_cast<float*>(smem + mp.qs);
   float* qz_s = reinterpret_cast<float*>(smem + mp.qz);
   int* qlen_s = reinterpret_cast<int*>(smem + mp.qlen);
@@ -576,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
       uint2 packed;
+      float ylo[4] = {0.f, 0.f, 0.f, 0.f};  // the scaled fp32 values (two-part mode: their low parts)
       float qscale;  // score scale of the vector: log2(e) / sqrt(D) over its fp16 scaling
       if (a.c.q_bits == 8) {
         // int8 query rows: codes (exact in fp16) with the row scale s_q folded
@@ -592,22 +618,36 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
           frexpf(am, &ex);
           e = 15 - ex;  // am * 2^e in [2^14, 2^15)
         }
-        packed.x = pack_half2(ldexpf(x[0], e), ldexpf(x[1], e));
-        packed.y = pack_half2(ldexpf(x[2], e), ldexpf(x[3], e));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ylo[j] = ldexpf(x[j], e);
+        packed.x = pack_half2(ylo[0], ylo[1]);
+        packed.y = pack_half2(ylo[2], ylo[3]);
         qscale = ldexpf(kLog2e * kInvSqrtD, -e);
       }
       if constexpr (ASYM) {  // the vector's sum exactly as the MMA sees it
         const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));
         const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&packed.y));
         float z = (f0.x + f0.y) + (f1.x + f1.y);
+        if constexpr (LOQ) {  // plus the low parts, as the second product sees them
+          const uint32_t l0 = pack_half2(ylo[0] - f0.x, ylo[1] - f0.y), l1 = pack_half2(ylo[2] - f1.x, ylo[3] - f1.y);
+          const float2 g0 = __half22float2(*reinterpret_cast<const __half2*>(&l0));
+          const float2 g1 = __half22float2(*reinterpret_cast<const __half2*>(&l1));
+          z += (g0.x + g0.y) + (g1.x + g1.y);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
         if (lane == 0) qz_s[v] = z;
       }
       {  // dims 4 lane .. +3 = 32t + 4kk + 0..3 of vector v = row g (+ 8)
-        uint32_t* f = qf + (((lane & 7) * 8 + (v & 7)) * 4 + (lane >> 3)) * 4 + (v >> 3);
-        f[0] = packed.x;
-        f[2] = packed.y;
+        const int at = (((lane & 7) * 8 + (v & 7)) * 4 + (lane >> 3)) * 4 + (v >> 3);
+        qf[at] = packed.x;
+        qf[at + 2] = packed.y;
+        if constexpr (LOQ) {  // two-part query: the low parts y - hi (exact in fp32)
+          const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));
+          const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&packed.y));
+          qlo[at] = pack_half2(ylo[0] - h0.x, ylo[1] - h0.y);
+          qlo[at + 2] = pack_half2(ylo[2] - h1.x, ylo[3] - h1.y);
+        }
       }
       if (lane == 0) {
         qs_s[v] = act ? qscale : 0.f;
@@ -632,10 +672,11 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
       if (blk < sp.nblk) {
         const uint8_t* stg = smem + s * T::kStageBytes;
         const float* meta = reinterpret_cast<const float*>(stg + T::kOffMeta + warp * F::kMB);
-        tile_block<KB, VB, ASYM>(stg + T::kOffK + warp * F::kKBB, stg + T::kOffV + warp * F::kVBB, meta + F::kKS,
-                                 meta + F::kVS, ASYM ? meta + F::kKO : nullptr, ASYM ? meta + F::kVO : nullptr,
-                                 blk * kBlock, sp.maxlen, len0, len1, qs0, qs1, qz0, qz1,
-                                 reinterpret_cast<const uint4*>(qf), st, lane, km, c64);
+        tile_block<KB, VB, ASYM, LOQ>(stg + T::kOffK + warp * F::kKBB, stg + T::kOffV + warp * F::kVBB,
+                                      meta + F::kKS, meta + F::kVS, ASYM ? meta + F::kKO : nullptr,
+                                      ASYM ? meta + F::kVO : nullptr, blk * kBlock, sp.maxlen, len0, len1, qs0, qs1,
+                                      qz0, qz1, reinterpret_cast<const uint4*>(qf),
+                                      reinterpret_cast<const uint4*>(qlo), st, lane, km, c64);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -739,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
   }
 }
 
-template <int KB, int VB, bool ASYM>
+template <int KB, int VB, bool ASYM, bool LOQ>
 struct TileKernel {
   using T = TileFmt<KB, VB, ASYM>;
   static int smem_bytes() { return tile_smem(T::kStages * T::kStageBytes, T::kStages).total; }
@@ -751,8 +792,8 @@ struct TileKernel {
     {
       std::lock_guard<std::mutex> lk(mu);
       if (!done.count(dev)) {
-        cudaFuncSetAttribute(prefill_tile_kernel<KB, VB, ASYM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
-        cudaFuncSetAttribute(prefill_tile_kernel<KB, VB, ASYM>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        cudaFuncSetAttribute(prefill_tile_kernel<KB, VB, ASYM, LOQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
+        cudaFuncSetAttribute(prefill_tile_kernel<KB, VB, ASYM, LOQ>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
         done[dev] = true;
       }
@@ -769,7 +810,7 @@ struct TileKernel {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tile_kernel<KB, VB, ASYM>, a, n_tiles, TR);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tile_kernel<KB, VB, ASYM, LOQ>, a, n_tiles, TR);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
@@ -780,21 +821,23 @@ struct TileKernel {
 bool prefill_tiles_supported(const CacheView& c) {
   const bool bits = ((c.k_bits == 8 || c.k_bits == 4) && (c.v_bits == 8 || c.v_bits == 4)) ||
                     (c.k_bits == 2 && c.v_bits == 2);
-  return bits && (c.q_bits == 0 || c.q_bits == 16 || c.q_bits == 8) && c.window == 0;
+  return bits && (c.q_bits == 0 || c.q_bits == 16 || c.q_bits == 8 || c.q_bits == 32) && c.window == 0;
 }
 
-template <bool ASYM>
+template <bool ASYM, bool LOQ>
 cudaError_t launch_tiles(const DecodeArgs& a, cudaStream_t s) {
-  if (a.c.k_bits == 8 && a.c.v_bits == 8) return TileKernel<8, 8, ASYM>::launch(a, s);
-  if (a.c.k_bits == 4 && a.c.v_bits == 4) return TileKernel<4, 4, ASYM>::launch(a, s);
-  if (a.c.k_bits == 4 && a.c.v_bits == 8) return TileKernel<4, 8, ASYM>::launch(a, s);
-  if (a.c.k_bits == 8 && a.c.v_bits == 4) return TileKernel<8, 4, ASYM>::launch(a, s);
-  if (a.c.k_bits == 2 && a.c.v_bits == 2) return TileKernel<2, 2, ASYM>::launch(a, s);
+  if (a.c.k_bits == 8 && a.c.v_bits == 8) return TileKernel<8, 8, ASYM, LOQ>::launch(a, s);
+  if (a.c.k_bits == 4 && a.c.v_bits == 4) return TileKernel<4, 4, ASYM, LOQ>::launch(a, s);
+  if (a.c.k_bits == 4 && a.c.v_bits == 8) return TileKernel<4, 8, ASYM, LOQ>::launch(a, s);
+  if (a.c.k_bits == 8 && a.c.v_bits == 4) return TileKernel<8, 4, ASYM, LOQ>::launch(a, s);
+  if (a.c.k_bits == 2 && a.c.v_bits == 2) return TileKernel<2, 2, ASYM, LOQ>::launch(a, s);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_prefill_tiles(const DecodeArgs& a, cudaStream_t s) {
-  return a.c.asym ? launch_tiles<true>(a, s) : launch_tiles<false>(a, s);
+  const bool loq = a.c.q_bits == 32;
+  if (a.c.asym) return loq ? launch_tiles<true, true>(a, s) : launch_tiles<true, false>(a, s);
+  return loq ? launch_tiles<false, true>(a, s) : launch_tiles<false, false>(a, s);
 }
 
 }  // namespace kvq

@@ -120,9 +120,12 @@ TILE_FORMATS = {
     "asym_int8_factor": dict(k_bits=8, v_bits=8, asym=True, channel_factor=True),
     "asym_int2": dict(k_bits=2, v_bits=2, asym=True),
     "qint8_asym_k4v4_factor": dict(k_bits=4, v_bits=4, asym=True, channel_factor=True, q_bits=8),
+    "q32_asym_int4_factor_outliers": dict(k_bits=4, v_bits=4, asym=True, channel_factor=True, outlier_channels=4,
+                                          q_bits=32),
+    "bf16": dict(k_bits=16, v_bits=16),
 }
 TILE_PATH_FORMATS = ["int8", "int4_factor", "k4v8_t3", "k8v4_chan", "asym_k4v8", "asym_int8_factor", "int2",
-                     "asym_int2", "qint8_int8", "qint8_asym_k4v4_factor"]
+                     "asym_int2", "qint8_int8", "qint8_asym_k4v4_factor", "q32_k8v4", "q32_asym_int4_factor_outliers"]
 
 
 @pytest.mark.parametrize("fmt", list(PREFILL_FORMATS))
@@ -218,7 +221,7 @@ def test_prefill_tiles_and_split_rows_agree_without_the_write():
     np.testing.assert_allclose(a[6], b[6], rtol=0, atol=TOL)
 
 
-@pytest.mark.parametrize("fmt", ["q32_k8v4"])
+@pytest.mark.parametrize("fmt", ["bf16"])
 def test_prefill_tiles_refuse_other_formats(fmt):
     from quantized_kv_cache_07_gb300 import _lib
     with pytest.raises(_lib.KvqError) as e:
