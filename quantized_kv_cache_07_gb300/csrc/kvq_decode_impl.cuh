@@ -112,7 +112,7 @@ struct SmemMap {
   int merge_ml;  // float m[4][8], l[4][8]
   int qh;        // 16-bit [8][128]: B-operand rows of the current query group
   int qlo;       // fp16 [32 lanes x 16] low parts of the query fragments, in fragment order
-  int qs;        // float [8] score scales, then float [8] sums of the fp16 query rows
+  int qs;        // float [8] score scales, [8] sums of the fp16 query rows, [8][2] offset terms
   int qraw;      // bf16 [2][8][128]: prefetched raw query rows (double buffer)
   int fraw;      // float [2][128]: prefetched per-channel key factor row
   int hdr;       // int4 [stages]
@@ -132,7 +132,7 @@ __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, i
   m.merge_ml = o; o += 2 * kConsumerWarps * kMaxGroup * 4;
   m.qh = o;       o += kMaxGroup * kHeadDim * 2;
   m.qlo = o;      o += loq ? kMaxGroup * kHeadDim * 2 : 0;  // two-part query only
-  m.qs = o;       o += kMaxGroup * 4 + 32;
+  m.qs = o;       o += 4 * kMaxGroup * 4;
   m.qraw = o;     o += 2 * kMaxGroup * kHeadDim * 2;
   m.fraw = o;     o += 2 * kHeadDim * 4;
   m.hdr = o;      o += stages * 16;
@@ -153,11 +153,25 @@ __host__ __device__ inline SmemMap smem_map(int stage_bytes_total, int stages, i
 // uint4) and every k-slice runs a second MMA with them into the same fp32
 // accumulator, so the score carries about 22 significant bits of the query
 // instead of 11.  km holds kMagicF16x2 for the 4-bit conversion (magic_f16x2).
-template <int KB, bool LOQ>
+//
+// With OFF (8-bit keys, one-part query) the codes enter the MMA with their
+// offset (s8x4_to_f16_off: 1152 + c) and the accumulators start at minus 1152
+// times the query's dimensions that they cover: acc the even k-slices (zi.x,
+// zi.y: queries 2t, 2t + 1), acc2 the odd ones (zi.z, zi.w), so acc + acc2 is
+// the code dot.  With int8 query codes every partial sum stays an integer
+// below 2^24: exact.  Each block's accumulators start afresh, so the offset's
+// rounding stays within the block.
+template <int KB, bool LOQ, bool OFF>
 __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&qf)[16], const uint4* qlo,
-                                            float (&acc)[4], int lane, uint32_t km) {
+                                            float (&acc)[4], int lane, uint32_t km, float4 zi) {
   // two accumulators halve the dependent MMA chain; summed at the end
   float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (OFF) {
+    acc[0] = acc[2] = zi.x;
+    acc[1] = acc[3] = zi.y;
+    acc2[0] = acc2[2] = zi.z;
+    acc2[1] = acc2[3] = zi.w;
+  }
   const uint4* p = reinterpret_cast<const uint4*>(kb) + lane;
   if constexpr (KB == 8) {
     const uint4 r0a = p[0], r0b = p[32], r1a = p[64], r1b = p[96];
@@ -171,8 +185,13 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
       for (int h = 0; h < 2; ++h) {
         const int kk = 2 * i + h;
         uint32_t a0, a1, a2, a3;
-        s8x4_to_f16(g0[kk], a0, a2);
-        s8x4_to_f16(g8[kk], a1, a3);
+        if constexpr (OFF) {
+          s8x4_to_f16_off(g0[kk], a0, a2);
+          s8x4_to_f16_off(g8[kk], a1, a3);
+        } else {
+          s8x4_to_f16(g0[kk], a0, a2);
+          s8x4_to_f16(g8[kk], a1, a3);
+        }
         float (&ac)[4] = h ? acc2 : acc;
         mma_f16(ac, a0, a1, a2, a3, qf[2 * kk], qf[2 * kk + 1]);
         if constexpr (LOQ) mma_f16(ac, a0, a1, a2, a3, h ? lo.z : lo.x, h ? lo.w : lo.y);
@@ -232,6 +251,11 @@ __device__ __forceinline__ void score_block(const uint8_t* kb, const uint32_t (&
 // bf16 blocks) weights p * s_v; with LOW (the two-part mode of code blocks, and
 // always for bf16 blocks) b0lo, b1lo hold their low parts and a second MMA per
 // slice adds them, so the weights carry about 22 significant bits instead of 11.
+//
+// The value codes are converted exactly (no offset as in score_block): the
+// value accumulators run over every block of a segment, and an offset of
+// about 1152 w per token would grow their fp32 rounding with the segment's
+// length.
 template <int VB, bool LOW>
 __device__ __forceinline__ void value_block(const uint8_t* vb, uint32_t b0, uint32_t b1, uint32_t b0lo,
                                             uint32_t b1lo, float (&O)[8][4], int lane, uint32_t km) {
@@ -413,6 +437,15 @@ struct WarpState {
   }
 };
 
+// Offset key codes (score_block with OFF): 8-bit keys with a one-part query.
+// 4-bit keys keep the exact conversion: an offset form (every nibble moved to
+// mantissa bits 4-7 by a shift) trades the fp16 subtractions for three more
+// integer shifts per word and measured slower.
+template <int KB, bool LOQ>
+struct OffsetKeys {
+  static constexpr bool kOn = !LOQ && KB == 8;
+};
+
 // NB (1 or 2) 16-token blocks of one warp: scores on the codes, per-token key
 // scale after the dot product, online softmax, value scale folded into the
 // weight, value MMA.  With NB = 2 the two blocks' chains interleave and share
@@ -425,9 +458,10 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
                                                const float* const (&ks)[NB], const float* const (&vs)[NB],
                                                const float* const (&ko)[NB], const float* const (&vo)[NB],
                                                const int (&valid)[NB], const uint32_t (&qf)[16],
-                                               const uint4* qlo, float qs0, float qs1, float qz0, float qz1,
-                                               WarpState& st, int lane, uint32_t km) {
+                                               const uint4* qlo, const float4* qzo, float qs0, float qs1, float qz0,
+                                               float qz1, WarpState& st, int lane, uint32_t km) {
   constexpr bool kBf16 = (KB == 16);
+  constexpr bool kOffK = OffsetKeys<KB, LOQ>::kOn;
   // offset-binary centre of the code conversion: c' = u - kKC
   constexpr float kKC = (KB == 8) ? 128.f : (KB == 4 ? 8.f : 2.f), kVC = (VB == 8) ? 128.f : (VB == 4 ? 8.f : 2.f);
   // token g's (and g + 8's) entry of a per-token record; 2-bit blocks hold one per block
@@ -436,10 +470,11 @@ __device__ __forceinline__ void process_blocks(const uint8_t* const (&kb)[NB], c
   float x[NB][4];
   float sv[NB][2];
   float mv[NB][2];
+  const float4 zi = kOffK ? qzo[t] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < NB; ++j) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    score_block<KB, LOQ>(kb[j], qf, qlo, acc, lane, km);
+    score_block<KB, LOQ, kOffK>(kb[j], qf, qlo, acc, lane, km, zi);
     float sk0 = 1.f, sk1 = 1.f;
     sv[j][0] = sv[j][1] = 1.f;
     const int i0 = kGroup ? 0 : g, i1 = kGroup ? 0 : g + 8;
@@ -769,6 +804,18 @@ __device__ __noinline__ void write_query_rows(const DecodeArgs& a, int buf, cons
           const int ft = lane >> 3, fi = (lane & 7) >> 1, fk = 2 * (lane & 1);
           *reinterpret_cast<uint2*>(qlo + (fi * 32 + 4 * q + ft) * 4 + fk) = lo;
         }
+      }
+      {
+        // offset terms of the key codes (score_block with OFF): minus 1152
+        // times the sums of the row as the MMA sees it over the even and the
+        // odd k-slices (dims with bit 2 clear or set; this lane's four dims
+        // share it), stored as float4 {even 2t, even 2t+1, odd 2t, odd 2t+1}
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&packed.y));
+        float zs = (f0.x + f0.y) + (f1.x + f1.y);
+#pragma unroll
+        for (int o = 16; o > 1; o >>= 1) zs += __shfl_xor_sync(kFull, zs, o);
+        if (lane < 2) qs[2 * kMaxGroup + (q >> 1) * 4 + 2 * lane + (q & 1)] = -kOffsetF16 * zs;
       }
       if constexpr (ASYM) {
         // sum of the fp16 row exactly as the MMA sees it (zero-point term)
@@ -1153,7 +1200,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       const uint8_t* const vbs[1] = {vb};
       const float* const nos[1] = {nullptr};
       const int val[1] = {min(kBlock, nw - j * kBlock)};
-      process_blocks<16, 16, 1, false, false>(kbs, vbs, nos, nos, nos, nos, val, qf, nullptr, qs0, qs1, 0.f, 0.f, st, lane,
+      process_blocks<16, 16, 1, false, false>(kbs, vbs, nos, nos, nos, nos, val, qf, nullptr, nullptr, qs0, qs1, 0.f, 0.f, st, lane,
                                        0u);
     }
     const size_t slot = size_t(P) + U + u;
@@ -1321,6 +1368,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       return;
     }
   }
+  // offset terms of the key codes (score_block with OFF), one float4 per t
+  const float4* qzo = reinterpret_cast<const float4*>(qs + 2 * kMaxGroup);
   // low query parts of code blocks (only for the two-part fp16 query, q_bits = 32)
   const uint4* qlo = LOQ ? reinterpret_cast<const uint4*>(qlo_s) + lane : nullptr;
   int s = 0;
@@ -1377,7 +1426,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const float* const kos[2] = {kop(j0), kop(j1)};
         const float* const vos[2] = {vop(j0), vop(j1)};
         const int vals[2] = {val(j0), val(j1)};
-        process_blocks<KB, VB, 2, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qs0, qs1, qz0, qz1, st, lane,
+        process_blocks<KB, VB, 2, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qzo, qs0, qs1, qz0, qz1, st, lane,
                                         km);
       } else {
         const uint8_t* const kbs[1] = {kp(j0)};
@@ -1387,7 +1436,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
         const float* const kos[1] = {kop(j0)};
         const float* const vos[1] = {vop(j0)};
         const int vals[1] = {val(j0)};
-        process_blocks<KB, VB, 1, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qs0, qs1, qz0, qz1, st, lane,
+        process_blocks<KB, VB, 1, ASYM, LOQ>(kbs, vbs, kss, vss, kos, vos, vals, qf, qlo, qzo, qs0, qs1, qz0, qz1, st, lane,
                                         km);
       }
     }

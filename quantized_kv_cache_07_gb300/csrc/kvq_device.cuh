@@ -147,6 +147,19 @@ __device__ __forceinline__ void s4x8_to_f16(uint32_t w, uint32_t km, uint32_t& p
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(p3) : "r"(d), "r"(sixteenth), "r"(m72));
 }
 
+// Offset conversion of int8 codes: the byte u = c + 128 stays under the magic,
+// 1024 + u = kOffsetF16 + c exactly, and the subtraction of the offset is left
+// to the caller, which folds it into the key contraction once per query row
+// (the accumulators of each block start at minus the offset times the
+// query's sum).
+constexpr float kOffsetF16 = 1152.f;
+
+// Four int8 codes (biased bytes of w) -> (1152 + c0, 1152 + c1), (1152 + c2, 1152 + c3).
+__device__ __forceinline__ void s8x4_to_f16_off(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = __byte_perm(w, 0x64646464u, 0x4140);
+  hi = __byte_perm(w, 0x64646464u, 0x4342);
+}
+
 // Sixteen 2-bit codes (biased fields u = c + 2, or the asymmetric u itself) of
 // w -> eight fp16 pairs.  Output 4h + r holds the fields at bits 8h + 2r (low
 // half) and 16 + 8h + 2r (high half): the field sits at 4^r * u under the
