@@ -54,7 +54,7 @@ struct TileFmt {
 };
 
 struct TileSmem {
-  int qf, qlo, qs, qz, qlen, cm, cl, rowseq, rowlen, bars, total;
+  int qf, qlo, qs, qz, zo, qlen, cm, cl, rowseq, rowlen, bars, total;
 };
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
@@ -70,6 +70,8 @@ __host__ __device__ inline TileSmem tile_smem(int ring_bytes, int stages) {
   o = align16(o + kTileQ * 4);
   m.qz = o;  // asymmetric blocks: sum of each fp16 query vector as the MMA sees it
   o = align16(o + kTileQ * 4);
+  m.zo = o;  // offset int8 keys: float4 per g {even g, even g + 8, odd g, odd g + 8}
+  o = align16(o + kTileQ * 2 * 4);
   m.qlen = o;
   o = align16(o + kTileQ * 4);
   m.cm = o;
@@ -107,6 +109,21 @@ __device__ __forceinline__ SubPass sub_pass_at(const int* rowseq, const int* row
   sp.maxlen = ml;
   sp.nblk = (ml + kBlock - 1) / kBlock;
   return sp;
+}
+
+// Int8 keys of the one-part query modes enter the score product with their
+// offset (s8x4_to_f16_r_off: 1152 + c, exact) and each block's accumulators
+// start at minus 1152 times the row's sum over the dims they cover (the even
+// k-slices for s, the odd ones for the second chain), as in the decode kernel.
+template <int KB, bool LOQ>
+struct TileOffsetKeys {
+  static constexpr bool kOn = !LOQ && KB == 8;
+};
+
+// Four int8 codes -> (1152 + c0, 1152 + c1), (1152 + c2, 1152 + c3); c64 as below.
+__device__ __forceinline__ void s8x4_to_f16_r_off(uint32_t w, uint32_t c64, uint32_t& lo, uint32_t& hi) {
+  lo = __byte_perm(w, c64, 0x4140);
+  hi = __byte_perm(w, c64, 0x4342);
 }
 
 // Four int8 codes -> fp16 pairs as s8x4_to_f16, with the byte constant 0x64
@@ -149,9 +166,11 @@ struct TileState {
 // of every lane (the fragment-native key order); qf holds the query tile in
 // the same order with rows g and g + 8 interleaved, so the A operand of slice
 // kk is one 16-byte load, its four registers in operand order.
-template <int KB, bool LOQ>
+// With OFF the accumulators start at zi: {even row g, even row g + 8, odd row
+// g, odd row g + 8} (TileOffsetKeys).
+template <int KB, bool LOQ, bool OFF>
 __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, const uint4* qlo, float (&s)[2][4],
-                                            int lane, uint32_t km, uint32_t c64) {
+                                            int lane, uint32_t km, uint32_t c64, float4 zi) {
   auto qa = [&](int kk, uint32_t (&r)[4]) {
     const uint4 u = qf[kk * 32 + lane];
     r[0] = u.x;
@@ -168,9 +187,14 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, 
       mma_f16(d, l.x, l.y, l.z, l.w, b0, b1);
     }
   };
-  float e[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // odd slices: a second chain
+  float e[2][4];  // odd slices: a second chain
 #pragma unroll
-  for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+  for (int n = 0; n < 2; ++n) {
+    s[n][0] = s[n][1] = OFF ? zi.x : 0.f;
+    s[n][2] = s[n][3] = OFF ? zi.y : 0.f;
+    e[n][0] = e[n][1] = OFF ? zi.z : 0.f;
+    e[n][2] = e[n][3] = OFF ? zi.w : 0.f;
+  }
   const uint4* p = reinterpret_cast<const uint4*>(kb) + lane;
   if constexpr (KB == 8) {
     const uint4 r0a = p[0], r0b = p[32], r1a = p[64], r1b = p[96];
@@ -180,8 +204,13 @@ __device__ __forceinline__ void tile_scores(const uint8_t* kb, const uint4* qf, 
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t a0, a1, a2, a3, q[4];
       qa(kk, q);
-      s8x4_to_f16_r(g0[kk], c64, a0, a2);  // tokens 0-7
-      s8x4_to_f16_r(g8[kk], c64, a1, a3);  // tokens 8-15
+      if constexpr (OFF) {
+        s8x4_to_f16_r_off(g0[kk], c64, a0, a2);  // tokens 0-7
+        s8x4_to_f16_r_off(g8[kk], c64, a1, a3);  // tokens 8-15
+      } else {
+        s8x4_to_f16_r(g0[kk], c64, a0, a2);
+        s8x4_to_f16_r(g8[kk], c64, a1, a3);
+      }
       float(&d)[2][4] = (kk & 1) ? e : s;
       mma2(d[0], kk, q, a0, a2);
       mma2(d[1], kk, q, a1, a3);
@@ -286,14 +315,16 @@ template <int KB, int VB, bool ASYM, bool LOQ>
 __device__ __forceinline__ void tile_block(const uint8_t* kb, const uint8_t* vb, const float* ks, const float* vs,
                                            const float* ko, const float* vo, int tok0, int maxlen, int len0,
                                            int len1, float qs0, float qs1, float qz0, float qz1, const uint4* qf,
-                                           const uint4* qlo, TileState& st, int lane, uint32_t km, uint32_t c64) {
+                                           const uint4* qlo, const float4* zo, TileState& st, int lane, uint32_t km,
+                                           uint32_t c64) {
   // offset-binary centre of the code conversion: c' = u - kKC (zero points: m' = m + kKC * s)
   constexpr float kKC = KB == 8 ? 128.f : (KB == 4 ? 8.f : 2.f), kVC = VB == 8 ? 128.f : (VB == 4 ? 8.f : 2.f);
   // 2-bit blocks: one scale (and zero point) for the whole block
   constexpr bool kGroup = KB == 2;
   const int t = lane & 3;
   float x[2][4];
-  tile_scores<KB, LOQ>(kb, qf, qlo, x, lane, km, c64);
+  constexpr bool kOff = TileOffsetKeys<KB, LOQ>::kOn;
+  tile_scores<KB, LOQ, kOff>(kb, qf, qlo, x, lane, km, c64, kOff ? zo[lane >> 2] : make_float4(0.f, 0.f, 0.f, 0.f));
   // this thread's tokens: 8n + 2t + j (n = 0, 1; j = 0, 1)
   const float2 k0 = kGroup ? make_float2(ks[0], ks[0]) : *reinterpret_cast<const float2*>(ks + 2 * t);
   const float2 k1 = kGroup ? make_float2(ks[0], ks[0]) : *reinterpret_cast<const float2*>(ks + 8 + 2 * t);
@@ -424,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
   uint32_t* qlo = reinterpret_cast<uint32_t*>(smem + mp.qlo);
   float* qs_s = reinterpret_cast<float*>(smem + mp.qs);
   float* qz_s = reinterpret_cast<float*>(smem + mp.qz);
+  float* zo_s = reinterpret_cast<float*>(smem + mp.zo);
   int* qlen_s = reinterpret_cast<int*>(smem + mp.qlen);
   float* cm = reinterpret_cast<float*>(smem + mp.cm);
   float* cl = reinterpret_cast<float*>(smem + mp.cl);
@@ -638,6 +670,16 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
         if (lane == 0) qz_s[v] = z;
       }
+      if constexpr (TileOffsetKeys<KB, LOQ>::kOn) {
+        // offset terms: minus 1152 times the vector's sums over the even and
+        // the odd k-slices (this lane's dims 4 lane .. +3 lie in slice lane & 7)
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&packed.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&packed.y));
+        float zs = (f0.x + f0.y) + (f1.x + f1.y);
+#pragma unroll
+        for (int o = 16; o > 1; o >>= 1) zs += __shfl_xor_sync(kFull, zs, o);
+        if (lane < 2) zo_s[(v & 7) * 4 + 2 * lane + (v >> 3)] = -kOffsetF16 * zs;
+      }
       {  // dims 4 lane .. +3 = 32t + 4kk + 0..3 of vector v = row g (+ 8)
         const int at = (((lane & 7) * 8 + (v & 7)) * 4 + (lane >> 3)) * 4 + (v >> 3);
         qf[at] = packed.x;
@@ -676,7 +718,8 @@ __global__ void __launch_bounds__(kThreads, 3) prefill_tile_kernel(const DecodeA
                                       meta + F::kKS, meta + F::kVS, ASYM ? meta + F::kKO : nullptr,
                                       ASYM ? meta + F::kVO : nullptr, blk * kBlock, sp.maxlen, len0, len1, qs0, qs1,
                                       qz0, qz1, reinterpret_cast<const uint4*>(qf),
-                                      reinterpret_cast<const uint4*>(qlo), st, lane, km, c64);
+                                      reinterpret_cast<const uint4*>(qlo), reinterpret_cast<const float4*>(zo_s), st,
+                                      lane, km, c64);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
