@@ -592,6 +592,29 @@ def test_value_scales_far_from_one_decode_correctly(exp2):
     assert run.err_bits() == 0
 
 
+@pytest.mark.parametrize("q_bits", [16, 8])
+@pytest.mark.parametrize("asym", [False, True])
+@pytest.mark.parametrize("bias", [4.0, 16.0])
+def test_biased_queries_on_int8_keys(bias, asym, q_bits):
+    """Queries with a large common component (every dimension shifted by
+    `bias`) against int8 keys of a few thousand tokens: the int8 key codes enter
+    the score product with their offset of 1152, and each block's accumulators
+    start at minus 1152 times the query's sums, which are largest relative to
+    the code dot for such queries.  The bf16 query is exact in the kernel's fp16
+    staging here (no per-channel factor), so the comparison sees the offset's
+    fp32 rounding; int8 query codes keep every partial sum an exact integer."""
+    from synth import f32_to_bf16_bits
+    w = small_workload(f"qbias_{bias}_{int(asym)}_{q_bits}", batch=2, len_range=(1500, 3000), asym=asym,
+                       q_bits=q_bits)
+    inp = make_inputs(w)
+    inp.q = f32_to_bf16_bits((O.bf16_to_f64(inp.q) + bias).astype(np.float32))
+    ref = oracle_decode(inp)
+    run = DeviceRun(inp)
+    out, lse = run.decode(out_fp32=True)
+    assert compare_outputs(inp, out, lse, ref, out_is_bf16=False) <= 1.0
+    assert run.err_bits() == 0
+
+
 def test_append_out_of_range_positions_are_flagged_and_skipped():
     """A sequence index outside the batch or a position beyond the block
     table's capacity sets KVQ_DEVERR_POSITION and writes nothing."""

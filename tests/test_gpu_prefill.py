@@ -41,7 +41,7 @@ def _write(lib, cache, inp, rows_by_seq, table, err):
                    err_word=err)
 
 
-def _run(fmt, chunk=24, fused=True, stream_ctas=0, seed=5, order="seq", heads=(8, 2)):
+def _run(fmt, chunk=24, fused=True, stream_ctas=0, seed=5, order="seq", heads=(8, 2), q_bias=0.0):
     """Prefix written first, then one kvq_prefill call over the last `chunk`
     positions of every sequence; rows grouped by sequence ("seq") or
     alternating between sequences ("interleaved")."""
@@ -72,6 +72,9 @@ def _run(fmt, chunk=24, fused=True, stream_ctas=0, seed=5, order="seq", heads=(8
     n = len(seq)
     from synth import query_rows
     qbits = query_rows(n, w.q_heads, seed)
+    if q_bias:
+        from synth import f32_to_bf16_bits
+        qbits = f32_to_bf16_bits((O.bf16_to_f64(qbits) + q_bias).astype(np.float32))
     out = torch.zeros((n, w.q_heads, 128), dtype=torch.float32, device="cuda")
     lse = torch.zeros((n, w.q_heads), dtype=torch.float32, device="cuda")
     nb = _lib.kvq_prefill_workspace_size(cache.desc, n, w.q_heads, stream_ctas)
@@ -188,6 +191,15 @@ def _check_against_oracle(res):
     o_ref, l_ref = _oracle(inp, qbits, seq, pos)
     assert np.max(np.abs(out - o_ref)) <= TOL
     assert np.max(np.abs(lse - l_ref)) <= TOL
+
+
+@pytest.mark.parametrize("fmt", ["int8", "qint8_int8"])
+@pytest.mark.parametrize("bias", [4.0, 16.0])
+def test_prefill_tiles_with_biased_queries(fmt, bias):
+    """Query rows with a large common component on int8 keys: the tile path's
+    score accumulators start at minus 1152 times each row's sums (the int8 key
+    codes enter with their offset), largest relative to the code dot here."""
+    _check_against_oracle(_run(fmt, order="interleaved", q_bias=bias))
 
 
 @pytest.mark.parametrize("fmt", TILE_PATH_FORMATS)
