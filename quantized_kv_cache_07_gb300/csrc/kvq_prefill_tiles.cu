@@ -18,9 +18,11 @@
 // four states are merged through shared memory at the end of a sub-pass.
 //
 // Scores: S (16 query vectors x 16 tokens) = Q (16 x 128, fp16, each row
-// scaled by a power of two) . K^T (codes converted exactly to fp16), two m16n8k16
-// products per 16-dim slice; the per-token key scale multiplies the scalar
-// after the dot product ([P3] "The axis choice is a kernel decision").
+// scaled by a power of two) . K^T (codes converted exactly to fp16; int8 codes
+// keep the conversion's offset, 1152 + c, and each block's accumulators start
+// at minus 1152 times the row's sums), two m16n8k16 products per 16-dim slice;
+// the per-token key scale multiplies the scalar after the dot product ([P3]
+// "The axis choice is a kernel decision").
 // Values: O (16 x 128) += (P * s_v) (16 x 16 tokens, fp16) . V (codes), the
 // value scale folded into the weight ([P2] "Keys and values need not have
 // identical error sensitivity").  Asymmetric blocks add the key zero-point
