@@ -494,19 +494,21 @@ class GpuArm:
             except Exception as e:  # capture unavailable: eager calls
                 e2e_graphs = None
                 e2e_timing = "eager calls (graph capture unavailable: %s)" % f"{type(e).__name__}: {e}"[:200]
-        for k in range(3):
-            (e2e_graphs[k % len(e2e_graphs)].replay() if e2e_graphs else e2e_step(k))
-            stream.synchronize()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        t0 = time.perf_counter()
-        for k in range(K):
+        def e2e_run(k):
             if e2e_graphs:
                 e2e_graphs[k % len(e2e_graphs)].replay()
             else:
                 e2e_step(k)
             stream.synchronize()
+
+        for k in range(3):  # warm-up
+            e2e_run(k)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for k in range(K):
+            e2e_run(k)
         e2e_s = (time.perf_counter() - t0) / K
         errbits = int(err.item())
         res = dict(ms_step=ms_total / K, ms_eager=ms_eager, timing="cuda graph of the K steps" if graph is not None
