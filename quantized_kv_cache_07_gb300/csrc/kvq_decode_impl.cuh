@@ -372,6 +372,11 @@ __device__ __forceinline__ float ex2(float x) {
 constexpr float kMaxSlack = 6.f;
 constexpr int kWeightExp = 15;
 constexpr int kSigma0 = 20;
+// Stream CTAs with at most this many virtual blocks hold their second stage
+// until the first has landed (window 4096-token workload: 36 per CTA, 20.6 ->
+// 20.1 us; int4 1k-8k: ~190, 46.4 -> 45.4 us).  Longer ranges keep the deep
+// initial queue (paged 2k-32k, ~1250 per CTA: 361.6 -> 365.6 us with the wait).
+constexpr long long kFirstStageFirstMax = 256;
 
 // A stream CTA owns at least this many blocks (fewer, deeper splits for tiny problems).
 constexpr int kMinBlocksPerCta = 16;
@@ -1324,6 +1329,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const Params prm) {
       if (++s == S) {
         s = 0;
         ph ^= 1u;
+      }
+      if (it == 1 && x < x1 && x1 - x0 <= kFirstStageFirstMax) {
+        // A short range: this stage's copies land before the next ones are
+        // issued, so every CTA's first stage is ahead of anyone's second in
+        // the memory queues and all consumers start early (timing only).
+        bool w_ok = true;
+        if (lane == 0) w_ok = mbar_wait(&full[0], 0u);
+        if (!__shfl_sync(kFull, w_ok ? 1 : 0, 0)) {
+          if (lane == 0) flag(a.err, KVQ_DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
       }
     }
     if (lane != 0) return;
