@@ -37,14 +37,17 @@
 //     the block's metadata record of scales and zero points) with cp.async.bulk
 //     into a ring of shared-memory stages guarded by mbarriers, one copy per run
 //     of consecutive physical blocks; four consumer warps each take one block per
-//     stage (two for 4-bit keys).
+//     stage (two for 4-bit keys).  A CTA with a short range lets its first
+//     stage land before it issues the second.
 //   * Programmatic dependent launch: each CTA lets the next kernel on the stream
 //     launch at once and waits for the previous one before reading memory.
 //   * The GQA group (G <= 8 query heads sharing the KV head) makes the two small
 //     contractions dense: S^T = Kcodes . Q^T and O^T += V^T . (p*s_v)^T run on
 //     mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens/dims on M, the query
-//     group on N.  Codes are converted exactly to fp16 in registers; the cache
-//     is stored in the fragment order so every lane reads 16 contiguous bytes.
+//     group on N.  Codes are converted exactly to fp16 in registers (int8 keys
+//     keep the conversion's offset, cancelled by the score accumulators' start
+//     value); the cache is stored in the fragment order so every lane reads 16
+//     contiguous bytes.
 //   * The query is scaled by an exact power of two into fp16's range; the score
 //     scale s_k * 2^-e * log2(e) / sqrt(D) is applied per score in fp32.  Query
 //     formats: fp16 (default), fp16 high + low parts for both the query and the
