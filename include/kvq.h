@@ -365,8 +365,8 @@ kvq_status kvq_decode_static_scratch(const kvq_cache_desc* cache, const void* q,
  *     split over that many stream CTAs, so rows of one sequence read
  *     overlapping prefixes (mostly from L2 when they run together).  Every
  *     cache format.
- *   0: the tile path when the cache format allows it and there are at least
- *     as many (tile, KV head) pairs as SMs; split rows otherwise.
+ *   0: the tile path when the cache format allows it and the (tile, KV head)
+ *     pairs number at least 9/16 of the SMs; split rows otherwise.
  * Both paths compute the same attention within the output tolerance (they
  * differ in rounding order only).
  *   q          : device bf16 [n][q_heads][128]

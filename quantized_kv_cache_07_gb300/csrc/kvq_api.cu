@@ -339,12 +339,16 @@ kvq_status kvq_prefill(const kvq_cache_desc* cache, const void* q, int32_t n, in
   if (stream_ctas == KVQ_PREFILL_TILES && !tiles_ok) return KVQ_ERR_UNSUPPORTED;
   bool tiles = stream_ctas == KVQ_PREFILL_TILES;
   if (stream_ctas == 0 && tiles_ok) {
-    // enough 16-vector tiles to fill the GPU: the tile path; else split rows
+    // Tiles once their CTAs fill at least 9/16 of the SMs; fewer tiles leave
+    // the long prefixes to too few CTAs and split rows (every row one query
+    // group of the decode split over all SMs) are faster.  Measured crossover
+    // (8k-32k prefixes, int8, 32/8 heads): split rows ahead at 48 and 64 tile
+    // CTAs (1.2-1.6x), tiles ahead at 96 (1.04-1.1x) and 128 (1.3x).
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess)
       return KVQ_ERR_CUDA;
-    tiles = prefill_tiles(n, q_heads, cache->num_kv_heads) >= (long long)sms;
+    tiles = prefill_tiles(n, q_heads, cache->num_kv_heads) * 16 >= 9ll * sms;
   }
   kvq::DecodeLayout L{};
   if (!tiles) {

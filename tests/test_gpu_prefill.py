@@ -198,8 +198,25 @@ def _check_against_oracle(res):
 def test_prefill_tiles_with_biased_queries(fmt, bias):
     """Query rows with a large common component on int8 keys: the tile path's
     score accumulators start at minus 1152 times each row's sums (the int8 key
-    codes enter with their offset), largest relative to the code dot here."""
-    _check_against_oracle(_run(fmt, order="interleaved", q_bias=bias))
+    codes enter with their offset), largest relative to the code dot here.
+    Both paths: the tile kernel and split rows (the decode kernel)."""
+    from quantized_kv_cache_07_gb300 import _lib
+    _check_against_oracle(_run(fmt, order="interleaved", q_bias=bias, stream_ctas=_lib.PREFILL_TILES))
+    _check_against_oracle(_run(fmt, order="interleaved", q_bias=bias, stream_ctas=7))
+
+
+def test_prefill_auto_takes_tiles_when_they_fill_the_gpu():
+    """stream_ctas = 0 takes the tile path once its (tile, KV head) CTAs number
+    at least 9/16 of the SMs: its outputs then equal the tile path's bit for bit."""
+    from quantized_kv_cache_07_gb300 import _lib
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    auto = _run("int8", chunk=64, fused=False, stream_ctas=0, heads=(32, 8))
+    rows = len(auto[3])
+    ctas = ((rows + 3) // 4) * 8  # 16 / G = 4 rows per tile, 8 KV heads
+    assert ctas * 16 >= 9 * sms
+    tiles = _run("int8", chunk=64, fused=False, stream_ctas=_lib.PREFILL_TILES, heads=(32, 8))
+    np.testing.assert_array_equal(auto[5], tiles[5])
+    np.testing.assert_array_equal(auto[6], tiles[6])
 
 
 @pytest.mark.parametrize("fmt", TILE_PATH_FORMATS)
