@@ -190,6 +190,8 @@ import numpy as np
 from synth import WORKLOADS, make_inputs
 from oracle import kvq_oracle as O
 w = WORKLOADS[{name!r}]
+if {batch}:
+    w = w.with_(batch={batch})
 if {bf16}:
     w = w.with_(k_bits=16, v_bits=16, window=0, channel_factor=False)
 if {asym}:
@@ -236,11 +238,14 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def start_cpu_sample(name: str, budget_s: float, bf16: bool = False, asym: bool = False, qbits: int = 16):
+def start_cpu_sample(name: str, budget_s: float, bf16: bool = False, asym: bool = False, qbits: int = 16,
+                     batch: int = 0):
     """Start the oracle's decode (dequantize + attention, float64) on a bounded
-    sample of the workload's units in a fresh single-threaded process."""
+    sample of the workload's units in a fresh single-threaded process (`batch`:
+    the workload with that many sequences instead)."""
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="", **CPU_THREAD_ENV)
-    code = CPU_SAMPLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, bf16=bf16, asym=asym, qbits=qbits)
+    code = CPU_SAMPLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s, bf16=bf16, asym=asym, qbits=qbits,
+                                     batch=batch)
     return subprocess.Popen([sys.executable, "-c", code], stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
                             env=env)
 
@@ -683,6 +688,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the headline cpu_baseline (per_config entries: a third)")
     ap.add_argument("--stream-ctas", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload with this many sequences instead (a smaller case of the same "
+                         "kernel, e.g. for a multi-pass profile); the line's workload name says so")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph of the steps")
     ap.add_argument("--soak", type=float, default=1.0,
                     help="seconds of untimed steps before each timed region (clock sampling, steady state)")
@@ -714,6 +722,8 @@ def main():
     _lib.load()
 
     w = WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = w.with_(batch=args.batch, name=f"{w.name}_batch{args.batch}")
     if args.asym:
         w = w.with_(asym=True)
     if args.q_bits != 16:
@@ -722,7 +732,8 @@ def main():
     # the oracle samples run on the host cores while the GPU is measured
     cpu_jobs = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_jobs[w.name] = start_cpu_sample(args.workload, args.cpu_budget, asym=w.asym, qbits=w.q_bits)
+        cpu_jobs[w.name] = start_cpu_sample(args.workload, args.cpu_budget, asym=w.asym, qbits=w.q_bits,
+                                            batch=args.batch)
         for n in per_config_names:
             if n != args.workload or w.asym or w.q_bits != 16:
                 cpu_jobs[n + "/per_config"] = start_cpu_sample(n, args.cpu_budget / 3)
@@ -865,10 +876,12 @@ def reference_arm(args, rank, world):
         return
     from synth import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = w.with_(batch=args.batch, name=f"{w.name}_batch{args.batch}")
     K = args.steps
     # bounded: about 60 s of oracle work for the whole timed run, split over K steps
     per_step_budget = min(60.0 / max(K, 1), 5.0)
-    d = run_cpu_sample(w.name, per_step_budget * K)
+    d = run_cpu_sample(args.workload, per_step_budget * K, batch=args.batch)
     gbs = d["bytes"] / d["seconds"] / 1e9
     ms = d["seconds"] / K * 1e3
     line = {
