@@ -213,7 +213,8 @@ def test_prefill_auto_takes_tiles_when_they_fill_the_gpu():
     auto = _run("int8", chunk=64, fused=False, stream_ctas=0, heads=(32, 8))
     rows = len(auto[3])
     ctas = ((rows + 3) // 4) * 8  # 16 / G = 4 rows per tile, 8 KV heads
-    assert ctas * 16 >= 9 * sms
+    if ctas * 16 < 9 * sms:
+        pytest.skip(f"{ctas} tile CTAs do not reach 9/16 of {sms} SMs on this GPU")
     tiles = _run("int8", chunk=64, fused=False, stream_ctas=_lib.PREFILL_TILES, heads=(32, 8))
     np.testing.assert_array_equal(auto[5], tiles[5])
     np.testing.assert_array_equal(auto[6], tiles[6])
